@@ -1,0 +1,401 @@
+/*
+ * pkd_oracle.c -- CPU oracle for single-query decode attention over a paged
+ * fp16 KV cache.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the slow, plain fp64 statement of
+ * what the CUDA library computes; only the tests, the package's smoke check
+ * and the benchmark's CPU-baseline leg may load it.  It shares no code,
+ * header, table or helper with the CUDA path.
+ *
+ * What it computes (the plain definition; prefetching changes timing only):
+ *
+ *   for sequence b, query head h, kv head g = h / (Hq / Hkv):
+ *     for logical token t in [0, L_b):
+ *        p   = block_tables[b][t / bs]          physical block (page)
+ *        k_t = K[p][g][t % bs][:],  v_t = V[p][g][t % bs][:]
+ *        s_t = scale * sum_d q[b][h][d] * k_t[d]
+ *     w_t = exp(s_t - max_u s_u) / sum_u exp(s_u - max_u s_u)
+ *     out[b][h][:] = sum_t w_t * v_t
+ *
+ * Sources:
+ *  - Paged KV cache, logical page -> physical page table: CSDN answer
+ *    "如何优化LLM推理引擎的内存访问延迟？", section 2 (paged cache and page
+ *    table) and section 3 (PagedAttention: look up the page table, load the
+ *    KV pages, blockwise attention).
+ *  - The block loop over a block table bt[] for one head, Q resident, Q*K^T
+ *    per K block, then logits*V per V block: review "Accelerating LLM
+ *    Inference Throughput via Asynchronous KV Cache Prefetching", section 3.2
+ *    (XFormers flow), section 3.4 (Algorithm 1, range [s, e) of block
+ *    indices), section 4.1 (the same scheme for V blocks).
+ *  - One (block, kv-head) tile is block_size x head_dim fp16 values: the
+ *    M_block = b * d_h * T_block of the same review's section 4.2.
+ *  - Scaled softmax, fp16 inputs and a split of the context into partitions
+ *    with a merge step: the benchmark spec of this library; the pages print
+ *    no softmax formula, so the textbook definition above is used.
+ *
+ * Readings where the pages are silent (each listed in the design notes):
+ *  - GQA: query head h reads kv head h / (Hq/Hkv) (contiguous groups).
+ *  - KV layout [num_blocks][num_kv_heads][block_size][head_dim], K and V
+ *    separate arrays.  Q and out are [num_seqs][num_q_heads][head_dim].
+ *  - context_len == 0 gives out = 0; a partition holding no token has
+ *    m = -inf, l = 0, o = 0 and is skipped by the merge.
+ *
+ * Precision: inputs are IEEE binary16, decoded exactly to double; all
+ * arithmetic is IEEE double in the order written above.
+ *
+ * Parity pins (tests, CPU only): numpy's float16 decoding of all 65536 bit
+ * patterns; torch's scaled_dot_product_attention over contiguous K/V; block
+ * permutation invariance; softmax weights summing to one; identical keys or
+ * scale 0 giving the mean of V; context length 1 giving v_0; a one-token
+ * spike per position; GQA equal to repeated-KV MHA; the log-sum-exp merge of
+ * partitions equal to the unsplit result; partition sums at scale 0 equal to
+ * the exact token counts; and mutation tests that plant mistakes in this
+ * file (compile-time PKD_ORACLE_MUTANT) and require some pin to fail.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifndef PKD_ORACLE_MUTANT
+#define PKD_ORACLE_MUTANT 0
+#endif
+
+/* ---------------------------------------------------------------------- */
+/* IEEE 754 binary16 -> double, from the format's definition:             */
+/*   sign 1 bit, exponent 5 bits (bias 15), fraction 10 bits;             */
+/*   e = 0: subnormal  (-1)^s * 2^-14 * (f / 1024)                        */
+/*   e = 31: inf (f = 0) or NaN;  else (-1)^s * 2^(e-15) * (1 + f/1024)   */
+/* ---------------------------------------------------------------------- */
+double pkd_oracle_half_to_double(uint16_t bits)
+{
+    int sign = (bits >> 15) & 1;
+    int e = (bits >> 10) & 0x1f;
+    int f = bits & 0x3ff;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)f, -24);            /* 2^-14 * f / 2^10 */
+    } else if (e == 31) {
+        v = (f == 0) ? INFINITY : NAN;
+    } else {
+        v = ldexp(1024.0 + (double)f, e - 25); /* 2^(e-15) * (1024+f) / 2^10 */
+    }
+    return sign ? -v : v;
+}
+
+static double g_half_table[65536];
+static pthread_once_t g_table_once = PTHREAD_ONCE_INIT;
+static void build_half_table(void)
+{
+    for (uint32_t i = 0; i < 65536u; ++i) g_half_table[i] = pkd_oracle_half_to_double((uint16_t)i);
+}
+static inline double h2d(uint16_t b) { return g_half_table[b]; }
+
+/* ---------------------------------------------------------------------- */
+/* Problem description shared by the entry points below.                   */
+/* ---------------------------------------------------------------------- */
+typedef struct {
+    const uint16_t *q, *k_cache, *v_cache;
+    const int32_t *block_tables, *context_lens;
+    int num_seqs, num_q_heads, num_kv_heads, head_dim, block_size;
+    int num_blocks, max_blocks_per_seq;
+    double scale;
+} problem_t;
+
+/* Address of the K (or V) row of logical token t of sequence b, kv head g.
+ * Returns NULL when the block table entry is outside the pool. */
+static const uint16_t *kv_row(const problem_t *P, const uint16_t *cache, int b, int g, int t)
+{
+    int logical_block = t / P->block_size;
+    int slot = t % P->block_size;
+#if PKD_ORACLE_MUTANT == 1      /* planted mistake: block and slot swapped */
+    logical_block = t % P->block_size;
+    slot = t / P->block_size;
+    if (slot >= P->block_size) slot = P->block_size - 1;
+    if (logical_block >= P->max_blocks_per_seq) logical_block = P->max_blocks_per_seq - 1;
+#endif
+    int p = P->block_tables[(size_t)b * P->max_blocks_per_seq + logical_block];
+    if (p < 0 || p >= P->num_blocks) return NULL;
+    size_t off = (((size_t)p * P->num_kv_heads + g) * P->block_size + slot) * P->head_dim;
+    return cache + off;
+}
+
+static int kv_head_of(const problem_t *P, int h)
+{
+    int group = P->num_q_heads / P->num_kv_heads;
+#if PKD_ORACLE_MUTANT == 2      /* planted mistake: interleaved instead of contiguous groups */
+    return h % P->num_kv_heads;
+#else
+    return h / group;
+#endif
+}
+
+/* Scores s_t for t in [t0, t1) of (b, h).  Returns -1 on a bad block id. */
+static int scores(const problem_t *P, int b, int h, int t0, int t1, double *s)
+{
+    int g = kv_head_of(P, h);
+    const uint16_t *qv = P->q + ((size_t)b * P->num_q_heads + h) * P->head_dim;
+    for (int t = t0; t < t1; ++t) {
+        const uint16_t *k = kv_row(P, P->k_cache, b, g, t);
+        if (!k) return -1;
+        double dot = 0.0;
+        for (int d = 0; d < P->head_dim; ++d) dot += h2d(qv[d]) * h2d(k[d]);
+#if PKD_ORACLE_MUTANT == 3      /* planted mistake: scale dropped */
+        s[t - t0] = dot;
+#else
+        s[t - t0] = P->scale * dot;
+#endif
+    }
+    return 0;
+}
+
+/* Softmax weights of (b, h) over [0, L_b) into w[0..L_b).  -1 on bad ids. */
+static int weights(const problem_t *P, int b, int h, double *w)
+{
+    int L = P->context_lens[b];
+#if PKD_ORACLE_MUTANT == 4      /* planted mistake: last token dropped */
+    if (L > 0) L -= 1;
+#endif
+    if (L <= 0) return 0;
+    if (scores(P, b, h, 0, L, w)) return -1;
+    double m = -INFINITY;
+    for (int t = 0; t < L; ++t) if (w[t] > m) m = w[t];
+    double z = 0.0;
+    for (int t = 0; t < L; ++t) { w[t] = exp(w[t] - m); z += w[t]; }
+#if PKD_ORACLE_MUTANT == 5      /* planted mistake: normalisation dropped */
+    z = 1.0;
+#endif
+    for (int t = 0; t < L; ++t) w[t] /= z;
+    return 0;
+}
+
+/* out[0..D) = sum_t w_t v_t for (b, h).  w is scratch of L_b doubles. */
+static int attend_row(const problem_t *P, int b, int h, double *w, double *out)
+{
+    int D = P->head_dim;
+    int L = P->context_lens[b];
+#if PKD_ORACLE_MUTANT == 4
+    if (L > 0) L -= 1;
+#endif
+    for (int d = 0; d < D; ++d) out[d] = 0.0;
+    if (L <= 0) return 0;
+    if (weights(P, b, h, w)) return -1;
+    int g = kv_head_of(P, h);
+    for (int t = 0; t < L; ++t) {
+#if PKD_ORACLE_MUTANT == 6      /* planted mistake: values read from the K cache */
+        const uint16_t *v = kv_row(P, P->k_cache, b, g, t);
+#else
+        const uint16_t *v = kv_row(P, P->v_cache, b, g, t);
+#endif
+        if (!v) return -1;
+        for (int d = 0; d < D; ++d) out[d] += w[t] * h2d(v[d]);
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Threaded driver over rows (b, h).                                       */
+/* ---------------------------------------------------------------------- */
+typedef struct {
+    const problem_t *P;
+    const int32_t *rows;   /* row ids b*Hq + h, or NULL for all */
+    int num_rows;
+    double *out;           /* [num_rows][D] */
+    int next;              /* work counter (guarded by mu) */
+    int status;
+    pthread_mutex_t mu;
+} job_t;
+
+static void *worker(void *arg)
+{
+    job_t *J = (job_t *)arg;
+    const problem_t *P = J->P;
+    int maxL = 0;
+    for (int b = 0; b < P->num_seqs; ++b) if (P->context_lens[b] > maxL) maxL = P->context_lens[b];
+    double *w = (double *)malloc(sizeof(double) * (size_t)(maxL > 0 ? maxL : 1));
+    if (!w) { pthread_mutex_lock(&J->mu); J->status = -2; pthread_mutex_unlock(&J->mu); return NULL; }
+    for (;;) {
+        pthread_mutex_lock(&J->mu);
+        int i = J->next++;
+        pthread_mutex_unlock(&J->mu);
+        if (i >= J->num_rows) break;
+        int row = J->rows ? J->rows[i] : i;
+        int b = row / P->num_q_heads, h = row % P->num_q_heads;
+        if (attend_row(P, b, h, w, J->out + (size_t)i * P->head_dim)) {
+            pthread_mutex_lock(&J->mu); J->status = -1; pthread_mutex_unlock(&J->mu);
+        }
+    }
+    free(w);
+    return NULL;
+}
+
+static int check_problem(const problem_t *P)
+{
+    if (!P->q || !P->k_cache || !P->v_cache || !P->block_tables || !P->context_lens) return -3;
+    if (P->num_seqs < 0 || P->num_q_heads <= 0 || P->num_kv_heads <= 0 || P->head_dim <= 0 ||
+        P->block_size <= 0 || P->max_blocks_per_seq <= 0 || P->num_blocks <= 0) return -3;
+    if (P->num_q_heads % P->num_kv_heads) return -3;
+    for (int b = 0; b < P->num_seqs; ++b) {
+        int L = P->context_lens[b];
+        if (L < 0 || L > P->max_blocks_per_seq * P->block_size) return -3;
+    }
+    return 0;
+}
+
+/*
+ * Exact attention for the listed rows (row = b * num_q_heads + h), or for
+ * every row when rows == NULL (then out is [num_seqs][num_q_heads][head_dim]).
+ * Returns 0; -1 if a used block-table entry is outside [0, num_blocks);
+ * -2 on allocation failure; -3 on a bad argument.
+ */
+int pkd_oracle_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                         const int32_t *block_tables, const int32_t *context_lens,
+                         int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                         int block_size, int num_blocks, int max_blocks_per_seq, double scale,
+                         const int32_t *rows, int num_rows, double *out, int num_threads)
+{
+    pthread_once(&g_table_once, build_half_table);
+    problem_t P = {q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads,
+                   num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, scale};
+    int rc = check_problem(&P);
+    if (rc) return rc;
+    job_t J;
+    J.P = &P; J.rows = rows; J.out = out; J.next = 0; J.status = 0;
+    J.num_rows = rows ? num_rows : num_seqs * num_q_heads;
+    if (rows) {
+        for (int i = 0; i < num_rows; ++i)
+            if (rows[i] < 0 || rows[i] >= num_seqs * num_q_heads) return -3;
+    }
+    pthread_mutex_init(&J.mu, NULL);
+    if (num_threads < 1) num_threads = 1;
+    if (num_threads > 1024) num_threads = 1024;
+    pthread_t *tid = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)num_threads);
+    if (!tid) { pthread_mutex_destroy(&J.mu); return -2; }
+    int started = 0;
+    for (int i = 0; i < num_threads; ++i) {
+        if (pthread_create(&tid[i], NULL, worker, &J) == 0) ++started;
+        else break;
+    }
+    if (started == 0) worker(&J);
+    for (int i = 0; i < started; ++i) pthread_join(tid[i], NULL);
+    free(tid);
+    pthread_mutex_destroy(&J.mu);
+    return J.status;
+}
+
+/* Softmax weights w[0..L_b) of one row (b, h).  Same return codes. */
+int pkd_oracle_weights(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                       const int32_t *block_tables, const int32_t *context_lens,
+                       int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                       int block_size, int num_blocks, int max_blocks_per_seq, double scale,
+                       int b, int h, double *w)
+{
+    pthread_once(&g_table_once, build_half_table);
+    problem_t P = {q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads,
+                   num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, scale};
+    int rc = check_problem(&P);
+    if (rc) return rc;
+    if (b < 0 || b >= num_seqs || h < 0 || h >= num_q_heads) return -3;
+    return weights(&P, b, h, w);
+}
+
+/*
+ * Per-partition statistics for a split of each context into partitions of
+ * partition_size tokens: partition j of sequence b covers logical tokens
+ * [j*P, min((j+1)*P, L_b)).  For each (b, h, j):
+ *   m = max_t s_t,  l = sum_t exp(s_t - m),  o[:] = sum_t exp(s_t - m) v_t
+ * (o unnormalised).  Partitions with no token: m = -inf, l = 0, o = 0.
+ * Layouts: m, l [num_seqs][num_q_heads][max_partitions];
+ *          o    [num_seqs][num_q_heads][max_partitions][head_dim].
+ */
+int pkd_oracle_partitions(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                          const int32_t *block_tables, const int32_t *context_lens,
+                          int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                          int block_size, int num_blocks, int max_blocks_per_seq, double scale,
+                          int partition_size, int max_partitions,
+                          double *m_out, double *l_out, double *o_out)
+{
+    pthread_once(&g_table_once, build_half_table);
+    problem_t P = {q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads,
+                   num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, scale};
+    int rc = check_problem(&P);
+    if (rc) return rc;
+    if (partition_size <= 0 || max_partitions <= 0) return -3;
+    int D = head_dim;
+    double *s = (double *)malloc(sizeof(double) * (size_t)partition_size);
+    if (!s) return -2;
+    for (int b = 0; b < num_seqs; ++b) {
+        int L = context_lens[b];
+        if ((L + partition_size - 1) / partition_size > max_partitions) { free(s); return -3; }
+        for (int h = 0; h < num_q_heads; ++h) {
+            int g = kv_head_of(&P, h);
+            for (int j = 0; j < max_partitions; ++j) {
+                size_t idx = ((size_t)b * num_q_heads + h) * max_partitions + j;
+                double *o = o_out + idx * D;
+                for (int d = 0; d < D; ++d) o[d] = 0.0;
+                int t0 = j * partition_size;
+                int t1 = t0 + partition_size;
+#if PKD_ORACLE_MUTANT == 7      /* planted mistake: partitions overlap by one token */
+                t1 += 1;
+#endif
+                if (t1 > L) t1 = L;
+                if (t0 >= t1) { m_out[idx] = -INFINITY; l_out[idx] = 0.0; continue; }
+                if (scores(&P, b, h, t0, t1, s)) { free(s); return -1; }
+                double m = -INFINITY;
+                for (int t = t0; t < t1; ++t) if (s[t - t0] > m) m = s[t - t0];
+                double l = 0.0;
+                for (int t = t0; t < t1; ++t) {
+                    double e = exp(s[t - t0] - m);
+                    l += e;
+                    const uint16_t *v = kv_row(&P, v_cache, b, g, t);
+                    if (!v) { free(s); return -1; }
+                    for (int d = 0; d < D; ++d) o[d] += e * h2d(v[d]);
+                }
+                m_out[idx] = m;
+                l_out[idx] = l;
+            }
+        }
+    }
+    free(s);
+    return 0;
+}
+
+/*
+ * Merge of partition statistics (log-sum-exp identity):
+ *   M = max_j m_j,  out = sum_j exp(m_j - M) o_j / sum_j exp(m_j - M) l_j,
+ * over the partitions that hold a token (j < ceil(L_b / P)); out = 0 when
+ * L_b = 0.  Layouts as in pkd_oracle_partitions; out [num_seqs][num_q_heads][D].
+ */
+int pkd_oracle_merge(const double *m_in, const double *l_in, const double *o_in,
+                     const int32_t *context_lens, int num_seqs, int num_q_heads, int head_dim,
+                     int partition_size, int max_partitions, double *out)
+{
+    if (!m_in || !l_in || !o_in || !context_lens || !out) return -3;
+    if (partition_size <= 0 || max_partitions <= 0 || head_dim <= 0) return -3;
+    int D = head_dim;
+    for (int b = 0; b < num_seqs; ++b) {
+        int L = context_lens[b];
+        int np = (L + partition_size - 1) / partition_size;
+        if (np > max_partitions) return -3;
+        for (int h = 0; h < num_q_heads; ++h) {
+            size_t base = ((size_t)b * num_q_heads + h) * max_partitions;
+            double *y = out + ((size_t)b * num_q_heads + h) * D;
+            for (int d = 0; d < D; ++d) y[d] = 0.0;
+            if (np == 0) continue;
+            double M = -INFINITY;
+            for (int j = 0; j < np; ++j) if (m_in[base + j] > M) M = m_in[base + j];
+            double z = 0.0;
+            for (int j = 0; j < np; ++j) {
+                double c = exp(m_in[base + j] - M);
+                z += c * l_in[base + j];
+                for (int d = 0; d < D; ++d) y[d] += c * o_in[(base + j) * D + d];
+            }
+            for (int d = 0; d < D; ++d) y[d] /= z;
+        }
+    }
+    return 0;
+}
+
+/* Which planted mistake (0 = none) this build carries; for the mutation tests. */
+int pkd_oracle_mutant(void) { return PKD_ORACLE_MUTANT; }

@@ -1,0 +1,298 @@
+"""Pins of the CPU oracle against facts fixed outside it.
+
+Each ``pin_*`` function checks the oracle (optionally a build with a planted
+mistake, ``mutant``) against something the pages or the mathematics fix:
+numpy's binary16 decoding, torch's scaled_dot_product_attention over
+contiguous K/V, closed forms (mean of V, a single token, a one-token spike),
+invariants (block permutation, weights summing to one, GQA == repeated MHA,
+masking), and the log-sum-exp identity for the partition merge.  The mutation
+test at the bottom requires every planted mistake to fail at least one pin.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+TOL = 1e-12
+
+
+# ---------------------------------------------------------------------------
+# Input construction independent of the oracle's gather: logical per-sequence
+# K/V rows are scattered into a pool through an explicit block permutation.
+# ---------------------------------------------------------------------------
+def scatter_problem(seed, lens, Hq, Hkv, D, BS, extra_blocks=3, mbps=None, logical_k=None,
+                    logical_v=None, q=None, pool_fill=None):
+    rng = np.random.default_rng(seed)
+    B = len(lens)
+    nbs = [-(-L // BS) for L in lens]
+    needed = sum(nbs)
+    NB = needed + extra_blocks
+    mbps = mbps or max(1, max(nbs) if nbs else 1)
+    perm = rng.permutation(NB)[:needed]
+    if pool_fill is None:
+        kp = rng.standard_normal((NB, Hkv, BS, D)).astype(np.float16)
+        vp = rng.standard_normal((NB, Hkv, BS, D)).astype(np.float16)
+    else:
+        kp = np.full((NB, Hkv, BS, D), pool_fill, np.float16)
+        vp = np.full((NB, Hkv, BS, D), pool_fill, np.float16)
+    if logical_k is None:
+        logical_k = [rng.standard_normal((Hkv, L, D)).astype(np.float16) for L in lens]
+    if logical_v is None:
+        logical_v = [rng.standard_normal((Hkv, L, D)).astype(np.float16) for L in lens]
+    if q is None:
+        q = rng.standard_normal((B, Hq, D)).astype(np.float16)
+    bt = np.full((B, mbps), -1, np.int32)
+    pos = 0
+    for b, L in enumerate(lens):
+        for i in range(nbs[b]):
+            p = int(perm[pos]); pos += 1
+            bt[b, i] = p
+            t0, t1 = i * BS, min(L, (i + 1) * BS)
+            kp[p, :, : t1 - t0, :] = logical_k[b][:, t0:t1, :]
+            vp[p, :, : t1 - t0, :] = logical_v[b][:, t0:t1, :]
+    cl = np.array(lens, np.int32)
+    return dict(q=q, k=kp, v=vp, bt=bt, cl=cl, lk=logical_k, lv=logical_v, perm=perm, NB=NB)
+
+
+def run(pr, scale, mutant=0, **kw):
+    return oracle.attention(pr["q"], pr["k"], pr["v"], pr["bt"], pr["cl"], scale, mutant=mutant, **kw)
+
+
+def sdpa_reference(pr, scale, Hq, Hkv):
+    """torch's scaled_dot_product_attention in fp64 over contiguous K/V."""
+    G = Hq // Hkv
+    outs = []
+    for b, L in enumerate(pr["cl"]):
+        D = pr["q"].shape[2]
+        if L == 0:
+            outs.append(np.zeros((Hq, D)))
+            continue
+        q = torch.from_numpy(pr["q"][b].astype(np.float64)).view(1, Hq, 1, D)
+        k = torch.from_numpy(pr["lk"][b].astype(np.float64)).repeat_interleave(G, 0).view(1, Hq, L, D)
+        v = torch.from_numpy(pr["lv"][b].astype(np.float64)).repeat_interleave(G, 0).view(1, Hq, L, D)
+        o = torch.nn.functional.scaled_dot_product_attention(q, k, v, scale=scale)
+        outs.append(o.view(Hq, D).numpy())
+    return np.stack(outs)
+
+
+# ---------------------------------------------------------------------------
+# Pins
+# ---------------------------------------------------------------------------
+def pin_half_decoder(mutant=0):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = oracle.half_to_double(bits)
+    nan = np.isnan(ref)
+    assert np.array_equal(nan, np.isnan(got))
+    assert np.array_equal(ref[~nan], got[~nan])
+
+
+def pin_sdpa_contiguous(mutant=0):
+    for seed, (lens, Hq, Hkv, D, BS) in enumerate([
+        ((37, 100), 4, 4, 64, 16),
+        ((1, 5, 16, 33), 8, 2, 32, 4),
+        ((70, 9, 48), 14, 2, 16, 8),
+        ((17,), 6, 3, 8, 16),
+    ]):
+        pr = scatter_problem(100 + seed, list(lens), Hq, Hkv, D, BS)
+        scale = 1.0 / math.sqrt(D)
+        got = run(pr, scale, mutant)
+        ref = sdpa_reference(pr, scale, Hq, Hkv)
+        assert np.max(np.abs(got - ref)) <= TOL * max(1.0, np.max(np.abs(ref)))
+
+
+def pin_permutation_invariance(mutant=0):
+    lens, Hq, Hkv, D, BS = [23, 64, 50], 6, 2, 16, 8
+    base = scatter_problem(7, lens, Hq, Hkv, D, BS)
+    other = scatter_problem(8, lens, Hq, Hkv, D, BS, logical_k=base["lk"], logical_v=base["lv"],
+                            q=base["q"])
+    assert not np.array_equal(base["bt"], other["bt"])
+    a = run(base, 0.25, mutant)
+    b = run(other, 0.25, mutant)
+    assert np.array_equal(a, b)
+
+
+def pin_weights_sum_to_one(mutant=0):
+    lens, Hq, Hkv, D, BS = [45, 3], 4, 2, 16, 16
+    pr = scatter_problem(11, lens, Hq, Hkv, D, BS)
+    for b, L in enumerate(lens):
+        for h in range(Hq):
+            w = oracle.weights(pr["q"], pr["k"], pr["v"], pr["bt"], pr["cl"], 0.25, b, h,
+                               mutant=mutant)
+            assert w.shape == (L,)
+            assert np.all(w >= 0)
+            assert abs(w.sum() - 1.0) <= TOL
+
+
+def pin_identical_keys_mean_of_v(mutant=0):
+    lens, Hq, Hkv, D, BS = [29, 64, 7], 4, 2, 16, 8
+    rng = np.random.default_rng(5)
+    row = rng.standard_normal(D).astype(np.float16)
+    lk = [np.broadcast_to(row, (Hkv, L, D)).copy() for L in lens]
+    pr = scatter_problem(12, lens, Hq, Hkv, D, BS, logical_k=lk)
+    got = run(pr, 0.3, mutant)
+    G = Hq // Hkv
+    for b in range(len(lens)):
+        for h in range(Hq):
+            ref = pr["lv"][b][h // G].astype(np.float64).mean(axis=0)
+            assert np.max(np.abs(got[b, h] - ref)) <= TOL
+
+
+def pin_scale_zero_mean_of_v(mutant=0):
+    lens, Hq, Hkv, D, BS = [31, 16], 4, 4, 8, 16
+    pr = scatter_problem(13, lens, Hq, Hkv, D, BS)
+    got = run(pr, 0.0, mutant)
+    for b in range(len(lens)):
+        for h in range(Hq):
+            ref = pr["lv"][b][h].astype(np.float64).mean(axis=0)
+            assert np.max(np.abs(got[b, h] - ref)) <= TOL
+
+
+def pin_single_token(mutant=0):
+    lens, Hq, Hkv, D, BS = [1, 1, 1], 6, 3, 16, 16
+    pr = scatter_problem(14, lens, Hq, Hkv, D, BS)
+    got = run(pr, 0.25, mutant)
+    G = Hq // Hkv
+    for b in range(3):
+        for h in range(Hq):
+            assert np.array_equal(got[b, h], pr["lv"][b][h // G][0].astype(np.float64))
+
+
+def pin_spike_every_position(mutant=0):
+    L, Hq, Hkv, D, BS = 37, 2, 1, 16, 16
+    for t_star in range(L):
+        q = np.ones((1, Hq, D), np.float16)
+        rng = np.random.default_rng(1000 + t_star)
+        lk = [rng.standard_normal((Hkv, L, D)).astype(np.float16)]
+        lk[0][:, t_star, :] = 1000.0
+        pr = scatter_problem(15 + t_star, [L], Hq, Hkv, D, BS, logical_k=lk, q=q)
+        got = run(pr, 0.25, mutant)
+        ref = pr["lv"][0][0, t_star].astype(np.float64)
+        for h in range(Hq):
+            assert np.array_equal(got[0, h], ref), t_star
+
+
+def pin_gqa_equals_repeated_mha(mutant=0):
+    lens, Hq, Hkv, D, BS = [40, 19], 14, 2, 16, 8
+    pr = scatter_problem(16, lens, Hq, Hkv, D, BS)
+    G = Hq // Hkv
+    mha = dict(pr)
+    mha["k"] = np.repeat(pr["k"], G, axis=1)
+    mha["v"] = np.repeat(pr["v"], G, axis=1)
+    a = run(pr, 0.25, mutant)
+    b = run(mha, 0.25, mutant)
+    assert np.array_equal(a, b)
+
+
+def pin_context_zero(mutant=0):
+    pr = scatter_problem(17, [0, 5], 2, 2, 8, 4, mbps=2)
+    got = run(pr, 0.5, mutant)
+    assert np.array_equal(got[0], np.zeros((2, 8)))
+
+
+def pin_nan_poison_ignored(mutant=0):
+    lens, Hq, Hkv, D, BS = [21, 9], 4, 2, 16, 8
+    clean = scatter_problem(18, lens, Hq, Hkv, D, BS)
+    poison = scatter_problem(18, lens, Hq, Hkv, D, BS, logical_k=clean["lk"], logical_v=clean["lv"],
+                             q=clean["q"], pool_fill=np.nan)
+    # unused pool blocks and tail slots hold NaN, used rows are identical
+    assert np.isnan(poison["k"]).any()
+    a = run(clean, 0.25, mutant)
+    b = run(poison, 0.25, mutant)
+    assert np.all(np.isfinite(b))
+    assert np.array_equal(a, b)
+
+
+def pin_partition_merge(mutant=0):
+    lens, Hq, Hkv, D, BS, P = [100, 33, 64, 1, 0], 6, 2, 16, 16, 32
+    pr = scatter_problem(19, lens, Hq, Hkv, D, BS, mbps=8)
+    full = run(pr, 0.25, mutant)
+    m, l, o = oracle.partitions(pr["q"], pr["k"], pr["v"], pr["bt"], pr["cl"], 0.25, P,
+                                mutant=mutant)
+    merged = oracle.merge(m, l, o, pr["cl"], P, mutant=mutant)
+    assert np.max(np.abs(merged - full)) <= TOL
+
+
+def pin_partition_counts_scale_zero(mutant=0):
+    lens, Hq, Hkv, D, BS, P = [100, 32, 1, 64, 0], 2, 1, 8, 16, 32
+    pr = scatter_problem(20, lens, Hq, Hkv, D, BS, mbps=8)
+    m, l, o = oracle.partitions(pr["q"], pr["k"], pr["v"], pr["bt"], pr["cl"], 0.0, P,
+                                max_partitions=4, mutant=mutant)
+    for b, L in enumerate(lens):
+        for j in range(4):
+            expect = max(0, min(P, L - j * P))
+            assert np.all(l[b, :, j] == expect), (b, j, l[b, :, j])
+            if expect == 0:
+                assert np.all(np.isneginf(m[b, :, j]))
+            else:
+                assert np.all(m[b, :, j] == 0.0)
+
+
+def pin_partition_max_is_max_score(mutant=0):
+    lens, Hq, Hkv, D, BS, P = [70], 2, 2, 16, 16, 32
+    pr = scatter_problem(21, lens, Hq, Hkv, D, BS)
+    m, l, o = oracle.partitions(pr["q"], pr["k"], pr["v"], pr["bt"], pr["cl"], 0.25, P,
+                                mutant=mutant)
+    for h in range(Hq):
+        q = pr["q"][0, h].astype(np.float64)
+        k = pr["lk"][0][h].astype(np.float64)
+        s = 0.25 * (k @ q)
+        for j in range(m.shape[2]):
+            seg = s[j * P: (j + 1) * P]
+            assert abs(m[0, h, j] - seg.max()) <= TOL
+            assert abs(l[0, h, j] - np.exp(seg - seg.max()).sum()) <= TOL * len(seg)
+
+
+PINS = [pin_half_decoder, pin_sdpa_contiguous, pin_permutation_invariance, pin_weights_sum_to_one,
+        pin_identical_keys_mean_of_v, pin_scale_zero_mean_of_v, pin_single_token,
+        pin_spike_every_position, pin_gqa_equals_repeated_mha, pin_context_zero,
+        pin_nan_poison_ignored, pin_partition_merge, pin_partition_counts_scale_zero,
+        pin_partition_max_is_max_score]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
+def test_oracle_pin(pin):
+    pin(0)
+
+
+def test_threads_do_not_change_result():
+    pr = scatter_problem(30, [77, 5, 130], 8, 2, 32, 16)
+    a = run(pr, 0.2, threads=1)
+    b = run(pr, 0.2, threads=7)
+    assert np.array_equal(a, b)
+
+
+def test_row_selection_matches_full():
+    pr = scatter_problem(31, [40, 12], 4, 2, 16, 8)
+    full = run(pr, 0.3)
+    rows = np.array([5, 0, 7, 2], np.int32)
+    sel = run(pr, 0.3, rows=rows)
+    for i, r in enumerate(rows):
+        assert np.array_equal(sel[i], full[r // 4, r % 4])
+
+
+def test_bad_block_id_is_reported():
+    pr = scatter_problem(32, [20], 2, 2, 8, 16)
+    pr["bt"][0, 1] = pr["NB"] + 5
+    with pytest.raises(oracle.OracleError):
+        run(pr, 0.3)
+
+
+MUTANTS = list(range(1, 8))
+
+
+@pytest.mark.parametrize("mutant", MUTANTS)
+def test_planted_mistake_fails_a_pin(mutant):
+    assert oracle.mutant_id(mutant) == mutant
+    failed = []
+    for pin in PINS:
+        if pin is pin_half_decoder:
+            continue
+        try:
+            pin(mutant)
+        except (AssertionError, oracle.OracleError):
+            failed.append(pin.__name__)
+    assert failed, f"planted mistake {mutant} passed every pin"
