@@ -1,0 +1,217 @@
+/*
+ * paged_decode.h -- C ABI of libpaged_decode.so: single-query decode
+ * attention over a paged fp16 KV cache, for NVIDIA GB300 (sm_103a).
+ *
+ * The operation (for every sequence b and query head h, kv head
+ * g = h / (num_q_heads / num_kv_heads)):
+ *
+ *   p_t   = block_tables[b][t / block_size]            (physical block)
+ *   s_t   = scale * dot(q[b][h][:], K[p_t][g][t % block_size][:])
+ *   out[b][h][:] = sum_{t < L_b} softmax(s)_t * V[p_t][g][t % block_size][:]
+ *
+ * Sources: the paged cache and its logical->physical page table are
+ * described in the CSDN answer "如何优化LLM推理引擎的内存访问延迟？"
+ * (section 2, section 3); the per-head loop over a block table, with Q
+ * resident, Q*K^T per K block and logits*V per V block, is section 3.2 and
+ * Algorithm 1 (section 3.4) of the review "Accelerating LLM Inference
+ * Throughput via Asynchronous KV Cache Prefetching"; its section 3.5 and
+ * section 4.1 give the asynchronous L2 prefetch of upcoming K and V blocks
+ * (cp.async.bulk.prefetch.L2) that the L2-prefetch variants issue.
+ *
+ * Layouts (all row-major, C order):
+ *   q, out        fp16 [num_seqs][num_q_heads][head_dim]
+ *   k_cache       fp16 [num_blocks][num_kv_heads][block_size][head_dim]
+ *   v_cache       fp16 same layout as k_cache
+ *   block_tables  int32 [num_seqs][max_blocks_per_seq]; entries at or past
+ *                 ceil(context_lens[b] / block_size) are never read as
+ *                 addresses (they may hold -1)
+ *   context_lens  int32 [num_seqs], each in [0, max_context_len]
+ * fp16 is IEEE binary16 passed as raw 16-bit words.  Every pointer named
+ * "device" must be CUDA device memory (or managed memory) of the current
+ * device.  K and V rows that are used must hold finite values.
+ *
+ * Ownership and threading: every buffer belongs to the caller.  The library
+ * allocates no memory, keeps no state between calls, and may be called from
+ * several host threads at once.  Work is enqueued on `stream` and the calls
+ * return without waiting for it.
+ *
+ * Errors: arguments are checked on the host before any launch; a failed
+ * check returns a status and launches nothing.  PKD_ERR_LAUNCH reports a
+ * CUDA launch failure.  Device-side problems (a block-table entry outside
+ * [0, num_blocks), or a bounded wait that ran out) are recorded in the
+ * optional `error_word` (device int, nullable): the kernel ORs PKD_DEVERR_*
+ * bits into it and skips the affected work; read it with
+ * pkd_read_device_error().
+ */
+#ifndef PAGED_DECODE_H_
+#define PAGED_DECODE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PKD_OK = 0,
+  PKD_ERR_NULL = 1,         /* a required pointer is NULL */
+  PKD_ERR_SHAPE = 2,        /* a size is out of range or inconsistent */
+  PKD_ERR_UNSUPPORTED = 3,  /* head_dim / block_size / group size not compiled */
+  PKD_ERR_ALIGN = 4,        /* a pointer is not 16-byte aligned */
+  PKD_ERR_WORKSPACE = 5,    /* workspace missing or smaller than required */
+  PKD_ERR_LAUNCH = 6,       /* the CUDA launch failed */
+  PKD_ERR_DEVICE = 7,       /* the device reported an error (error word set) */
+  PKD_ERR_CUDA = 8          /* a CUDA runtime query failed */
+} pkd_status;
+
+/* Bits of the device error word. */
+#define PKD_DEVERR_BAD_BLOCK 1u /* a used block-table entry was outside [0, num_blocks) */
+#define PKD_DEVERR_TIMEOUT 2u   /* a bounded wait on a shared-memory barrier ran out */
+
+/* How K/V tiles reach the arithmetic.  All variants give the same result. */
+typedef enum {
+  PKD_VARIANT_AUTO = 0,        /* the fastest variant for the shape */
+  PKD_VARIANT_NO_PREFETCH = 1, /* each warp loads its current blocks (16-byte loads) */
+  PKD_VARIANT_L2_PREFETCH = 2, /* as 1, plus cp.async.bulk.prefetch.L2 of blocks ahead */
+  PKD_VARIANT_TMA_STAGED = 3   /* bulk tensor copies into a shared-memory ring, plus L2 prefetch */
+} pkd_variant;
+
+/*
+ * paged_decode_attention -- the whole operation, one partition per
+ * (sequence, kv head): out[b][h][:] as defined above.  No workspace.
+ *
+ *   q, k_cache, v_cache, block_tables, context_lens : device, layouts above
+ *   out            device fp16 [num_seqs][num_q_heads][head_dim] (written)
+ *   num_seqs       >= 0 (0: nothing is launched)
+ *   num_q_heads    multiple of num_kv_heads; group = num_q_heads/num_kv_heads
+ *                  in 1..8
+ *   head_dim       64 or 128
+ *   block_size     16 or 32
+ *   num_blocks     physical blocks in k_cache / v_cache (> 0)
+ *   max_blocks_per_seq  row length of block_tables (> 0)
+ *   max_context_len     host upper bound of context_lens (sizes the grid)
+ *   scale          softmax scale applied to q.k (e.g. 1/sqrt(head_dim))
+ *   stream         CUDA stream (0 = legacy default stream)
+ * Sequences with context length 0 get out = 0.
+ */
+pkd_status paged_decode_attention(const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* block_tables, const int32_t* context_lens, void* out,
+                                  int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                  int block_size, int num_blocks, int max_blocks_per_seq,
+                                  int max_context_len, float scale, cudaStream_t stream);
+
+/*
+ * paged_decode_attention_ex -- as paged_decode_attention, with control over
+ * the context split and the data path.
+ *
+ *   partition_size  tokens per context partition (split-K): 0 = choose
+ *                   automatically from the shape and the GPU; -1 = never
+ *                   split; otherwise a positive multiple of 32 (and of
+ *                   block_size).  A sequence longer than one partition is
+ *                   computed by one CTA per (sequence, kv head, partition)
+ *                   and merged by the split-K reduce; shorter ones are
+ *                   written directly.
+ *   variant         pkd_variant
+ *   prefetch_distance  how many warp steps ahead the L2 prefetch runs
+ *                   (0 = default); ignored by PKD_VARIANT_NO_PREFETCH
+ *   workspace, workspace_bytes  device scratch of at least
+ *                   paged_decode_workspace_size(...) bytes, 256-byte aligned
+ *                   (may be NULL when no sequence is split)
+ *   error_word      device int or NULL; see "Errors" above
+ * Calls that share a workspace must not overlap on the GPU.
+ */
+pkd_status paged_decode_attention_ex(const void* q, const void* k_cache, const void* v_cache,
+                                     const int32_t* block_tables, const int32_t* context_lens,
+                                     void* out, int num_seqs, int num_q_heads, int num_kv_heads,
+                                     int head_dim, int block_size, int num_blocks,
+                                     int max_blocks_per_seq, int max_context_len, float scale,
+                                     int partition_size, int variant, int prefetch_distance,
+                                     void* workspace, size_t workspace_bytes, int* error_word,
+                                     cudaStream_t stream);
+
+/*
+ * The partition size paged_decode_attention_ex uses when given 0 with this
+ * `variant` (a positive multiple of 32, or -1 when it would not split), for
+ * the current device.  Returns -2 on invalid sizes.
+ */
+int paged_decode_auto_partition_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                     int block_size, int max_context_len, int variant);
+
+/*
+ * Workspace bytes paged_decode_attention_ex needs for a split into
+ * partitions of partition_size tokens (0 = automatic for `variant`, as
+ * above): the fp32
+ * partials [num_seqs][num_q_heads][NP][head_dim] and the per-partition
+ * max and sum [num_seqs][num_q_heads][NP], NP = ceil(max_context_len /
+ * partition_size), each region 256-byte aligned.  0 when nothing splits.
+ */
+size_t paged_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                   int block_size, int max_context_len, int partition_size,
+                                   int variant);
+
+/*
+ * paged_decode_partitions -- the first split-K kernel alone: for every
+ * (b, h) and partition j < ceil(L_b / partition_size), covering logical
+ * tokens [j*P, min((j+1)*P, L_b)):
+ *   max_logits[b][h][j] = max_t s_t
+ *   exp_sums[b][h][j]   = sum_t exp(s_t - max_logits)
+ *   tmp_out[b][h][j][:] = sum_t exp(s_t - max_logits) * v_t   (not normalised)
+ * Entries of partitions past ceil(L_b / P) are not written.
+ *   tmp_out     device fp32 [num_seqs][num_q_heads][max_num_partitions][head_dim]
+ *   max_logits, exp_sums  device fp32 [num_seqs][num_q_heads][max_num_partitions]
+ *   max_num_partitions >= ceil(max_context_len / partition_size)
+ * partition_size is a positive multiple of 32 and of block_size.
+ */
+pkd_status paged_decode_partitions(const void* q, const void* k_cache, const void* v_cache,
+                                   const int32_t* block_tables, const int32_t* context_lens,
+                                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                   int block_size, int num_blocks, int max_blocks_per_seq,
+                                   int max_context_len, float scale, int partition_size,
+                                   int variant, int prefetch_distance, float* tmp_out,
+                                   float* max_logits, float* exp_sums, int max_num_partitions,
+                                   int* error_word, cudaStream_t stream);
+
+/*
+ * paged_decode_reduce -- the split-K merge (log-sum-exp identity):
+ *   M = max_j max_logits[b][h][j],  w_j = exp(max_logits_j - M)
+ *   out[b][h][:] = sum_j w_j * tmp_out[b][h][j][:] / sum_j w_j * exp_sums[b][h][j]
+ * over j < ceil(L_b / partition_size).  Sequences with
+ * ceil(L_b / partition_size) <= min_partitions_to_merge are left untouched
+ * (pass 0 to merge every sequence; a sequence with L_b = 0 then gets 0).
+ * Layouts as in paged_decode_partitions; out device fp16.
+ */
+pkd_status paged_decode_reduce(const float* tmp_out, const float* max_logits, const float* exp_sums,
+                               const int32_t* context_lens, void* out, int num_seqs, int num_q_heads,
+                               int head_dim, int partition_size, int max_num_partitions,
+                               int min_partitions_to_merge, cudaStream_t stream);
+
+/*
+ * paged_decode_validate_tables -- debug check: ORs PKD_DEVERR_BAD_BLOCK into
+ * *error_word (device int, required) if any entry
+ * block_tables[b][i], i < ceil(context_lens[b] / block_size), lies outside
+ * [0, num_blocks), or a context length is negative or longer than the row.
+ */
+pkd_status paged_decode_validate_tables(const int32_t* block_tables, const int32_t* context_lens,
+                                        int num_seqs, int max_blocks_per_seq, int block_size,
+                                        int num_blocks, int* error_word, cudaStream_t stream);
+
+/*
+ * pkd_read_device_error -- synchronises `stream`, copies *error_word to
+ * *host_bits, and returns PKD_OK when it is 0, PKD_ERR_DEVICE otherwise.
+ * Clears the word when `clear` is non-zero.
+ */
+pkd_status pkd_read_device_error(int* error_word, unsigned* host_bits, int clear, cudaStream_t stream);
+
+/* Static text for a status code. */
+const char* pkd_status_string(int status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int pkd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_DECODE_H_ */

@@ -1,0 +1,358 @@
+// pkd_api.cu -- the C ABI of libpaged_decode.so (declared in paged_decode.h):
+// argument checks, the split-K policy, workspace layout and launches.
+#include <cmath>
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/paged_decode.h"
+#include "pkd_aux.cuh"
+#include "pkd_launch.cuh"
+
+namespace {
+
+constexpr unsigned long long kWaitBudgetNs = 100ull * 1000ull * 1000ull;  // 100 ms per bounded wait
+constexpr int kDefaultPrefetchDistance = 2;
+constexpr int kMinAutoPartition = 256;
+constexpr int kTargetWaves = 4;      // split until the grid covers this many waves
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct Shape {
+  int num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq,
+      max_context_len;
+};
+
+pkd_status check_shape(const Shape& s) {
+  if (s.num_seqs < 0 || s.num_q_heads <= 0 || s.num_kv_heads <= 0 || s.head_dim <= 0 ||
+      s.block_size <= 0 || s.num_blocks <= 0 || s.max_blocks_per_seq <= 0 || s.max_context_len < 0)
+    return PKD_ERR_SHAPE;
+  if (s.num_q_heads % s.num_kv_heads != 0) return PKD_ERR_SHAPE;
+  const int G = s.num_q_heads / s.num_kv_heads;
+  if (G < 1 || G > 8) return PKD_ERR_UNSUPPORTED;
+  if (s.head_dim != 64 && s.head_dim != 128) return PKD_ERR_UNSUPPORTED;
+  if (s.block_size != 16 && s.block_size != 32) return PKD_ERR_UNSUPPORTED;
+  if ((long long)s.max_context_len > (long long)s.max_blocks_per_seq * s.block_size) return PKD_ERR_SHAPE;
+  return PKD_OK;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+int resolve_variant(int variant) {
+  return variant == PKD_VARIANT_AUTO ? PKD_VARIANT_TMA_STAGED : variant;
+}
+
+// Resident CTAs per SM the kernels of a data path are built for.
+int ctas_per_sm(int variant) { return resolve_variant(variant) == PKD_VARIANT_TMA_STAGED ? 1 : 2; }
+
+// Partition size for a split into about kTargetWaves waves of CTAs, or -1.
+int auto_partition(const Shape& s, int variant = PKD_VARIANT_AUTO) {
+  const long long units = (long long)s.num_seqs * s.num_kv_heads;
+  if (units <= 0 || s.max_context_len <= kMinAutoPartition) return -1;
+  int sms = sm_count();
+  if (sms <= 0) sms = 148;
+  const long long want = (long long)kTargetWaves * sms * ctas_per_sm(variant);
+  if (units >= want) return -1;
+  const long long np = (want + units - 1) / units;
+  long long p = (s.max_context_len + np - 1) / np;
+  p = (long long)round_up((size_t)p, 32);
+  if (p < kMinAutoPartition) p = kMinAutoPartition;
+  if (p >= s.max_context_len) return -1;
+  return (int)p;
+}
+
+struct Workspace {
+  float* tmp_out;
+  float* max_logits;
+  float* exp_sums;
+  size_t bytes;
+};
+
+Workspace layout(void* base, int num_seqs, int num_q_heads, int head_dim, int np) {
+  const size_t rows = (size_t)num_seqs * num_q_heads * np;
+  const size_t a = round_up(rows * head_dim * sizeof(float), 256);
+  const size_t m = round_up(rows * sizeof(float), 256);
+  Workspace w;
+  unsigned char* p = static_cast<unsigned char*>(base);
+  w.tmp_out = reinterpret_cast<float*>(p);
+  w.max_logits = reinterpret_cast<float*>(p ? p + a : nullptr);
+  w.exp_sums = reinterpret_cast<float*>(p ? p + a + m : nullptr);
+  w.bytes = a + 2 * m;
+  return w;
+}
+
+pkd_status launch_decode(int variant, int D, int BS, int G, const pkd::DecodeParams& p,
+                         long long grid, cudaStream_t stream) {
+  if (grid <= 0) return PKD_OK;
+  if (grid > 0x7fffffffLL) return PKD_ERR_SHAPE;
+  cudaError_t e;
+  switch (variant) {
+    case PKD_VARIANT_NO_PREFETCH: e = pkd::launch_decode_no_prefetch(D, BS, G, p, grid, stream); break;
+    case PKD_VARIANT_L2_PREFETCH: e = pkd::launch_decode_l2_prefetch(D, BS, G, p, grid, stream); break;
+    case PKD_VARIANT_TMA_STAGED: e = pkd::launch_decode_tma_staged(D, BS, G, p, grid, stream); break;
+    default: return PKD_ERR_SHAPE;
+  }
+  return e == cudaSuccess ? PKD_OK : PKD_ERR_LAUNCH;
+}
+
+pkd_status launch_reduce(const float* tmp_out, const float* max_logits, const float* exp_sums,
+                         const int32_t* context_lens, void* out, int num_seqs, int num_q_heads,
+                         int head_dim, int partition_size, int max_num_partitions, int min_merge,
+                         cudaStream_t stream) {
+  const long long grid = (long long)num_seqs * num_q_heads;
+  if (grid <= 0) return PKD_OK;
+  if (grid > 0x7fffffffLL) return PKD_ERR_SHAPE;
+  const size_t smem = (size_t)max_num_partitions * sizeof(float);
+  if (smem > 48 * 1024) return PKD_ERR_SHAPE;
+  __half* o = static_cast<__half*>(out);
+  if (head_dim == 128) {
+    pkd::paged_decode_reduce_kernel<128><<<(unsigned)grid, 128, smem, stream>>>(
+        tmp_out, max_logits, exp_sums, context_lens, o, num_q_heads, partition_size,
+        max_num_partitions, min_merge);
+  } else if (head_dim == 64) {
+    pkd::paged_decode_reduce_kernel<64><<<(unsigned)grid, 64, smem, stream>>>(
+        tmp_out, max_logits, exp_sums, context_lens, o, num_q_heads, partition_size,
+        max_num_partitions, min_merge);
+  } else {
+    return PKD_ERR_UNSUPPORTED;
+  }
+  return cudaGetLastError() == cudaSuccess ? PKD_OK : PKD_ERR_LAUNCH;
+}
+
+pkd_status check_inputs(const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* block_tables, const int32_t* context_lens) {
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens) return PKD_ERR_NULL;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(block_tables, 4) ||
+      !aligned(context_lens, 4))
+    return PKD_ERR_ALIGN;
+  return PKD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pkd_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+
+const char* pkd_status_string(int status) {
+  switch (status) {
+    case PKD_OK: return "ok";
+    case PKD_ERR_NULL: return "a required pointer is NULL";
+    case PKD_ERR_SHAPE: return "a size is out of range or inconsistent";
+    case PKD_ERR_UNSUPPORTED: return "head_dim, block_size or group size not supported";
+    case PKD_ERR_ALIGN: return "a pointer is not suitably aligned";
+    case PKD_ERR_WORKSPACE: return "workspace missing or too small";
+    case PKD_ERR_LAUNCH: return "CUDA kernel launch failed";
+    case PKD_ERR_DEVICE: return "the device reported an error";
+    case PKD_ERR_CUDA: return "a CUDA runtime call failed";
+    default: return "unknown status";
+  }
+}
+
+int paged_decode_auto_partition_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                     int block_size, int max_context_len, int variant) {
+  Shape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, 1, 1 << 30, max_context_len};
+  if (check_shape(s) != PKD_OK) return -2;
+  if (variant < PKD_VARIANT_AUTO || variant > PKD_VARIANT_TMA_STAGED) return -2;
+  return auto_partition(s, variant);
+}
+
+size_t paged_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                   int block_size, int max_context_len, int partition_size,
+                                   int variant) {
+  Shape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, 1, 1 << 30, max_context_len};
+  if (check_shape(s) != PKD_OK) return 0;
+  if (variant < PKD_VARIANT_AUTO || variant > PKD_VARIANT_TMA_STAGED) return 0;
+  int P = partition_size == 0 ? auto_partition(s, variant) : partition_size;
+  if (P <= 0 || max_context_len <= P) return 0;
+  const int np = (max_context_len + P - 1) / P;
+  return layout(nullptr, num_seqs, num_q_heads, head_dim, np).bytes;
+}
+
+pkd_status paged_decode_attention_ex(const void* q, const void* k_cache, const void* v_cache,
+                                     const int32_t* block_tables, const int32_t* context_lens,
+                                     void* out, int num_seqs, int num_q_heads, int num_kv_heads,
+                                     int head_dim, int block_size, int num_blocks,
+                                     int max_blocks_per_seq, int max_context_len, float scale,
+                                     int partition_size, int variant, int prefetch_distance,
+                                     void* workspace, size_t workspace_bytes, int* error_word,
+                                     cudaStream_t stream) {
+  Shape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq,
+          max_context_len};
+  pkd_status st = check_shape(s);
+  if (st != PKD_OK) return st;
+  if (num_seqs == 0) return PKD_OK;
+  st = check_inputs(q, k_cache, v_cache, block_tables, context_lens);
+  if (st != PKD_OK) return st;
+  if (!out) return PKD_ERR_NULL;
+  if (!aligned(out, 16) || (error_word && !aligned(error_word, 4))) return PKD_ERR_ALIGN;
+  if (!std::isfinite(scale)) return PKD_ERR_SHAPE;
+  if (variant < PKD_VARIANT_AUTO || variant > PKD_VARIANT_TMA_STAGED) return PKD_ERR_SHAPE;
+  if (prefetch_distance < 0) return PKD_ERR_SHAPE;
+  int P;
+  if (partition_size == 0) {
+    P = auto_partition(s, variant);
+  } else if (partition_size == -1) {
+    P = -1;
+  } else {
+    if (partition_size < 0 || partition_size % 32 != 0 || partition_size % block_size != 0)
+      return PKD_ERR_SHAPE;
+    P = partition_size;
+  }
+  const bool split = P > 0 && max_context_len > P;
+  int np = 1;
+  if (split) np = (max_context_len + P - 1) / P;
+  else P = max_context_len > 0 ? (int)round_up((size_t)max_context_len, 32) : 32;
+
+  pkd::DecodeParams p{};
+  p.q = static_cast<const __half*>(q);
+  p.k_cache = static_cast<const __half*>(k_cache);
+  p.v_cache = static_cast<const __half*>(v_cache);
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.out = static_cast<__half*>(out);
+  p.error_word = error_word;
+  p.num_seqs = num_seqs;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.num_blocks = num_blocks;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.partition_size = P;
+  p.max_partitions = np;
+  p.mode = 0;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.prefetch_distance = prefetch_distance == 0 ? kDefaultPrefetchDistance : prefetch_distance;
+  p.timeout_ns = kWaitBudgetNs;
+  if (split) {
+    if (!workspace) return PKD_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return PKD_ERR_ALIGN;
+    Workspace w = layout(workspace, num_seqs, num_q_heads, head_dim, np);
+    if (workspace_bytes < w.bytes) return PKD_ERR_WORKSPACE;
+    p.tmp_out = w.tmp_out;
+    p.max_logits = w.max_logits;
+    p.exp_sums = w.exp_sums;
+  }
+  const int G = num_q_heads / num_kv_heads;
+  const long long grid = (long long)num_seqs * num_kv_heads * np;
+  st = launch_decode(resolve_variant(variant), head_dim, block_size, G, p, grid, stream);
+  if (st != PKD_OK || !split) return st;
+  return launch_reduce(p.tmp_out, p.max_logits, p.exp_sums, context_lens, out, num_seqs, num_q_heads,
+                       head_dim, P, np, /*min_merge=*/1, stream);
+}
+
+pkd_status paged_decode_attention(const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* block_tables, const int32_t* context_lens, void* out,
+                                  int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                  int block_size, int num_blocks, int max_blocks_per_seq,
+                                  int max_context_len, float scale, cudaStream_t stream) {
+  return paged_decode_attention_ex(q, k_cache, v_cache, block_tables, context_lens, out, num_seqs,
+                                   num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                                   max_blocks_per_seq, max_context_len, scale, /*partition_size=*/-1,
+                                   PKD_VARIANT_AUTO, 0, nullptr, 0, nullptr, stream);
+}
+
+pkd_status paged_decode_partitions(const void* q, const void* k_cache, const void* v_cache,
+                                   const int32_t* block_tables, const int32_t* context_lens,
+                                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                   int block_size, int num_blocks, int max_blocks_per_seq,
+                                   int max_context_len, float scale, int partition_size,
+                                   int variant, int prefetch_distance, float* tmp_out,
+                                   float* max_logits, float* exp_sums, int max_num_partitions,
+                                   int* error_word, cudaStream_t stream) {
+  Shape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq,
+          max_context_len};
+  pkd_status st = check_shape(s);
+  if (st != PKD_OK) return st;
+  if (num_seqs == 0) return PKD_OK;
+  st = check_inputs(q, k_cache, v_cache, block_tables, context_lens);
+  if (st != PKD_OK) return st;
+  if (!tmp_out || !max_logits || !exp_sums) return PKD_ERR_NULL;
+  if (!aligned(tmp_out, 16) || !aligned(max_logits, 4) || !aligned(exp_sums, 4) ||
+      (error_word && !aligned(error_word, 4)))
+    return PKD_ERR_ALIGN;
+  if (!std::isfinite(scale)) return PKD_ERR_SHAPE;
+  if (variant < PKD_VARIANT_AUTO || variant > PKD_VARIANT_TMA_STAGED || prefetch_distance < 0)
+    return PKD_ERR_SHAPE;
+  if (partition_size <= 0 || partition_size % 32 != 0 || partition_size % block_size != 0)
+    return PKD_ERR_SHAPE;
+  const int need = (max_context_len + partition_size - 1) / partition_size;
+  if (max_num_partitions < (need > 0 ? need : 1)) return PKD_ERR_SHAPE;
+  pkd::DecodeParams p{};
+  p.q = static_cast<const __half*>(q);
+  p.k_cache = static_cast<const __half*>(k_cache);
+  p.v_cache = static_cast<const __half*>(v_cache);
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.out = nullptr;
+  p.tmp_out = tmp_out;
+  p.max_logits = max_logits;
+  p.exp_sums = exp_sums;
+  p.error_word = error_word;
+  p.num_seqs = num_seqs;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.num_blocks = num_blocks;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.partition_size = partition_size;
+  p.max_partitions = max_num_partitions;
+  p.mode = 1;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.prefetch_distance = prefetch_distance == 0 ? kDefaultPrefetchDistance : prefetch_distance;
+  p.timeout_ns = kWaitBudgetNs;
+  const int G = num_q_heads / num_kv_heads;
+  const long long grid = (long long)num_seqs * num_kv_heads * max_num_partitions;
+  return launch_decode(resolve_variant(variant), head_dim, block_size, G, p, grid, stream);
+}
+
+pkd_status paged_decode_reduce(const float* tmp_out, const float* max_logits, const float* exp_sums,
+                               const int32_t* context_lens, void* out, int num_seqs, int num_q_heads,
+                               int head_dim, int partition_size, int max_num_partitions,
+                               int min_partitions_to_merge, cudaStream_t stream) {
+  if (num_seqs < 0 || num_q_heads <= 0 || partition_size <= 0 || max_num_partitions <= 0 ||
+      min_partitions_to_merge < 0)
+    return PKD_ERR_SHAPE;
+  if (head_dim != 64 && head_dim != 128) return PKD_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return PKD_OK;
+  if (!tmp_out || !max_logits || !exp_sums || !context_lens || !out) return PKD_ERR_NULL;
+  if (!aligned(tmp_out, 4) || !aligned(max_logits, 4) || !aligned(exp_sums, 4) ||
+      !aligned(context_lens, 4) || !aligned(out, 2))
+    return PKD_ERR_ALIGN;
+  return launch_reduce(tmp_out, max_logits, exp_sums, context_lens, out, num_seqs, num_q_heads, head_dim,
+                       partition_size, max_num_partitions, min_partitions_to_merge, stream);
+}
+
+pkd_status paged_decode_validate_tables(const int32_t* block_tables, const int32_t* context_lens,
+                                        int num_seqs, int max_blocks_per_seq, int block_size,
+                                        int num_blocks, int* error_word, cudaStream_t stream) {
+  if (num_seqs < 0 || max_blocks_per_seq <= 0 || block_size <= 0 || num_blocks <= 0) return PKD_ERR_SHAPE;
+  if (num_seqs == 0) return PKD_OK;
+  if (!block_tables || !context_lens || !error_word) return PKD_ERR_NULL;
+  if (!aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(error_word, 4)) return PKD_ERR_ALIGN;
+  pkd::validate_tables_kernel<<<num_seqs, 128, 0, stream>>>(block_tables, context_lens, num_seqs,
+                                                            max_blocks_per_seq, block_size, num_blocks,
+                                                            error_word);
+  return cudaGetLastError() == cudaSuccess ? PKD_OK : PKD_ERR_LAUNCH;
+}
+
+pkd_status pkd_read_device_error(int* error_word, unsigned* host_bits, int clear, cudaStream_t stream) {
+  if (!error_word || !host_bits) return PKD_ERR_NULL;
+  unsigned v = 0;
+  if (cudaMemcpyAsync(&v, error_word, sizeof(unsigned), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return PKD_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return PKD_ERR_CUDA;
+  *host_bits = v;
+  if (clear) {
+    if (cudaMemsetAsync(error_word, 0, sizeof(int), stream) != cudaSuccess) return PKD_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return PKD_ERR_CUDA;
+  }
+  return v == 0 ? PKD_OK : PKD_ERR_DEVICE;
+}
+
+}  // extern "C"

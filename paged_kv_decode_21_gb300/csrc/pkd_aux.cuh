@@ -1,0 +1,74 @@
+// pkd_aux.cuh -- the split-K merge kernel and the block-table validator.
+#pragma once
+#include <cstdint>
+#include <cuda_fp16.h>
+#include "pkd_decode.cuh"
+
+namespace pkd {
+
+// ---------------------------------------------------------------------------
+// Split-K merge: one CTA of D threads per (b, h).
+template <int D>
+__global__ void __launch_bounds__(D) paged_decode_reduce_kernel(
+    const float* __restrict__ tmp_out, const float* __restrict__ max_logits,
+    const float* __restrict__ exp_sums, const int32_t* __restrict__ context_lens, __half* out,
+    int num_q_heads, int partition_size, int max_partitions, int min_partitions_to_merge) {
+  extern __shared__ float wsm[];  // [max_partitions] weights, then [1] 1/Z
+  const int row = blockIdx.x;     // b * Hq + h
+  const int b = row / num_q_heads;
+  const int L = context_lens[b];
+  const int np = (L + partition_size - 1) / partition_size;
+  if (np <= min_partitions_to_merge) return;
+  const int d = threadIdx.x;
+  if (np <= 0) {
+    out[(size_t)row * D + d] = __float2half_rn(0.f);
+    return;
+  }
+  const float* ml = max_logits + (size_t)row * max_partitions;
+  const float* es = exp_sums + (size_t)row * max_partitions;
+  // global max over partitions (warp 0)
+  __shared__ float s_max, s_invz;
+  if (threadIdx.x < 32) {
+    float M = -INFINITY;
+    for (int jj = threadIdx.x; jj < np; jj += 32) M = fmaxf(M, ml[jj]);
+#pragma unroll
+    for (int msk = 16; msk > 0; msk >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, msk));
+    float Z = 0.f;
+    for (int jj = threadIdx.x; jj < np; jj += 32) {
+      const float w = __expf(ml[jj] - M);
+      wsm[jj] = w;
+      Z = fmaf(w, es[jj], Z);
+    }
+#pragma unroll
+    for (int msk = 16; msk > 0; msk >>= 1) Z += __shfl_xor_sync(0xffffffffu, Z, msk);
+    if (threadIdx.x == 0) {
+      s_max = M;
+      s_invz = 1.f / Z;
+    }
+  }
+  __syncthreads();
+  const float* to = tmp_out + (size_t)row * max_partitions * D + d;
+  float o = 0.f;
+  for (int jj = 0; jj < np; ++jj) o = fmaf(wsm[jj], to[(size_t)jj * D], o);
+  out[(size_t)row * D + d] = __float2half_rn(o * s_invz);
+}
+
+// ---------------------------------------------------------------------------
+__global__ void validate_tables_kernel(const int32_t* block_tables, const int32_t* context_lens,
+                                       int num_seqs, int max_blocks_per_seq, int block_size,
+                                       int num_blocks, int* error_word) {
+  const int b = blockIdx.x;
+  if (b >= num_seqs) return;
+  const int L = context_lens[b];
+  if (L < 0 || L > max_blocks_per_seq * block_size) {
+    if (threadIdx.x == 0) record_error(error_word, kErrBadBlock);
+    return;
+  }
+  const int nb = (L + block_size - 1) / block_size;
+  for (int i = threadIdx.x; i < nb; i += blockDim.x) {
+    const int p = block_tables[(size_t)b * max_blocks_per_seq + i];
+    if (p < 0 || p >= num_blocks) record_error(error_word, kErrBadBlock);
+  }
+}
+
+}  // namespace pkd

@@ -1,0 +1,242 @@
+"""ctypes binding of libpaged_decode.so (argument marshalling only).
+
+Every function here has the name of the C entry point it calls (see
+``include/paged_decode.h``) and takes torch tensors for device buffers; the
+work itself runs in the library's CUDA kernels on the current (or given)
+stream.  There is no fallback: if the library is missing, loading fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpaged_decode.so")
+
+PKD_OK = 0
+STATUS_NAMES = {0: "PKD_OK", 1: "PKD_ERR_NULL", 2: "PKD_ERR_SHAPE", 3: "PKD_ERR_UNSUPPORTED",
+                4: "PKD_ERR_ALIGN", 5: "PKD_ERR_WORKSPACE", 6: "PKD_ERR_LAUNCH",
+                7: "PKD_ERR_DEVICE", 8: "PKD_ERR_CUDA"}
+VARIANTS = {"auto": 0, "no_prefetch": 1, "l2_prefetch": 2, "tma_staged": 3}
+DEVERR_BAD_BLOCK = 1
+DEVERR_TIMEOUT = 2
+
+_lock = threading.Lock()
+_lib = None
+
+
+class PagedDecodeError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        msg = lib().pkd_status_string(status).decode()
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)} ({msg})")
+
+
+def lib():
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m paged_kv_decode_21_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        attn = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, F]
+        L.paged_decode_attention.argtypes = attn + [P]
+        L.paged_decode_attention.restype = I
+        L.paged_decode_attention_ex.argtypes = attn + [I, I, I, P, S, P, P]
+        L.paged_decode_attention_ex.restype = I
+        L.paged_decode_auto_partition_size.argtypes = [I, I, I, I, I, I, I]
+        L.paged_decode_auto_partition_size.restype = I
+        L.paged_decode_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
+        L.paged_decode_workspace_size.restype = S
+        L.paged_decode_partitions.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, I, I,
+                                              P, P, P, I, P, P]
+        L.paged_decode_partitions.restype = I
+        L.paged_decode_reduce.argtypes = [P, P, P, P, P, I, I, I, I, I, I, P]
+        L.paged_decode_reduce.restype = I
+        L.paged_decode_validate_tables.argtypes = [P, P, I, I, I, I, P, P]
+        L.paged_decode_validate_tables.restype = I
+        L.pkd_read_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint), I, P]
+        L.pkd_read_device_error.restype = I
+        L.pkd_status_string.argtypes = [I]
+        L.pkd_status_string.restype = ctypes.c_char_p
+        L.pkd_version.argtypes = []
+        L.pkd_version.restype = I
+        _lib = L
+        return L
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _check(status: int, what: str):
+    if status != PKD_OK:
+        raise PagedDecodeError(status, what)
+
+
+def _want(t: torch.Tensor, name: str, dtype, dim=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dim is not None and t.dim() != dim:
+        raise ValueError(f"{name} must have {dim} dimensions")
+
+
+def _shape(q, k_cache, v_cache, block_tables, context_lens):
+    _want(q, "q", torch.float16, 3)
+    _want(k_cache, "k_cache", torch.float16, 4)
+    _want(v_cache, "v_cache", torch.float16, 4)
+    _want(block_tables, "block_tables", torch.int32, 2)
+    _want(context_lens, "context_lens", torch.int32, 1)
+    B, Hq, D = q.shape
+    NB, Hkv, BS, D2 = k_cache.shape
+    if D2 != D or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("k_cache / v_cache shape mismatch")
+    if block_tables.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("block_tables / context_lens batch mismatch")
+    return B, Hq, Hkv, D, BS, NB, block_tables.shape[1]
+
+
+def _max_len(context_lens, max_context_len):
+    if max_context_len is not None:
+        return int(max_context_len)
+    return int(context_lens.max().item()) if context_lens.numel() else 0
+
+
+def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale, out=None,
+                           max_context_len=None, stream=None) -> torch.Tensor:
+    """Unsplit decode attention (no workspace); returns ``out``."""
+    B, Hq, Hkv, D, BS, NB, MB = _shape(q, k_cache, v_cache, block_tables, context_lens)
+    if out is None:
+        out = torch.empty_like(q)
+    _want(out, "out", torch.float16, 3)
+    st = lib().paged_decode_attention(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                      _ptr(context_lens), _ptr(out), B, Hq, Hkv, D, BS, NB, MB,
+                                      _max_len(context_lens, max_context_len), float(scale),
+                                      _stream(stream))
+    _check(st, "paged_decode_attention")
+    return out
+
+
+def _variant(variant) -> int:
+    return VARIANTS[variant] if isinstance(variant, str) else int(variant)
+
+
+def paged_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                max_context_len, partition_size=0, variant="auto") -> int:
+    return int(lib().paged_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                 block_size, max_context_len, partition_size,
+                                                 _variant(variant)))
+
+
+def paged_decode_auto_partition_size(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                     max_context_len, variant="auto") -> int:
+    return int(lib().paged_decode_auto_partition_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                      block_size, max_context_len, _variant(variant)))
+
+
+def alloc_workspace(nbytes: int, device) -> Optional[torch.Tensor]:
+    """A 256-byte aligned device buffer of at least ``nbytes`` (None for 0)."""
+    if nbytes <= 0:
+        return None
+    buf = torch.empty(nbytes + 256, dtype=torch.uint8, device=device)
+    off = (-buf.data_ptr()) % 256
+    return buf[off:off + nbytes]
+
+
+def paged_decode_attention_ex(q, k_cache, v_cache, block_tables, context_lens, scale, out=None,
+                              max_context_len=None, partition_size=0, variant="auto",
+                              prefetch_distance=0, workspace=None, error_word=None,
+                              stream=None) -> torch.Tensor:
+    """Decode attention with split-K and data-path control; returns ``out``.
+
+    ``workspace`` (uint8 CUDA tensor, 256-byte aligned) is allocated here when
+    None and a split is needed."""
+    B, Hq, Hkv, D, BS, NB, MB = _shape(q, k_cache, v_cache, block_tables, context_lens)
+    if out is None:
+        out = torch.empty_like(q)
+    _want(out, "out", torch.float16, 3)
+    ml = _max_len(context_lens, max_context_len)
+    var = _variant(variant)
+    if workspace is None:
+        need = paged_decode_workspace_size(B, Hq, Hkv, D, BS, ml, partition_size, var)
+        workspace = alloc_workspace(need, q.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().paged_decode_attention_ex(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                         _ptr(context_lens), _ptr(out), B, Hq, Hkv, D, BS, NB, MB,
+                                         ml, float(scale), int(partition_size), var,
+                                         int(prefetch_distance), _ptr(workspace), wbytes,
+                                         _ptr(error_word), _stream(stream))
+    _check(st, "paged_decode_attention_ex")
+    return out
+
+
+def paged_decode_partitions(q, k_cache, v_cache, block_tables, context_lens, scale, partition_size,
+                            tmp_out, max_logits, exp_sums, max_context_len=None, variant="auto",
+                            prefetch_distance=0, error_word=None, stream=None):
+    """First split-K kernel alone: per-partition (max_logits, exp_sums, tmp_out)."""
+    B, Hq, Hkv, D, BS, NB, MB = _shape(q, k_cache, v_cache, block_tables, context_lens)
+    for t, n in ((tmp_out, "tmp_out"), (max_logits, "max_logits"), (exp_sums, "exp_sums")):
+        _want(t, n, torch.float32)
+    npmax = max_logits.shape[-1]
+    var = _variant(variant)
+    st = lib().paged_decode_partitions(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                       _ptr(context_lens), B, Hq, Hkv, D, BS, NB, MB,
+                                       _max_len(context_lens, max_context_len), float(scale),
+                                       int(partition_size), var, int(prefetch_distance),
+                                       _ptr(tmp_out), _ptr(max_logits), _ptr(exp_sums), npmax,
+                                       _ptr(error_word), _stream(stream))
+    _check(st, "paged_decode_partitions")
+
+
+def paged_decode_reduce(tmp_out, max_logits, exp_sums, context_lens, out, partition_size,
+                        min_partitions_to_merge=0, stream=None):
+    """Split-K merge of per-partition statistics into ``out``."""
+    B, Hq, NP, D = tmp_out.shape
+    st = lib().paged_decode_reduce(_ptr(tmp_out), _ptr(max_logits), _ptr(exp_sums),
+                                   _ptr(context_lens), _ptr(out), B, Hq, D, int(partition_size),
+                                   NP, int(min_partitions_to_merge), _stream(stream))
+    _check(st, "paged_decode_reduce")
+    return out
+
+
+def paged_decode_validate_tables(block_tables, context_lens, block_size, num_blocks, error_word,
+                                 stream=None):
+    B, MB = block_tables.shape
+    st = lib().paged_decode_validate_tables(_ptr(block_tables), _ptr(context_lens), B, MB,
+                                            int(block_size), int(num_blocks), _ptr(error_word),
+                                            _stream(stream))
+    _check(st, "paged_decode_validate_tables")
+
+
+def pkd_read_device_error(error_word, clear=True, stream=None) -> int:
+    """Synchronise and return the device error bits (0 = none)."""
+    bits = ctypes.c_uint(0)
+    st = lib().pkd_read_device_error(_ptr(error_word), ctypes.byref(bits), int(bool(clear)),
+                                     _stream(stream))
+    if st not in (PKD_OK, 7):
+        _check(st, "pkd_read_device_error")
+    return int(bits.value)
+
+
+def pkd_version() -> int:
+    return int(lib().pkd_version())

@@ -1,0 +1,37 @@
+"""Shared test helpers: tolerances, comparison against the oracle, input prep."""
+import numpy as np
+import torch
+
+import oracle
+from paged_kv_decode_21_gb300 import workloads
+
+# fp16 output, fp32 accumulation: element-wise bound and mean bound against
+# the fp64 oracle (the library's stated parity contract).
+MAX_ABS_TOL = 4e-3
+MEAN_ABS_TOL = 5e-4
+
+
+def oracle_out(inp: workloads.DecodeInputs, rows=None, threads=None):
+    return oracle.attention(inp.q.cpu(), inp.k_cache.cpu(), inp.v_cache.cpu(), inp.block_tables.cpu(),
+                            inp.context_lens.cpu(), inp.scale, rows=rows, threads=threads)
+
+
+def assert_close(got_fp16: torch.Tensor, ref: np.ndarray, what=""):
+    got = got_fp16.detach().cpu().to(torch.float64).numpy()
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    err = np.abs(got - ref)
+    mx, mean = float(err.max(initial=0.0)), float(err.mean()) if err.size else 0.0
+    assert mx <= MAX_ABS_TOL and mean <= MEAN_ABS_TOL, f"{what}: max|err|={mx:.3e} mean|err|={mean:.3e}"
+    return mx, mean
+
+
+def sample_rows(num_seqs, num_q_heads, n, seed=0):
+    rng = np.random.default_rng(seed)
+    total = num_seqs * num_q_heads
+    n = min(n, total)
+    rows = rng.choice(total, size=n, replace=False).astype(np.int32)
+    # always include the first and last rows
+    rows[0] = 0
+    rows[-1] = total - 1
+    return np.unique(rows)
