@@ -1,0 +1,400 @@
+"""Benchmark: paged single-query decode attention on GB300.
+
+One step = one call of paged_decode_attention_ex (every stage of the hot
+path: block-table gather, Q.K^T, online softmax, P.V, and the split-K merge
+when the shape splits) over one batch of synthetic inputs already resident
+in HBM.  The default workload is the Llama2-7B-shaped MHA decode (batch 64,
+32 q / 32 kv heads, head_dim 128, block_size 16, context 2048).
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle
+instead.  ``--sweep`` prints one line per (workload, variant) to stdout.
+
+Timing: W warm-up calls, then K timed calls, each bracketed by CUDA events
+on the launching stream, with an L2 flush (a 2x-L2 buffer write) between
+calls; the inputs are also larger than L2.  value = algorithmic bytes (K and
+V rows used, Q, out) per call / mean call time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from paged_kv_decode_21_gb300 import traffic, workloads  # noqa: E402
+
+METRIC = "paged decode-attention achieved HBM GB/s (% of GB300 peak); μs per call"
+DEFAULT_CONFIG = "llama2_7b_mha"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["paged_kv_decode_21_gb300/csrc/pkd_decode.cuh", "paged_kv_decode_21_gb300/csrc/pkd_ptx.cuh",
+                  "paged_kv_decode_21_gb300/csrc/pkd_launch.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+
+
+def describe(cfg: workloads.DecodeConfig) -> str:
+    if cfg.context_lens is not None:
+        lens = sorted(set(cfg.context_lens))
+        ltxt = f"context_len={lens[0]}" if len(lens) == 1 else f"context_lens={lens}"
+    else:
+        ltxt = f"context_lens~U[{cfg.len_range[0]},{cfg.len_range[1]}]"
+    ptxt = f", partition={cfg.partition_size}" if cfg.partition_size else ""
+    return (f"{cfg.name}: batch={cfg.num_seqs}, {cfg.num_q_heads} q / {cfg.num_kv_heads} kv heads, "
+            f"head_dim={cfg.head_dim}, block_size={cfg.block_size}, {ltxt}{ptxt}, fp16")
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str, variant: str):
+    """dram bytes per launch from the committed ncu capture, if it matches this kernel."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    ent = rec.get("entries", {}).get(f"{workload}/{variant}")
+    if not ent or ent.get("kernel_hash") != kernel_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed loop runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.samples = []
+        self.proc = None
+        self.idx = device_index
+
+    def __enter__(self):
+        try:
+            bus = torch.cuda.get_device_properties(self.idx).pci_bus_id
+        except Exception:
+            bus = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if bus:
+            cmd += ["-i", str(bus)]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append([x.strip() for x in line.split(",")])
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for s in self.samples:
+            try:
+                sm.append(float(s[0]))
+                mx.append(float(s[1]))
+            except Exception:
+                continue
+            for n, v in zip(names, s[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def time_gpu(args, cfg, variant, dev, inp, steps, warmup, with_e2e=True, with_clocks=True):
+    """Kernel-resident timing (+ optional end-to-end leg) of one workload and variant."""
+    from paged_kv_decode_21_gb300 import ops
+    stream = torch.cuda.current_stream(dev)
+    lens = inp.context_lens.cpu().tolist()
+    algo = traffic.algorithmic_bytes(lens, inp.num_q_heads, inp.num_kv_heads, inp.head_dim)
+    P = args.partition_size if args.partition_size is not None else (cfg.partition_size or 0)
+    var = ops.VARIANTS[variant]
+    need = ops.paged_decode_workspace_size(inp.num_seqs, inp.num_q_heads, inp.num_kv_heads,
+                                           inp.head_dim, inp.block_size, inp.max_context_len, P, var)
+    ws = ops.alloc_workspace(need, dev)
+    eff_P = P if P != 0 else ops.paged_decode_auto_partition_size(
+        inp.num_seqs, inp.num_q_heads, inp.num_kv_heads, inp.head_dim, inp.block_size,
+        inp.max_context_len, var)
+    split = eff_P > 0 and inp.max_context_len > eff_P
+    out = torch.empty_like(inp.q)
+    ew = torch.zeros(1, dtype=torch.int32, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+
+    def call():
+        ops.paged_decode_attention_ex(inp.q, inp.k_cache, inp.v_cache, inp.block_tables,
+                                      inp.context_lens, inp.scale, out=out,
+                                      max_context_len=inp.max_context_len, partition_size=P,
+                                      variant=variant, prefetch_distance=args.prefetch_distance,
+                                      workspace=ws, error_word=ew, stream=stream)
+
+    for _ in range(warmup):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    sampler = ClockSampler(dev.index or 0) if with_clocks else None
+    if sampler:
+        sampler.__enter__()
+    if torch.distributed.is_initialized():
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter()
+    torch.cuda.nvtx.range_push("timed")
+    for i in range(steps):
+        flush.zero_()
+        starts[i].record(stream)
+        call()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    torch.cuda.nvtx.range_pop()
+    t_wall = time.perf_counter() - t_wall
+    if sampler:
+        sampler.__exit__(None, None, None)
+    times_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    errbits = ops.pkd_read_device_error(ew)
+    res = {
+        "algo_bytes": algo, "mean_ms": statistics.mean(times_ms), "median_ms": statistics.median(times_ms),
+        "min_ms": min(times_ms), "wall_s": t_wall, "launches_per_call": 2 if split else 1,
+        "partition_size": eff_P if split else -1, "device_error": errbits,
+        "clocks": sampler.summary() if sampler else None,
+    }
+    if with_e2e:
+        res["e2e"] = time_e2e(call, inp, out, stream, dev, algo, max(3, min(20, steps // 10)))
+    return res
+
+
+def time_e2e(call, inp, out, stream, dev, algo, steps):
+    """Same call with the inputs copied from pinned host memory every step and
+    the result copied back; events bracket copies + call."""
+    names = ["q", "k_cache", "v_cache", "block_tables", "context_lens"]
+    host = {n: getattr(inp, n).cpu().pin_memory() for n in names}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out.numel() * out.element_size()
+    st = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    en = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps + 1):
+        if i > 0:
+            st[i - 1].record(stream)
+        for n in names:
+            getattr(inp, n).copy_(host[n], non_blocking=True)
+        call()
+        out_h.copy_(out, non_blocking=True)
+        if i > 0:
+            en[i - 1].record(stream)
+    torch.cuda.synchronize(dev)
+    ms = statistics.mean(s.elapsed_time(e) for s, e in zip(st, en))
+    return {"value": round(algo / (ms * 1e-3) / 1e9, 2), "unit": "GB/s", "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+def cpu_oracle_rate(inp, target_s=10.0, max_passes=50):
+    """The oracle, as it stands, on the host cores: passes over the whole
+    workload until about target_s seconds; returns (GB/s, cores, sample)."""
+    import oracle
+    cores = os.cpu_count() or 1
+    cpu = inp.to("cpu")
+    lens = cpu.context_lens.tolist()
+    algo = traffic.algorithmic_bytes(lens, cpu.num_q_heads, cpu.num_kv_heads, cpu.head_dim)
+    passes, t = 0, 0.0
+    while passes < max_passes and (t < target_s or passes == 0):
+        t0 = time.perf_counter()
+        oracle.attention(cpu.q, cpu.k_cache, cpu.v_cache, cpu.block_tables, cpu.context_lens, cpu.scale,
+                         threads=cores)
+        t += time.perf_counter() - t0
+        passes += 1
+    sample = f"{passes} full pass(es) over the workload ({algo / 1e9:.3f} GB each), {t:.1f} s"
+    return algo * passes / t / 1e9, cores, sample, t / passes
+
+
+def make_workload(name, dev, batch=None):
+    import dataclasses
+    cfg = workloads.CONFIGS[name]
+    if batch is not None and batch != cfg.num_seqs:
+        lens = None if cfg.context_lens is None else tuple(cfg.context_lens[:1]) * batch
+        cfg = dataclasses.replace(cfg, name=f"{cfg.name}_b{batch}", num_seqs=batch, context_lens=lens)
+    return cfg, workloads.make_inputs(cfg, device=dev)
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    cfg = workloads.CONFIGS[args.config]
+    inp = workloads.make_inputs(cfg, device="cuda" if torch.cuda.is_available() else "cpu")
+    import oracle
+    cores = os.cpu_count() or 1
+    cpu = inp.to("cpu")
+    lens = cpu.context_lens.tolist()
+    algo = traffic.algorithmic_bytes(lens, cpu.num_q_heads, cpu.num_kv_heads, cpu.head_dim)
+    for _ in range(args.warmup):
+        oracle.attention(cpu.q, cpu.k_cache, cpu.v_cache, cpu.block_tables, cpu.context_lens, cpu.scale,
+                         threads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.attention(cpu.q, cpu.k_cache, cpu.v_cache, cpu.block_tables, cpu.context_lens, cpu.scale,
+                         threads=cores)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = algo / dt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": describe(cfg), "impl": "CPU fp64 oracle (plain C, pthreads)"},
+        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"each step is one full pass over the workload ({algo / 1e9:.3f} GB)"},
+        "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=list(workloads.CONFIGS))
+    ap.add_argument("--variant", default="auto", choices=["auto", "no_prefetch", "l2_prefetch", "tma_staged"])
+    ap.add_argument("--partition-size", type=int, default=None)
+    ap.add_argument("--prefetch-distance", type=int, default=0)
+    ap.add_argument("--sweep", action="store_true", help="every workload x variant, one line each")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--batch", type=int, default=None, help="override the workload's batch (profiling runs)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    if args.impl == "reference":
+        return run_reference(args)
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from paged_kv_decode_21_gb300 import build as pkd_build
+    from paged_kv_decode_21_gb300 import ops
+    if rank == 0 or ws == 1:
+        pkd_build.build()
+    if ws > 1:
+        torch.distributed.barrier()
+    ops.lib()
+    peak, peak_kind = hbm_peak()
+
+    if args.sweep:
+        for name in workloads.CONFIG_ORDER[1:]:
+            cfg, inp = make_workload(name, dev)
+            for variant in ["no_prefetch", "l2_prefetch", "tma_staged"]:
+                r = time_gpu(args, cfg, variant, dev, inp, min(args.steps, 200), args.warmup,
+                             with_e2e=False, with_clocks=False)
+                gbs = r["algo_bytes"] / (r["mean_ms"] * 1e-3) / 1e9
+                print(json.dumps({"workload": name, "variant": variant, "us_per_call": round(r["mean_ms"] * 1e3, 2),
+                                  "us_min": round(r["min_ms"] * 1e3, 2), "GB_s": round(gbs, 1),
+                                  "frac_of_peak": round(gbs / peak, 4), "partition_size": r["partition_size"],
+                                  "launches_per_call": r["launches_per_call"],
+                                  "device_error": r["device_error"]}), flush=True)
+            del inp
+            torch.cuda.empty_cache()
+        return 0
+
+    cfg, inp = make_workload(args.config, dev, args.batch)
+    variant = args.variant
+    r = time_gpu(args, cfg, variant, dev, inp, args.steps, args.warmup, with_e2e=not args.no_e2e)
+    # max over ranks of the per-call time
+    mean_ms = r["mean_ms"]
+    if ws > 1:
+        t = torch.tensor([mean_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        mean_ms = float(t.item())
+    value = ws * r["algo_bytes"] / (mean_ms * 1e-3) / 1e9
+    achieved = r["algo_bytes"] / (r["mean_ms"] * 1e-3) / 1e9
+    resolved = "tma_staged" if variant == "auto" else variant
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(mean_ms, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16 in, f32 arithmetic", "data": "synthetic",
+        "config": {"workload": describe(cfg), "variant": resolved,
+                   "partition_size": r["partition_size"],
+                   "us_per_call": round(mean_ms * 1e3, 2), "us_per_call_median": round(r["median_ms"] * 1e3, 2),
+                   "us_per_call_min": round(r["min_ms"] * 1e3, 2),
+                   "algorithmic_bytes_per_call": r["algo_bytes"],
+                   "l2": "inputs larger than L2 and an L2 flush (2x L2 write) before every timed call",
+                   "parallelism": f"replicas x{ws} (no collective)"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                     "traffic": ncu_traffic(cfg.name, resolved),
+                     "kernel": f"paged_decode_kernel<{cfg.head_dim},{cfg.block_size},{cfg.group},{resolved}>"},
+        "gpu_launches": r["launches_per_call"] * args.steps,
+        "clocks": r["clocks"],
+        "e2e": r.get("e2e"),
+        "device_error_bits": r["device_error"],
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        v, cores, sample, _ = cpu_oracle_rate(inp)
+        line["cpu_baseline"] = {"value": round(v, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

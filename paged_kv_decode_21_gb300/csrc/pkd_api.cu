@@ -50,7 +50,10 @@ int resolve_variant(int variant) {
 }
 
 // Resident CTAs per SM the kernels of a data path are built for.
-int ctas_per_sm(int variant) { return resolve_variant(variant) == PKD_VARIANT_TMA_STAGED ? 1 : 2; }
+int ctas_per_sm(int variant) {
+  (void)variant;  // every data path keeps two CTAs of four warps per SM
+  return 2;
+}
 
 // Partition size for a split into about kTargetWaves waves of CTAs, or -1.
 int auto_partition(const Shape& s, int variant = PKD_VARIANT_AUTO) {

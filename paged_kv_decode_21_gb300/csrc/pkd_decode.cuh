@@ -80,18 +80,19 @@ struct DecodeTraits {
   static constexpr int TILE_ELEMS = BS * D; // one (block, head) tile
   static constexpr int TILE_BYTES = TILE_ELEMS * 2;
   static constexpr bool kTma = VARIANT == kTmaStaged;
-  // The staged variant runs one CTA of 8 warps per SM (2 warps per SM
-  // sub-partition, so up to 255 registers a thread); the register-direct
-  // variants run two CTAs of 4 warps.
-  static constexpr int NW = kTma ? 8 : 4;
-  static constexpr int MIN_BLOCKS = kTma ? 1 : 2;
+  // Two resident CTAs of 4 warps per SM (2 warps per SM sub-partition, so up
+  // to 255 registers a thread); two CTAs let one CTA's start-up overlap the
+  // other's tail.
+  static constexpr int NW = 4;
+  static constexpr int MIN_BLOCKS = 2;
   static constexpr int THREADS = NW * 32;
   // Staging unit of the staged variant: one 16-row group of K and of V
-  // (each 16*D contiguous halves).  Every warp owns SW slots of its own.
+  // (each 16*D contiguous halves).  Every warp owns SW slots of its own,
+  // about 96 KiB of slots per CTA.
   static constexpr int SUB_ELEMS = 16 * D;
   static constexpr int SUB_BYTES = SUB_ELEMS * 2;
   static constexpr int SLOT_BYTES = 2 * SUB_BYTES;
-  static constexpr int SW_RAW = (192 * 1024) / (NW * SLOT_BYTES);
+  static constexpr int SW_RAW = (96 * 1024) / (NW * SLOT_BYTES);
   static constexpr int SW = kTma ? (SW_RAW > 8 ? 8 : (SW_RAW < 2 ? 2 : SW_RAW)) : 0;
   static constexpr int RING_BYTES = NW * SW * SLOT_BYTES;
   static constexpr int P_BYTES = NW * 16 * 8 * 4;           // per-warp p rows [16][8]

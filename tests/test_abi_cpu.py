@@ -110,6 +110,6 @@ def test_auto_partition_policy(L):
     assert p > 0 and p % 32 == 0 and p < 32768
     assert L.paged_decode_auto_partition_size(2, 8, 3, 128, 16, 100, 0) == -2
     assert L.paged_decode_auto_partition_size(2, 8, 1, 128, 16, 32768, 7) == -2
-    # the register-direct variants keep two CTAs per SM resident, so split no less
-    p1 = L.paged_decode_auto_partition_size(2, 8, 1, 128, 16, 32768, 1)
-    assert 0 < p1 <= p
+    for variant in (1, 2, 3):
+        p1 = L.paged_decode_auto_partition_size(2, 8, 1, 128, 16, 32768, variant)
+        assert 0 < p1 and p1 % 32 == 0
