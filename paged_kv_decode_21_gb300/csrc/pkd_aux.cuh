@@ -18,7 +18,9 @@ __global__ void __launch_bounds__(D) paged_decode_reduce_kernel(
   const int b = row / num_q_heads;
   const int L = context_lens[b];
   const int np = (L + partition_size - 1) / partition_size;
-  if (np <= min_partitions_to_merge) return;
+  // min_partitions_to_merge > 0: those sequences were written by the
+  // partition kernel itself; 0 merges every sequence (empty ones get zeros)
+  if (min_partitions_to_merge > 0 && np <= min_partitions_to_merge) return;
   const int d = threadIdx.x;
   if (np <= 0) {
     out[(size_t)row * D + d] = __float2half_rn(0.f);

@@ -230,6 +230,29 @@ def test_partitions_match_oracle(variant):
     assert_close(out, oracle_out(inp), "reduce of oracle partials")
 
 
+def test_reduce_merges_every_sequence_when_min_is_zero():
+    # empty and single-partition sequences included: merged from partials alone
+    lens = [0, 40, 300, 0, 1]
+    P = 64
+    inp = workloads.make_custom(len(lens), 8, 2, 128, 16, lens, seed=31, device="cuda")
+    NP = -(-max(lens) // P)
+    tmp = torch.zeros(len(lens), 8, NP, 128, dtype=torch.float32, device="cuda")
+    ml = torch.zeros(len(lens), 8, NP, dtype=torch.float32, device="cuda")
+    es = torch.zeros(len(lens), 8, NP, dtype=torch.float32, device="cuda")
+    ops.paged_decode_partitions(inp.q, inp.k_cache, inp.v_cache, inp.block_tables, inp.context_lens,
+                                inp.scale, P, tmp, ml, es, max_context_len=max(lens))
+    out = torch.full_like(inp.q, float("nan"))
+    ops.paged_decode_reduce(tmp, ml, es, inp.context_lens, out, P, min_partitions_to_merge=0)
+    assert torch.all(out[0] == 0) and torch.all(out[3] == 0)
+    assert_close(out, oracle_out(inp), "partitions + reduce(min=0)")
+    # min = 1 leaves sequences with at most one partition untouched
+    out1 = torch.full_like(inp.q, 7.0)
+    ops.paged_decode_reduce(tmp, ml, es, inp.context_lens, out1, P, min_partitions_to_merge=1)
+    for b in (0, 1, 3, 4):
+        assert torch.all(out1[b] == 7.0)
+    assert torch.equal(out1[2], out[2])
+
+
 # --------------------------------------------------------------------------- device errors
 @pytest.mark.parametrize("variant", VARIANTS)
 def test_bad_block_id_sets_error_word(variant):
