@@ -204,6 +204,38 @@ pkd_status paged_decode_validate_tables(const int32_t* block_tables, const int32
  */
 pkd_status pkd_read_device_error(int* error_word, unsigned* host_bits, int clear, cudaStream_t stream);
 
+/*
+ * paged_decode_attention_static_scratch -- the split-K path of
+ * paged_decode_attention_ex for callers that cannot allocate device memory
+ * (code running under another framework's allocator, plugins that only
+ * receive input and output pointers, processes that reserved the whole pool
+ * ahead of time).  The pages have no counterpart: this is a property of the
+ * library interface, not of the method.
+ *
+ * The caller passes inputs and the output exactly as for
+ * paged_decode_attention_ex (same meanings; partition_size 0 = automatic,
+ * otherwise a positive multiple of 32 and of block_size).  The per-partition
+ * partials live in a library-owned device array of PKD_STATIC_SCRATCH_BYTES
+ * bytes that every GPU which loads the library holds until the process
+ * exits; no memory is allocated and no allocating routine is called.
+ *   - A shape whose partials need more than PKD_STATIC_SCRATCH_BYTES
+ *     (B * Hq * NP * (head_dim + 2) * 4 bytes plus alignment) is rejected
+ *     with PKD_ERR_WORKSPACE before anything is launched.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call shares the one array, and each call leaves its partials in
+ *     it; nothing in it needs to start at zero.  Calls that overlap on the
+ *     GPU (other streams, other host threads) race on the array: serialise
+ *     them.
+ */
+#define PKD_STATIC_SCRATCH_BYTES (64u << 20)
+pkd_status paged_decode_attention_static_scratch(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    const int32_t* context_lens, void* out, int num_seqs, int num_q_heads, int num_kv_heads,
+    int head_dim, int block_size, int num_blocks, int max_blocks_per_seq, int max_context_len,
+    float scale, int partition_size, int variant, int prefetch_distance, int* error_word,
+    cudaStream_t stream);
+
 /* Static text for a status code. */
 const char* pkd_status_string(int status);
 

@@ -65,6 +65,8 @@ def lib():
         L.paged_decode_validate_tables.restype = I
         L.pkd_read_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint), I, P]
         L.pkd_read_device_error.restype = I
+        L.paged_decode_attention_static_scratch.argtypes = attn + [I, I, I, P, P]
+        L.paged_decode_attention_static_scratch.restype = I
         L.pkd_status_string.argtypes = [I]
         L.pkd_status_string.restype = ctypes.c_char_p
         L.pkd_version.argtypes = []
@@ -240,3 +242,24 @@ def pkd_read_device_error(error_word, clear=True, stream=None) -> int:
 
 def pkd_version() -> int:
     return int(lib().pkd_version())
+
+
+def paged_decode_attention_static_scratch(q, k_cache, v_cache, block_tables, context_lens, scale,
+                                          out=None, max_context_len=None, partition_size=0,
+                                          variant="auto", prefetch_distance=0, error_word=None,
+                                          stream=None) -> torch.Tensor:
+    """Split-K decode attention whose partials live in the library's own
+    fixed device array, for callers that cannot allocate device memory; the
+    caller still provides the inputs and ``out``.  Calls must not overlap on
+    the GPU (they share the array)."""
+    B, Hq, Hkv, D, BS, NB, MB = _shape(q, k_cache, v_cache, block_tables, context_lens)
+    if out is None:
+        out = torch.empty_like(q)
+    _want(out, "out", torch.float16, 3)
+    st = lib().paged_decode_attention_static_scratch(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens), _ptr(out),
+        B, Hq, Hkv, D, BS, NB, MB, _max_len(context_lens, max_context_len), float(scale),
+        int(partition_size), _variant(variant), int(prefetch_distance), _ptr(error_word),
+        _stream(stream))
+    _check(st, "paged_decode_attention_static_scratch")
+    return out
