@@ -150,6 +150,17 @@ def dist_env():
     return ws, rank, local
 
 
+def aggregate_over_ranks(mean_ms: float, algo_bytes: int, world_size: int, device=None):
+    """Whole-job value of N replicas: each rank ran the same workload; the
+    job's per-call time is the max over ranks, and the job moved N x the
+    bytes.  Returns (max per-call ms, aggregate GB/s)."""
+    if world_size > 1:
+        t = torch.tensor([mean_ms], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        mean_ms = float(t.item())
+    return mean_ms, world_size * algo_bytes / (mean_ms * 1e-3) / 1e9
+
+
 def time_gpu(args, cfg, variant, dev, inp, steps, warmup, with_e2e=True, with_clocks=True):
     """Kernel-resident timing (+ optional end-to-end leg) of one workload and variant."""
     from paged_kv_decode_21_gb300 import ops
@@ -355,13 +366,7 @@ def main():
     cfg, inp = make_workload(args.config, dev, args.batch)
     variant = args.variant
     r = time_gpu(args, cfg, variant, dev, inp, args.steps, args.warmup, with_e2e=not args.no_e2e)
-    # max over ranks of the per-call time
-    mean_ms = r["mean_ms"]
-    if ws > 1:
-        t = torch.tensor([mean_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        mean_ms = float(t.item())
-    value = ws * r["algo_bytes"] / (mean_ms * 1e-3) / 1e9
+    mean_ms, value = aggregate_over_ranks(r["mean_ms"], r["algo_bytes"], ws, dev)
     achieved = r["algo_bytes"] / (r["mean_ms"] * 1e-3) / 1e9
     resolved = "tma_staged" if variant == "auto" else variant
     line = {
