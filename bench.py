@@ -323,6 +323,9 @@ def main():
     ap.add_argument("--partition-size", type=int, default=None)
     ap.add_argument("--prefetch-distance", type=int, default=0)
     ap.add_argument("--sweep", action="store_true", help="every workload x variant, one line each")
+    ap.add_argument("--sweep-configs", default=",".join(workloads.CONFIG_ORDER[1:]))
+    ap.add_argument("--sweep-variants", default="no_prefetch,l2_prefetch,tma_staged")
+    ap.add_argument("--sweep-partitions", default="", help="comma list of partition sizes (default: the config's)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch (profiling runs)")
@@ -348,17 +351,22 @@ def main():
     peak, peak_kind = hbm_peak()
 
     if args.sweep:
-        for name in workloads.CONFIG_ORDER[1:]:
-            cfg, inp = make_workload(name, dev)
-            for variant in ["no_prefetch", "l2_prefetch", "tma_staged"]:
-                r = time_gpu(args, cfg, variant, dev, inp, min(args.steps, 200), args.warmup,
-                             with_e2e=False, with_clocks=False)
-                gbs = r["algo_bytes"] / (r["mean_ms"] * 1e-3) / 1e9
-                print(json.dumps({"workload": name, "variant": variant, "us_per_call": round(r["mean_ms"] * 1e3, 2),
-                                  "us_min": round(r["min_ms"] * 1e3, 2), "GB_s": round(gbs, 1),
-                                  "frac_of_peak": round(gbs / peak, 4), "partition_size": r["partition_size"],
-                                  "launches_per_call": r["launches_per_call"],
-                                  "device_error": r["device_error"]}), flush=True)
+        parts = [int(x) for x in args.sweep_partitions.split(",") if x.strip()] or [None]
+        for name in args.sweep_configs.split(","):
+            cfg, inp = make_workload(name, dev, args.batch)
+            for variant in args.sweep_variants.split(","):
+                for part in parts:
+                    args.partition_size = part
+                    r = time_gpu(args, cfg, variant, dev, inp, min(args.steps, 200), args.warmup,
+                                 with_e2e=False, with_clocks=False)
+                    gbs = r["algo_bytes"] / (r["mean_ms"] * 1e-3) / 1e9
+                    print(json.dumps({"workload": name, "variant": variant,
+                                      "us_per_call": round(r["mean_ms"] * 1e3, 2),
+                                      "us_min": round(r["min_ms"] * 1e3, 2), "GB_s": round(gbs, 1),
+                                      "frac_of_peak": round(gbs / peak, 4),
+                                      "partition_size": r["partition_size"],
+                                      "launches_per_call": r["launches_per_call"],
+                                      "device_error": r["device_error"]}), flush=True)
             del inp
             torch.cuda.empty_cache()
         return 0

@@ -13,8 +13,9 @@ namespace {
 
 constexpr unsigned long long kWaitBudgetNs = 100ull * 1000ull * 1000ull;  // 100 ms per bounded wait
 constexpr int kDefaultPrefetchDistance = 2;
-constexpr int kMinAutoPartition = 256;
-constexpr int kTargetWaves = 4;      // split until the grid covers this many waves
+constexpr int kMinAutoPartition = 512;
+constexpr int kMaxAutoPartition = 2048;
+constexpr int kTargetWaves = 6;      // split when the grid would cover fewer waves than this
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -49,24 +50,30 @@ int resolve_variant(int variant) {
   return variant == PKD_VARIANT_AUTO ? PKD_VARIANT_TMA_STAGED : variant;
 }
 
-// Resident CTAs per SM the kernels of a data path are built for.
-int ctas_per_sm(int variant) {
-  (void)variant;  // every data path keeps two CTAs of four warps per SM
-  return 2;
+// Resident CTAs per SM the kernel of a data path and group size is built for
+// (mirrors DecodeTraits::MIN_BLOCKS).
+int ctas_per_sm(int variant, int group) {
+  return (resolve_variant(variant) == PKD_VARIANT_TMA_STAGED && group >= 2 && group <= 5) ? 3 : 2;
 }
 
-// Partition size for a split into about kTargetWaves waves of CTAs, or -1.
+// Partition size for the automatic split, or -1 for none.  A shape is split
+// only when its (sequence, kv head) units would give the GPU fewer than
+// kTargetWaves waves of resident CTAs; the partition is then the largest
+// power of two (at most kMaxAutoPartition, at least kMinAutoPartition tokens)
+// that yields enough CTAs.  Powers of two keep partition boundaries aligned
+// with the blocks of every sequence.
 int auto_partition(const Shape& s, int variant = PKD_VARIANT_AUTO) {
   const long long units = (long long)s.num_seqs * s.num_kv_heads;
   if (units <= 0 || s.max_context_len <= kMinAutoPartition) return -1;
   int sms = sm_count();
   if (sms <= 0) sms = 148;
-  const long long want = (long long)kTargetWaves * sms * ctas_per_sm(variant);
+  const long long want =
+      (long long)kTargetWaves * sms * ctas_per_sm(variant, s.num_q_heads / s.num_kv_heads);
   if (units >= want) return -1;
   const long long np = (want + units - 1) / units;
-  long long p = (s.max_context_len + np - 1) / np;
-  p = (long long)round_up((size_t)p, 32);
-  if (p < kMinAutoPartition) p = kMinAutoPartition;
+  const long long per = (s.max_context_len + np - 1) / np;
+  long long p = kMinAutoPartition;
+  while (p * 2 <= per && p * 2 <= kMaxAutoPartition) p *= 2;
   if (p >= s.max_context_len) return -1;
   return (int)p;
 }

@@ -80,22 +80,23 @@ struct DecodeTraits {
   static constexpr int TILE_ELEMS = BS * D; // one (block, head) tile
   static constexpr int TILE_BYTES = TILE_ELEMS * 2;
   static constexpr bool kTma = VARIANT == kTmaStaged;
-  // Two resident CTAs of 4 warps per SM (2 warps per SM sub-partition, so up
-  // to 255 registers a thread); two CTAs let one CTA's start-up overlap the
-  // other's tail.
+  // CTAs of 4 warps.  Resident CTAs per SM: 2 (up to 255 registers a
+  // thread, 2 warps per SM sub-partition), or 3 for the staged variant at
+  // group sizes 2..5, whose state fits in 168 registers; more warps hide more
+  // latency, and several CTAs let one CTA's start-up overlap another's tail.
   static constexpr int NW = 4;
-  static constexpr int MIN_BLOCKS = 2;
+  static constexpr int MIN_BLOCKS = (kTma && G >= 2 && G <= 5) ? 3 : 2;
   static constexpr int THREADS = NW * 32;
   // Staging unit of the staged variant: one 16-row group of K and of V
-  // (each 16*D contiguous halves).  Every warp owns SW slots of its own,
-  // about 96 KiB of slots per CTA.
+  // (each 16*D contiguous halves).  Every warp owns SW slots of its own:
+  // about 96 KiB of slots per CTA at 2 CTAs per SM, 64 KiB at 3.
   static constexpr int SUB_ELEMS = 16 * D;
   static constexpr int SUB_BYTES = SUB_ELEMS * 2;
   static constexpr int SLOT_BYTES = 2 * SUB_BYTES;
-  static constexpr int SW_RAW = (96 * 1024) / (NW * SLOT_BYTES);
+  static constexpr int SW_RAW = ((MIN_BLOCKS == 3 ? 64 : 96) * 1024) / (NW * SLOT_BYTES);
   static constexpr int SW = kTma ? (SW_RAW > 8 ? 8 : (SW_RAW < 2 ? 2 : SW_RAW)) : 0;
   static constexpr int RING_BYTES = NW * SW * SLOT_BYTES;
-  static constexpr int P_BYTES = NW * 16 * 8 * 4;           // per-warp p rows [16][8]
+  static constexpr int P_BYTES = NW * 16 * 8 * 8;           // per-warp p rows [16][8] as (p, p)
   static constexpr int MERGE_BYTES = NW * G * (D + 2) * 4;  // per-warp m, l, acc
   static constexpr int BAR_BYTES = NW * SW * 8;
   // layout: [ring / merge area][p rows][barriers]; the merge reuses the ring
@@ -121,6 +122,15 @@ __device__ __forceinline__ uint4 lds128(const void* p) {
   return *reinterpret_cast<const uint4*>(p);
 }
 
+// 2^x by the SFU approximation (ex2.approx, relative error about 2^-22;
+// ex2(-inf) = +0); subnormal results flush to zero, which only drops weights
+// below 2^-126 of the running maximum.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ float2 h2f2(uint32_t u) {
   return __half22float2(*reinterpret_cast<const __half2*>(&u));
 }
@@ -132,16 +142,18 @@ struct WarpDecoder {
   using T = DecodeTraits<D, BS, G, VARIANT>;
   static constexpr int LPR = T::LPR, RPW = T::RPW, TPL = T::TPL;
 
-  float2 q2[G][4];  // q[h][8*ds + 2c .. +2) for c < 4
-  float acc[G][8];  // sum_t p_t v_t[8*ds + c] over this lane's rows
-  float m[G];       // running max (log2 domain), warp-uniform
-  float l[G];       // running sum of p over this lane's score slots
+  float2 q2[G][4];   // q[h][8*ds + 2c .. +2) for c < 4
+  float2 acc[G][4];  // sum_t p_t v_t[8*ds + 2c .. +2) over this lane's rows
+  float m[G];        // running max (log2 domain), warp-uniform
+  float l[G];        // running sum of p over this lane's score slots
   int lane, rh, ds;
+  int perm;          // this lane's row order: local row i is row i ^ perm of its half
 
   __device__ __forceinline__ void init(const __half* qrow0, int lane_) {
     lane = lane_;
     rh = lane / LPR;
     ds = lane % LPR;
+    perm = (ds >> 1) & (TPL - 1);
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       uint4 u = *reinterpret_cast<const uint4*>(qrow0 + (size_t)h * D + ds * 8);
@@ -152,13 +164,21 @@ struct WarpDecoder {
       m[h] = -INFINITY;
       l[h] = 0.f;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) acc[h][c] = 0.f;
+      for (int c = 0; c < 4; ++c) acc[h][c] = make_float2(0.f, 0.f);
     }
   }
 
-  // Scores of one 16-row group.  krow(i) gives the 16 bytes of row
-  // RPW*i + rh at slice ds.  Returns, in s2[h], the log2-domain score of row
-  // RPW*((ds>>1)&(TPL-1)) + rh (duplicated in lanes ds, ds^1).
+  // Row (within a 16-row group) that this lane reads at local index i.
+  __device__ __forceinline__ int k_row(int i) const { return RPW * (i ^ perm) + rh; }
+
+  // Scores of one 16-row group.  krow(i) gives the 16 bytes of row k_row(i)
+  // at slice ds.  Returns, in s2[h], the log2-domain score of row
+  // my_score_row() (duplicated in lanes ds, ds^1).
+  //
+  // The transpose-reduce: at each level the partner lane (lane ^ mask) has
+  // the opposite bit of `perm`, so its local index j + n/2 holds the same row
+  // as our local index j; every lane keeps part[j] and sends part[j + n/2],
+  // with no lane-dependent selects.
   template <typename KRow>
   __device__ __forceinline__ void scores(KRow krow, float scale_log2, float (&s2)[G]) {
     float part[TPL][G];
@@ -180,15 +200,11 @@ struct WarpDecoder {
     for (int lvl = 0; (TPL >> lvl) > 1; ++lvl) {
       const int n = TPL >> lvl;
       const int mask = (LPR / 2) >> lvl;
-      const bool hi = (lane & mask) != 0;
 #pragma unroll
       for (int j = 0; j < n / 2; ++j) {
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          float send = hi ? part[j][h] : part[j + n / 2][h];
-          float keep = hi ? part[j + n / 2][h] : part[j][h];
-          part[j][h] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
-        }
+        for (int h = 0; h < G; ++h)
+          part[j][h] += __shfl_xor_sync(0xffffffffu, part[j + n / 2][h], mask);
       }
     }
 #pragma unroll
@@ -198,10 +214,10 @@ struct WarpDecoder {
     }
   }
 
-  __device__ __forceinline__ int my_score_row() const { return RPW * ((ds >> 1) & (TPL - 1)) + rh; }
+  __device__ __forceinline__ int my_score_row() const { return RPW * perm + rh; }
 
   // Online-softmax update with scores s2 (masked rows already -inf); writes
-  // p into prow (16 x 8 floats) and leaves it visible to the warp.
+  // p into prow as (p, p) pairs, [16 rows][8 heads][2], visible to the warp.
   __device__ __forceinline__ void softmax_update(float (&s2)[G], float* prow) {
     bool need = false;
 #pragma unroll
@@ -213,10 +229,11 @@ struct WarpDecoder {
 #pragma unroll
         for (int msk = 2; msk < 32; msk <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, msk));
         const float mn = fmaxf(m[h], mx);
-        const float alpha = (mn == -INFINITY) ? 1.f : exp2f(m[h] - mn);  // m = -inf -> 0
+        const float alpha = (mn == -INFINITY) ? 1.f : ex2_approx(m[h] - mn);  // m = -inf -> 0
         l[h] *= alpha;
+        const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) acc[h][c] *= alpha;
+        for (int c = 0; c < 4; ++c) acc[h][c] = fmul2(acc[h][c], a2);
         m[h] = mn;
       }
     }
@@ -225,13 +242,13 @@ struct WarpDecoder {
     for (int h = 0; h < 8; ++h) p[h] = 0.f;
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      p[h] = exp2f(s2[h] - m[h]);
+      p[h] = ex2_approx(s2[h] - m[h]);
       l[h] += p[h];
     }
     if ((ds & 1) == 0) {
-      float4* dst = reinterpret_cast<float4*>(prow + my_score_row() * 8);
-      dst[0] = make_float4(p[0], p[1], p[2], p[3]);
-      dst[1] = make_float4(p[4], p[5], p[6], p[7]);
+      float4* dst = reinterpret_cast<float4*>(prow + my_score_row() * 16);
+#pragma unroll
+      for (int h2 = 0; h2 < (G + 1) / 2; ++h2) dst[h2] = make_float4(p[2 * h2], p[2 * h2], p[2 * h2 + 1], p[2 * h2 + 1]);
     }
     __syncwarp();
   }
@@ -245,15 +262,18 @@ struct WarpDecoder {
       const int r = RPW * i + rh;
       if (valid >= 16 || r < valid) {
         uint4 u = vrow(i);
-        float2 v0 = h2f2(u.x), v1 = h2f2(u.y), v2 = h2f2(u.z), v3 = h2f2(u.w);
-        const float4 pa = *reinterpret_cast<const float4*>(prow + r * 8);
-        const float4 pb = *reinterpret_cast<const float4*>(prow + r * 8 + 4);
-        const float pv[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
-        const float vv[8] = {v0.x, v0.y, v1.x, v1.y, v2.x, v2.y, v3.x, v3.y};
+        const float2 vv[4] = {h2f2(u.x), h2f2(u.y), h2f2(u.z), h2f2(u.w)};
+        float2 pv[2 * ((G + 1) / 2)];
+#pragma unroll
+        for (int h2 = 0; h2 < (G + 1) / 2; ++h2) {
+          const float4 pp = *reinterpret_cast<const float4*>(prow + r * 16 + 4 * h2);
+          pv[2 * h2] = make_float2(pp.x, pp.y);
+          pv[2 * h2 + 1] = make_float2(pp.z, pp.w);
+        }
 #pragma unroll
         for (int h = 0; h < G; ++h) {
 #pragma unroll
-          for (int c = 0; c < 8; ++c) acc[h][c] = fmaf(pv[h], vv[c], acc[h][c]);
+          for (int c = 0; c < 4; ++c) acc[h][c] = ffma2(pv[h], vv[c], acc[h][c]);
         }
       }
     }
@@ -268,10 +288,13 @@ struct WarpDecoder {
 #pragma unroll
       for (int msk = 1; msk < 32; msk <<= 1) lv += __shfl_xor_sync(0xffffffffu, lv, msk);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        float a = acc[h][c];
+      for (int c = 0; c < 4; ++c) {
+        float2 a = acc[h][c];
 #pragma unroll
-        for (int msk = LPR; msk < 32; msk <<= 1) a += __shfl_xor_sync(0xffffffffu, a, msk);
+        for (int msk = LPR; msk < 32; msk <<= 1) {
+          a.x += __shfl_xor_sync(0xffffffffu, a.x, msk);
+          a.y += __shfl_xor_sync(0xffffffffu, a.y, msk);
+        }
         acc[h][c] = a;
       }
       if (lane == 0) {
@@ -280,8 +303,8 @@ struct WarpDecoder {
       }
       if (rh == 0) {
         float4* dst = reinterpret_cast<float4*>(mrg_acc + h * D + ds * 8);
-        dst[0] = make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
-        dst[1] = make_float4(acc[h][4], acc[h][5], acc[h][6], acc[h][7]);
+        dst[0] = make_float4(acc[h][0].x, acc[h][0].y, acc[h][1].x, acc[h][1].y);
+        dst[1] = make_float4(acc[h][2].x, acc[h][2].y, acc[h][3].x, acc[h][3].y);
       }
     }
   }
@@ -352,8 +375,9 @@ __global__ void __launch_bounds__(DecodeTraits<D, BS, G, VARIANT>::THREADS,
 
   WarpDecoder<D, BS, G, VARIANT> wd;
   wd.init(P.q + ((size_t)b * P.num_q_heads + h0) * D, lane);
-  float* prow = p_rows + warp * (16 * 8);
-  const int row_off = wd.rh * D + wd.ds * 8;  // element offset of (row rh, slice ds)
+  float* prow = p_rows + warp * (16 * 16);
+  const int col_off = wd.ds * 8;              // element offset of slice ds in a row
+  const int row_off = wd.rh * D + col_off;    // ... and of (row rh, slice ds)
 
   if constexpr (T::kTma) {
     // -------------------------------------------------------- staged path
@@ -364,42 +388,52 @@ __global__ void __launch_bounds__(DecodeTraits<D, BS, G, VARIANT>::THREADS,
       fence_mbarrier_init();
     }
     __syncwarp();
-    // lane 0 issues the bulk copies of one row group into `slot`
-    auto issue = [&](const SubCursor<BS, NW>& c, int slot) {
-      const int pb = bt[c.k];
-      if (pb < 0 || pb >= P.num_blocks) {
-        record_error(P.error_word, kErrBadBlock);
-        mbar_arrive(&full[slot]);
-      } else {
-        unsigned char* dst = ring + (size_t)slot * T::SLOT_BYTES;
-        const size_t off = (size_t)pb * block_stride + (size_t)c.rg * T::SUB_ELEMS;
-        mbar_arrive_expect_tx(&full[slot], 2 * T::SUB_BYTES);
-        bulk_copy_g2s(dst, kbase + off, T::SUB_BYTES, &full[slot]);
-        bulk_copy_g2s(dst + T::SUB_BYTES, vbase + off, T::SUB_BYTES, &full[slot]);
-      }
-      if (c.rg == 0 && pd > 0) {
-        const int kp = c.k + NW * pd;
-        if (kp < nblk) {
-          const int pp = bt[kp];
-          if (pp >= 0 && pp < P.num_blocks) {
-            prefetch_l2_bulk(kbase + (size_t)pp * block_stride, T::TILE_BYTES);
-            prefetch_l2_bulk(vbase + (size_t)pp * block_stride, T::TILE_BYTES);
-          }
-        }
-      }
-    };
+    // Block ids are read one step ahead into registers (every lane holds the
+    // same values), so no global load sits on the critical path of the
+    // lane-0 branch that issues copies:
+    //   ic_pb  the block of the next row group to copy (issue cursor ic)
+    //   pf_pb  the block `pd` of this warp's iterations beyond it, for L2
     SubCursor<BS, NW> ic, cc;
     ic.start(warp);
     cc.start(warp);
-    for (int s = 0; s < T::SW && ic.live(nblk); ++s) {
-      if (lane == 0) issue(ic, s);
-      ic.advance(t0, t1);  // every lane keeps the same cursor
-    }
+    auto block_id = [&](int k) { return k < nblk ? bt[k] : -1; };
+    int ic_pb = block_id(ic.k);
+    int pf_k = warp + NW * pd;
+    int pf_pb = pd > 0 ? block_id(pf_k) : -1;
+    uint32_t bad_slots = 0;  // bit s: the row group in slot s has an invalid block id
+    // issue the row group at ic into `slot`; then advance ic (all lanes)
+    auto issue_next = [&](int slot) {
+      const bool bad = ic_pb < 0 || ic_pb >= P.num_blocks;
+      bad_slots = bad ? (bad_slots | (1u << slot)) : (bad_slots & ~(1u << slot));
+      if (lane == 0) {
+        if (bad) {
+          record_error(P.error_word, kErrBadBlock);
+          mbar_arrive(&full[slot]);
+        } else {
+          unsigned char* dst = ring + (size_t)slot * T::SLOT_BYTES;
+          const size_t off = (size_t)ic_pb * block_stride + (size_t)ic.rg * T::SUB_ELEMS;
+          mbar_arrive_expect_tx(&full[slot], 2 * T::SUB_BYTES);
+          bulk_copy_g2s(dst, kbase + off, T::SUB_BYTES, &full[slot]);
+          bulk_copy_g2s(dst + T::SUB_BYTES, vbase + off, T::SUB_BYTES, &full[slot]);
+        }
+      }
+      if (ic.rg == 0 && pd > 0) {
+        if (lane == 0 && pf_pb >= 0 && pf_pb < P.num_blocks) {
+          prefetch_l2_bulk(kbase + (size_t)pf_pb * block_stride, T::TILE_BYTES);
+          prefetch_l2_bulk(vbase + (size_t)pf_pb * block_stride, T::TILE_BYTES);
+        }
+        pf_k += NW;
+        pf_pb = block_id(pf_k);
+      }
+      const int k_before = ic.k;
+      ic.advance(t0, t1);
+      if (ic.k != k_before) ic_pb = block_id(ic.k);
+    };
+    for (int s = 0; s < T::SW && ic.live(nblk); ++s) issue_next(s);
     bool abort = false;
     for (int u = 0; cc.live(nblk) && !abort; ++u) {
       const int slot = u % T::SW;
-      const int pb = bt[cc.k];
-      const bool bad = pb < 0 || pb >= P.num_blocks;
+      const bool bad = (bad_slots >> slot) & 1u;
       const bool ok = mbar_wait_bounded(&full[slot], (u / T::SW) & 1, P.timeout_ns);
       if (!ok) {
         if (lane == 0) record_error(P.error_word, kErrTimeout);
@@ -408,10 +442,10 @@ __global__ void __launch_bounds__(DecodeTraits<D, BS, G, VARIANT>::THREADS,
       }
       if (!bad) {
         const int valid = min(16, t1 - (t0 + cc.k * BS + cc.rg * 16));
-        const __half* kg = reinterpret_cast<const __half*>(ring + (size_t)slot * T::SLOT_BYTES) + row_off;
-        const __half* vg = kg + T::SUB_ELEMS;
+        const __half* kg = reinterpret_cast<const __half*>(ring + (size_t)slot * T::SLOT_BYTES) + col_off;
+        const __half* vg = kg + T::SUB_ELEMS + wd.rh * D;
         float s2[G];
-        wd.scores([&](int i) { return lds128(kg + i * RPW * D); }, P.scale_log2, s2);
+        wd.scores([&](int i) { return lds128(kg + wd.k_row(i) * D); }, P.scale_log2, s2);
         if (wd.my_score_row() >= valid) {
 #pragma unroll
           for (int h = 0; h < G; ++h) s2[h] = -INFINITY;
@@ -421,37 +455,34 @@ __global__ void __launch_bounds__(DecodeTraits<D, BS, G, VARIANT>::THREADS,
       }
       __syncwarp();
       if (ic.live(nblk)) {
-        if (lane == 0) {
-          fence_proxy_async_smem();  // our generic reads of the slot precede the next copy into it
-          issue(ic, slot);
-        }
-        ic.advance(t0, t1);
+        if (lane == 0) fence_proxy_async_smem();  // our reads of the slot precede the next copy into it
+        issue_next(slot);
       }
       cc.advance(t0, t1);
     }
   } else {
     // -------------------------------------------------- register-direct path
+    // block ids one iteration ahead in registers: pb for this block, and pp
+    // for the block `pd` iterations later that the L2 prefetch targets
+    const bool use_pf = VARIANT == kL2Prefetch && pd > 0;
     int pb_next = (warp < nblk) ? bt[warp] : 0;
+    int pp_next = (use_pf && warp + NW * pd < nblk) ? bt[warp + NW * pd] : -1;
     for (int k = warp; k < nblk; k += NW) {
       const int pb = pb_next;
       if (k + NW < nblk) pb_next = bt[k + NW];
+      const int pp = pp_next;
+      if (use_pf) pp_next = (k + NW * (pd + 1) < nblk) ? bt[k + NW * (pd + 1)] : -1;
+      if (use_pf && lane == 0 && pp >= 0 && pp < P.num_blocks) {
+        // Algorithm 1: prefetch the block this warp takes `pd` iterations later
+        prefetch_l2_bulk(kbase + (size_t)pp * block_stride, T::TILE_BYTES);
+        prefetch_l2_bulk(vbase + (size_t)pp * block_stride, T::TILE_BYTES);
+      }
       if (pb < 0 || pb >= P.num_blocks) {
         if (lane == 0) record_error(P.error_word, kErrBadBlock);
         continue;
       }
-      if (VARIANT == kL2Prefetch && lane == 0 && pd > 0) {
-        // Algorithm 1: prefetch the block this warp takes `pd` iterations later
-        const int kp = k + NW * pd;
-        if (kp < nblk) {
-          const int pp = bt[kp];
-          if (pp >= 0 && pp < P.num_blocks) {
-            prefetch_l2_bulk(kbase + (size_t)pp * block_stride, T::TILE_BYTES);
-            prefetch_l2_bulk(vbase + (size_t)pp * block_stride, T::TILE_BYTES);
-          }
-        }
-      }
       const int valid_blk = min(BS, t1 - (t0 + k * BS));
-      const __half* kt = kbase + (size_t)pb * block_stride + row_off;
+      const __half* kt = kbase + (size_t)pb * block_stride + col_off;
       const __half* vt = vbase + (size_t)pb * block_stride + row_off;
 #pragma unroll
       for (int rg = 0; rg < T::RG; ++rg) {
@@ -459,7 +490,7 @@ __global__ void __launch_bounds__(DecodeTraits<D, BS, G, VARIANT>::THREADS,
         if (valid <= 0) break;
         uint4 kr[TPL];
 #pragma unroll
-        for (int i = 0; i < TPL; ++i) kr[i] = ldg_stream(kt + (rg * 16 + i * RPW) * D);
+        for (int i = 0; i < TPL; ++i) kr[i] = ldg_stream(kt + (rg * 16 + wd.k_row(i)) * D);
         uint4 vr[TPL];
         constexpr bool early_v = G <= 4;
         if (early_v) {
@@ -499,7 +530,7 @@ __global__ void __launch_bounds__(DecodeTraits<D, BS, G, VARIANT>::THREADS,
 #pragma unroll
     for (int w = 0; w < NW; ++w) {
       const float mw = mrg_m[w * G + h];
-      const float c = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+      const float c = (mw == -INFINITY) ? 0.f : ex2_approx(mw - M);
       Z = fmaf(c, mrg_l[w * G + h], Z);
       O = fmaf(c, mrg_acc[(w * G + h) * D + d], O);
     }

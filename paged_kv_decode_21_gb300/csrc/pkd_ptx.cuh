@@ -28,24 +28,10 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 }
 
 // ---------------------------------------------------------------- packed fp32
-__device__ __forceinline__ unsigned long long f2_bits(float2 v) {
-  return *reinterpret_cast<unsigned long long*>(&v);
-}
-__device__ __forceinline__ float2 bits_f2(unsigned long long v) {
-  return *reinterpret_cast<float2*>(&v);
-}
-// d = a * b + c, lane-wise on (x, y), round to nearest.
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-  unsigned long long d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)), "l"(f2_bits(c)));
-  return bits_f2(d);
-}
-// d = a * b, lane-wise.
-__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
-  unsigned long long d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)));
-  return bits_f2(d);
-}
+// d = a * b + c, lane-wise on (x, y), round to nearest (fma.rn.f32x2).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+// d = a * b, lane-wise (mul.rn.f32x2).
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
 
 // ---------------------------------------------------------------- L2 prefetch
 // Asynchronous bulk prefetch of [p, p + bytes) into L2; bytes multiple of 16,
