@@ -97,11 +97,17 @@ struct DecodeTraits {
   static constexpr int SW = kTma ? (SW_RAW > 8 ? 8 : (SW_RAW < 2 ? 2 : SW_RAW)) : 0;
   static constexpr int RING_BYTES = NW * SW * SLOT_BYTES;
   static constexpr int P_BYTES = NW * 16 * 8 * 8;           // per-warp p rows [16][8] as (p, p)
-  static constexpr int MERGE_BYTES = NW * G * (D + 2) * 4;  // per-warp m, l, acc
+  // merge area: per warp the running shift m, the exact maximum mt and l
+  // ([NW][G] each), then acc [NW][G][D] on a 16-byte boundary
+  static constexpr int MRG_ACC_OFF = (3 * NW * G + 3) / 4 * 4;  // floats
+  static constexpr int MERGE_BYTES = (MRG_ACC_OFF + NW * G * D) * 4;
   static constexpr int BAR_BYTES = NW * SW * 8;
   // layout: [ring / merge area][p rows][barriers]; the merge reuses the ring
   static constexpr int MAIN_BYTES = RING_BYTES > MERGE_BYTES ? RING_BYTES : MERGE_BYTES;
   static constexpr int SMEM_BYTES = MAIN_BYTES + P_BYTES + BAR_BYTES;
+  // every shared-memory region is accessed with 16-byte (and 8-byte barrier) operations
+  static_assert(MAIN_BYTES % 16 == 0 && P_BYTES % 16 == 0, "shared-memory regions must stay 16-byte aligned");
+  static_assert(SLOT_BYTES % 16 == 0, "bulk-copy slots must be 16-byte aligned");
 };
 
 // ---------------------------------------------------------------------------
@@ -144,7 +150,8 @@ struct WarpDecoder {
 
   float2 q2[G][4];   // q[h][8*ds + 2c .. +2) for c < 4
   float2 acc[G][4];  // sum_t p_t v_t[8*ds + 2c .. +2) over this lane's rows
-  float m[G];        // running max (log2 domain), warp-uniform
+  float m[G];        // running shift (log2 domain), warp-uniform; lags the maximum by <= TAU
+  float mt[G];       // exact maximum of the scores this lane has seen (log2 domain)
   float l[G];        // running sum of p over this lane's score slots
   int lane, rh, ds;
   int perm;          // this lane's row order: local row i is row i ^ perm of its half
@@ -162,6 +169,7 @@ struct WarpDecoder {
       q2[h][2] = h2f2(u.z);
       q2[h][3] = h2f2(u.w);
       m[h] = -INFINITY;
+      mt[h] = -INFINITY;
       l[h] = 0.f;
 #pragma unroll
       for (int c = 0; c < 4; ++c) acc[h][c] = make_float2(0.f, 0.f);
@@ -244,6 +252,7 @@ struct WarpDecoder {
     for (int h = 0; h < G; ++h) {
       p[h] = ex2_approx(s2[h] - m[h]);
       l[h] += p[h];
+      mt[h] = fmaxf(mt[h], s2[h]);
     }
     if ((ds & 1) == 0) {
       float4* dst = reinterpret_cast<float4*>(prow + my_score_row() * 16);
@@ -281,12 +290,16 @@ struct WarpDecoder {
   }
 
   // Reduce this warp's state and store (m, l, acc) to the merge area.
-  __device__ __forceinline__ void store_warp(float* mrg_m, float* mrg_l, float* mrg_acc) {
+  __device__ __forceinline__ void store_warp(float* mrg_m, float* mrg_mt, float* mrg_l, float* mrg_acc) {
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       float lv = (ds & 1) ? 0.f : l[h];
+      float mx = mt[h];
 #pragma unroll
-      for (int msk = 1; msk < 32; msk <<= 1) lv += __shfl_xor_sync(0xffffffffu, lv, msk);
+      for (int msk = 1; msk < 32; msk <<= 1) {
+        lv += __shfl_xor_sync(0xffffffffu, lv, msk);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, msk));
+      }
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         float2 a = acc[h][c];
@@ -299,6 +312,7 @@ struct WarpDecoder {
       }
       if (lane == 0) {
         mrg_m[h] = m[h];
+        mrg_mt[h] = mx;
         mrg_l[h] = lv;
       }
       if (rh == 0) {
@@ -516,16 +530,17 @@ __global__ void __launch_bounds__(DecodeTraits<D, BS, G, VARIANT>::THREADS,
   // ------------------------------------------------------------------ merge
   __syncthreads();  // every warp is done with the ring that the merge area reuses
   float* mrg = reinterpret_cast<float*>(smem);
-  float* mrg_m = mrg;                 // [NW][G]
-  float* mrg_l = mrg + NW * G;        // [NW][G]
-  float* mrg_acc = mrg + 2 * NW * G;  // [NW][G][D]
-  wd.store_warp(mrg_m + warp * G, mrg_l + warp * G, mrg_acc + warp * G * D);
+  float* mrg_m = mrg;                 // [NW][G] running shift
+  float* mrg_mt = mrg + NW * G;       // [NW][G] exact maximum
+  float* mrg_l = mrg + 2 * NW * G;    // [NW][G]
+  float* mrg_acc = mrg + T::MRG_ACC_OFF;  // [NW][G][D]
+  wd.store_warp(mrg_m + warp * G, mrg_mt + warp * G, mrg_l + warp * G, mrg_acc + warp * G * D);
   __syncthreads();
   for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
     const int h = i / D, d = i % D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, mrg_m[w * G + h]);
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, mrg_mt[w * G + h]);  // the exact maximum
     float Z = 0.f, O = 0.f;
 #pragma unroll
     for (int w = 0; w < NW; ++w) {

@@ -2,16 +2,29 @@
 #pragma once
 #include <cuda_runtime.h>
 #include "pkd_decode.cuh"
+#include "pkd_decode_ws.cuh"
 
 namespace pkd {
 
+// The staged data path switches to the warp-specialised kernel from this
+// group size on (QK and PV in separate warps; see pkd_decode_ws.cuh).
+constexpr int kWsMinGroup = 6;
+
 template <int D, int BS, int G, int VARIANT>
 cudaError_t launch_decode_inst(const DecodeParams& p, long long grid, cudaStream_t stream) {
-  using T = DecodeTraits<D, BS, G, VARIANT>;
-  auto* fn = paged_decode_kernel<D, BS, G, VARIANT>;
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
-  if (e != cudaSuccess) return e;
-  fn<<<(unsigned)grid, T::THREADS, T::SMEM_BYTES, stream>>>(p);
+  if constexpr (VARIANT == kTmaStaged && G >= kWsMinGroup) {
+    using T = WsTraits<D, BS, G>;
+    auto* fn = paged_decode_ws_kernel<D, BS, G>;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    fn<<<(unsigned)grid, T::THREADS, T::SMEM_BYTES, stream>>>(p);
+  } else {
+    using T = DecodeTraits<D, BS, G, VARIANT>;
+    auto* fn = paged_decode_kernel<D, BS, G, VARIANT>;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    fn<<<(unsigned)grid, T::THREADS, T::SMEM_BYTES, stream>>>(p);
+  }
   return cudaGetLastError();
 }
 
