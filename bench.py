@@ -37,8 +37,8 @@ from paged_kv_decode_21_gb300 import traffic, workloads  # noqa: E402
 METRIC = "paged decode-attention achieved HBM GB/s (% of GB300 peak); μs per call"
 DEFAULT_CONFIG = "llama2_7b_mha"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["paged_kv_decode_21_gb300/csrc/pkd_decode.cuh", "paged_kv_decode_21_gb300/csrc/pkd_ptx.cuh",
-                  "paged_kv_decode_21_gb300/csrc/pkd_launch.cuh"]
+KERNEL_SOURCES = ["paged_kv_decode_21_gb300/csrc/pkd_decode.cuh", "paged_kv_decode_21_gb300/csrc/pkd_decode_ws.cuh",
+                  "paged_kv_decode_21_gb300/csrc/pkd_ptx.cuh", "paged_kv_decode_21_gb300/csrc/pkd_launch.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 
 

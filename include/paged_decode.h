@@ -198,6 +198,17 @@ pkd_status paged_decode_validate_tables(const int32_t* block_tables, const int32
                                         int num_blocks, int* error_word, cudaStream_t stream);
 
 /*
+ * pkd_selftest_bounded_wait -- exercises the failure path of the library's
+ * bounded waits without faulting or hanging the GPU: launches one CTA that
+ * waits on a shared-memory barrier nothing will complete; after budget_ns
+ * nanoseconds (1e3 .. 1e8) of the GPU's global timer the wait gives up, ORs
+ * PKD_DEVERR_TIMEOUT into *error_word (device int, required) and the kernel
+ * returns normally.  Every wait in the decode kernels behaves the same way
+ * with a 100 ms budget.
+ */
+pkd_status pkd_selftest_bounded_wait(int* error_word, unsigned long long budget_ns, cudaStream_t stream);
+
+/*
  * pkd_read_device_error -- synchronises `stream`, copies *error_word to
  * *host_bits, and returns PKD_OK when it is 0, PKD_ERR_DEVICE otherwise.
  * Clears the word when `clear` is non-zero.

@@ -351,6 +351,14 @@ pkd_status paged_decode_validate_tables(const int32_t* block_tables, const int32
   return cudaGetLastError() == cudaSuccess ? PKD_OK : PKD_ERR_LAUNCH;
 }
 
+pkd_status pkd_selftest_bounded_wait(int* error_word, unsigned long long budget_ns, cudaStream_t stream) {
+  if (!error_word) return PKD_ERR_NULL;
+  if (!aligned(error_word, 4)) return PKD_ERR_ALIGN;
+  if (budget_ns < 1000ull || budget_ns > kWaitBudgetNs) return PKD_ERR_SHAPE;
+  pkd::selftest_bounded_wait_kernel<<<1, 32, 0, stream>>>(error_word, budget_ns);
+  return cudaGetLastError() == cudaSuccess ? PKD_OK : PKD_ERR_LAUNCH;
+}
+
 pkd_status pkd_read_device_error(int* error_word, unsigned* host_bits, int clear, cudaStream_t stream) {
   if (!error_word || !host_bits) return PKD_ERR_NULL;
   unsigned v = 0;

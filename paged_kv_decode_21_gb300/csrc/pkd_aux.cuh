@@ -73,4 +73,19 @@ __global__ void validate_tables_kernel(const int32_t* block_tables, const int32_
   }
 }
 
+// ---------------------------------------------------------------------------
+// Self-test of the bounded waits: one CTA waits on a shared-memory barrier
+// that no thread or copy will ever complete.  The wait gives up after
+// budget_ns of %globaltimer, records kErrTimeout and the kernel returns.
+__global__ void selftest_bounded_wait_kernel(int* error_word, unsigned long long budget_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  const bool ok = mbar_wait_bounded(&bar, 0, budget_ns);
+  if (!ok && threadIdx.x == 0) record_error(error_word, kErrTimeout);
+}
+
 }  // namespace pkd

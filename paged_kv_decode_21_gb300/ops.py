@@ -63,6 +63,8 @@ def lib():
         L.paged_decode_reduce.restype = I
         L.paged_decode_validate_tables.argtypes = [P, P, I, I, I, I, P, P]
         L.paged_decode_validate_tables.restype = I
+        L.pkd_selftest_bounded_wait.argtypes = [P, ctypes.c_ulonglong, P]
+        L.pkd_selftest_bounded_wait.restype = I
         L.pkd_read_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint), I, P]
         L.pkd_read_device_error.restype = I
         L.paged_decode_attention_static_scratch.argtypes = attn + [I, I, I, P, P]
@@ -238,6 +240,12 @@ def pkd_read_device_error(error_word, clear=True, stream=None) -> int:
     if st not in (PKD_OK, 7):
         _check(st, "pkd_read_device_error")
     return int(bits.value)
+
+
+def pkd_selftest_bounded_wait(error_word, budget_ns=1_000_000, stream=None):
+    """Launch the bounded-wait self-test (a wait that can only time out)."""
+    _check(lib().pkd_selftest_bounded_wait(_ptr(error_word), int(budget_ns), _stream(stream)),
+           "pkd_selftest_bounded_wait")
 
 
 def pkd_version() -> int:

@@ -87,6 +87,13 @@ def test_split_needs_workspace(L):
     assert call_ex(L, P=32, maxlen=100, ws=small, wsb=16) == 5
 
 
+def test_selftest_argument_checks(L):
+    assert L.pkd_selftest_bounded_wait(None, 1000000, None) == 1
+    assert L.pkd_selftest_bounded_wait(MISALIGNED, 1000000, None) == 4
+    assert L.pkd_selftest_bounded_wait(FAKE, 10, None) == 2           # budget too short
+    assert L.pkd_selftest_bounded_wait(FAKE, 10**9, None) == 2        # budget too long
+
+
 def test_empty_batch_is_a_no_op(L):
     assert call_ex(L, B=0) == 0
 

@@ -270,6 +270,16 @@ def test_bad_block_id_sets_error_word(variant):
     assert ops.pkd_read_device_error(ew3) == 0
 
 
+def test_bounded_wait_times_out_and_reports():
+    # a barrier nothing completes: the wait must give up and set the timeout bit
+    ew = errword()
+    ops.pkd_selftest_bounded_wait(ew, budget_ns=2_000_000)
+    assert ops.pkd_read_device_error(ew) == ops.DEVERR_TIMEOUT
+    # the context is still usable afterwards
+    inp = workloads.make_inputs(workloads.CONFIGS["tiny"], device="cuda")
+    assert_close(run_ex(inp, "tma_staged", -1), oracle_out(inp), "after self-test")
+
+
 # --------------------------------------------------------------------------- full-size configs
 FULL = ["llama2_7b_mha", "llama3_8b_gqa4", "qwen25_7b_gqa7", "qwen25_14b_gqa5_splitk"]
 
