@@ -266,23 +266,48 @@ struct WarpDecoder {
   // Rows at or past `valid` (0..16) are skipped (their V may be garbage).
   template <typename VRow>
   __device__ __forceinline__ void accumulate(VRow vrow, const float* prow, int valid) {
-#pragma unroll
-    for (int i = 0; i < TPL; ++i) {
+    // rows are software-pipelined: row i+1's V and p loads are issued before
+    // row i's FMAs, which hides the load latency
+    constexpr int NH2 = (G + 1) / 2;
+    auto load_row = [&](int i, uint4& v, float4 (&pp)[NH2]) {
+      v = vrow(i);
       const int r = RPW * i + rh;
-      if (valid >= 16 || r < valid) {
-        uint4 u = vrow(i);
-        const float2 vv[4] = {h2f2(u.x), h2f2(u.y), h2f2(u.z), h2f2(u.w)};
-        float2 pv[2 * ((G + 1) / 2)];
 #pragma unroll
-        for (int h2 = 0; h2 < (G + 1) / 2; ++h2) {
-          const float4 pp = *reinterpret_cast<const float4*>(prow + r * 16 + 4 * h2);
-          pv[2 * h2] = make_float2(pp.x, pp.y);
-          pv[2 * h2 + 1] = make_float2(pp.z, pp.w);
+      for (int h2 = 0; h2 < NH2; ++h2) pp[h2] = *reinterpret_cast<const float4*>(prow + r * 16 + 4 * h2);
+    };
+    auto fma_row = [&](const uint4& v4, const float4 (&pp)[NH2]) {
+      const float2 vv[4] = {h2f2(v4.x), h2f2(v4.y), h2f2(v4.z), h2f2(v4.w)};
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float2 pv = (h & 1) ? make_float2(pp[h / 2].z, pp[h / 2].w) : make_float2(pp[h / 2].x, pp[h / 2].y);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[h][c] = ffma2(pv, vv[c], acc[h][c]);
+      }
+    };
+    if (valid >= 16) {
+      uint4 vc;
+      float4 pc[NH2];
+      load_row(0, vc, pc);
+#pragma unroll
+      for (int i = 0; i < TPL; ++i) {
+        uint4 vn;
+        float4 pn[NH2];
+        if (i + 1 < TPL) load_row(i + 1, vn, pn);
+        fma_row(vc, pc);
+        if (i + 1 < TPL) {
+          vc = vn;
+#pragma unroll
+          for (int h2 = 0; h2 < NH2; ++h2) pc[h2] = pn[h2];
         }
+      }
+    } else {
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) acc[h][c] = ffma2(pv[h], vv[c], acc[h][c]);
+      for (int i = 0; i < TPL; ++i) {
+        if (RPW * i + rh < valid) {
+          uint4 vc;
+          float4 pc[NH2];
+          load_row(i, vc, pc);
+          fma_row(vc, pc);
         }
       }
     }

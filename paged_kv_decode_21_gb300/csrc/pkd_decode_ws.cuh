@@ -311,23 +311,50 @@ __global__ void __launch_bounds__(WsTraits<D, BS, G>::THREADS, WsTraits<D, BS, G
         const int valid = min(16, t1 - (t0 + cc.k * BS + cc.rg * 16));
         const __half* vg =
             reinterpret_cast<const __half*>(ring + (size_t)slot * T::SLOT_BYTES) + T::SUB_ELEMS + rh * D + ds * 8;
-#pragma unroll
-        for (int i = 0; i < TPL; ++i) {
+        // rows are software-pipelined: row i+1's V and p loads are issued
+        // before row i's FMAs, which hides the shared-memory latency
+        constexpr int NH2 = (G + 1) / 2;
+        auto load_row = [&](int i, uint4& v, float4 (&pp)[NH2]) {
+          v = lds128(vg + i * RPW * D);
           const int r = RPW * i + rh;
-          if (valid >= 16 || r < valid) {
-            const uint4 vv4 = lds128(vg + i * RPW * D);
-            const float2 vv[4] = {h2f2(vv4.x), h2f2(vv4.y), h2f2(vv4.z), h2f2(vv4.w)};
-            float2 pv[2 * ((G + 1) / 2)];
 #pragma unroll
-            for (int h2 = 0; h2 < (G + 1) / 2; ++h2) {
-              const float4 pp = *reinterpret_cast<const float4*>(pb + r * 16 + 4 * h2);
-              pv[2 * h2] = make_float2(pp.x, pp.y);
-              pv[2 * h2 + 1] = make_float2(pp.z, pp.w);
+          for (int h2 = 0; h2 < NH2; ++h2) pp[h2] = *reinterpret_cast<const float4*>(pb + r * 16 + 4 * h2);
+        };
+        auto fma_row = [&](const uint4& v4, const float4 (&pp)[NH2]) {
+          const float2 vv[4] = {h2f2(v4.x), h2f2(v4.y), h2f2(v4.z), h2f2(v4.w)};
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            const float2 pv = (h & 1) ? make_float2(pp[h / 2].z, pp[h / 2].w) : make_float2(pp[h / 2].x, pp[h / 2].y);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[h][c] = ffma2(pv, vv[c], acc[h][c]);
+          }
+        };
+        if (valid >= 16) {
+          uint4 vc;
+          float4 pc[NH2];
+          load_row(0, vc, pc);
+#pragma unroll
+          for (int i = 0; i < TPL; ++i) {
+            uint4 vn;
+            float4 pn[NH2];
+            if (i + 1 < TPL) load_row(i + 1, vn, pn);
+            fma_row(vc, pc);
+            if (i + 1 < TPL) {
+              vc = vn;
+#pragma unroll
+              for (int h2 = 0; h2 < NH2; ++h2) pc[h2] = pn[h2];
             }
+          }
+        } else {
 #pragma unroll
-            for (int h = 0; h < G; ++h)
-#pragma unroll
-              for (int c = 0; c < 4; ++c) acc[h][c] = ffma2(pv[h], vv[c], acc[h][c]);
+          for (int i = 0; i < TPL; ++i) {
+            const int r = RPW * i + rh;
+            if (r < valid) {
+              uint4 vc;
+              float4 pc[NH2];
+              load_row(i, vc, pc);
+              fma_row(vc, pc);
+            }
           }
         }
       }
