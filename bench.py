@@ -168,7 +168,7 @@ def time_gpu(args, cfg, variant, dev, inp, steps, warmup, with_e2e=True, with_cl
     lens = inp.context_lens.cpu().tolist()
     algo = traffic.algorithmic_bytes(lens, inp.num_q_heads, inp.num_kv_heads, inp.head_dim)
     P = args.partition_size if args.partition_size is not None else (cfg.partition_size or 0)
-    var = ops.VARIANTS[variant]
+    var = ops._variant(variant)
     need = ops.paged_decode_workspace_size(inp.num_seqs, inp.num_q_heads, inp.num_kv_heads,
                                            inp.head_dim, inp.block_size, inp.max_context_len, P, var)
     ws = ops.alloc_workspace(need, dev)
@@ -319,13 +319,15 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=list(workloads.CONFIGS))
-    ap.add_argument("--variant", default="auto", choices=["auto", "no_prefetch", "l2_prefetch", "tma_staged"])
+    ap.add_argument("--variant", default="auto",
+                    help="auto|no_prefetch|l2_prefetch|tma_staged, optionally +l2_hints (L2 eviction priorities)")
     ap.add_argument("--partition-size", type=int, default=None)
     ap.add_argument("--prefetch-distance", type=int, default=0)
     ap.add_argument("--sweep", action="store_true", help="every workload x variant, one line each")
     ap.add_argument("--sweep-configs", default=",".join(workloads.CONFIG_ORDER[1:]))
     ap.add_argument("--sweep-variants", default="no_prefetch,l2_prefetch,tma_staged")
     ap.add_argument("--sweep-partitions", default="", help="comma list of partition sizes (default: the config's)")
+    ap.add_argument("--sweep-pd", default="", help="comma list of prefetch distances (default: the library's)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch (profiling runs)")
@@ -352,11 +354,14 @@ def main():
 
     if args.sweep:
         parts = [int(x) for x in args.sweep_partitions.split(",") if x.strip()] or [None]
+        pds = [int(x) for x in args.sweep_pd.split(",") if x.strip()] or [args.prefetch_distance]
+        combos = [(p_, d_) for p_ in parts for d_ in pds]
         for name in args.sweep_configs.split(","):
             cfg, inp = make_workload(name, dev, args.batch)
             for variant in args.sweep_variants.split(","):
-                for part in parts:
+                for part, pdist in combos:
                     args.partition_size = part
+                    args.prefetch_distance = pdist
                     r = time_gpu(args, cfg, variant, dev, inp, min(args.steps, 200), args.warmup,
                                  with_e2e=False, with_clocks=False)
                     gbs = r["algo_bytes"] / (r["mean_ms"] * 1e-3) / 1e9
@@ -365,6 +370,7 @@ def main():
                                       "us_min": round(r["min_ms"] * 1e3, 2), "GB_s": round(gbs, 1),
                                       "frac_of_peak": round(gbs / peak, 4),
                                       "partition_size": r["partition_size"],
+                                      "prefetch_distance": pdist or "default",
                                       "launches_per_call": r["launches_per_call"],
                                       "device_error": r["device_error"]}), flush=True)
             del inp
@@ -376,7 +382,7 @@ def main():
     r = time_gpu(args, cfg, variant, dev, inp, args.steps, args.warmup, with_e2e=not args.no_e2e)
     mean_ms, value = aggregate_over_ranks(r["mean_ms"], r["algo_bytes"], ws, dev)
     achieved = r["algo_bytes"] / (r["mean_ms"] * 1e-3) / 1e9
-    resolved = "tma_staged" if variant == "auto" else variant
+    resolved = "tma_staged+l2_hints" if variant == "auto" else variant
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(mean_ms, 5), "higher_is_better": True,

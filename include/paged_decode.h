@@ -72,11 +72,23 @@ typedef enum {
 
 /* How K/V tiles reach the arithmetic.  All variants give the same result. */
 typedef enum {
-  PKD_VARIANT_AUTO = 0,        /* the fastest variant for the shape */
+  PKD_VARIANT_AUTO = 0,        /* the fastest: TMA_STAGED with PKD_FLAG_L2_EVICT_HINTS */
   PKD_VARIANT_NO_PREFETCH = 1, /* each warp loads its current blocks (16-byte loads) */
   PKD_VARIANT_L2_PREFETCH = 2, /* as 1, plus cp.async.bulk.prefetch.L2 of blocks ahead */
   PKD_VARIANT_TMA_STAGED = 3   /* bulk tensor copies into a shared-memory ring, plus L2 prefetch */
 } pkd_variant;
+
+/*
+ * Flag bits that may be ORed into a `variant` argument.
+ *   PKD_FLAG_L2_EVICT_HINTS  give the KV stream L2 eviction priorities: the
+ *       loads or bulk copies that consume a K/V tile mark it evict_first (it
+ *       is never read again), and L2 prefetches of tiles ahead mark them
+ *       evict_last until they are consumed.  This is the "adjust eviction
+ *       priority" mitigation for prefetched blocks overflowing L2 in section
+ *       4.2 of the review "Accelerating LLM Inference Throughput via
+ *       Asynchronous KV Cache Prefetching".  Results are unchanged.
+ */
+#define PKD_FLAG_L2_EVICT_HINTS 0x100
 
 /*
  * paged_decode_attention -- the whole operation, one partition per
@@ -113,9 +125,9 @@ pkd_status paged_decode_attention(const void* q, const void* k_cache, const void
  *                   computed by one CTA per (sequence, kv head, partition)
  *                   and merged by the split-K reduce; shorter ones are
  *                   written directly.
- *   variant         pkd_variant
- *   prefetch_distance  how many warp steps ahead the L2 prefetch runs
- *                   (0 = default); ignored by PKD_VARIANT_NO_PREFETCH
+ *   variant         pkd_variant, optionally ORed with PKD_FLAG_* bits
+ *   prefetch_distance  how many of a warp's iterations ahead the L2 prefetch
+ *                   runs (0 = default, 1); ignored by PKD_VARIANT_NO_PREFETCH
  *   workspace, workspace_bytes  device scratch of at least
  *                   paged_decode_workspace_size(...) bytes, 256-byte aligned
  *                   (may be NULL when no sequence is split)

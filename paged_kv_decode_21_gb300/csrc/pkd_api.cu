@@ -12,7 +12,7 @@
 namespace {
 
 constexpr unsigned long long kWaitBudgetNs = 100ull * 1000ull * 1000ull;  // 100 ms per bounded wait
-constexpr int kDefaultPrefetchDistance = 2;
+constexpr int kDefaultPrefetchDistance = 1;  // measured best or tied on every workload
 constexpr int kMinAutoPartition = 512;
 constexpr int kMaxAutoPartition = 2048;
 constexpr int kTargetWaves = 6;      // split when the grid would cover fewer waves than this
@@ -46,7 +46,15 @@ int sm_count() {
   return n;
 }
 
+// `variant` carries the data path in its low byte and PKD_FLAG_* bits above.
+int variant_path(int variant) { return variant & 0xff; }
+bool variant_ok(int variant) {
+  const int path = variant_path(variant);
+  return variant >= 0 && path <= PKD_VARIANT_TMA_STAGED && (variant & ~0xff & ~PKD_FLAG_L2_EVICT_HINTS) == 0;
+}
+
 int resolve_variant(int variant) {
+  variant = variant_path(variant);
   return variant == PKD_VARIANT_AUTO ? PKD_VARIANT_TMA_STAGED : variant;
 }
 
@@ -170,7 +178,7 @@ int paged_decode_auto_partition_size(int num_seqs, int num_q_heads, int num_kv_h
                                      int block_size, int max_context_len, int variant) {
   Shape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, 1, 1 << 30, max_context_len};
   if (check_shape(s) != PKD_OK) return -2;
-  if (variant < PKD_VARIANT_AUTO || variant > PKD_VARIANT_TMA_STAGED) return -2;
+  if (!variant_ok(variant)) return -2;
   return auto_partition(s, variant);
 }
 
@@ -179,7 +187,7 @@ size_t paged_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_hea
                                    int variant) {
   Shape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, 1, 1 << 30, max_context_len};
   if (check_shape(s) != PKD_OK) return 0;
-  if (variant < PKD_VARIANT_AUTO || variant > PKD_VARIANT_TMA_STAGED) return 0;
+  if (!variant_ok(variant)) return 0;
   int P = partition_size == 0 ? auto_partition(s, variant) : partition_size;
   if (P <= 0 || max_context_len <= P) return 0;
   const int np = (max_context_len + P - 1) / P;
@@ -204,7 +212,7 @@ pkd_status paged_decode_attention_ex(const void* q, const void* k_cache, const v
   if (!out) return PKD_ERR_NULL;
   if (!aligned(out, 16) || (error_word && !aligned(error_word, 4))) return PKD_ERR_ALIGN;
   if (!std::isfinite(scale)) return PKD_ERR_SHAPE;
-  if (variant < PKD_VARIANT_AUTO || variant > PKD_VARIANT_TMA_STAGED) return PKD_ERR_SHAPE;
+  if (!variant_ok(variant)) return PKD_ERR_SHAPE;
   if (prefetch_distance < 0) return PKD_ERR_SHAPE;
   int P;
   if (partition_size == 0) {
@@ -239,6 +247,8 @@ pkd_status paged_decode_attention_ex(const void* q, const void* k_cache, const v
   p.mode = 0;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.prefetch_distance = prefetch_distance == 0 ? kDefaultPrefetchDistance : prefetch_distance;
+  // the automatic variant is the staged path with the L2 eviction priorities
+  p.l2_hints = ((variant & PKD_FLAG_L2_EVICT_HINTS) || variant_path(variant) == PKD_VARIANT_AUTO) ? 1 : 0;
   p.timeout_ns = kWaitBudgetNs;
   if (split) {
     if (!workspace) return PKD_ERR_WORKSPACE;
@@ -288,7 +298,7 @@ pkd_status paged_decode_partitions(const void* q, const void* k_cache, const voi
       (error_word && !aligned(error_word, 4)))
     return PKD_ERR_ALIGN;
   if (!std::isfinite(scale)) return PKD_ERR_SHAPE;
-  if (variant < PKD_VARIANT_AUTO || variant > PKD_VARIANT_TMA_STAGED || prefetch_distance < 0)
+  if (!variant_ok(variant) || prefetch_distance < 0)
     return PKD_ERR_SHAPE;
   if (partition_size <= 0 || partition_size % 32 != 0 || partition_size % block_size != 0)
     return PKD_ERR_SHAPE;
@@ -315,6 +325,8 @@ pkd_status paged_decode_partitions(const void* q, const void* k_cache, const voi
   p.mode = 1;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.prefetch_distance = prefetch_distance == 0 ? kDefaultPrefetchDistance : prefetch_distance;
+  // the automatic variant is the staged path with the L2 eviction priorities
+  p.l2_hints = ((variant & PKD_FLAG_L2_EVICT_HINTS) || variant_path(variant) == PKD_VARIANT_AUTO) ? 1 : 0;
   p.timeout_ns = kWaitBudgetNs;
   const int G = num_q_heads / num_kv_heads;
   const long long grid = (long long)num_seqs * num_kv_heads * max_num_partitions;

@@ -65,6 +65,7 @@ struct DecodeParams {
   int mode;             // 0: final out when one partition, partials otherwise; 1: partials always
   float scale_log2;     // softmax scale * log2(e)
   int prefetch_distance;
+  int l2_hints;         // 1: evict_first on consuming loads/copies, evict_last on prefetches
   unsigned long long timeout_ns;
 };
 
@@ -121,6 +122,15 @@ __device__ __forceinline__ uint4 ldg_stream(const void* p) {
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint4 ldg_stream(const void* p, const L2Hints& h) {
+  if (!h.on) return ldg_stream(p);
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p), "l"(h.evict_first));
   return r;
 }
 
@@ -408,6 +418,7 @@ __global__ void __launch_bounds__(DecodeTraits<D, BS, G, VARIANT>::THREADS,
   const __half* kbase = P.k_cache + (size_t)g * head_stride;
   const __half* vbase = P.v_cache + (size_t)g * head_stride;
   const int pd = P.prefetch_distance;
+  const L2Hints l2h = make_l2_hints(P.l2_hints != 0);
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -452,14 +463,14 @@ __global__ void __launch_bounds__(DecodeTraits<D, BS, G, VARIANT>::THREADS,
           unsigned char* dst = ring + (size_t)slot * T::SLOT_BYTES;
           const size_t off = (size_t)ic_pb * block_stride + (size_t)ic.rg * T::SUB_ELEMS;
           mbar_arrive_expect_tx(&full[slot], 2 * T::SUB_BYTES);
-          bulk_copy_g2s(dst, kbase + off, T::SUB_BYTES, &full[slot]);
-          bulk_copy_g2s(dst + T::SUB_BYTES, vbase + off, T::SUB_BYTES, &full[slot]);
+          bulk_copy_g2s(dst, kbase + off, T::SUB_BYTES, &full[slot], l2h);
+          bulk_copy_g2s(dst + T::SUB_BYTES, vbase + off, T::SUB_BYTES, &full[slot], l2h);
         }
       }
       if (ic.rg == 0 && pd > 0) {
         if (lane == 0 && pf_pb >= 0 && pf_pb < P.num_blocks) {
-          prefetch_l2_bulk(kbase + (size_t)pf_pb * block_stride, T::TILE_BYTES);
-          prefetch_l2_bulk(vbase + (size_t)pf_pb * block_stride, T::TILE_BYTES);
+          prefetch_l2_bulk(kbase + (size_t)pf_pb * block_stride, T::TILE_BYTES, l2h);
+          prefetch_l2_bulk(vbase + (size_t)pf_pb * block_stride, T::TILE_BYTES, l2h);
         }
         pf_k += NW;
         pf_pb = block_id(pf_k);
@@ -513,8 +524,8 @@ __global__ void __launch_bounds__(DecodeTraits<D, BS, G, VARIANT>::THREADS,
       if (use_pf) pp_next = (k + NW * (pd + 1) < nblk) ? bt[k + NW * (pd + 1)] : -1;
       if (use_pf && lane == 0 && pp >= 0 && pp < P.num_blocks) {
         // Algorithm 1: prefetch the block this warp takes `pd` iterations later
-        prefetch_l2_bulk(kbase + (size_t)pp * block_stride, T::TILE_BYTES);
-        prefetch_l2_bulk(vbase + (size_t)pp * block_stride, T::TILE_BYTES);
+        prefetch_l2_bulk(kbase + (size_t)pp * block_stride, T::TILE_BYTES, l2h);
+        prefetch_l2_bulk(vbase + (size_t)pp * block_stride, T::TILE_BYTES, l2h);
       }
       if (pb < 0 || pb >= P.num_blocks) {
         if (lane == 0) record_error(P.error_word, kErrBadBlock);
@@ -529,12 +540,12 @@ __global__ void __launch_bounds__(DecodeTraits<D, BS, G, VARIANT>::THREADS,
         if (valid <= 0) break;
         uint4 kr[TPL];
 #pragma unroll
-        for (int i = 0; i < TPL; ++i) kr[i] = ldg_stream(kt + (rg * 16 + wd.k_row(i)) * D);
+        for (int i = 0; i < TPL; ++i) kr[i] = ldg_stream(kt + (rg * 16 + wd.k_row(i)) * D, l2h);
         uint4 vr[TPL];
         constexpr bool early_v = G <= 4;
         if (early_v) {
 #pragma unroll
-          for (int i = 0; i < TPL; ++i) vr[i] = ldg_stream(vt + (rg * 16 + i * RPW) * D);
+          for (int i = 0; i < TPL; ++i) vr[i] = ldg_stream(vt + (rg * 16 + i * RPW) * D, l2h);
         }
         float s2[G];
         wd.scores([&](int i) { return kr[i]; }, P.scale_log2, s2);
@@ -545,7 +556,7 @@ __global__ void __launch_bounds__(DecodeTraits<D, BS, G, VARIANT>::THREADS,
         wd.softmax_update(s2, prow);
         if (!early_v) {
 #pragma unroll
-          for (int i = 0; i < TPL; ++i) vr[i] = ldg_stream(vt + (rg * 16 + i * RPW) * D);
+          for (int i = 0; i < TPL; ++i) vr[i] = ldg_stream(vt + (rg * 16 + i * RPW) * D, l2h);
         }
         wd.accumulate([&](int i) { return vr[i]; }, prow, valid);
       }

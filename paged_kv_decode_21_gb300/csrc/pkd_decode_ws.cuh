@@ -93,6 +93,7 @@ __global__ void __launch_bounds__(WsTraits<D, BS, G>::THREADS, WsTraits<D, BS, G
   const __half* kbase = P.k_cache + (size_t)g * head_stride;
   const __half* vbase = P.v_cache + (size_t)g * head_stride;
   const int pd = P.prefetch_distance;
+  const L2Hints l2h = make_l2_hints(P.l2_hints != 0);
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -155,15 +156,17 @@ __global__ void __launch_bounds__(WsTraits<D, BS, G>::THREADS, WsTraits<D, BS, G
 #pragma unroll
         for (int i = 0; i < TPL; ++i) {
           const uint4 kv = lds128(kg + (RPW * (i ^ perm) + rh) * D);
-          const float2 k0 = h2f2(kv.x), k1 = h2f2(kv.y), k2 = h2f2(kv.z), k3 = h2f2(kv.w);
+          const float2 kk[4] = {h2f2(kv.x), h2f2(kv.y), h2f2(kv.z), h2f2(kv.w)};
+          // d-pair outermost: the G chains issue back to back
+          float2 a[G];
 #pragma unroll
-          for (int h = 0; h < G; ++h) {
-            float2 a = fmul2(q2[h][0], k0);
-            a = ffma2(q2[h][1], k1, a);
-            a = ffma2(q2[h][2], k2, a);
-            a = ffma2(q2[h][3], k3, a);
-            part[i][h] = a.x + a.y;
-          }
+          for (int h = 0; h < G; ++h) a[h] = fmul2(q2[h][0], kk[0]);
+#pragma unroll
+          for (int c = 1; c < 4; ++c)
+#pragma unroll
+            for (int h = 0; h < G; ++h) a[h] = ffma2(q2[h][c], kk[c], a[h]);
+#pragma unroll
+          for (int h = 0; h < G; ++h) part[i][h] = a[h].x + a[h].y;
         }
 #pragma unroll
         for (int lvl = 0; (TPL >> lvl) > 1; ++lvl) {
@@ -269,14 +272,14 @@ __global__ void __launch_bounds__(WsTraits<D, BS, G>::THREADS, WsTraits<D, BS, G
           unsigned char* dst = ring + (size_t)slot * T::SLOT_BYTES;
           const size_t off = (size_t)ic_pb * block_stride + (size_t)ic.rg * T::SUB_ELEMS;
           mbar_arrive_expect_tx(&full[slot], 2 * T::SUB_BYTES);
-          bulk_copy_g2s(dst, kbase + off, T::SUB_BYTES, &full[slot]);
-          bulk_copy_g2s(dst + T::SUB_BYTES, vbase + off, T::SUB_BYTES, &full[slot]);
+          bulk_copy_g2s(dst, kbase + off, T::SUB_BYTES, &full[slot], l2h);
+          bulk_copy_g2s(dst + T::SUB_BYTES, vbase + off, T::SUB_BYTES, &full[slot], l2h);
         }
       }
       if (ic.rg == 0 && pd > 0) {
         if (lane == 0 && pf_pb >= 0 && pf_pb < P.num_blocks) {
-          prefetch_l2_bulk(kbase + (size_t)pf_pb * block_stride, T::TILE_BYTES);
-          prefetch_l2_bulk(vbase + (size_t)pf_pb * block_stride, T::TILE_BYTES);
+          prefetch_l2_bulk(kbase + (size_t)pf_pb * block_stride, T::TILE_BYTES, l2h);
+          prefetch_l2_bulk(vbase + (size_t)pf_pb * block_stride, T::TILE_BYTES, l2h);
         }
         pf_k += NS;
         pf_pb = block_id(pf_k);

@@ -109,4 +109,46 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
       : "memory");
 }
 
+// ---------------------------------------------------------------- L2 policies
+// Optional L2 eviction priorities for the KV stream: tiles are read exactly
+// once, so the consuming load/copy marks them evict_first, while a tile that
+// was prefetched ahead of use is marked evict_last until it is consumed.
+struct L2Hints {
+  bool on;
+  uint64_t evict_first;
+  uint64_t evict_last;
+};
+
+__device__ __forceinline__ L2Hints make_l2_hints(bool on) {
+  L2Hints h{on, 0, 0};
+  if (on) {
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(h.evict_first));
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(h.evict_last));
+  }
+  return h;
+}
+
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes, const L2Hints& h) {
+  if (h.on) {
+    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(p), "r"(bytes),
+                 "l"(h.evict_last)
+                 : "memory");
+  } else {
+    prefetch_l2_bulk(p, bytes);
+  }
+}
+
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                              const L2Hints& h) {
+  if (h.on) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+        "%4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(h.evict_first)
+        : "memory");
+  } else {
+    bulk_copy_g2s(dst, src, bytes, bar);
+  }
+}
+
 }  // namespace pkd

@@ -141,8 +141,20 @@ def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scal
     return out
 
 
+FLAG_L2_EVICT_HINTS = 0x100
+
+
 def _variant(variant) -> int:
-    return VARIANTS[variant] if isinstance(variant, str) else int(variant)
+    """A data-path name ("tma_staged", optionally "+l2_hints") or its integer code."""
+    if isinstance(variant, str):
+        name, _, flag = variant.partition("+")
+        code = VARIANTS[name]
+        if flag:
+            if flag != "l2_hints":
+                raise ValueError(f"unknown variant flag {flag!r}")
+            code |= FLAG_L2_EVICT_HINTS
+        return code
+    return int(variant)
 
 
 def paged_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,

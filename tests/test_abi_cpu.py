@@ -70,6 +70,12 @@ def test_shape_checks(L):
     assert call_ex(L, var=9) == 2
 
 
+def test_variant_flags(L):
+    assert call_ex(L, var=0x100 | 3, D=96) == 3        # flag accepted; fails later on head_dim
+    assert call_ex(L, var=0x200 | 3) == 2              # unknown flag bit
+    assert L.paged_decode_workspace_size(2, 8, 2, 128, 16, 100, 32, 0x100 | 2) > 0
+
+
 def test_unsupported_shapes(L):
     assert call_ex(L, D=96) == 3
     assert call_ex(L, BS=8) == 3

@@ -270,6 +270,17 @@ def test_bad_block_id_sets_error_word(variant):
     assert ops.pkd_read_device_error(ew3) == 0
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("partition", [-1, 64])
+def test_l2_eviction_hints_change_nothing(variant, partition):
+    # the hints only set L2 eviction priorities: outputs are bitwise equal
+    inp = workloads.make_custom(4, 28, 4, 128, 16, [300, 17, 129, 64], seed=37, device="cuda")
+    a = run_ex(inp, variant, partition)
+    b = run_ex(inp, variant + "+l2_hints", partition)
+    assert torch.equal(a, b)
+    assert_close(b, oracle_out(inp), "with L2 hints")
+
+
 def test_bounded_wait_times_out_and_reports():
     # a barrier nothing completes: the wait must give up and set the timeout bit
     ew = errword()
