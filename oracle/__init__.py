@@ -58,6 +58,8 @@ def _load(mutant: int = 0):
         lib.pkd_oracle_partitions.restype = I
         lib.pkd_oracle_merge.argtypes = [P, P, P, P, I, I, I, I, I, P]
         lib.pkd_oracle_merge.restype = I
+        lib.pkd_oracle_append.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I]
+        lib.pkd_oracle_append.restype = I
         lib.pkd_oracle_half_to_double.argtypes = [ctypes.c_uint16]
         lib.pkd_oracle_half_to_double.restype = D
         lib.pkd_oracle_mutant.argtypes = []
@@ -165,6 +167,27 @@ def merge(m, l, o, context_lens, partition_size, mutant: int = 0) -> np.ndarray:
                               int(partition_size), NP, _ptr(out))
     _check(rc, "merge")
     return out
+
+
+def append(k_new, v_new, block_tables, context_lens, k_cache, v_cache, mutant: int = 0,
+           check: bool = True):
+    """Write each sequence's new K/V row at logical position context_lens[b];
+    returns new (k_cache, v_cache) arrays (float16) and leaves the inputs alone."""
+    lib = _load(mutant)
+    kn = _np(k_new, np.float16).view(np.uint16)
+    vn = _np(v_new, np.float16).view(np.uint16)
+    bt = _np(block_tables, np.int32)
+    cl = _np(context_lens, np.int32)
+    kc = _np(k_cache, np.float16).copy().view(np.uint16)
+    vc = _np(v_cache, np.float16).copy().view(np.uint16)
+    NB, Hkv, BS, D = kc.shape
+    B = cl.shape[0]
+    assert kn.shape == (B, Hkv, D) and vn.shape == (B, Hkv, D)
+    rc = lib.pkd_oracle_append(_ptr(kn), _ptr(vn), _ptr(bt), _ptr(cl), _ptr(kc), _ptr(vc), B, Hkv, D, BS,
+                               NB, bt.shape[1])
+    if check:
+        _check(rc, "append")
+    return kc.view(np.float16), vc.view(np.float16)
 
 
 def half_to_double(bits) -> np.ndarray:

@@ -49,7 +49,8 @@
  * scale 0 giving the mean of V; context length 1 giving v_0; a one-token
  * spike per position; GQA equal to repeated-KV MHA; the log-sum-exp merge of
  * partitions equal to the unsplit result; partition sums at scale 0 equal to
- * the exact token counts; and mutation tests that plant mistakes in this
+ * the exact token counts; append-then-attend equal to SDPA over the grown
+ * contiguous sequence; and mutation tests that plant mistakes in this
  * file (compile-time PKD_ORACLE_MUTANT) and require some pin to fail.
  */
 #include <math.h>
@@ -395,6 +396,51 @@ int pkd_oracle_merge(const double *m_in, const double *l_in, const double *o_in,
         }
     }
     return 0;
+}
+
+/*
+ * Append of one new token per sequence into the paged cache (the cache write
+ * that precedes each decode step): with L = context_lens[b] (the length
+ * before the append), for every kv head g
+ *   p = block_tables[b][L / bs],  K[p][g][L % bs][:] = k_new[b][g][:],
+ *                                 V[p][g][L % bs][:] = v_new[b][g][:].
+ * Operates on the caller's arrays in place (raw binary16 words).  Returns 0;
+ * -1 if a sequence has no room in its table row or its block id is outside
+ * [0, num_blocks) (that sequence is skipped); -3 on a bad argument.
+ * Source: CSDN answer "如何优化LLM推理引擎的内存访问延迟？", section 2 (each
+ * sequence's KV lives in pages listed by its page table; new tokens go into
+ * the sequence's pages in logical order).
+ */
+int pkd_oracle_append(const uint16_t *k_new, const uint16_t *v_new, const int32_t *block_tables,
+                      const int32_t *context_lens, uint16_t *k_cache, uint16_t *v_cache, int num_seqs,
+                      int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                      int max_blocks_per_seq)
+{
+    if (!k_new || !v_new || !block_tables || !context_lens || !k_cache || !v_cache) return -3;
+    if (num_seqs < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0 ||
+        max_blocks_per_seq <= 0)
+        return -3;
+    int status = 0;
+    for (int b = 0; b < num_seqs; ++b) {
+        int L = context_lens[b];
+        int logical_block = L / block_size;
+        int slot = L % block_size;
+#if PKD_ORACLE_MUTANT == 8      /* planted mistake: writes the last existing slot instead of the next */
+        if (L > 0) { logical_block = (L - 1) / block_size; slot = (L - 1) % block_size; }
+#endif
+        if (L < 0 || logical_block >= max_blocks_per_seq) { status = -1; continue; }
+        int p = block_tables[(size_t)b * max_blocks_per_seq + logical_block];
+        if (p < 0 || p >= num_blocks) { status = -1; continue; }
+        for (int g = 0; g < num_kv_heads; ++g) {
+            size_t dst = (((size_t)p * num_kv_heads + g) * block_size + slot) * head_dim;
+            size_t src = ((size_t)b * num_kv_heads + g) * head_dim;
+            for (int d = 0; d < head_dim; ++d) {
+                k_cache[dst + d] = k_new[src + d];
+                v_cache[dst + d] = v_new[src + d];
+            }
+        }
+    }
+    return status;
 }
 
 /* Which planted mistake (0 = none) this build carries; for the mutation tests. */

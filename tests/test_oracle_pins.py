@@ -246,11 +246,55 @@ def pin_partition_max_is_max_score(mutant=0):
             assert abs(l[0, h, j] - np.exp(seg - seg.max()).sum()) <= TOL * len(seg)
 
 
+def pin_append_then_attend(mutant=0):
+    # the first L tokens are scattered independently; the oracle appends token L;
+    # attention over L+1 tokens must equal SDPA over the grown logical sequence
+    for seed, (lens, Hq, Hkv, D, BS) in enumerate([((15, 16, 17, 0, 31), 6, 3, 16, 16),
+                                                   ((7, 8, 1), 4, 4, 8, 8)]):
+        rng = np.random.default_rng(300 + seed)
+        full = [L + 1 for L in lens]
+        grown = scatter_problem(400 + seed, full, Hq, Hkv, D, BS, mbps=4)
+        before = dict(grown)
+        # the pool as it was before the append: the new slot holds noise
+        k_old, v_old = grown["k"].copy(), grown["v"].copy()
+        for b, L in enumerate(lens):
+            p = grown["bt"][b, L // BS]
+            k_old[p, :, L % BS, :] = rng.standard_normal((Hkv, D)).astype(np.float16)
+            v_old[p, :, L % BS, :] = rng.standard_normal((Hkv, D)).astype(np.float16)
+        k_new = np.stack([grown["lk"][b][:, L, :] for b, L in enumerate(lens)])
+        v_new = np.stack([grown["lv"][b][:, L, :] for b, L in enumerate(lens)])
+        kc, vc = oracle.append(k_new, v_new, grown["bt"], np.array(lens, np.int32), k_old, v_old,
+                               mutant=mutant)
+        after = dict(before, k=kc, v=vc)
+        scale = 1.0 / math.sqrt(D)
+        got = run(after, scale, mutant)
+        ref = sdpa_reference(grown, scale, Hq, Hkv)
+        assert np.max(np.abs(got - ref)) <= TOL * max(1.0, np.max(np.abs(ref)))
+
+
+def pin_append_changes_one_row_per_head(mutant=0):
+    lens, Hkv, D, BS = [5, 16, 0], 2, 8, 16
+    pr = scatter_problem(500, [L + 1 for L in lens], 2, Hkv, D, BS, mbps=3)
+    rng = np.random.default_rng(501)
+    k_new = rng.standard_normal((3, Hkv, D)).astype(np.float16)
+    v_new = rng.standard_normal((3, Hkv, D)).astype(np.float16)
+    kc, vc = oracle.append(k_new, v_new, pr["bt"], np.array(lens, np.int32), pr["k"], pr["v"],
+                           mutant=mutant)
+    changed = np.zeros(pr["k"].shape[:3], bool)
+    for b, L in enumerate(lens):
+        p = pr["bt"][b, L // BS]
+        changed[p, :, L % BS] = True
+        assert np.array_equal(kc[p, :, L % BS], k_new[b])
+        assert np.array_equal(vc[p, :, L % BS], v_new[b])
+    assert np.array_equal(kc[~changed], pr["k"][~changed])
+    assert np.array_equal(vc[~changed], pr["v"][~changed])
+
+
 PINS = [pin_half_decoder, pin_sdpa_contiguous, pin_permutation_invariance, pin_weights_sum_to_one,
         pin_identical_keys_mean_of_v, pin_scale_zero_mean_of_v, pin_single_token,
         pin_spike_every_position, pin_gqa_equals_repeated_mha, pin_context_zero,
         pin_nan_poison_ignored, pin_partition_merge, pin_partition_counts_scale_zero,
-        pin_partition_max_is_max_score]
+        pin_partition_max_is_max_score, pin_append_then_attend, pin_append_changes_one_row_per_head]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -274,6 +318,13 @@ def test_row_selection_matches_full():
         assert np.array_equal(sel[i], full[r // 4, r % 4])
 
 
+def test_append_without_room_is_reported():
+    pr = scatter_problem(33, [32], 2, 2, 8, 16, mbps=2)
+    k_new = np.zeros((1, 2, 8), np.float16)
+    with pytest.raises(oracle.OracleError):
+        oracle.append(k_new, k_new, pr["bt"], np.array([32], np.int32), pr["k"], pr["v"])
+
+
 def test_bad_block_id_is_reported():
     pr = scatter_problem(32, [20], 2, 2, 8, 16)
     pr["bt"][0, 1] = pr["NB"] + 5
@@ -281,7 +332,7 @@ def test_bad_block_id_is_reported():
         run(pr, 0.3)
 
 
-MUTANTS = list(range(1, 8))
+MUTANTS = list(range(1, 9))
 
 
 @pytest.mark.parametrize("mutant", MUTANTS)
