@@ -225,6 +225,70 @@ def time_gpu(args, cfg, variant, dev, inp, steps, warmup, with_e2e=True, with_cl
     return res
 
 
+def time_append(cfg, inp, dev, steps, warmup, peak):
+    """The cache write before a decode step: paged_kv_append of token L-1 of
+    every sequence (its slot exists), timed alone and followed by the decode
+    call over the L tokens, each with an L2 flush before the timed region."""
+    from paged_kv_decode_21_gb300 import ops
+    stream = torch.cuda.current_stream(dev)
+    B, Hkv, D = inp.num_seqs, inp.num_kv_heads, inp.head_dim
+    g = torch.Generator(device=dev).manual_seed(cfg.seed + 99)
+    k_new = workloads.randn_f16((B, Hkv, D), g, dev)
+    v_new = workloads.randn_f16((B, Hkv, D), g, dev)
+    pos = (inp.context_lens - 1).clamp(min=0)
+    out = torch.empty_like(inp.q)
+    ew = torch.zeros(1, dtype=torch.int32, device=dev)
+    need = ops.paged_decode_workspace_size(B, inp.num_q_heads, Hkv, D, inp.block_size,
+                                           inp.max_context_len, 0, 0)
+    ws = ops.alloc_workspace(need, dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+
+    def append():
+        ops.paged_kv_append(k_new, v_new, inp.block_tables, pos, inp.k_cache, inp.v_cache,
+                            error_word=ew, stream=stream)
+
+    def decode():
+        ops.paged_decode_attention_ex(inp.q, inp.k_cache, inp.v_cache, inp.block_tables,
+                                      inp.context_lens, inp.scale, out=out,
+                                      max_context_len=inp.max_context_len, workspace=ws,
+                                      error_word=ew, stream=stream)
+
+    def both():
+        append()
+        decode()
+
+    def timed(fn):
+        for _ in range(warmup):
+            flush.zero_()
+            fn()
+        torch.cuda.synchronize(dev)
+        st = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        en = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        for i in range(steps):
+            flush.zero_()
+            st[i].record(stream)
+            fn()
+            en[i].record(stream)
+        torch.cuda.synchronize(dev)
+        return statistics.mean(a.elapsed_time(b) for a, b in zip(st, en)) * 1e3
+
+    n = min(steps, 500)
+    steps = n
+    t_app = timed(append)
+    t_dec = timed(decode)
+    t_both = timed(both)
+    # algorithmic bytes of the append: new K and V rows read once, written once
+    app_bytes = 2 * 2 * B * Hkv * D * 2
+    return {"mode": "paged_kv_append", "workload": describe(cfg), "steps": n,
+            "append_us": round(t_app, 3), "append_bytes": app_bytes,
+            "append_GB_s": round(app_bytes / (t_app * 1e-6) / 1e9, 1),
+            "append_frac_of_peak": round(app_bytes / (t_app * 1e-6) / 1e9 / peak, 4),
+            "decode_us": round(t_dec, 2), "append_then_decode_us": round(t_both, 2),
+            "device_error": ops.pkd_read_device_error(ew),
+            "l2": "an L2 flush (2x L2 write) before every timed call"}
+
+
 def time_e2e(call, inp, out, stream, dev, algo, steps):
     """Same call with the inputs copied from pinned host memory every step and
     the result copied back; events bracket copies + call."""
@@ -328,6 +392,14 @@ def main():
     ap.add_argument("--sweep-variants", default="no_prefetch,l2_prefetch,tma_staged")
     ap.add_argument("--sweep-partitions", default="", help="comma list of partition sizes (default: the config's)")
     ap.add_argument("--sweep-pd", default="", help="comma list of prefetch distances (default: the library's)")
+    ap.add_argument("--fig4", action="store_true",
+                    help="batch x context grid on the MHA shape: each data path's speed over NO_PREFETCH")
+    ap.add_argument("--fig4-config", default=DEFAULT_CONFIG,
+                    help="workload whose head shape the grid uses (batch and context are swept)")
+    ap.add_argument("--fig4-batches", default="1,4,16,64,128,256")
+    ap.add_argument("--fig4-contexts", default="512,1024,2048,4096,8192")
+    ap.add_argument("--append", action="store_true",
+                    help="time paged_kv_append alone and in front of the decode call, on --config")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch (profiling runs)")
@@ -351,6 +423,43 @@ def main():
         torch.distributed.barrier()
     ops.lib()
     peak, peak_kind = hbm_peak()
+
+    if args.fig4:
+        import dataclasses
+        base = workloads.CONFIGS[args.fig4_config]
+        for L in [int(x) for x in args.fig4_contexts.split(",")]:
+            for B in [int(x) for x in args.fig4_batches.split(",")]:
+                cfg = dataclasses.replace(base, name=f"{base.name}_b{B}_L{L}", num_seqs=B,
+                                          context_lens=(L,) * B, len_range=None, num_blocks=None,
+                                          partition_size=0)
+                inp = workloads.make_inputs(cfg, device=dev)
+                res = {}
+                for variant in ("no_prefetch", "l2_prefetch", "tma_staged", "auto"):
+                    args.partition_size = None
+                    r = time_gpu(args, cfg, variant, dev, inp, min(args.steps, 50), args.warmup,
+                                 with_e2e=False, with_clocks=False)
+                    res[variant] = r
+                base_us = res["no_prefetch"]["mean_ms"] * 1e3
+                line = {"shape": f"{cfg.num_q_heads}q/{cfg.num_kv_heads}kv", "batch": B, "context": L,
+                        "algo_bytes": res["auto"]["algo_bytes"],
+                        "partition_size": res["auto"]["partition_size"],
+                        "auto_variant": ops.variant_name(ops.paged_decode_auto_variant(
+                            B, cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim, cfg.block_size, L,
+                            res["auto"]["partition_size"]))}
+                for variant, r in res.items():
+                    us = r["mean_ms"] * 1e3
+                    gbs = r["algo_bytes"] / (r["mean_ms"] * 1e-3) / 1e9
+                    line[variant] = {"us": round(us, 2), "frac_of_peak": round(gbs / peak, 4),
+                                     "speedup_vs_no_prefetch": round(base_us / us, 3)}
+                print(json.dumps(line), flush=True)
+                del inp
+                torch.cuda.empty_cache()
+        return 0
+
+    if args.append:
+        cfg, inp = make_workload(args.config, dev, args.batch)
+        print(json.dumps(time_append(cfg, inp, dev, args.steps, args.warmup, peak)), flush=True)
+        return 0
 
     if args.sweep:
         parts = [int(x) for x in args.sweep_partitions.split(",") if x.strip()] or [None]
@@ -382,7 +491,11 @@ def main():
     r = time_gpu(args, cfg, variant, dev, inp, args.steps, args.warmup, with_e2e=not args.no_e2e)
     mean_ms, value = aggregate_over_ranks(r["mean_ms"], r["algo_bytes"], ws, dev)
     achieved = r["algo_bytes"] / (r["mean_ms"] * 1e-3) / 1e9
-    resolved = "tma_staged+l2_hints" if variant == "auto" else variant
+    resolved = variant
+    if variant == "auto":
+        resolved = ops.variant_name(ops.paged_decode_auto_variant(
+            cfg.num_seqs, cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim, cfg.block_size,
+            inp.max_context_len, r["partition_size"]))
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(mean_ms, 5), "higher_is_better": True,

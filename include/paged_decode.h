@@ -72,10 +72,13 @@ typedef enum {
 
 /* How K/V tiles reach the arithmetic.  All variants give the same result. */
 typedef enum {
-  PKD_VARIANT_AUTO = 0,        /* the fastest: TMA_STAGED with PKD_FLAG_L2_EVICT_HINTS */
+  PKD_VARIANT_AUTO = 0,        /* chosen per launch, see paged_decode_auto_variant */
   PKD_VARIANT_NO_PREFETCH = 1, /* each warp loads its current blocks (16-byte loads) */
   PKD_VARIANT_L2_PREFETCH = 2, /* as 1, plus cp.async.bulk.prefetch.L2 of blocks ahead */
-  PKD_VARIANT_TMA_STAGED = 3   /* bulk tensor copies into a shared-memory ring, plus L2 prefetch */
+  PKD_VARIANT_TMA_STAGED = 3,  /* bulk copies into a shared-memory ring, plus L2 prefetch */
+  PKD_VARIANT_TMA_MMA = 4      /* 128-byte-swizzled tensor copies into a shared-memory ring, plus
+                                  L2 prefetch; Q.K^T and P.V on the tensor cores (mma, fp16
+                                  operands, fp32 accumulation; p rounded to fp16 for P.V) */
 } pkd_variant;
 
 /*
@@ -159,6 +162,19 @@ int paged_decode_auto_partition_size(int num_seqs, int num_q_heads, int num_kv_h
  * max and sum [num_seqs][num_q_heads][NP], NP = ceil(max_context_len /
  * partition_size), each region 256-byte aligned.  0 when nothing splits.
  */
+/*
+ * paged_decode_auto_variant -- the variant value (data path ORed with
+ * PKD_FLAG_* bits) that PKD_VARIANT_AUTO runs for this shape, on the current
+ * device, given partition_size as passed to paged_decode_attention_ex (0 =
+ * automatic, -1 = unsplit, or a partition).  It is TMA_STAGED |
+ * PKD_FLAG_L2_EVICT_HINTS, except for group size 1 with at most 512 tokens
+ * per CTA and between 1 and 16 CTAs per SM, where it is NO_PREFETCH (plain
+ * loads: a warp handles too few blocks for the staged ring to pay off).
+ * Returns -2 on an invalid shape or partition size.
+ */
+int paged_decode_auto_variant(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                              int block_size, int max_context_len, int partition_size);
+
 size_t paged_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                                    int block_size, int max_context_len, int partition_size,
                                    int variant);
@@ -208,6 +224,38 @@ pkd_status paged_decode_reduce(const float* tmp_out, const float* max_logits, co
 pkd_status paged_decode_validate_tables(const int32_t* block_tables, const int32_t* context_lens,
                                         int num_seqs, int max_blocks_per_seq, int block_size,
                                         int num_blocks, int* error_word, cudaStream_t stream);
+
+/*
+ * paged_kv_append -- the cache write that precedes each decode step: stores
+ * one new token's K and V rows per sequence into the paged cache, at the
+ * sequence's next logical position.  With L = context_lens[b] (the length
+ * BEFORE the append) and for every kv head g:
+ *   p = block_tables[b][L / block_size]
+ *   K[p][g][L % block_size][:] = k_new[b][g][:]
+ *   V[p][g][L % block_size][:] = v_new[b][g][:]
+ * Source: the CSDN answer "如何优化LLM推理引擎的内存访问延迟？", section 2:
+ * each sequence's KV lives in the pages its page table lists, filled in
+ * logical order.  The caller allocates block_tables[b][L / block_size]
+ * beforehand when L is a multiple of block_size, and raises context_lens[b]
+ * to L + 1 afterwards (the library does neither).
+ *
+ *   k_new, v_new   device fp16 [num_seqs][num_kv_heads][head_dim], 16-byte aligned
+ *   block_tables, context_lens   device int32, layouts as for the decode calls
+ *   k_cache, v_cache   device fp16 [num_blocks][num_kv_heads][block_size][head_dim],
+ *                  16-byte aligned, written in place (only the target rows)
+ *   head_dim       any positive multiple of 8; block_size any positive size
+ *   error_word     device int, nullable: PKD_DEVERR_BAD_BLOCK is ORed in for a
+ *                  sequence with L < 0, L / block_size >= max_blocks_per_seq,
+ *                  or a table entry outside [0, num_blocks); such a sequence
+ *                  is skipped (nothing is written for it).
+ * Every other row of the caches is left untouched, bit for bit.  Two
+ * sequences whose targets coincide (a shared block) race: the caller keeps
+ * appended-to blocks private to one sequence.
+ */
+pkd_status paged_kv_append(const void* k_new, const void* v_new, const int32_t* block_tables,
+                           const int32_t* context_lens, void* k_cache, void* v_cache, int num_seqs,
+                           int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                           int max_blocks_per_seq, int* error_word, cudaStream_t stream);
 
 /*
  * pkd_selftest_bounded_wait -- exercises the failure path of the library's

@@ -1,5 +1,6 @@
 // pkd_api.cu -- the C ABI of libpaged_decode.so (declared in paged_decode.h):
 // argument checks, the split-K policy, workspace layout and launches.
+#include <algorithm>
 #include <cmath>
 #include <cstddef>
 #include <cstdint>
@@ -50,12 +51,34 @@ int sm_count() {
 int variant_path(int variant) { return variant & 0xff; }
 bool variant_ok(int variant) {
   const int path = variant_path(variant);
-  return variant >= 0 && path <= PKD_VARIANT_TMA_STAGED && (variant & ~0xff & ~PKD_FLAG_L2_EVICT_HINTS) == 0;
+  return variant >= 0 && path <= PKD_VARIANT_TMA_MMA && (variant & ~0xff & ~PKD_FLAG_L2_EVICT_HINTS) == 0;
 }
 
 int resolve_variant(int variant) {
   variant = variant_path(variant);
   return variant == PKD_VARIANT_AUTO ? PKD_VARIANT_TMA_STAGED : variant;
+}
+
+// What the automatic variant runs for one launch: the data path and whether
+// the L2 eviction priorities are on.  The staged path with priorities is the
+// fastest wherever a CTA streams a long run of blocks, and when the grid is
+// smaller than the GPU (each CTA's latency is exposed).  One case goes to
+// plain 16-byte loads: group size 1 with at most kShortCtaTokens tokens per
+// CTA and between 1 and kShortCtaMaxWaves CTAs per SM.  There a warp handles
+// only a few blocks, the staged ring's fill time is not paid back, and the
+// batch x context sweep measured the plain loads 6-15% faster (at 4096+ such
+// CTAs the two tie, and beyond that the staged path is ahead again).
+constexpr int kShortCtaTokens = 512;
+constexpr int kShortCtaMaxWaves = 16;
+
+int pick_auto(int variant, int group, long long grid, long long tokens_per_cta) {
+  if (variant_path(variant) != PKD_VARIANT_AUTO) return variant;
+  int sms = sm_count();
+  if (sms <= 0) sms = 148;
+  if (group == 1 && tokens_per_cta <= kShortCtaTokens && grid >= sms &&
+      grid <= (long long)kShortCtaMaxWaves * sms)
+    return PKD_VARIANT_NO_PREFETCH;
+  return PKD_VARIANT_TMA_STAGED | PKD_FLAG_L2_EVICT_HINTS;
 }
 
 // Resident CTAs per SM the kernel of a data path and group size is built for
@@ -115,6 +138,7 @@ pkd_status launch_decode(int variant, int D, int BS, int G, const pkd::DecodePar
     case PKD_VARIANT_NO_PREFETCH: e = pkd::launch_decode_no_prefetch(D, BS, G, p, grid, stream); break;
     case PKD_VARIANT_L2_PREFETCH: e = pkd::launch_decode_l2_prefetch(D, BS, G, p, grid, stream); break;
     case PKD_VARIANT_TMA_STAGED: e = pkd::launch_decode_tma_staged(D, BS, G, p, grid, stream); break;
+    case PKD_VARIANT_TMA_MMA: e = pkd::launch_decode_tma_mma(D, BS, G, p, grid, stream); break;
     default: return PKD_ERR_SHAPE;
   }
   return e == cudaSuccess ? PKD_OK : PKD_ERR_LAUNCH;
@@ -182,6 +206,21 @@ int paged_decode_auto_partition_size(int num_seqs, int num_q_heads, int num_kv_h
   return auto_partition(s, variant);
 }
 
+int paged_decode_auto_variant(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                              int block_size, int max_context_len, int partition_size) {
+  Shape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, 1, 1 << 30, max_context_len};
+  if (check_shape(s) != PKD_OK) return -2;
+  if (partition_size < -1 || (partition_size > 0 && (partition_size % 32 != 0 ||
+                                                     partition_size % block_size != 0)))
+    return -2;
+  int P = partition_size == 0 ? auto_partition(s) : partition_size;
+  const bool split = P > 0 && max_context_len > P;
+  const long long np = split ? (max_context_len + P - 1) / P : 1;
+  const long long tokens = split ? P : (long long)round_up((size_t)(max_context_len > 0 ? max_context_len : 1), 32);
+  return pick_auto(PKD_VARIANT_AUTO, num_q_heads / num_kv_heads, (long long)num_seqs * num_kv_heads * np,
+                   tokens);
+}
+
 size_t paged_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                                    int block_size, int max_context_len, int partition_size,
                                    int variant) {
@@ -247,8 +286,10 @@ pkd_status paged_decode_attention_ex(const void* q, const void* k_cache, const v
   p.mode = 0;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.prefetch_distance = prefetch_distance == 0 ? kDefaultPrefetchDistance : prefetch_distance;
-  // the automatic variant is the staged path with the L2 eviction priorities
-  p.l2_hints = ((variant & PKD_FLAG_L2_EVICT_HINTS) || variant_path(variant) == PKD_VARIANT_AUTO) ? 1 : 0;
+  const int G = num_q_heads / num_kv_heads;
+  const long long grid = (long long)num_seqs * num_kv_heads * np;
+  variant = pick_auto(variant, G, grid, P);
+  p.l2_hints = (variant & PKD_FLAG_L2_EVICT_HINTS) ? 1 : 0;
   p.timeout_ns = kWaitBudgetNs;
   if (split) {
     if (!workspace) return PKD_ERR_WORKSPACE;
@@ -259,9 +300,7 @@ pkd_status paged_decode_attention_ex(const void* q, const void* k_cache, const v
     p.max_logits = w.max_logits;
     p.exp_sums = w.exp_sums;
   }
-  const int G = num_q_heads / num_kv_heads;
-  const long long grid = (long long)num_seqs * num_kv_heads * np;
-  st = launch_decode(resolve_variant(variant), head_dim, block_size, G, p, grid, stream);
+  st = launch_decode(variant_path(variant), head_dim, block_size, G, p, grid, stream);
   if (st != PKD_OK || !split) return st;
   return launch_reduce(p.tmp_out, p.max_logits, p.exp_sums, context_lens, out, num_seqs, num_q_heads,
                        head_dim, P, np, /*min_merge=*/1, stream);
@@ -325,12 +364,12 @@ pkd_status paged_decode_partitions(const void* q, const void* k_cache, const voi
   p.mode = 1;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.prefetch_distance = prefetch_distance == 0 ? kDefaultPrefetchDistance : prefetch_distance;
-  // the automatic variant is the staged path with the L2 eviction priorities
-  p.l2_hints = ((variant & PKD_FLAG_L2_EVICT_HINTS) || variant_path(variant) == PKD_VARIANT_AUTO) ? 1 : 0;
-  p.timeout_ns = kWaitBudgetNs;
   const int G = num_q_heads / num_kv_heads;
   const long long grid = (long long)num_seqs * num_kv_heads * max_num_partitions;
-  return launch_decode(resolve_variant(variant), head_dim, block_size, G, p, grid, stream);
+  variant = pick_auto(variant, G, grid, partition_size);
+  p.l2_hints = (variant & PKD_FLAG_L2_EVICT_HINTS) ? 1 : 0;
+  p.timeout_ns = kWaitBudgetNs;
+  return launch_decode(variant_path(variant), head_dim, block_size, G, p, grid, stream);
 }
 
 pkd_status paged_decode_reduce(const float* tmp_out, const float* max_logits, const float* exp_sums,
@@ -360,6 +399,32 @@ pkd_status paged_decode_validate_tables(const int32_t* block_tables, const int32
   pkd::validate_tables_kernel<<<num_seqs, 128, 0, stream>>>(block_tables, context_lens, num_seqs,
                                                             max_blocks_per_seq, block_size, num_blocks,
                                                             error_word);
+  return cudaGetLastError() == cudaSuccess ? PKD_OK : PKD_ERR_LAUNCH;
+}
+
+pkd_status paged_kv_append(const void* k_new, const void* v_new, const int32_t* block_tables,
+                           const int32_t* context_lens, void* k_cache, void* v_cache, int num_seqs,
+                           int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                           int max_blocks_per_seq, int* error_word, cudaStream_t stream) {
+  if (num_seqs < 0 || num_kv_heads <= 0 || head_dim <= 0 || head_dim % 8 != 0 || block_size <= 0 ||
+      num_blocks <= 0 || max_blocks_per_seq <= 0)
+    return PKD_ERR_SHAPE;
+  if (num_seqs == 0) return PKD_OK;
+  if (!k_new || !v_new || !block_tables || !context_lens || !k_cache || !v_cache) return PKD_ERR_NULL;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(block_tables, 4) || !aligned(context_lens, 4) || (error_word && !aligned(error_word, 4)))
+    return PKD_ERR_ALIGN;
+  const int chunks = head_dim / 8;
+  const long long total = (long long)num_seqs * num_kv_heads * chunks;
+  int sms = 152;
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long want = (total + 255) / 256;
+  const int grid = (int)std::min<long long>(want, (long long)sms * 8);
+  pkd::paged_kv_append_kernel<<<grid, 256, 0, stream>>>(
+      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), block_tables, context_lens,
+      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), num_seqs, num_kv_heads, chunks,
+      block_size, num_blocks, max_blocks_per_seq, error_word);
   return cudaGetLastError() == cudaSuccess ? PKD_OK : PKD_ERR_LAUNCH;
 }
 

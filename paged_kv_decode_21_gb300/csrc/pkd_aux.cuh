@@ -1,4 +1,5 @@
-// pkd_aux.cuh -- the split-K merge kernel and the block-table validator.
+// pkd_aux.cuh -- the split-K merge kernel, the paged KV append kernel and the
+// block-table validator.
 #pragma once
 #include <cstdint>
 #include <cuda_fp16.h>
@@ -53,6 +54,49 @@ __global__ void __launch_bounds__(D) paged_decode_reduce_kernel(
   float o = 0.f;
   for (int jj = 0; jj < np; ++jj) o = fmaf(wsm[jj], to[(size_t)jj * D], o);
   out[(size_t)row * D + d] = __float2half_rn(o * s_invz);
+}
+
+// ---------------------------------------------------------------------------
+// Paged KV append: the new token of sequence b sits at logical position
+// L = context_lens[b], i.e. in physical block block_tables[b][L / BS], slot
+// L % BS, for every kv head.  One thread moves one 16-byte chunk of the K
+// row and the same chunk of the V row; a grid-stride loop covers
+// num_seqs * Hkv * (D / 8) chunks.  Plain write-back stores: the rows are
+// read by the decode step that follows, so they may as well stay in L2.
+// Sequences without room in their table row, or whose entry is outside
+// [0, num_blocks), are skipped and recorded as kErrBadBlock.
+__global__ void __launch_bounds__(256) paged_kv_append_kernel(
+    const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
+    const int32_t* __restrict__ block_tables, const int32_t* __restrict__ context_lens,
+    uint4* __restrict__ k_cache, uint4* __restrict__ v_cache, int num_seqs, int num_kv_heads,
+    int chunks_per_row, int block_size, int num_blocks, int max_blocks_per_seq, int* error_word) {
+  const long long total = (long long)num_seqs * num_kv_heads * chunks_per_row;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const long long row = i / chunks_per_row;  // b * Hkv + g
+    const int c = (int)(i - row * chunks_per_row);
+    const int b = (int)(row / num_kv_heads);
+    const int g = (int)(row - (long long)b * num_kv_heads);
+    // the new rows do not depend on the table walk: load them first so their
+    // latency overlaps the dependent context-length -> block-id loads
+    const uint4 kv = __ldg(k_new + i);
+    const uint4 vv = __ldg(v_new + i);
+    const int L = __ldg(context_lens + b);
+    const int lb = L / block_size;
+    if (L < 0 || lb >= max_blocks_per_seq) {
+      if (g == 0 && c == 0) record_error(error_word, kErrBadBlock);
+      continue;
+    }
+    const int p = __ldg(block_tables + (size_t)b * max_blocks_per_seq + lb);
+    if (p < 0 || p >= num_blocks) {
+      if (g == 0 && c == 0) record_error(error_word, kErrBadBlock);
+      continue;
+    }
+    const size_t dst = (((size_t)p * num_kv_heads + g) * block_size + (L - lb * block_size)) *
+                           (size_t)chunks_per_row + c;
+    k_cache[dst] = kv;
+    v_cache[dst] = vv;
+  }
 }
 
 // ---------------------------------------------------------------------------

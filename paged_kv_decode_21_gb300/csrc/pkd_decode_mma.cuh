@@ -1,0 +1,412 @@
+// pkd_decode_mma.cuh -- decode attention with Q.K^T and P.V on the tensor
+// cores (sm_103a), for the group sizes where the fp32 FMA path runs out of
+// issue slots before HBM runs out of bandwidth.
+//
+// The work split is the one of paged_decode_kernel: one CTA per (sequence b,
+// kv head g, partition j); NW warps take the partition's 16-token sub-tiles
+// in the stride-NW block order of Algorithm 1 of the review "Accelerating LLM
+// Inference Throughput via Asynchronous KV Cache Prefetching" (section 3.4);
+// each warp keeps its own online-softmax state, merged at the end.
+//
+// Staging.  Lane 0 of every warp streams its sub-tiles into a private ring of
+// shared-memory slots with 3-D tensor copies (cp.async.bulk.tensor; the
+// tensor map views a cache as [num_blocks][num_kv_heads * block_size][D]).
+// A box is 16 rows x 64 halves (128 bytes) with the 128-byte swizzle, so the
+// 16-byte chunk j of row r lands at chunk j ^ (r % 8): the eight rows an
+// ldmatrix reads in one phase fall in eight different bank groups.  Tiles
+// beyond the ring are prefetched into L2 (cp.async.bulk.prefetch.L2), the
+// pairing of SRAM staging with L2 prefetch that the blog post "KV Cache
+// Prefetching：三层预取如何隐藏 KV 访问延迟" suggests (section 2.3).
+//
+// Arithmetic per 16-token sub-tile, with mma.m16n8k16 (fp16 operands, fp32
+// accumulators), c = lane % 4 and r = lane / 4:
+//   S  = Q . K^T     M = the group's query heads (padded to 16 rows; rows 8..15
+//                    are zero), N = 8 tokens (two n-tiles), K = 16 dims per
+//                    step.  Q is held as A fragments for the whole CTA; K^T
+//                    comes from ldmatrix (non-transposed) of the K rows.
+//                    Lane (r, c) receives S[head r][tokens 2c, 2c+1, 8+2c, 9+2c].
+//   softmax          fp32, log2 domain, lazy running max per head (the four
+//                    lanes of a head agree through a 2-step butterfly).
+//   O^T += V^T . P^T M = 16 dims per m-tile, N = 8 heads, K = 16 tokens.  V^T
+//                    comes from ldmatrix.trans of the V rows; P^T's B fragment
+//                    is exactly the lane's own four p values packed to fp16
+//                    (tokens 2c, 2c+1 | 8+2c, 9+2c of head r), so no shuffle or
+//                    shared-memory round trip sits between the two products.
+// P is rounded to fp16 for the second product (relative error <= 2^-11 per
+// weight); the normaliser sums the fp32 values.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include "pkd_decode.cuh"
+#include "pkd_ptx.cuh"
+
+namespace pkd {
+
+// ---------------------------------------------------------------- primitives
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// d += A . B for one m16n8k16 tile; A rows 8..15 are zero (a1 = a3 = 0).
+__device__ __forceinline__ void mma_16816_top(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0,
+                                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+
+// d += A . B for one full m16n8k16 tile.
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// 3-D tiled tensor copy of the box at (x, y, z) into shared memory at `dst`,
+// completing its bytes on `bar`; x (innermost, elements) is a multiple of 64.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tmap, uint64_t* bar, int x,
+                                            int y, int z, const L2Hints& h) {
+  if (h.on) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)),
+        "l"(h.evict_first)
+        : "memory");
+  } else {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+  }
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
+// ---------------------------------------------------------------- layout
+template <int D, int BS, int G>
+struct MmaTraits {
+  static_assert(D == 64 || D == 128, "head_dim");
+  static_assert(BS == 16 || BS == 32, "block_size");
+  static_assert(G >= 1 && G <= 8, "group size: the heads fill one 8-wide n-tile");
+  static constexpr int NW = 4;
+  static constexpr int THREADS = NW * 32;
+  static constexpr int MIN_BLOCKS = 2;
+  static constexpr int KSTEPS = D / 16;       // QK k-steps and PV m-tiles
+  static constexpr int NBOX = D / 64;         // 64-column boxes per 16-row sub-tile
+  static constexpr int BOX_BYTES = 16 * 128;  // one swizzled box
+  static constexpr int SUB_BYTES = NBOX * BOX_BYTES;      // K (or V) of one sub-tile
+  static constexpr int SLOT_BYTES = 2 * SUB_BYTES;        // K then V
+  static constexpr int TILE_BYTES = BS * D * 2;           // one (block, head) tile in HBM
+  // about 96 KiB of ring per CTA (two CTAs per SM)
+  static constexpr int SW_RAW = (96 * 1024) / (NW * SLOT_BYTES);
+  static constexpr int SW = SW_RAW > 8 ? 8 : (SW_RAW < 2 ? 2 : SW_RAW);
+  static constexpr int RING_BYTES = NW * SW * SLOT_BYTES;
+  // merge area: m, mt, l as [NW][8] each, then acc [NW][G][D]
+  static constexpr int MRG_ACC_OFF = 3 * NW * 8;  // floats (a multiple of 4)
+  static constexpr int MERGE_BYTES = (MRG_ACC_OFF + NW * G * D) * 4;
+  static constexpr int MAIN_BYTES = RING_BYTES > MERGE_BYTES ? RING_BYTES : MERGE_BYTES;
+  static constexpr int BAR_BYTES = NW * SW * 8;
+  // the swizzle needs 1024-byte aligned boxes: the kernel aligns the base
+  static constexpr int SMEM_BYTES = 1024 + MAIN_BYTES + BAR_BYTES;
+  static_assert(BOX_BYTES % 1024 == 0 && SLOT_BYTES % 1024 == 0, "boxes must stay 1024-byte aligned");
+  static_assert(MAIN_BYTES % 16 == 0, "barriers must stay 8-byte aligned");
+};
+
+// ---------------------------------------------------------------- kernel
+template <int D, int BS, int G>
+__global__ void __launch_bounds__(MmaTraits<D, BS, G>::THREADS, MmaTraits<D, BS, G>::MIN_BLOCKS)
+    paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                            const __grid_constant__ CUtensorMap tmap_v, const DecodeParams P) {
+  using T = MmaTraits<D, BS, G>;
+  constexpr int NW = T::NW, SW = T::SW, KS = T::KSTEPS;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // 1024-byte aligned base for the swizzled boxes
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  unsigned char* smem = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::MAIN_BYTES);
+
+  const int np_grid = P.max_partitions;
+  const int j = blockIdx.x % np_grid;
+  const int bg = blockIdx.x / np_grid;
+  const int g = bg % P.num_kv_heads;
+  const int b = bg / P.num_kv_heads;
+  const int L = P.context_lens[b];
+  const int PS = P.partition_size;
+  const int np_b = (L + PS - 1) / PS;
+  const bool final_out = (P.mode == 0) && np_b <= 1;
+  const int h0 = g * G;
+
+  if (L <= 0) {
+    if (final_out && j == 0) {
+      for (int i = threadIdx.x; i < G * D; i += blockDim.x)
+        P.out[((size_t)b * P.num_q_heads + h0) * D + i] = __float2half_rn(0.f);
+    }
+    return;
+  }
+  if (j >= np_b) return;
+
+  const int t0 = j * PS;
+  const int t1 = min(t0 + PS, L);
+  const int nblk = (t1 - t0 + BS - 1) / BS;
+  const int32_t* bt = P.block_tables + (size_t)b * P.max_blocks_per_seq + t0 / BS;
+  const size_t head_stride = (size_t)BS * D;
+  const size_t block_stride = (size_t)P.num_kv_heads * head_stride;
+  const __half* kbase = P.k_cache + (size_t)g * head_stride;
+  const __half* vbase = P.v_cache + (size_t)g * head_stride;
+  const int pd = P.prefetch_distance;
+  const L2Hints l2h = make_l2_hints(P.l2_hints != 0);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int r = lane / 4;  // head row of S, dim row of O^T
+  const int c = lane % 4;
+
+  // Q as A fragments: qa[k][0] = q[r][16k + 2c .. +2), qa[k][1] = q[r][16k + 8 + 2c .. +2)
+  uint32_t qa[KS][2];
+  {
+    const __half* qr = P.q + ((size_t)b * P.num_q_heads + h0 + r) * D;
+#pragma unroll
+    for (int k = 0; k < KS; ++k) {
+      qa[k][0] = r < G ? *reinterpret_cast<const uint32_t*>(qr + 16 * k + 2 * c) : 0u;
+      qa[k][1] = r < G ? *reinterpret_cast<const uint32_t*>(qr + 16 * k + 8 + 2 * c) : 0u;
+    }
+  }
+  float o[KS][4];  // O^T m-tile k: [dim 16k + r | 16k + 8 + r] x [head 2c | 2c + 1]
+#pragma unroll
+  for (int k = 0; k < KS; ++k) o[k][0] = o[k][1] = o[k][2] = o[k][3] = 0.f;
+  float m = -INFINITY;   // running shift of head r (log2 domain), equal in the head's 4 lanes
+  float mt = -INFINITY;  // exact maximum of this lane's scores
+  float l = 0.f;         // sum of this lane's p values
+
+  // ldmatrix row addresses: lane l addresses row (l & 7) + 8 * (l >> 4) of the
+  // sub-tile, 16-byte chunk 2s + ((l >> 3) & 1) for step s; with the swizzle
+  // the chunk offset of step s is ((2s & 7) ^ x) * 16, x = chunk bit ^ row % 8.
+  uint32_t lm_off[4];
+  {
+    const int row = (lane & 7) + 8 * (lane >> 4);
+    const int x = ((lane >> 3) & 1) ^ (row & 7);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) lm_off[i] = row * 128 + (((2 * i) ^ x) << 4);
+  }
+
+  uint64_t* full = bars + warp * SW;
+  unsigned char* ring = smem + (size_t)warp * SW * T::SLOT_BYTES;
+  if (threadIdx.x == 0) {
+    prefetch_tensormap(&tmap_k);
+    prefetch_tensormap(&tmap_v);
+  }
+  if (lane == 0) {
+    for (int s = 0; s < SW; ++s) mbar_init(&full[s], 1);
+    fence_mbarrier_init();
+  }
+  __syncwarp();
+
+  SubCursor<BS, NW> ic, cc;
+  ic.start(warp);
+  cc.start(warp);
+  auto block_id = [&](int k) { return k < nblk ? bt[k] : -1; };
+  int ic_pb = block_id(ic.k);
+  int pf_k = warp + NW * pd;
+  int pf_pb = pd > 0 ? block_id(pf_k) : -1;
+  uint32_t bad_slots = 0;
+  auto issue_next = [&](int slot) {
+    const bool bad = ic_pb < 0 || ic_pb >= P.num_blocks;
+    bad_slots = bad ? (bad_slots | (1u << slot)) : (bad_slots & ~(1u << slot));
+    if (lane == 0) {
+      if (bad) {
+        record_error(P.error_word, kErrBadBlock);
+        mbar_arrive(&full[slot]);
+      } else {
+        const uint32_t dst = smem_u32(ring + (size_t)slot * T::SLOT_BYTES);
+        const int y = g * BS + ic.rg * 16;
+        mbar_arrive_expect_tx(&full[slot], T::SLOT_BYTES);
+#pragma unroll
+        for (int hb = 0; hb < T::NBOX; ++hb) {
+          tma_load_3d(dst + hb * T::BOX_BYTES, &tmap_k, &full[slot], 64 * hb, y, ic_pb, l2h);
+          tma_load_3d(dst + T::SUB_BYTES + hb * T::BOX_BYTES, &tmap_v, &full[slot], 64 * hb, y, ic_pb, l2h);
+        }
+      }
+    }
+    if (ic.rg == 0 && pd > 0) {
+      if (lane == 0 && pf_pb >= 0 && pf_pb < P.num_blocks) {
+        prefetch_l2_bulk(kbase + (size_t)pf_pb * block_stride, T::TILE_BYTES, l2h);
+        prefetch_l2_bulk(vbase + (size_t)pf_pb * block_stride, T::TILE_BYTES, l2h);
+      }
+      pf_k += NW;
+      pf_pb = block_id(pf_k);
+    }
+    const int k_before = ic.k;
+    ic.advance(t0, t1);
+    if (ic.k != k_before) ic_pb = block_id(ic.k);
+  };
+  int issued = 0;  // sub-tiles issued into the ring so far
+  for (int s = 0; s < SW && ic.live(nblk); ++s, ++issued) issue_next(s);
+
+  int u = 0;
+  for (; cc.live(nblk); ++u) {
+    const int slot = u % SW;
+    const bool bad = (bad_slots >> slot) & 1u;
+    if (!mbar_wait_bounded(&full[slot], (u / SW) & 1, P.timeout_ns)) {
+      if (lane == 0) record_error(P.error_word, kErrTimeout);
+      // let the copies still in flight land (each wait bounded again)
+      for (int v = u + 1; v < issued; ++v) mbar_wait_bounded(&full[v % SW], (v / SW) & 1, P.timeout_ns);
+      break;
+    }
+    if (!bad) {
+      const int valid = min(16, t1 - (t0 + cc.k * BS + cc.rg * 16));
+      unsigned char* kslot = ring + (size_t)slot * T::SLOT_BYTES;
+      const uint32_t ks = smem_u32(kslot);
+      const uint32_t vs = ks + T::SUB_BYTES;
+      if (valid < 16) {
+        // rows past the context may hold anything (NaN included): zero the V
+        // rows so that p = 0 times them stays 0; masked K rows get -inf below
+        for (int i = lane; i < (16 - valid) * T::NBOX * 8; i += 32) {
+          const int row = valid + i / (T::NBOX * 8);
+          const int rest = i % (T::NBOX * 8);
+          *reinterpret_cast<uint4*>(kslot + T::SUB_BYTES + (rest / 8) * T::BOX_BYTES + row * 128 +
+                                    (rest % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();  // ordered before the next tensor copy into this slot
+        __syncwarp();
+      }
+      // ---- S = Q K^T: two n-tiles (tokens 0..7, 8..15)
+      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int k = 0; k < KS; ++k) {
+        uint32_t kb[4];
+        ldsm_x4(ks + (k / 4) * T::BOX_BYTES + lm_off[k % 4], kb);
+        mma_16816_top(s0, qa[k][0], qa[k][1], kb[0], kb[1]);
+        mma_16816_top(s1, qa[k][0], qa[k][1], kb[2], kb[3]);
+      }
+      // ---- online softmax for head r over tokens 2c, 2c+1, 8+2c, 9+2c
+      float sc[4] = {s0[0] * P.scale_log2, s0[1] * P.scale_log2, s1[0] * P.scale_log2,
+                     s1[1] * P.scale_log2};
+      if (valid < 16) {
+        if (2 * c >= valid) sc[0] = -INFINITY;
+        if (2 * c + 1 >= valid) sc[1] = -INFINITY;
+        if (8 + 2 * c >= valid) sc[2] = -INFINITY;
+        if (9 + 2 * c >= valid) sc[3] = -INFINITY;
+      }
+      const float lmax = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+      mt = fmaxf(mt, lmax);
+      if (__any_sync(0xffffffffu, lmax > m + kLazyTau)) {
+        float mx = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float mn = fmaxf(m, mx);
+        const float alpha = (mn == -INFINITY) ? 1.f : ex2_approx(m - mn);
+        l *= alpha;
+        m = mn;
+        // O^T columns are heads 2c, 2c+1, whose shifts live in lanes 8c, 8c+4
+        const float a_lo = __shfl_sync(0xffffffffu, alpha, 8 * c);
+        const float a_hi = __shfl_sync(0xffffffffu, alpha, 8 * c + 4);
+#pragma unroll
+        for (int k = 0; k < KS; ++k) {
+          o[k][0] *= a_lo;
+          o[k][1] *= a_hi;
+          o[k][2] *= a_lo;
+          o[k][3] *= a_hi;
+        }
+      }
+      const float p0 = ex2_approx(sc[0] - m), p1 = ex2_approx(sc[1] - m);
+      const float p2 = ex2_approx(sc[2] - m), p3 = ex2_approx(sc[3] - m);
+      l += (p0 + p1) + (p2 + p3);
+      const uint32_t pb0 = pack_half2(p0, p1);  // P^T[tokens 2c, 2c+1][head r]
+      const uint32_t pb1 = pack_half2(p2, p3);  // P^T[tokens 8+2c, 9+2c][head r]
+      // ---- O^T += V^T P^T, one m-tile of 16 dims per step
+#pragma unroll
+      for (int k = 0; k < KS; ++k) {
+        uint32_t va[4];
+        ldsm_x4_trans(vs + (k / 4) * T::BOX_BYTES + lm_off[k % 4], va);
+        mma_16816(o[k], va, pb0, pb1);
+      }
+    }
+    __syncwarp();
+    if (ic.live(nblk)) {
+      if (lane == 0) fence_proxy_async_smem();  // our reads of the slot precede the next copy into it
+      issue_next(slot);
+      ++issued;
+    }
+    cc.advance(t0, t1);
+  }
+
+  // ------------------------------------------------------------------ merge
+  __syncthreads();  // every warp is done with the ring that the merge area reuses
+  float* mrg = reinterpret_cast<float*>(smem);
+  float* mrg_m = mrg;                  // [NW][8] running shift
+  float* mrg_mt = mrg + NW * 8;        // [NW][8] exact maximum
+  float* mrg_l = mrg + 2 * NW * 8;     // [NW][8]
+  float* mrg_acc = mrg + T::MRG_ACC_OFF;  // [NW][G][D]
+  {
+    float lv = l + __shfl_xor_sync(0xffffffffu, l, 1);
+    lv += __shfl_xor_sync(0xffffffffu, lv, 2);
+    float mx = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    if (c == 0) {
+      mrg_m[warp * 8 + r] = m;
+      mrg_mt[warp * 8 + r] = mx;
+      mrg_l[warp * 8 + r] = lv;
+    }
+    float* acc = mrg_acc + warp * G * D;
+#pragma unroll
+    for (int k = 0; k < KS; ++k) {
+      if (2 * c < G) {
+        acc[(2 * c) * D + 16 * k + r] = o[k][0];
+        acc[(2 * c) * D + 16 * k + 8 + r] = o[k][2];
+      }
+      if (2 * c + 1 < G) {
+        acc[(2 * c + 1) * D + 16 * k + r] = o[k][1];
+        acc[(2 * c + 1) * D + 16 * k + 8 + r] = o[k][3];
+      }
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
+    const int h = i / D, d = i % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, mrg_mt[w * 8 + h]);  // the exact maximum
+    float Z = 0.f, O = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const float mw = mrg_m[w * 8 + h];
+      const float cw = (mw == -INFINITY) ? 0.f : ex2_approx(mw - M);
+      Z = fmaf(cw, mrg_l[w * 8 + h], Z);
+      O = fmaf(cw, mrg_acc[(w * G + h) * D + d], O);
+    }
+    const size_t row = (size_t)b * P.num_q_heads + h0 + h;
+    if (final_out) {
+      P.out[row * D + d] = __float2half_rn(O / Z);
+    } else {
+      const size_t pidx = row * P.max_partitions + j;
+      P.tmp_out[pidx * D + d] = O;
+      if (d == 0) {
+        P.max_logits[pidx] = M * 0.69314718055994530942f;  // log2 units -> natural
+        P.exp_sums[pidx] = Z;
+      }
+    }
+  }
+}
+
+}  // namespace pkd

@@ -21,7 +21,7 @@ PKD_OK = 0
 STATUS_NAMES = {0: "PKD_OK", 1: "PKD_ERR_NULL", 2: "PKD_ERR_SHAPE", 3: "PKD_ERR_UNSUPPORTED",
                 4: "PKD_ERR_ALIGN", 5: "PKD_ERR_WORKSPACE", 6: "PKD_ERR_LAUNCH",
                 7: "PKD_ERR_DEVICE", 8: "PKD_ERR_CUDA"}
-VARIANTS = {"auto": 0, "no_prefetch": 1, "l2_prefetch": 2, "tma_staged": 3}
+VARIANTS = {"auto": 0, "no_prefetch": 1, "l2_prefetch": 2, "tma_staged": 3, "tma_mma": 4}
 DEVERR_BAD_BLOCK = 1
 DEVERR_TIMEOUT = 2
 
@@ -54,6 +54,8 @@ def lib():
         L.paged_decode_attention_ex.restype = I
         L.paged_decode_auto_partition_size.argtypes = [I, I, I, I, I, I, I]
         L.paged_decode_auto_partition_size.restype = I
+        L.paged_decode_auto_variant.argtypes = [I, I, I, I, I, I, I]
+        L.paged_decode_auto_variant.restype = I
         L.paged_decode_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
         L.paged_decode_workspace_size.restype = S
         L.paged_decode_partitions.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, I, I,
@@ -63,6 +65,8 @@ def lib():
         L.paged_decode_reduce.restype = I
         L.paged_decode_validate_tables.argtypes = [P, P, I, I, I, I, P, P]
         L.paged_decode_validate_tables.restype = I
+        L.paged_kv_append.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, P]
+        L.paged_kv_append.restype = I
         L.pkd_selftest_bounded_wait.argtypes = [P, ctypes.c_ulonglong, P]
         L.pkd_selftest_bounded_wait.restype = I
         L.pkd_read_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint), I, P]
@@ -170,6 +174,23 @@ def paged_decode_auto_partition_size(num_seqs, num_q_heads, num_kv_heads, head_d
                                                       block_size, max_context_len, _variant(variant)))
 
 
+def paged_decode_auto_variant(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                              max_context_len, partition_size=0) -> int:
+    """The variant value (path | flags) that "auto" runs for this shape."""
+    v = lib().paged_decode_auto_variant(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                        max_context_len, partition_size)
+    if v < 0:
+        raise PagedDecodeError(2, "paged_decode_auto_variant")
+    return v
+
+
+def variant_name(v: int) -> str:
+    """Name of a variant value, e.g. 'tma_staged+l2_hints'."""
+    names = {n: k for k, n in VARIANTS.items()}
+    base = names[v & 0xff]
+    return base + ("+l2_hints" if v & FLAG_L2_EVICT_HINTS else "")
+
+
 def alloc_workspace(nbytes: int, device) -> Optional[torch.Tensor]:
     """A 256-byte aligned device buffer of at least ``nbytes`` (None for 0)."""
     if nbytes <= 0:
@@ -242,6 +263,30 @@ def paged_decode_validate_tables(block_tables, context_lens, block_size, num_blo
                                             int(block_size), int(num_blocks), _ptr(error_word),
                                             _stream(stream))
     _check(st, "paged_decode_validate_tables")
+
+
+def paged_kv_append(k_new, v_new, block_tables, context_lens, k_cache, v_cache, error_word=None,
+                    stream=None):
+    """Write each sequence's new K/V row ([B][Hkv][D]) into the paged caches,
+    in place, at logical position context_lens[b]."""
+    _want(k_new, "k_new", torch.float16, 3)
+    _want(v_new, "v_new", torch.float16, 3)
+    _want(k_cache, "k_cache", torch.float16, 4)
+    _want(v_cache, "v_cache", torch.float16, 4)
+    _want(block_tables, "block_tables", torch.int32, 2)
+    _want(context_lens, "context_lens", torch.int32, 1)
+    NB, Hkv, BS, D = k_cache.shape
+    B = context_lens.shape[0]
+    if tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("k_cache / v_cache shape mismatch")
+    if tuple(k_new.shape) != (B, Hkv, D) or tuple(v_new.shape) != (B, Hkv, D):
+        raise ValueError("k_new / v_new must be [num_seqs][num_kv_heads][head_dim]")
+    if block_tables.shape[0] != B:
+        raise ValueError("block_tables / context_lens batch mismatch")
+    st = lib().paged_kv_append(_ptr(k_new), _ptr(v_new), _ptr(block_tables), _ptr(context_lens),
+                               _ptr(k_cache), _ptr(v_cache), B, Hkv, D, BS, NB,
+                               block_tables.shape[1], _ptr(error_word), _stream(stream))
+    _check(st, "paged_kv_append")
 
 
 def pkd_read_device_error(error_word, clear=True, stream=None) -> int:

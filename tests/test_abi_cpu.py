@@ -30,7 +30,8 @@ def declared_functions():
 def test_header_declares_entry_points():
     names = declared_functions()
     for n in ["paged_decode_attention", "paged_decode_attention_ex", "paged_decode_reduce",
-              "paged_decode_partitions", "paged_decode_workspace_size", "pkd_status_string"]:
+              "paged_decode_partitions", "paged_decode_workspace_size", "paged_kv_append",
+              "pkd_status_string"]:
         assert n in names
 
 
@@ -73,6 +74,8 @@ def test_shape_checks(L):
 def test_variant_flags(L):
     assert call_ex(L, var=0x100 | 3, D=96) == 3        # flag accepted; fails later on head_dim
     assert call_ex(L, var=0x200 | 3) == 2              # unknown flag bit
+    assert call_ex(L, var=4, D=96) == 3                # the tensor-core path is a known variant
+    assert call_ex(L, var=5) == 2                      # past the last variant
     assert L.paged_decode_workspace_size(2, 8, 2, 128, 16, 100, 32, 0x100 | 2) > 0
 
 
@@ -98,6 +101,38 @@ def test_selftest_argument_checks(L):
     assert L.pkd_selftest_bounded_wait(MISALIGNED, 1000000, None) == 4
     assert L.pkd_selftest_bounded_wait(FAKE, 10, None) == 2           # budget too short
     assert L.pkd_selftest_bounded_wait(FAKE, 10**9, None) == 2        # budget too long
+
+
+def test_append_argument_checks(L):
+    # (k_new, v_new, bt, cl, kc, vc, B, Hkv, D, BS, NB, MB, err, stream); nothing is launched
+    def call(*, ptrs=(FAKE,) * 6, B=2, Hkv=2, D=64, BS=16, NB=4, MB=2, err=None):
+        return L.paged_kv_append(*ptrs, B, Hkv, D, BS, NB, MB, err, None)
+    assert call(B=0) == 0                                      # empty batch: a no-op
+    assert call(ptrs=(FAKE, None, FAKE, FAKE, FAKE, FAKE)) == 1
+    assert call(D=12) == 2                                     # head_dim not a multiple of 8
+    assert call(BS=0) == 2 and call(NB=0) == 2 and call(MB=0) == 2 and call(B=-1) == 2
+    assert call(ptrs=(FAKE, FAKE, FAKE, FAKE, MISALIGNED, FAKE)) == 4
+    assert call(err=MISALIGNED) == 4
+
+
+def test_auto_variant_policy(L):
+    from paged_kv_decode_21_gb300 import ops
+    # no GPU here: the library assumes 148 SMs; the cases sit far from the
+    # thresholds, so they hold for 152 as well
+    av = ops.paged_decode_auto_variant
+    staged = ops.VARIANTS["tma_staged"] | ops.FLAG_L2_EVICT_HINTS
+    plain = ops.VARIANTS["no_prefetch"]
+    assert av(64, 32, 32, 128, 16, 2048) == staged      # long CTAs
+    assert av(64, 32, 32, 128, 16, 512) == plain        # 2048 CTAs of 512 tokens
+    assert av(16, 32, 32, 128, 16, 2048) == plain       # split at 512: 2048 CTAs
+    assert av(256, 32, 32, 128, 16, 512) == staged      # 8192 CTAs: many waves
+    assert av(1, 32, 32, 128, 16, 1024) == staged       # fewer CTAs than SMs
+    assert av(64, 32, 8, 128, 16, 512) == staged        # GQA always staged
+    assert av(64, 32, 32, 128, 16, 512, -1) == plain
+    assert av(64, 32, 32, 128, 16, 4096, 256) == staged  # 16384 CTAs
+    assert ops.variant_name(staged) == "tma_staged+l2_hints"
+    with pytest.raises(ops.PagedDecodeError):
+        av(64, 32, 32, 128, 16, 512, 100)               # partition not a multiple of 32
 
 
 def test_empty_batch_is_a_no_op(L):

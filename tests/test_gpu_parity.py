@@ -17,7 +17,7 @@ from paged_kv_decode_21_gb300 import ops, workloads
 
 pytestmark = pytest.mark.gpu
 
-VARIANTS = ["no_prefetch", "l2_prefetch", "tma_staged"]
+VARIANTS = ["no_prefetch", "l2_prefetch", "tma_staged", "tma_mma"]
 
 
 @pytest.fixture(scope="module", autouse=True)
