@@ -52,6 +52,8 @@ def _load(mutant: int = 0):
         common = [P, P, P, P, P, I, I, I, I, I, I, I, D]
         lib.pkd_oracle_attention.argtypes = common + [P, I, P, I]
         lib.pkd_oracle_attention.restype = I
+        lib.pkd_oracle_attention_multi.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, D, P, I, P, I]
+        lib.pkd_oracle_attention_multi.restype = I
         lib.pkd_oracle_weights.argtypes = common + [I, I, P]
         lib.pkd_oracle_weights.restype = I
         lib.pkd_oracle_partitions.argtypes = common + [I, I, P, P, P]
@@ -123,6 +125,32 @@ def attention(q, k_cache, v_cache, block_tables, context_lens, scale, rows=None,
     rc = lib.pkd_oracle_attention(_ptr(qa), _ptr(ka), _ptr(va), _ptr(bt), _ptr(cl), B, Hq, Hkv, D,
                                   BS, NB, MB, float(scale), rp, nr, _ptr(out), int(threads))
     _check(rc, "attention")
+    return out
+
+
+def attention_multi(q, k_cache, v_cache, block_tables, context_lens, scale, rows=None,
+                    threads=None, mutant: int = 0) -> np.ndarray:
+    """Exact fp64 attention of q_len new tokens per sequence, q [B][q_len][Hq][D]:
+    query jq sits at position L_b - q_len + jq and sees tokens up to and including
+    itself.  ``rows`` ((b*q_len + jq)*Hq + h ids) selects rows; returns
+    [B][q_len][Hq][D] when ``rows`` is None, else [len(rows)][D]."""
+    lib = _load(mutant)
+    qm = _np(q, np.float16)
+    B, QL, Hq, D = qm.shape
+    qa, ka, va, bt, cl, (_, _, Hkv, _, BS, NB, MB) = _problem(qm.reshape(B, QL * Hq, D), k_cache,
+                                                              v_cache, block_tables, context_lens)
+    if threads is None:
+        threads = os.cpu_count() or 1
+    if rows is None:
+        out = np.empty((B, QL, Hq, D), np.float64)
+        rp, nr = None, 0
+    else:
+        ra = _np(rows, np.int32).reshape(-1)
+        out = np.empty((ra.shape[0], D), np.float64)
+        rp, nr = _ptr(ra), ra.shape[0]
+    rc = lib.pkd_oracle_attention_multi(_ptr(qa), _ptr(ka), _ptr(va), _ptr(bt), _ptr(cl), B, QL, Hq, Hkv,
+                                        D, BS, NB, MB, float(scale), rp, nr, _ptr(out), int(threads))
+    _check(rc, "attention_multi")
     return out
 
 

@@ -17,6 +17,15 @@
  *     w_t = exp(s_t - max_u s_u) / sum_u exp(s_u - max_u s_u)
  *     out[b][h][:] = sum_t w_t * v_t
  *
+ * Multi-token queries (pkd_oracle_attention_multi): q and out are
+ * [num_seqs][q_len][num_q_heads][head_dim]; the q_len new tokens are the
+ * last q_len positions of each sequence (already in the cache), and query jq
+ * attends to the tokens t < L_b - q_len + jq + 1, i.e. up to and including
+ * its own position (causal among the new tokens).  A query with no visible
+ * token gets out = 0.  Source: the review's section 7.4 names working
+ * together with speculative decoding as a direction; verifying q_len draft
+ * tokens in one pass is that case.  The causal rule is the plain reading.
+ *
  * Sources:
  *  - Paged KV cache, logical page -> physical page table: CSDN answer
  *    "如何优化LLM推理引擎的内存访问延迟？", section 2 (paged cache and page
@@ -50,7 +59,9 @@
  * spike per position; GQA equal to repeated-KV MHA; the log-sum-exp merge of
  * partitions equal to the unsplit result; partition sums at scale 0 equal to
  * the exact token counts; append-then-attend equal to SDPA over the grown
- * contiguous sequence; and mutation tests that plant mistakes in this
+ * contiguous sequence; multi-token queries equal to SDPA with an explicit
+ * causal mask, independent of tokens after each query's position, and equal
+ * to single-query decode for the last query; and mutation tests that plant mistakes in this
  * file (compile-time PKD_ORACLE_MUTANT) and require some pin to fail.
  */
 #include <math.h>
@@ -102,7 +113,20 @@ typedef struct {
     int num_seqs, num_q_heads, num_kv_heads, head_dim, block_size;
     int num_blocks, max_blocks_per_seq;
     double scale;
+    int q_len;      /* query tokens per sequence (1: single-query decode) */
 } problem_t;
+
+/* Tokens that query jq of sequence b attends to: query jq sits at position
+ * L_b - q_len + jq and sees every token up to and including itself (the
+ * causal rule among the new tokens); with q_len = 1 this is L_b. */
+static int visible(const problem_t *P, int b, int jq)
+{
+    int n = P->context_lens[b] - P->q_len + jq + 1;
+#if PKD_ORACLE_MUTANT == 9      /* planted mistake: a query does not see its own token */
+    if (P->q_len > 1) n -= 1;
+#endif
+    return n > 0 ? n : 0;
+}
 
 /* Address of the K (or V) row of logical token t of sequence b, kv head g.
  * Returns NULL when the block table entry is outside the pool. */
@@ -132,11 +156,12 @@ static int kv_head_of(const problem_t *P, int h)
 #endif
 }
 
-/* Scores s_t for t in [t0, t1) of (b, h).  Returns -1 on a bad block id. */
-static int scores(const problem_t *P, int b, int h, int t0, int t1, double *s)
+/* Scores s_t for t in [t0, t1) of query jq, head h of sequence b.  Returns
+ * -1 on a bad block id. */
+static int scores(const problem_t *P, int b, int jq, int h, int t0, int t1, double *s)
 {
     int g = kv_head_of(P, h);
-    const uint16_t *qv = P->q + ((size_t)b * P->num_q_heads + h) * P->head_dim;
+    const uint16_t *qv = P->q + (((size_t)b * P->q_len + jq) * P->num_q_heads + h) * P->head_dim;
     for (int t = t0; t < t1; ++t) {
         const uint16_t *k = kv_row(P, P->k_cache, b, g, t);
         if (!k) return -1;
@@ -151,15 +176,15 @@ static int scores(const problem_t *P, int b, int h, int t0, int t1, double *s)
     return 0;
 }
 
-/* Softmax weights of (b, h) over [0, L_b) into w[0..L_b).  -1 on bad ids. */
-static int weights(const problem_t *P, int b, int h, double *w)
+/* Softmax weights of (b, jq, h) over its visible tokens into w.  -1 on bad ids. */
+static int weights(const problem_t *P, int b, int jq, int h, double *w)
 {
-    int L = P->context_lens[b];
+    int L = visible(P, b, jq);
 #if PKD_ORACLE_MUTANT == 4      /* planted mistake: last token dropped */
     if (L > 0) L -= 1;
 #endif
     if (L <= 0) return 0;
-    if (scores(P, b, h, 0, L, w)) return -1;
+    if (scores(P, b, jq, h, 0, L, w)) return -1;
     double m = -INFINITY;
     for (int t = 0; t < L; ++t) if (w[t] > m) m = w[t];
     double z = 0.0;
@@ -171,17 +196,17 @@ static int weights(const problem_t *P, int b, int h, double *w)
     return 0;
 }
 
-/* out[0..D) = sum_t w_t v_t for (b, h).  w is scratch of L_b doubles. */
-static int attend_row(const problem_t *P, int b, int h, double *w, double *out)
+/* out[0..D) = sum_t w_t v_t for (b, jq, h).  w is scratch of L_b doubles. */
+static int attend_row(const problem_t *P, int b, int jq, int h, double *w, double *out)
 {
     int D = P->head_dim;
-    int L = P->context_lens[b];
+    int L = visible(P, b, jq);
 #if PKD_ORACLE_MUTANT == 4
     if (L > 0) L -= 1;
 #endif
     for (int d = 0; d < D; ++d) out[d] = 0.0;
     if (L <= 0) return 0;
-    if (weights(P, b, h, w)) return -1;
+    if (weights(P, b, jq, h, w)) return -1;
     int g = kv_head_of(P, h);
     for (int t = 0; t < L; ++t) {
 #if PKD_ORACLE_MUTANT == 6      /* planted mistake: values read from the K cache */
@@ -200,7 +225,7 @@ static int attend_row(const problem_t *P, int b, int h, double *w, double *out)
 /* ---------------------------------------------------------------------- */
 typedef struct {
     const problem_t *P;
-    const int32_t *rows;   /* row ids b*Hq + h, or NULL for all */
+    const int32_t *rows;   /* row ids (b*q_len + jq)*Hq + h, or NULL for all */
     int num_rows;
     double *out;           /* [num_rows][D] */
     int next;              /* work counter (guarded by mu) */
@@ -222,8 +247,10 @@ static void *worker(void *arg)
         pthread_mutex_unlock(&J->mu);
         if (i >= J->num_rows) break;
         int row = J->rows ? J->rows[i] : i;
-        int b = row / P->num_q_heads, h = row % P->num_q_heads;
-        if (attend_row(P, b, h, w, J->out + (size_t)i * P->head_dim)) {
+        int h = row % P->num_q_heads;
+        int bj = row / P->num_q_heads;
+        int b = bj / P->q_len, jq = bj % P->q_len;
+        if (attend_row(P, b, jq, h, w, J->out + (size_t)i * P->head_dim)) {
             pthread_mutex_lock(&J->mu); J->status = -1; pthread_mutex_unlock(&J->mu);
         }
     }
@@ -237,6 +264,7 @@ static int check_problem(const problem_t *P)
     if (P->num_seqs < 0 || P->num_q_heads <= 0 || P->num_kv_heads <= 0 || P->head_dim <= 0 ||
         P->block_size <= 0 || P->max_blocks_per_seq <= 0 || P->num_blocks <= 0) return -3;
     if (P->num_q_heads % P->num_kv_heads) return -3;
+    if (P->q_len < 1) return -3;
     for (int b = 0; b < P->num_seqs; ++b) {
         int L = P->context_lens[b];
         if (L < 0 || L > P->max_blocks_per_seq * P->block_size) return -3;
@@ -250,23 +278,25 @@ static int check_problem(const problem_t *P)
  * Returns 0; -1 if a used block-table entry is outside [0, num_blocks);
  * -2 on allocation failure; -3 on a bad argument.
  */
-int pkd_oracle_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
-                         const int32_t *block_tables, const int32_t *context_lens,
-                         int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-                         int block_size, int num_blocks, int max_blocks_per_seq, double scale,
-                         const int32_t *rows, int num_rows, double *out, int num_threads)
+int pkd_oracle_attention_multi(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                               const int32_t *block_tables, const int32_t *context_lens,
+                               int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
+                               int head_dim, int block_size, int num_blocks, int max_blocks_per_seq,
+                               double scale, const int32_t *rows, int num_rows, double *out,
+                               int num_threads)
 {
     pthread_once(&g_table_once, build_half_table);
     problem_t P = {q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads,
-                   num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, scale};
+                   num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, scale, q_len};
     int rc = check_problem(&P);
     if (rc) return rc;
     job_t J;
+    const int total = num_seqs * q_len * num_q_heads;
     J.P = &P; J.rows = rows; J.out = out; J.next = 0; J.status = 0;
-    J.num_rows = rows ? num_rows : num_seqs * num_q_heads;
+    J.num_rows = rows ? num_rows : total;
     if (rows) {
         for (int i = 0; i < num_rows; ++i)
-            if (rows[i] < 0 || rows[i] >= num_seqs * num_q_heads) return -3;
+            if (rows[i] < 0 || rows[i] >= total) return -3;
     }
     pthread_mutex_init(&J.mu, NULL);
     if (num_threads < 1) num_threads = 1;
@@ -285,6 +315,18 @@ int pkd_oracle_attention(const uint16_t *q, const uint16_t *k_cache, const uint1
     return J.status;
 }
 
+/* Single-query decode (q_len = 1): rows b * num_q_heads + h. */
+int pkd_oracle_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                         const int32_t *block_tables, const int32_t *context_lens,
+                         int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                         int block_size, int num_blocks, int max_blocks_per_seq, double scale,
+                         const int32_t *rows, int num_rows, double *out, int num_threads)
+{
+    return pkd_oracle_attention_multi(q, k_cache, v_cache, block_tables, context_lens, num_seqs, 1,
+                                      num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                                      max_blocks_per_seq, scale, rows, num_rows, out, num_threads);
+}
+
 /* Softmax weights w[0..L_b) of one row (b, h).  Same return codes. */
 int pkd_oracle_weights(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
                        const int32_t *block_tables, const int32_t *context_lens,
@@ -294,11 +336,11 @@ int pkd_oracle_weights(const uint16_t *q, const uint16_t *k_cache, const uint16_
 {
     pthread_once(&g_table_once, build_half_table);
     problem_t P = {q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads,
-                   num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, scale};
+                   num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, scale, 1};
     int rc = check_problem(&P);
     if (rc) return rc;
     if (b < 0 || b >= num_seqs || h < 0 || h >= num_q_heads) return -3;
-    return weights(&P, b, h, w);
+    return weights(&P, b, 0, h, w);
 }
 
 /*
@@ -319,7 +361,7 @@ int pkd_oracle_partitions(const uint16_t *q, const uint16_t *k_cache, const uint
 {
     pthread_once(&g_table_once, build_half_table);
     problem_t P = {q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads,
-                   num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, scale};
+                   num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, scale, 1};
     int rc = check_problem(&P);
     if (rc) return rc;
     if (partition_size <= 0 || max_partitions <= 0) return -3;
@@ -342,7 +384,7 @@ int pkd_oracle_partitions(const uint16_t *q, const uint16_t *k_cache, const uint
 #endif
                 if (t1 > L) t1 = L;
                 if (t0 >= t1) { m_out[idx] = -INFINITY; l_out[idx] = 0.0; continue; }
-                if (scores(&P, b, h, t0, t1, s)) { free(s); return -1; }
+                if (scores(&P, b, 0, h, t0, t1, s)) { free(s); return -1; }
                 double m = -INFINITY;
                 for (int t = t0; t < t1; ++t) if (s[t - t0] > m) m = s[t - t0];
                 double l = 0.0;

@@ -290,11 +290,87 @@ def pin_append_changes_one_row_per_head(mutant=0):
     assert np.array_equal(vc[~changed], pr["v"][~changed])
 
 
+def multi_problem(seed, lens, q_len, Hq, Hkv, D, BS):
+    pr = scatter_problem(seed, lens, Hq, Hkv, D, BS)
+    rng = np.random.default_rng(seed + 1)
+    pr["qm"] = rng.standard_normal((len(lens), q_len, Hq, D)).astype(np.float16)
+    return pr
+
+
+def causal_sdpa_reference(pr, scale, Hq, Hkv):
+    """SDPA in fp64 with an explicit boolean mask: query jq of a sequence of
+    length L sits at position L - q_len + jq and sees keys t <= that position;
+    rows that see no key are zero."""
+    G = Hq // Hkv
+    B, QL, _, D = pr["qm"].shape
+    out = np.zeros((B, QL, Hq, D))
+    for b, L in enumerate(pr["cl"]):
+        L = int(L)
+        if L == 0:
+            continue
+        q = torch.from_numpy(pr["qm"][b].astype(np.float64)).permute(1, 0, 2).reshape(1, Hq, QL, D)
+        k = torch.from_numpy(pr["lk"][b].astype(np.float64)).repeat_interleave(G, 0).view(1, Hq, L, D)
+        v = torch.from_numpy(pr["lv"][b].astype(np.float64)).repeat_interleave(G, 0).view(1, Hq, L, D)
+        pos = torch.arange(QL).view(QL, 1) + (L - QL)
+        mask = torch.arange(L).view(1, L) <= pos
+        o = torch.nn.functional.scaled_dot_product_attention(q, k, v, attn_mask=mask, scale=scale)
+        o = o.view(Hq, QL, D).permute(1, 0, 2).numpy()
+        seen = mask.any(dim=1).numpy()
+        out[b][seen] = o[seen]
+    return out
+
+
+def pin_multi_query_causal_sdpa(mutant=0):
+    for seed, (lens, q_len, Hq, Hkv, D, BS) in enumerate([
+        ((37, 100, 4), 4, 8, 2, 32, 16),
+        ((16, 17, 9), 7, 7, 1, 16, 8),
+        ((2, 30), 4, 4, 4, 8, 4),          # the first sequence is shorter than q_len
+        ((50,), 2, 6, 3, 16, 16),
+    ]):
+        pr = multi_problem(600 + seed, list(lens), q_len, Hq, Hkv, D, BS)
+        scale = 1.0 / math.sqrt(D)
+        got = oracle.attention_multi(pr["qm"], pr["k"], pr["v"], pr["bt"], pr["cl"], scale, mutant=mutant)
+        ref = causal_sdpa_reference(pr, scale, Hq, Hkv)
+        assert np.max(np.abs(got - ref)) <= TOL * max(1.0, np.max(np.abs(ref)))
+
+
+def pin_multi_query_ignores_the_future(mutant=0):
+    # query jq's output cannot depend on tokens after its position; the next
+    # query (which sees one more token) does
+    lens, q_len, Hq, Hkv, D, BS = [40], 5, 4, 2, 16, 8
+    base = multi_problem(700, lens, q_len, Hq, Hkv, D, BS)
+    scale = 0.3
+    a = oracle.attention_multi(base["qm"], base["k"], base["v"], base["bt"], base["cl"], scale, mutant=mutant)
+    L = lens[0]
+    for jq in range(q_len - 1):
+        pos = L - q_len + jq
+        lk = [base["lk"][0].copy()]
+        lv = [base["lv"][0].copy()]
+        lk[0][:, pos + 1:, :] = np.float16(3.0)
+        lv[0][:, pos + 1:, :] = np.float16(-2.0)
+        other = scatter_problem(700, lens, Hq, Hkv, D, BS, logical_k=lk, logical_v=lv, q=base["q"])
+        b = oracle.attention_multi(base["qm"], other["k"], other["v"], other["bt"], other["cl"], scale,
+                                   mutant=mutant)
+        assert np.array_equal(a[0, : jq + 1], b[0, : jq + 1])
+        assert not np.allclose(a[0, jq + 1], b[0, jq + 1])
+
+
+def pin_multi_query_last_is_single_query(mutant=0):
+    # the last new token sees the whole context: plain decode of that query
+    lens, q_len, Hq, Hkv, D, BS = [33, 64, 5], 3, 6, 2, 16, 16
+    pr = multi_problem(800, lens, q_len, Hq, Hkv, D, BS)
+    got = oracle.attention_multi(pr["qm"], pr["k"], pr["v"], pr["bt"], pr["cl"], 0.25, mutant=mutant)
+    single = oracle.attention(np.ascontiguousarray(pr["qm"][:, -1]), pr["k"], pr["v"], pr["bt"], pr["cl"],
+                              0.25, mutant=mutant)
+    assert np.array_equal(got[:, -1], single)
+
+
 PINS = [pin_half_decoder, pin_sdpa_contiguous, pin_permutation_invariance, pin_weights_sum_to_one,
         pin_identical_keys_mean_of_v, pin_scale_zero_mean_of_v, pin_single_token,
         pin_spike_every_position, pin_gqa_equals_repeated_mha, pin_context_zero,
         pin_nan_poison_ignored, pin_partition_merge, pin_partition_counts_scale_zero,
-        pin_partition_max_is_max_score, pin_append_then_attend, pin_append_changes_one_row_per_head]
+        pin_partition_max_is_max_score, pin_append_then_attend, pin_append_changes_one_row_per_head,
+        pin_multi_query_causal_sdpa, pin_multi_query_ignores_the_future, pin_multi_query_last_is_single_query]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -332,7 +408,7 @@ def test_bad_block_id_is_reported():
         run(pr, 0.3)
 
 
-MUTANTS = list(range(1, 9))
+MUTANTS = list(range(1, 10))
 
 
 @pytest.mark.parametrize("mutant", MUTANTS)
