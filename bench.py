@@ -38,7 +38,8 @@ METRIC = "paged decode-attention achieved HBM GB/s (% of GB300 peak); μs per ca
 DEFAULT_CONFIG = "llama2_7b_mha"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["paged_kv_decode_21_gb300/csrc/pkd_decode.cuh", "paged_kv_decode_21_gb300/csrc/pkd_decode_ws.cuh",
-                  "paged_kv_decode_21_gb300/csrc/pkd_ptx.cuh", "paged_kv_decode_21_gb300/csrc/pkd_launch.cuh"]
+                  "paged_kv_decode_21_gb300/csrc/pkd_decode_mma.cuh", "paged_kv_decode_21_gb300/csrc/pkd_ptx.cuh",
+                  "paged_kv_decode_21_gb300/csrc/pkd_launch.cuh", "paged_kv_decode_21_gb300/csrc/pkd_inst_tma_mma.cu"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 
 
@@ -68,6 +69,17 @@ def kernel_hash() -> str:
         with open(os.path.join(ROOT, p), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
+
+
+def kernel_name(cfg: workloads.DecodeConfig, variant: str) -> str:
+    """The decode kernel a resolved variant launches for a shape."""
+    path = variant.split("+")[0]
+    shape = f"{cfg.head_dim},{cfg.block_size},{cfg.group}"
+    if path == "tma_mma":
+        return f"paged_decode_mma_kernel<{shape}>"
+    if path == "tma_staged" and cfg.group >= 6:
+        return f"paged_decode_ws_kernel<{shape}>"
+    return f"paged_decode_kernel<{shape},{variant}>"
 
 
 def ncu_traffic(workload: str, variant: str):
@@ -187,6 +199,24 @@ def time_gpu(args, cfg, variant, dev, inp, steps, warmup, with_e2e=True, with_cl
                                       max_context_len=inp.max_context_len, partition_size=P,
                                       variant=variant, prefetch_distance=args.prefetch_distance,
                                       workspace=ws, error_word=ew, stream=stream)
+
+    q_len = getattr(args, "q_len", 1)
+    if q_len > 1:
+        # q_len new tokens per sequence (causal among them): the K/V stream is
+        # the same, q and out grow by q_len
+        g = torch.Generator(device=dev).manual_seed(cfg.seed + 5)
+        qm = workloads.randn_f16((inp.num_seqs, q_len, inp.num_q_heads, inp.head_dim), g, dev)
+        out = torch.empty_like(qm)
+        algo += (q_len - 1) * 2 * inp.num_seqs * inp.num_q_heads * inp.head_dim * 2
+        need = ops.paged_decode_multi_workspace_size(inp.num_seqs, q_len, inp.num_q_heads, inp.num_kv_heads,
+                                                     inp.head_dim, inp.block_size, inp.max_context_len, P)
+        ws = ops.alloc_workspace(need, dev)
+
+        def call():  # noqa: F811
+            ops.paged_decode_attention_multi(qm, inp.k_cache, inp.v_cache, inp.block_tables,
+                                             inp.context_lens, inp.scale, out=out,
+                                             max_context_len=inp.max_context_len, partition_size=P,
+                                             workspace=ws, error_word=ew, stream=stream)
 
     for _ in range(warmup):
         flush.zero_()
@@ -396,6 +426,7 @@ def main():
                     help="batch x context grid on the MHA shape: each data path's speed over NO_PREFETCH")
     ap.add_argument("--fig4-config", default=DEFAULT_CONFIG,
                     help="workload whose head shape the grid uses (batch and context are swept)")
+    ap.add_argument("--fig4-variants", default="no_prefetch,l2_prefetch,tma_staged,tma_mma,auto")
     ap.add_argument("--fig4-batches", default="1,4,16,64,128,256")
     ap.add_argument("--fig4-contexts", default="512,1024,2048,4096,8192")
     ap.add_argument("--append", action="store_true",
@@ -403,6 +434,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch (profiling runs)")
+    ap.add_argument("--q-len", type=int, default=1,
+                    help="query tokens per sequence (> 1: multi-token queries, causal among them)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -434,7 +467,8 @@ def main():
                                           partition_size=0)
                 inp = workloads.make_inputs(cfg, device=dev)
                 res = {}
-                for variant in ("no_prefetch", "l2_prefetch", "tma_staged", "auto"):
+                for variant in ["no_prefetch"] + [v for v in args.fig4_variants.split(",")
+                                                  if v and v != "no_prefetch"]:
                     args.partition_size = None
                     r = time_gpu(args, cfg, variant, dev, inp, min(args.steps, 50), args.warmup,
                                  with_e2e=False, with_clocks=False)
@@ -492,7 +526,9 @@ def main():
     mean_ms, value = aggregate_over_ranks(r["mean_ms"], r["algo_bytes"], ws, dev)
     achieved = r["algo_bytes"] / (r["mean_ms"] * 1e-3) / 1e9
     resolved = variant
-    if variant == "auto":
+    if args.q_len > 1:
+        resolved = "tma_mma"
+    elif variant == "auto":
         resolved = ops.variant_name(ops.paged_decode_auto_variant(
             cfg.num_seqs, cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim, cfg.block_size,
             inp.max_context_len, r["partition_size"]))
@@ -500,7 +536,8 @@ def main():
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(mean_ms, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16 in, f32 arithmetic", "data": "synthetic",
-        "config": {"workload": describe(cfg), "variant": resolved,
+        "config": {"workload": describe(cfg) + (f", q_len={args.q_len} (causal)" if args.q_len > 1 else ""),
+                   "variant": resolved,
                    "partition_size": r["partition_size"],
                    "us_per_call": round(mean_ms * 1e3, 2), "us_per_call_median": round(r["median_ms"] * 1e3, 2),
                    "us_per_call_min": round(r["min_ms"] * 1e3, 2),
@@ -510,7 +547,7 @@ def main():
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "traffic": ncu_traffic(cfg.name, resolved),
-                     "kernel": f"paged_decode_kernel<{cfg.head_dim},{cfg.block_size},{cfg.group},{resolved}>"},
+                     "kernel": kernel_name(cfg, resolved)},
         "gpu_launches": r["launches_per_call"] * args.steps,
         "clocks": r["clocks"],
         "e2e": r.get("e2e"),

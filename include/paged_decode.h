@@ -166,10 +166,10 @@ int paged_decode_auto_partition_size(int num_seqs, int num_q_heads, int num_kv_h
  * paged_decode_auto_variant -- the variant value (data path ORed with
  * PKD_FLAG_* bits) that PKD_VARIANT_AUTO runs for this shape, on the current
  * device, given partition_size as passed to paged_decode_attention_ex (0 =
- * automatic, -1 = unsplit, or a partition).  It is TMA_STAGED |
- * PKD_FLAG_L2_EVICT_HINTS, except for group size 1 with at most 512 tokens
- * per CTA and between 1 and 16 CTAs per SM, where it is NO_PREFETCH (plain
- * loads: a warp handles too few blocks for the staged ring to pay off).
+ * automatic, -1 = unsplit, or a partition).  It is TMA_MMA, except for group
+ * size 1 with at most 512 tokens per CTA and between 1 and 16 CTAs per SM,
+ * where it is NO_PREFETCH (plain loads: a warp handles too few blocks for a
+ * shared-memory ring to pay off).
  * Returns -2 on an invalid shape or partition size.
  */
 int paged_decode_auto_variant(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
@@ -224,6 +224,41 @@ pkd_status paged_decode_reduce(const float* tmp_out, const float* max_logits, co
 pkd_status paged_decode_validate_tables(const int32_t* block_tables, const int32_t* context_lens,
                                         int num_seqs, int max_blocks_per_seq, int block_size,
                                         int num_blocks, int* error_word, cudaStream_t stream);
+
+/*
+ * paged_decode_attention_multi -- decode of q_len > 1 new tokens per
+ * sequence at once (verifying q_len draft tokens of speculative decoding in
+ * one pass; the review "Accelerating LLM Inference Throughput via
+ * Asynchronous KV Cache Prefetching", section 7.4, names working together
+ * with speculative decoding as a direction).  The q_len new tokens are the
+ * last q_len positions of each sequence and are already in the cache
+ * (paged_kv_append, or the caller's own write); query jq of sequence b sits
+ * at position L_b - q_len + jq and attends to every token up to and including
+ * its own position:
+ *   out[b][jq][h][:] = sum_{t <= L_b - q_len + jq} softmax(s)_t * V[..t..]
+ * A query that sees no token (L_b - q_len + jq < 0) gets out = 0.
+ *
+ *   q, out         device fp16 [num_seqs][q_len][num_q_heads][head_dim]
+ *   q_len          >= 1 (1 gives single-query decode)
+ *   other arguments as for paged_decode_attention_ex; context_lens[b] counts
+ *   the new tokens.  Runs the tensor-core path (PKD_VARIANT_TMA_MMA): each
+ *   CTA serves 16 / G query tokens of one (sequence, kv head, partition), so
+ *   every K/V tile is read once per group of 16 / G query tokens.
+ *   workspace      required when the context is split
+ *                  (paged_decode_multi_workspace_size bytes, 256-byte aligned)
+ */
+pkd_status paged_decode_attention_multi(const void* q, const void* k_cache, const void* v_cache,
+                                        const int32_t* block_tables, const int32_t* context_lens,
+                                        void* out, int num_seqs, int q_len, int num_q_heads,
+                                        int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                        int max_blocks_per_seq, int max_context_len, float scale,
+                                        int partition_size, void* workspace, size_t workspace_bytes,
+                                        int* error_word, cudaStream_t stream);
+
+/* Workspace bytes paged_decode_attention_multi needs (0 = none). */
+size_t paged_decode_multi_workspace_size(int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
+                                         int head_dim, int block_size, int max_context_len,
+                                         int partition_size);
 
 /*
  * paged_kv_append -- the cache write that precedes each decode step: stores

@@ -56,18 +56,21 @@ bool variant_ok(int variant) {
 
 int resolve_variant(int variant) {
   variant = variant_path(variant);
-  return variant == PKD_VARIANT_AUTO ? PKD_VARIANT_TMA_STAGED : variant;
+  return variant == PKD_VARIANT_AUTO ? PKD_VARIANT_TMA_MMA : variant;
 }
 
 // What the automatic variant runs for one launch: the data path and whether
-// the L2 eviction priorities are on.  The staged path with priorities is the
-// fastest wherever a CTA streams a long run of blocks, and when the grid is
-// smaller than the GPU (each CTA's latency is exposed).  One case goes to
+// the L2 eviction priorities are on.  The tensor-core path (swizzled tensor
+// copies into a ring, mma for both products) is the fastest wherever a CTA
+// streams a long run of blocks, at every group size, and when the grid is
+// smaller than the GPU (each CTA's latency is exposed); the eviction
+// priorities measured neutral on it, so they stay off.  One case goes to
 // plain 16-byte loads: group size 1 with at most kShortCtaTokens tokens per
 // CTA and between 1 and kShortCtaMaxWaves CTAs per SM.  There a warp handles
-// only a few blocks, the staged ring's fill time is not paid back, and the
-// batch x context sweep measured the plain loads 6-15% faster (at 4096+ such
-// CTAs the two tie, and beyond that the staged path is ahead again).
+// only a few blocks, a ring's fill time is not paid back, and the batch x
+// context sweep measured the plain loads 5-15% faster (at 4096+ such CTAs
+// they tie, and beyond that the ring is ahead again).  At group sizes >= 2
+// the tensor-core path wins even there: the plain-load path is issue-bound.
 constexpr int kShortCtaTokens = 512;
 constexpr int kShortCtaMaxWaves = 16;
 
@@ -78,7 +81,7 @@ int pick_auto(int variant, int group, long long grid, long long tokens_per_cta) 
   if (group == 1 && tokens_per_cta <= kShortCtaTokens && grid >= sms &&
       grid <= (long long)kShortCtaMaxWaves * sms)
     return PKD_VARIANT_NO_PREFETCH;
-  return PKD_VARIANT_TMA_STAGED | PKD_FLAG_L2_EVICT_HINTS;
+  return PKD_VARIANT_TMA_MMA;
 }
 
 // Resident CTAs per SM the kernel of a data path and group size is built for
@@ -93,8 +96,8 @@ int ctas_per_sm(int variant, int group) {
 // power of two (at most kMaxAutoPartition, at least kMinAutoPartition tokens)
 // that yields enough CTAs.  Powers of two keep partition boundaries aligned
 // with the blocks of every sequence.
-int auto_partition(const Shape& s, int variant = PKD_VARIANT_AUTO) {
-  const long long units = (long long)s.num_seqs * s.num_kv_heads;
+int auto_partition(const Shape& s, int variant = PKD_VARIANT_AUTO, int q_chunks = 1) {
+  const long long units = (long long)s.num_seqs * s.num_kv_heads * q_chunks;
   if (units <= 0 || s.max_context_len <= kMinAutoPartition) return -1;
   int sms = sm_count();
   if (sms <= 0) sms = 148;
@@ -233,18 +236,30 @@ size_t paged_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_hea
   return layout(nullptr, num_seqs, num_q_heads, head_dim, np).bytes;
 }
 
-pkd_status paged_decode_attention_ex(const void* q, const void* k_cache, const void* v_cache,
-                                     const int32_t* block_tables, const int32_t* context_lens,
-                                     void* out, int num_seqs, int num_q_heads, int num_kv_heads,
-                                     int head_dim, int block_size, int num_blocks,
-                                     int max_blocks_per_seq, int max_context_len, float scale,
-                                     int partition_size, int variant, int prefetch_distance,
-                                     void* workspace, size_t workspace_bytes, int* error_word,
-                                     cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Query chunks per (sequence, kv head) of q_len query tokens: the
+// multi-token kernel serves 16 / G query tokens per CTA.
+int query_chunks(int q_len, int G) {
+  if (q_len <= 1) return 1;
+  const int qc = 16 / G;
+  return (q_len + qc - 1) / qc;
+}
+
+// Decode of q_len query tokens per sequence (q_len = 1: single-query decode).
+pkd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, const int32_t* context_lens, void* out, int num_seqs,
+                       int q_len, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                       int num_blocks, int max_blocks_per_seq, int max_context_len, float scale,
+                       int partition_size, int variant, int prefetch_distance, void* workspace,
+                       size_t workspace_bytes, int* error_word, cudaStream_t stream) {
   Shape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq,
           max_context_len};
   pkd_status st = check_shape(s);
   if (st != PKD_OK) return st;
+  if (q_len < 1) return PKD_ERR_SHAPE;
   if (num_seqs == 0) return PKD_OK;
   st = check_inputs(q, k_cache, v_cache, block_tables, context_lens);
   if (st != PKD_OK) return st;
@@ -253,9 +268,17 @@ pkd_status paged_decode_attention_ex(const void* q, const void* k_cache, const v
   if (!std::isfinite(scale)) return PKD_ERR_SHAPE;
   if (!variant_ok(variant)) return PKD_ERR_SHAPE;
   if (prefetch_distance < 0) return PKD_ERR_SHAPE;
+  const int G = num_q_heads / num_kv_heads;
+  const int q_chunks = query_chunks(q_len, G);
+  if (q_len > 1) {
+    // several query tokens per sequence: the tensor-core path only
+    const int path = variant_path(variant);
+    if (path != PKD_VARIANT_AUTO && path != PKD_VARIANT_TMA_MMA) return PKD_ERR_UNSUPPORTED;
+    variant = PKD_VARIANT_TMA_MMA | (variant & PKD_FLAG_L2_EVICT_HINTS);
+  }
   int P;
   if (partition_size == 0) {
-    P = auto_partition(s, variant);
+    P = auto_partition(s, variant, q_chunks);
   } else if (partition_size == -1) {
     P = -1;
   } else {
@@ -284,17 +307,19 @@ pkd_status paged_decode_attention_ex(const void* q, const void* k_cache, const v
   p.partition_size = P;
   p.max_partitions = np;
   p.mode = 0;
+  p.q_len = q_len;
+  p.q_chunks = q_chunks;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.prefetch_distance = prefetch_distance == 0 ? kDefaultPrefetchDistance : prefetch_distance;
-  const int G = num_q_heads / num_kv_heads;
-  const long long grid = (long long)num_seqs * num_kv_heads * np;
+  const long long grid = (long long)num_seqs * num_kv_heads * q_chunks * np;
   variant = pick_auto(variant, G, grid, P);
   p.l2_hints = (variant & PKD_FLAG_L2_EVICT_HINTS) ? 1 : 0;
   p.timeout_ns = kWaitBudgetNs;
   if (split) {
+    // partial rows are (sequence, query token, head)
     if (!workspace) return PKD_ERR_WORKSPACE;
     if (!aligned(workspace, 256)) return PKD_ERR_ALIGN;
-    Workspace w = layout(workspace, num_seqs, num_q_heads, head_dim, np);
+    Workspace w = layout(workspace, num_seqs * q_len, num_q_heads, head_dim, np);
     if (workspace_bytes < w.bytes) return PKD_ERR_WORKSPACE;
     p.tmp_out = w.tmp_out;
     p.max_logits = w.max_logits;
@@ -302,8 +327,52 @@ pkd_status paged_decode_attention_ex(const void* q, const void* k_cache, const v
   }
   st = launch_decode(variant_path(variant), head_dim, block_size, G, p, grid, stream);
   if (st != PKD_OK || !split) return st;
-  return launch_reduce(p.tmp_out, p.max_logits, p.exp_sums, context_lens, out, num_seqs, num_q_heads,
+  // the merge sees q_len * Hq rows per sequence
+  return launch_reduce(p.tmp_out, p.max_logits, p.exp_sums, context_lens, out, num_seqs, q_len * num_q_heads,
                        head_dim, P, np, /*min_merge=*/1, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+pkd_status paged_decode_attention_ex(const void* q, const void* k_cache, const void* v_cache,
+                                     const int32_t* block_tables, const int32_t* context_lens,
+                                     void* out, int num_seqs, int num_q_heads, int num_kv_heads,
+                                     int head_dim, int block_size, int num_blocks,
+                                     int max_blocks_per_seq, int max_context_len, float scale,
+                                     int partition_size, int variant, int prefetch_distance,
+                                     void* workspace, size_t workspace_bytes, int* error_word,
+                                     cudaStream_t stream) {
+  return decode_impl(q, k_cache, v_cache, block_tables, context_lens, out, num_seqs, 1, num_q_heads,
+                     num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, max_context_len,
+                     scale, partition_size, variant, prefetch_distance, workspace, workspace_bytes,
+                     error_word, stream);
+}
+
+pkd_status paged_decode_attention_multi(const void* q, const void* k_cache, const void* v_cache,
+                                        const int32_t* block_tables, const int32_t* context_lens,
+                                        void* out, int num_seqs, int q_len, int num_q_heads,
+                                        int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                        int max_blocks_per_seq, int max_context_len, float scale,
+                                        int partition_size, void* workspace, size_t workspace_bytes,
+                                        int* error_word, cudaStream_t stream) {
+  return decode_impl(q, k_cache, v_cache, block_tables, context_lens, out, num_seqs, q_len, num_q_heads,
+                     num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, max_context_len,
+                     scale, partition_size, PKD_VARIANT_TMA_MMA, 0, workspace, workspace_bytes,
+                     error_word, stream);
+}
+
+size_t paged_decode_multi_workspace_size(int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
+                                         int head_dim, int block_size, int max_context_len,
+                                         int partition_size) {
+  Shape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, 1, 1 << 30, max_context_len};
+  if (check_shape(s) != PKD_OK || q_len < 1) return 0;
+  const int qch = query_chunks(q_len, num_q_heads / num_kv_heads);
+  int P = partition_size == 0 ? auto_partition(s, PKD_VARIANT_TMA_MMA, qch) : partition_size;
+  if (P <= 0 || max_context_len <= P) return 0;
+  const int np = (max_context_len + P - 1) / P;
+  return layout(nullptr, num_seqs * q_len, num_q_heads, head_dim, np).bytes;
 }
 
 pkd_status paged_decode_attention(const void* q, const void* k_cache, const void* v_cache,
@@ -362,6 +431,8 @@ pkd_status paged_decode_partitions(const void* q, const void* k_cache, const voi
   p.partition_size = partition_size;
   p.max_partitions = max_num_partitions;
   p.mode = 1;
+  p.q_len = 1;
+  p.q_chunks = 1;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.prefetch_distance = prefetch_distance == 0 ? kDefaultPrefetchDistance : prefetch_distance;
   const int G = num_q_heads / num_kv_heads;

@@ -38,7 +38,7 @@ __global__ void __launch_bounds__(D) paged_decode_reduce_kernel(
     for (int msk = 16; msk > 0; msk >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, msk));
     float Z = 0.f;
     for (int jj = threadIdx.x; jj < np; jj += 32) {
-      const float w = __expf(ml[jj] - M);
+      const float w = ml[jj] == -INFINITY ? 0.f : __expf(ml[jj] - M);
       wsm[jj] = w;
       Z = fmaf(w, es[jj], Z);
     }
@@ -46,7 +46,7 @@ __global__ void __launch_bounds__(D) paged_decode_reduce_kernel(
     for (int msk = 16; msk > 0; msk >>= 1) Z += __shfl_xor_sync(0xffffffffu, Z, msk);
     if (threadIdx.x == 0) {
       s_max = M;
-      s_invz = 1.f / Z;
+      s_invz = Z > 0.f ? 1.f / Z : 0.f;  // Z = 0: a query that saw no token (multi-token queries)
     }
   }
   __syncthreads();

@@ -63,6 +63,8 @@ struct DecodeParams {
   int partition_size;   // tokens per partition (multiple of 32)
   int max_partitions;   // NP: grid stride and partial-array stride
   int mode;             // 0: final out when one partition, partials otherwise; 1: partials always
+  int q_len;            // query tokens per sequence (1: single-query decode; > 1 tensor-core path only)
+  int q_chunks;         // query chunks per (sequence, kv head) in the grid (1 when q_len == 1)
   float scale_log2;     // softmax scale * log2(e)
   int prefetch_distance;
   int l2_hints;         // 1: evict_first on consuming loads/copies, evict_last on prefetches

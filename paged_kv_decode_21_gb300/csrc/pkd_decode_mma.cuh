@@ -34,6 +34,14 @@
 //                    shared-memory round trip sits between the two products.
 // P is rounded to fp16 for the second product (relative error <= 2^-11 per
 // weight); the normaliser sums the fp32 values.
+//
+// Multi-token queries (QC > 1): a CTA serves QC consecutive query tokens of
+// its sequence, so the 16 rows of the tile are (query token r / G, head
+// r % G).  Query jq sits at position L - q_len + jq and sees the tokens
+// before and at its position (causal among the new tokens): row r masks
+// tokens at or past min(partition end, L - q_len + jq + 1).  Rows 8..15 then
+// hold real queries: every lane keeps softmax state for rows r and r + 8,
+// and P.V runs one n-tile per 8 rows.
 #pragma once
 #include <cstdint>
 #include <cuda.h>
@@ -104,12 +112,19 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
+// Query tokens per CTA of the multi-token kernel for group size G.
+constexpr int mma_query_chunk(int G) { return 16 / G; }
+
 // ---------------------------------------------------------------- layout
-template <int D, int BS, int G>
+// QC: query tokens per CTA (1 = single-query decode).
+template <int D, int BS, int G, int QC>
 struct MmaTraits {
   static_assert(D == 64 || D == 128, "head_dim");
   static_assert(BS == 16 || BS == 32, "block_size");
-  static_assert(G >= 1 && G <= 8, "group size: the heads fill one 8-wide n-tile");
+  static_assert(G >= 1 && G <= 8, "group size");
+  static constexpr int ROWS = G * QC;          // query rows of the 16-row tile in use
+  static_assert(QC >= 1 && ROWS <= 16, "the CTA's queries fill one 16-row tile");
+  static constexpr int NT = ROWS > 8 ? 2 : 1;  // 8-row halves in use (P.V n-tiles)
   static constexpr int NW = 4;
   static constexpr int THREADS = NW * 32;
   static constexpr int MIN_BLOCKS = 2;
@@ -123,9 +138,9 @@ struct MmaTraits {
   static constexpr int SW_RAW = (96 * 1024) / (NW * SLOT_BYTES);
   static constexpr int SW = SW_RAW > 8 ? 8 : (SW_RAW < 2 ? 2 : SW_RAW);
   static constexpr int RING_BYTES = NW * SW * SLOT_BYTES;
-  // merge area: m, mt, l as [NW][8] each, then acc [NW][G][D]
-  static constexpr int MRG_ACC_OFF = 3 * NW * 8;  // floats (a multiple of 4)
-  static constexpr int MERGE_BYTES = (MRG_ACC_OFF + NW * G * D) * 4;
+  // merge area: m, mt, l as [NW][16] each, then acc [NW][ROWS][D]
+  static constexpr int MRG_ACC_OFF = 3 * NW * 16;  // floats (a multiple of 4)
+  static constexpr int MERGE_BYTES = (MRG_ACC_OFF + NW * ROWS * D) * 4;
   static constexpr int MAIN_BYTES = RING_BYTES > MERGE_BYTES ? RING_BYTES : MERGE_BYTES;
   static constexpr int BAR_BYTES = NW * SW * 8;
   // the swizzle needs 1024-byte aligned boxes: the kernel aligns the base
@@ -135,41 +150,51 @@ struct MmaTraits {
 };
 
 // ---------------------------------------------------------------- kernel
-template <int D, int BS, int G>
-__global__ void __launch_bounds__(MmaTraits<D, BS, G>::THREADS, MmaTraits<D, BS, G>::MIN_BLOCKS)
+template <int D, int BS, int G, int QC>
+__global__ void __launch_bounds__(MmaTraits<D, BS, G, QC>::THREADS, MmaTraits<D, BS, G, QC>::MIN_BLOCKS)
     paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                             const __grid_constant__ CUtensorMap tmap_v, const DecodeParams P) {
-  using T = MmaTraits<D, BS, G>;
-  constexpr int NW = T::NW, SW = T::SW, KS = T::KSTEPS;
+  using T = MmaTraits<D, BS, G, QC>;
+  constexpr int NW = T::NW, SW = T::SW, KS = T::KSTEPS, NT = T::NT, ROWS = T::ROWS;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // 1024-byte aligned base for the swizzled boxes
   const uint32_t raw_u32 = smem_u32(smem_raw);
   unsigned char* smem = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::MAIN_BYTES);
 
+  // work item: partition j fastest, then the query chunk, then (b, g)
   const int np_grid = P.max_partitions;
   const int j = blockIdx.x % np_grid;
-  const int bg = blockIdx.x / np_grid;
+  const int rest = blockIdx.x / np_grid;
+  const int qc = rest % P.q_chunks;
+  const int bg = rest / P.q_chunks;
   const int g = bg % P.num_kv_heads;
   const int b = bg / P.num_kv_heads;
   const int L = P.context_lens[b];
+  const int QL = P.q_len;
+  const int jq0 = qc * QC;               // first query token of this CTA
+  const int nq = min(QC, QL - jq0);      // its query tokens (>= 1)
   const int PS = P.partition_size;
   const int np_b = (L + PS - 1) / PS;
   const bool final_out = (P.mode == 0) && np_b <= 1;
   const int h0 = g * G;
+  const int Hq = P.num_q_heads;
+  // output / partial row of tile row rr (< G * nq)
+  auto out_row = [&](int rr) { return ((size_t)b * QL + jq0 + rr / G) * Hq + h0 + rr % G; };
 
   if (L <= 0) {
     if (final_out && j == 0) {
-      for (int i = threadIdx.x; i < G * D; i += blockDim.x)
-        P.out[((size_t)b * P.num_q_heads + h0) * D + i] = __float2half_rn(0.f);
+      for (int i = threadIdx.x; i < G * nq * D; i += blockDim.x)
+        P.out[out_row(i / D) * D + i % D] = __float2half_rn(0.f);
     }
     return;
   }
   if (j >= np_b) return;
 
   const int t0 = j * PS;
-  const int t1 = min(t0 + PS, L);
-  const int nblk = (t1 - t0 + BS - 1) / BS;
+  // the chunk's last query sees tokens < L - QL + jq0 + nq; nothing past that is read
+  const int t1 = min(min(t0 + PS, L), L - QL + jq0 + nq);
+  const int nblk = t1 > t0 ? (t1 - t0 + BS - 1) / BS : 0;
   const int32_t* bt = P.block_tables + (size_t)b * P.max_blocks_per_seq + t0 / BS;
   const size_t head_stride = (size_t)BS * D;
   const size_t block_stride = (size_t)P.num_kv_heads * head_stride;
@@ -180,25 +205,44 @@ __global__ void __launch_bounds__(MmaTraits<D, BS, G>::THREADS, MmaTraits<D, BS,
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  const int r = lane / 4;  // head row of S, dim row of O^T
+  const int r = lane / 4;  // tile row (of each 8-row half) in S, dim row of O^T
   const int c = lane % 4;
 
-  // Q as A fragments: qa[k][0] = q[r][16k + 2c .. +2), qa[k][1] = q[r][16k + 8 + 2c .. +2)
-  uint32_t qa[KS][2];
-  {
-    const __half* qr = P.q + ((size_t)b * P.num_q_heads + h0 + r) * D;
+  // token limit of the lane's rows r + 8 * hf: tokens at or past it are masked
+  int lim[NT];
+#pragma unroll
+  for (int hf = 0; hf < NT; ++hf) {
+    const int rr = r + 8 * hf;
+    lim[hf] = rr < G * nq ? min(t1, L - QL + jq0 + rr / G + 1) : t1;
+  }
+  const int lim_min = NT == 2 ? min(lim[0], lim[NT - 1]) : lim[0];
+
+  // Q as A fragments: qa[k] = {row r, row r+8} x {dims 16k + 2c, 16k + 8 + 2c}
+  uint32_t qa[KS][4];
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    const int rr = r + 8 * hf;
+    const bool live = hf < NT && rr < G * nq;
+    const __half* qr = P.q + (live ? out_row(rr) * D : 0);
 #pragma unroll
     for (int k = 0; k < KS; ++k) {
-      qa[k][0] = r < G ? *reinterpret_cast<const uint32_t*>(qr + 16 * k + 2 * c) : 0u;
-      qa[k][1] = r < G ? *reinterpret_cast<const uint32_t*>(qr + 16 * k + 8 + 2 * c) : 0u;
+      qa[k][hf] = live ? *reinterpret_cast<const uint32_t*>(qr + 16 * k + 2 * c) : 0u;
+      qa[k][2 + hf] = live ? *reinterpret_cast<const uint32_t*>(qr + 16 * k + 8 + 2 * c) : 0u;
     }
   }
-  float o[KS][4];  // O^T m-tile k: [dim 16k + r | 16k + 8 + r] x [head 2c | 2c + 1]
+  // O^T m-tile k, n-tile hf: [dim 16k + r | 16k + 8 + r] x [row 8hf + 2c | 8hf + 2c + 1]
+  float o[KS][NT][4];
 #pragma unroll
-  for (int k = 0; k < KS; ++k) o[k][0] = o[k][1] = o[k][2] = o[k][3] = 0.f;
-  float m = -INFINITY;   // running shift of head r (log2 domain), equal in the head's 4 lanes
-  float mt = -INFINITY;  // exact maximum of this lane's scores
-  float l = 0.f;         // sum of this lane's p values
+  for (int k = 0; k < KS; ++k)
+#pragma unroll
+    for (int hf = 0; hf < NT; ++hf) o[k][hf][0] = o[k][hf][1] = o[k][hf][2] = o[k][hf][3] = 0.f;
+  float m[NT], mt[NT], l[NT];  // per row r + 8hf: running shift, exact maximum, sum of p
+#pragma unroll
+  for (int hf = 0; hf < NT; ++hf) {
+    m[hf] = -INFINITY;
+    mt[hf] = -INFINITY;
+    l[hf] = 0.f;
+  }
 
   // ldmatrix row addresses: lane l addresses row (l & 7) + 8 * (l >> 4) of the
   // sub-tile, 16-byte chunk 2s + ((l >> 3) & 1) for step s; with the swizzle
@@ -264,8 +308,7 @@ __global__ void __launch_bounds__(MmaTraits<D, BS, G>::THREADS, MmaTraits<D, BS,
   int issued = 0;  // sub-tiles issued into the ring so far
   for (int s = 0; s < SW && ic.live(nblk); ++s, ++issued) issue_next(s);
 
-  int u = 0;
-  for (; cc.live(nblk); ++u) {
+  for (int u = 0; cc.live(nblk); ++u) {
     const int slot = u % SW;
     const bool bad = (bad_slots >> slot) & 1u;
     if (!mbar_wait_bounded(&full[slot], (u / SW) & 1, P.timeout_ns)) {
@@ -275,18 +318,19 @@ __global__ void __launch_bounds__(MmaTraits<D, BS, G>::THREADS, MmaTraits<D, BS,
       break;
     }
     if (!bad) {
-      const int valid = min(16, t1 - (t0 + cc.k * BS + cc.rg * 16));
+      const int base = t0 + cc.k * BS + cc.rg * 16;  // token of the sub-tile's row 0
+      const int valid = min(16, t1 - base);
       unsigned char* kslot = ring + (size_t)slot * T::SLOT_BYTES;
       const uint32_t ks = smem_u32(kslot);
       const uint32_t vs = ks + T::SUB_BYTES;
       if (valid < 16) {
-        // rows past the context may hold anything (NaN included): zero the V
-        // rows so that p = 0 times them stays 0; masked K rows get -inf below
+        // rows past the CTA's tokens may hold anything (NaN included): zero the
+        // V rows so that p = 0 times them stays 0; masked K rows get -inf below
         for (int i = lane; i < (16 - valid) * T::NBOX * 8; i += 32) {
           const int row = valid + i / (T::NBOX * 8);
-          const int rest = i % (T::NBOX * 8);
-          *reinterpret_cast<uint4*>(kslot + T::SUB_BYTES + (rest / 8) * T::BOX_BYTES + row * 128 +
-                                    (rest % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+          const int rest8 = i % (T::NBOX * 8);
+          *reinterpret_cast<uint4*>(kslot + T::SUB_BYTES + (rest8 / 8) * T::BOX_BYTES + row * 128 +
+                                    (rest8 % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
         }
         fence_proxy_async_smem();  // ordered before the next tensor copy into this slot
         __syncwarp();
@@ -297,49 +341,81 @@ __global__ void __launch_bounds__(MmaTraits<D, BS, G>::THREADS, MmaTraits<D, BS,
       for (int k = 0; k < KS; ++k) {
         uint32_t kb[4];
         ldsm_x4(ks + (k / 4) * T::BOX_BYTES + lm_off[k % 4], kb);
-        mma_16816_top(s0, qa[k][0], qa[k][1], kb[0], kb[1]);
-        mma_16816_top(s1, qa[k][0], qa[k][1], kb[2], kb[3]);
-      }
-      // ---- online softmax for head r over tokens 2c, 2c+1, 8+2c, 9+2c
-      float sc[4] = {s0[0] * P.scale_log2, s0[1] * P.scale_log2, s1[0] * P.scale_log2,
-                     s1[1] * P.scale_log2};
-      if (valid < 16) {
-        if (2 * c >= valid) sc[0] = -INFINITY;
-        if (2 * c + 1 >= valid) sc[1] = -INFINITY;
-        if (8 + 2 * c >= valid) sc[2] = -INFINITY;
-        if (9 + 2 * c >= valid) sc[3] = -INFINITY;
-      }
-      const float lmax = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
-      mt = fmaxf(mt, lmax);
-      if (__any_sync(0xffffffffu, lmax > m + kLazyTau)) {
-        float mx = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float mn = fmaxf(m, mx);
-        const float alpha = (mn == -INFINITY) ? 1.f : ex2_approx(m - mn);
-        l *= alpha;
-        m = mn;
-        // O^T columns are heads 2c, 2c+1, whose shifts live in lanes 8c, 8c+4
-        const float a_lo = __shfl_sync(0xffffffffu, alpha, 8 * c);
-        const float a_hi = __shfl_sync(0xffffffffu, alpha, 8 * c + 4);
-#pragma unroll
-        for (int k = 0; k < KS; ++k) {
-          o[k][0] *= a_lo;
-          o[k][1] *= a_hi;
-          o[k][2] *= a_lo;
-          o[k][3] *= a_hi;
+        if constexpr (NT == 1) {
+          mma_16816_top(s0, qa[k][0], qa[k][2], kb[0], kb[1]);
+          mma_16816_top(s1, qa[k][0], qa[k][2], kb[2], kb[3]);
+        } else {
+          mma_16816(s0, qa[k], kb[0], kb[1]);
+          mma_16816(s1, qa[k], kb[2], kb[3]);
         }
       }
-      const float p0 = ex2_approx(sc[0] - m), p1 = ex2_approx(sc[1] - m);
-      const float p2 = ex2_approx(sc[2] - m), p3 = ex2_approx(sc[3] - m);
-      l += (p0 + p1) + (p2 + p3);
-      const uint32_t pb0 = pack_half2(p0, p1);  // P^T[tokens 2c, 2c+1][head r]
-      const uint32_t pb1 = pack_half2(p2, p3);  // P^T[tokens 8+2c, 9+2c][head r]
+      // ---- online softmax of rows r + 8hf over tokens 2c, 2c+1, 8+2c, 9+2c
+      float sc[NT][4];
+#pragma unroll
+      for (int hf = 0; hf < NT; ++hf) {
+        sc[hf][0] = s0[2 * hf] * P.scale_log2;
+        sc[hf][1] = s0[2 * hf + 1] * P.scale_log2;
+        sc[hf][2] = s1[2 * hf] * P.scale_log2;
+        sc[hf][3] = s1[2 * hf + 1] * P.scale_log2;
+      }
+      if (base + 16 > lim_min) {
+#pragma unroll
+        for (int hf = 0; hf < NT; ++hf) {
+          const int lt = lim[hf] - base;  // tokens of the sub-tile this row sees
+          if (2 * c >= lt) sc[hf][0] = -INFINITY;
+          if (2 * c + 1 >= lt) sc[hf][1] = -INFINITY;
+          if (8 + 2 * c >= lt) sc[hf][2] = -INFINITY;
+          if (9 + 2 * c >= lt) sc[hf][3] = -INFINITY;
+        }
+      }
+      float lmax[NT];
+      bool need = false;
+#pragma unroll
+      for (int hf = 0; hf < NT; ++hf) {
+        lmax[hf] = fmaxf(fmaxf(sc[hf][0], sc[hf][1]), fmaxf(sc[hf][2], sc[hf][3]));
+        mt[hf] = fmaxf(mt[hf], lmax[hf]);
+        need |= lmax[hf] > m[hf] + kLazyTau;
+      }
+      if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+        for (int hf = 0; hf < NT; ++hf) {
+          float mx = fmaxf(lmax[hf], __shfl_xor_sync(0xffffffffu, lmax[hf], 1));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+          const float mn = fmaxf(m[hf], mx);
+          const float alpha = (mn == -INFINITY) ? 1.f : ex2_approx(m[hf] - mn);
+          l[hf] *= alpha;
+          m[hf] = mn;
+          // O^T columns 8hf + 2c, 8hf + 2c + 1: their shifts live in lanes 8c, 8c + 4
+          const float a_lo = __shfl_sync(0xffffffffu, alpha, 8 * c);
+          const float a_hi = __shfl_sync(0xffffffffu, alpha, 8 * c + 4);
+#pragma unroll
+          for (int k = 0; k < KS; ++k) {
+            o[k][hf][0] *= a_lo;
+            o[k][hf][1] *= a_hi;
+            o[k][hf][2] *= a_lo;
+            o[k][hf][3] *= a_hi;
+          }
+        }
+      }
+      uint32_t pb[NT][2];
+#pragma unroll
+      for (int hf = 0; hf < NT; ++hf) {
+        // a row that has seen no token yet keeps m = -inf: shift by 0 so that
+        // its masked scores give p = 0 rather than NaN
+        const float mu = m[hf] == -INFINITY ? 0.f : m[hf];
+        const float p0 = ex2_approx(sc[hf][0] - mu), p1 = ex2_approx(sc[hf][1] - mu);
+        const float p2 = ex2_approx(sc[hf][2] - mu), p3 = ex2_approx(sc[hf][3] - mu);
+        l[hf] += (p0 + p1) + (p2 + p3);
+        pb[hf][0] = pack_half2(p0, p1);  // P^T[tokens 2c, 2c+1][row 8hf + r]
+        pb[hf][1] = pack_half2(p2, p3);  // P^T[tokens 8+2c, 9+2c][row 8hf + r]
+      }
       // ---- O^T += V^T P^T, one m-tile of 16 dims per step
 #pragma unroll
       for (int k = 0; k < KS; ++k) {
         uint32_t va[4];
         ldsm_x4_trans(vs + (k / 4) * T::BOX_BYTES + lm_off[k % 4], va);
-        mma_16816(o[k], va, pb0, pb1);
+#pragma unroll
+        for (int hf = 0; hf < NT; ++hf) mma_16816(o[k][hf], va, pb[hf][0], pb[hf][1]);
       }
     }
     __syncwarp();
@@ -354,55 +430,57 @@ __global__ void __launch_bounds__(MmaTraits<D, BS, G>::THREADS, MmaTraits<D, BS,
   // ------------------------------------------------------------------ merge
   __syncthreads();  // every warp is done with the ring that the merge area reuses
   float* mrg = reinterpret_cast<float*>(smem);
-  float* mrg_m = mrg;                  // [NW][8] running shift
-  float* mrg_mt = mrg + NW * 8;        // [NW][8] exact maximum
-  float* mrg_l = mrg + 2 * NW * 8;     // [NW][8]
-  float* mrg_acc = mrg + T::MRG_ACC_OFF;  // [NW][G][D]
-  {
-    float lv = l + __shfl_xor_sync(0xffffffffu, l, 1);
+  float* mrg_m = mrg;                   // [NW][16] running shift
+  float* mrg_mt = mrg + NW * 16;        // [NW][16] exact maximum
+  float* mrg_l = mrg + 2 * NW * 16;     // [NW][16]
+  float* mrg_acc = mrg + T::MRG_ACC_OFF;  // [NW][ROWS][D]
+#pragma unroll
+  for (int hf = 0; hf < NT; ++hf) {
+    float lv = l[hf] + __shfl_xor_sync(0xffffffffu, l[hf], 1);
     lv += __shfl_xor_sync(0xffffffffu, lv, 2);
-    float mx = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
+    float mx = fmaxf(mt[hf], __shfl_xor_sync(0xffffffffu, mt[hf], 1));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
     if (c == 0) {
-      mrg_m[warp * 8 + r] = m;
-      mrg_mt[warp * 8 + r] = mx;
-      mrg_l[warp * 8 + r] = lv;
+      mrg_m[warp * 16 + 8 * hf + r] = m[hf];
+      mrg_mt[warp * 16 + 8 * hf + r] = mx;
+      mrg_l[warp * 16 + 8 * hf + r] = lv;
     }
-    float* acc = mrg_acc + warp * G * D;
+    float* acc = mrg_acc + warp * ROWS * D;
+    const int ra = 8 * hf + 2 * c;
 #pragma unroll
     for (int k = 0; k < KS; ++k) {
-      if (2 * c < G) {
-        acc[(2 * c) * D + 16 * k + r] = o[k][0];
-        acc[(2 * c) * D + 16 * k + 8 + r] = o[k][2];
+      if (ra < ROWS) {
+        acc[ra * D + 16 * k + r] = o[k][hf][0];
+        acc[ra * D + 16 * k + 8 + r] = o[k][hf][2];
       }
-      if (2 * c + 1 < G) {
-        acc[(2 * c + 1) * D + 16 * k + r] = o[k][1];
-        acc[(2 * c + 1) * D + 16 * k + 8 + r] = o[k][3];
+      if (ra + 1 < ROWS) {
+        acc[(ra + 1) * D + 16 * k + r] = o[k][hf][1];
+        acc[(ra + 1) * D + 16 * k + 8 + r] = o[k][hf][3];
       }
     }
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
-    const int h = i / D, d = i % D;
+  for (int i = threadIdx.x; i < G * nq * D; i += blockDim.x) {
+    const int rr = i / D, d = i % D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, mrg_mt[w * 8 + h]);  // the exact maximum
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, mrg_mt[w * 16 + rr]);  // the exact maximum
     float Z = 0.f, O = 0.f;
 #pragma unroll
     for (int w = 0; w < NW; ++w) {
-      const float mw = mrg_m[w * 8 + h];
+      const float mw = mrg_m[w * 16 + rr];
       const float cw = (mw == -INFINITY) ? 0.f : ex2_approx(mw - M);
-      Z = fmaf(cw, mrg_l[w * 8 + h], Z);
-      O = fmaf(cw, mrg_acc[(w * G + h) * D + d], O);
+      Z = fmaf(cw, mrg_l[w * 16 + rr], Z);
+      O = fmaf(cw, mrg_acc[(w * ROWS + rr) * D + d], O);
     }
-    const size_t row = (size_t)b * P.num_q_heads + h0 + h;
+    const size_t row = out_row(rr);
     if (final_out) {
-      P.out[row * D + d] = __float2half_rn(O / Z);
+      P.out[row * D + d] = __float2half_rn(Z > 0.f ? O / Z : 0.f);  // Z = 0: the query saw no token
     } else {
       const size_t pidx = row * P.max_partitions + j;
       P.tmp_out[pidx * D + d] = O;
       if (d == 0) {
-        P.max_logits[pidx] = M * 0.69314718055994530942f;  // log2 units -> natural
+        P.max_logits[pidx] = M * 0.69314718055994530942f;  // log2 units -> natural; -inf if empty
         P.exp_sums[pidx] = Z;
       }
     }

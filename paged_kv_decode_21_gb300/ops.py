@@ -65,6 +65,11 @@ def lib():
         L.paged_decode_reduce.restype = I
         L.paged_decode_validate_tables.argtypes = [P, P, I, I, I, I, P, P]
         L.paged_decode_validate_tables.restype = I
+        L.paged_decode_attention_multi.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, I, P, S,
+                                                   P, P]
+        L.paged_decode_attention_multi.restype = I
+        L.paged_decode_multi_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
+        L.paged_decode_multi_workspace_size.restype = S
         L.paged_kv_append.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, P]
         L.paged_kv_append.restype = I
         L.pkd_selftest_bounded_wait.argtypes = [P, ctypes.c_ulonglong, P]
@@ -263,6 +268,35 @@ def paged_decode_validate_tables(block_tables, context_lens, block_size, num_blo
                                             int(block_size), int(num_blocks), _ptr(error_word),
                                             _stream(stream))
     _check(st, "paged_decode_validate_tables")
+
+
+def paged_decode_multi_workspace_size(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size,
+                                      max_context_len, partition_size=0) -> int:
+    return int(lib().paged_decode_multi_workspace_size(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim,
+                                                       block_size, max_context_len, partition_size))
+
+
+def paged_decode_attention_multi(q, k_cache, v_cache, block_tables, context_lens, scale, out=None,
+                                 max_context_len=None, partition_size=0, workspace=None,
+                                 error_word=None, stream=None) -> torch.Tensor:
+    """q_len new tokens per sequence, q [B][q_len][Hq][D]; causal among them."""
+    _want(q, "q", torch.float16, 4)
+    B, QL, Hq, D = q.shape
+    _, _, Hkv, _, BS, NB, MB = _shape(q.view(B, QL * Hq, D), k_cache, v_cache, block_tables, context_lens)
+    if out is None:
+        out = torch.empty_like(q)
+    _want(out, "out", torch.float16, 4)
+    maxlen = _max_len(context_lens, max_context_len)
+    need = paged_decode_multi_workspace_size(B, QL, Hq, Hkv, D, BS, maxlen, partition_size)
+    if workspace is None:
+        workspace = alloc_workspace(need, q.device)
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().paged_decode_attention_multi(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                            _ptr(context_lens), _ptr(out), B, QL, Hq, Hkv, D, BS, NB, MB,
+                                            maxlen, float(scale), int(partition_size), _ptr(workspace), wsb,
+                                            _ptr(error_word), _stream(stream))
+    _check(st, "paged_decode_attention_multi")
+    return out
 
 
 def paged_kv_append(k_new, v_new, block_tables, context_lens, k_cache, v_cache, error_word=None,

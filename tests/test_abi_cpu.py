@@ -103,6 +103,26 @@ def test_selftest_argument_checks(L):
     assert L.pkd_selftest_bounded_wait(FAKE, 10**9, None) == 2        # budget too long
 
 
+def test_multi_query_argument_checks(L):
+    # (q, k, v, bt, cl, out, B, q_len, Hq, Hkv, D, BS, NB, MB, maxlen, scale, P, ws, wsb, err, stream)
+    def call(*, ptrs=(FAKE,) * 6, B=2, QL=3, Hq=8, Hkv=2, D=128, BS=16, NB=64, MB=8, maxlen=100, P=-1,
+             ws=None, wsb=0):
+        return L.paged_decode_attention_multi(*ptrs, B, QL, Hq, Hkv, D, BS, NB, MB, maxlen,
+                                              ctypes.c_float(0.1), P, ws, wsb, None, None)
+    assert call(B=0) == 0                                     # empty batch: a no-op
+    assert call(QL=0) == 2                                    # at least one query token
+    assert call(ptrs=(None,) + (FAKE,) * 5) == 1
+    assert call(D=96) == 3 and call(Hq=18) == 3               # head_dim; group of 9
+    assert call(P=64, maxlen=100) == 5                        # split without a workspace
+    assert call(ptrs=(FAKE,) * 5 + (MISALIGNED,)) == 4
+    # partials are (sequence, query token, head) rows
+    ws = L.paged_decode_multi_workspace_size(2, 3, 8, 2, 128, 16, 100, 64)
+    one = L.paged_decode_workspace_size(6, 8, 2, 128, 16, 100, 64, 4)
+    assert ws == one > 0
+    assert L.paged_decode_multi_workspace_size(2, 3, 8, 2, 128, 16, 100, -1) == 0
+    assert L.paged_decode_multi_workspace_size(2, 0, 8, 2, 128, 16, 100, 64) == 0
+
+
 def test_append_argument_checks(L):
     # (k_new, v_new, bt, cl, kc, vc, B, Hkv, D, BS, NB, MB, err, stream); nothing is launched
     def call(*, ptrs=(FAKE,) * 6, B=2, Hkv=2, D=64, BS=16, NB=4, MB=2, err=None):
@@ -120,7 +140,7 @@ def test_auto_variant_policy(L):
     # no GPU here: the library assumes 148 SMs; the cases sit far from the
     # thresholds, so they hold for 152 as well
     av = ops.paged_decode_auto_variant
-    staged = ops.VARIANTS["tma_staged"] | ops.FLAG_L2_EVICT_HINTS
+    staged = ops.VARIANTS["tma_mma"]
     plain = ops.VARIANTS["no_prefetch"]
     assert av(64, 32, 32, 128, 16, 2048) == staged      # long CTAs
     assert av(64, 32, 32, 128, 16, 512) == plain        # 2048 CTAs of 512 tokens
@@ -130,7 +150,8 @@ def test_auto_variant_policy(L):
     assert av(64, 32, 8, 128, 16, 512) == staged        # GQA always staged
     assert av(64, 32, 32, 128, 16, 512, -1) == plain
     assert av(64, 32, 32, 128, 16, 4096, 256) == staged  # 16384 CTAs
-    assert ops.variant_name(staged) == "tma_staged+l2_hints"
+    assert ops.variant_name(staged) == "tma_mma"
+    assert ops.variant_name(ops.VARIANTS["tma_staged"] | ops.FLAG_L2_EVICT_HINTS) == "tma_staged+l2_hints"
     with pytest.raises(ops.PagedDecodeError):
         av(64, 32, 32, 128, 16, 512, 100)               # partition not a multiple of 32
 
