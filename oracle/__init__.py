@@ -62,6 +62,16 @@ def _load(mutant: int = 0):
         lib.pkd_oracle_merge.restype = I
         lib.pkd_oracle_append.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I]
         lib.pkd_oracle_append.restype = I
+        lib.pkd_oracle_attention_fp8.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, D, D, D, P, I, P, I]
+        lib.pkd_oracle_attention_fp8.restype = I
+        lib.pkd_oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        lib.pkd_oracle_e4m3_to_double.restype = D
+        lib.pkd_oracle_float_to_e4m3.argtypes = [ctypes.c_float]
+        lib.pkd_oracle_float_to_e4m3.restype = ctypes.c_uint8
+        lib.pkd_oracle_quantize_e4m3.argtypes = [P, I, ctypes.c_float, P]
+        lib.pkd_oracle_quantize_e4m3.restype = None
+        lib.pkd_oracle_append_fp8.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, ctypes.c_float, ctypes.c_float]
+        lib.pkd_oracle_append_fp8.restype = I
         lib.pkd_oracle_half_to_double.argtypes = [ctypes.c_uint16]
         lib.pkd_oracle_half_to_double.restype = D
         lib.pkd_oracle_mutant.argtypes = []
@@ -216,6 +226,85 @@ def append(k_new, v_new, block_tables, context_lens, k_cache, v_cache, mutant: i
     if check:
         _check(rc, "append")
     return kc.view(np.float16), vc.view(np.float16)
+
+
+def e4m3_to_double(bits, mutant: int = 0) -> np.ndarray:
+    """Decode E4M3 bytes (the format's definition) to float64."""
+    lib = _load(mutant)
+    b = np.asarray(bits, dtype=np.uint8).reshape(-1)
+    return np.array([lib.pkd_oracle_e4m3_to_double(int(x)) for x in b], np.float64)
+
+
+def float_to_e4m3(x, mutant: int = 0) -> np.ndarray:
+    """Round float32 values to E4M3 bytes (nearest-even, saturating at 448)."""
+    lib = _load(mutant)
+    f = np.asarray(x, dtype=np.float32).reshape(-1)
+    return np.array([lib.pkd_oracle_float_to_e4m3(float(v)) for v in f], np.uint8)
+
+
+def quantize_e4m3(x_fp16, scale: float, mutant: int = 0) -> np.ndarray:
+    """E4M3 bytes of fp16 values: e4m3(fp32(x) / scale), the division in fp32."""
+    lib = _load(mutant)
+    xa = _np(x_fp16, np.float16)
+    flat = np.ascontiguousarray(xa.reshape(-1)).view(np.uint16)
+    out = np.empty(flat.shape[0], np.uint8)
+    lib.pkd_oracle_quantize_e4m3(_ptr(flat), int(flat.shape[0]), float(scale), _ptr(out))
+    return out.reshape(xa.shape)
+
+
+def attention_fp8(q, k_cache8, v_cache8, block_tables, context_lens, scale, k_scale, v_scale, rows=None,
+                  threads=None, mutant: int = 0) -> np.ndarray:
+    """Exact fp64 attention over E4M3 caches (value = e4m3(byte) * k_scale / v_scale).
+    q is [B][Hq][D] (single query) or [B][q_len][Hq][D] (causal multi-token)."""
+    lib = _load(mutant)
+    qm = _np(q, np.float16)
+    single = qm.ndim == 3
+    if single:
+        qm = qm[:, None]
+    B, QL, Hq, D = qm.shape
+    k8 = _np(k_cache8, np.uint8)
+    v8 = _np(v_cache8, np.uint8)
+    bt = _np(block_tables, np.int32)
+    cl = _np(context_lens, np.int32)
+    NB, Hkv, BS, D2 = k8.shape
+    assert D2 == D and v8.shape == k8.shape and bt.shape[0] == B and cl.shape == (B,)
+    qa = np.ascontiguousarray(qm).view(np.uint16)
+    if threads is None:
+        threads = os.cpu_count() or 1
+    if rows is None:
+        out = np.empty((B, QL, Hq, D), np.float64)
+        rp, nr = None, 0
+    else:
+        ra = _np(rows, np.int32).reshape(-1)
+        out = np.empty((ra.shape[0], D), np.float64)
+        rp, nr = _ptr(ra), ra.shape[0]
+    rc = lib.pkd_oracle_attention_fp8(_ptr(qa), _ptr(k8), _ptr(v8), _ptr(bt), _ptr(cl), B, QL, Hq, Hkv, D, BS,
+                                      NB, bt.shape[1], float(scale), float(k_scale), float(v_scale), rp, nr,
+                                      _ptr(out), int(threads))
+    _check(rc, "attention_fp8")
+    if rows is None and single:
+        return out[:, 0]
+    return out
+
+
+def append_fp8(k_new, v_new, block_tables, context_lens, k_cache8, v_cache8, k_scale, v_scale,
+               mutant: int = 0, check: bool = True):
+    """FP8 cache write: returns new (k_cache8, v_cache8) with each sequence's new row
+    quantized into position context_lens[b]; the inputs are left alone."""
+    lib = _load(mutant)
+    kn = _np(k_new, np.float16).view(np.uint16)
+    vn = _np(v_new, np.float16).view(np.uint16)
+    bt = _np(block_tables, np.int32)
+    cl = _np(context_lens, np.int32)
+    kc = _np(k_cache8, np.uint8).copy()
+    vc = _np(v_cache8, np.uint8).copy()
+    NB, Hkv, BS, D = kc.shape
+    B = cl.shape[0]
+    rc = lib.pkd_oracle_append_fp8(_ptr(kn), _ptr(vn), _ptr(bt), _ptr(cl), _ptr(kc), _ptr(vc), B, Hkv, D, BS,
+                                   NB, bt.shape[1], float(k_scale), float(v_scale))
+    if check:
+        _check(rc, "append_fp8")
+    return kc, vc
 
 
 def half_to_double(bits) -> np.ndarray:

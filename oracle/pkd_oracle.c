@@ -105,15 +105,101 @@ static void build_half_table(void)
 static inline double h2d(uint16_t b) { return g_half_table[b]; }
 
 /* ---------------------------------------------------------------------- */
+/* FP8 E4M3 (the OCP 8-bit float "E4M3", no infinities) -> double, from   */
+/* the format's definition: sign 1 bit, exponent 4 bits (bias 7),         */
+/* mantissa 3 bits;  e = 0: subnormal (-1)^s * 2^-6 * (m / 8);            */
+/* e = 15 and m = 7: NaN;  else (-1)^s * 2^(e-7) * (1 + m/8).  Largest    */
+/* finite magnitude 448.                                                   */
+/* ---------------------------------------------------------------------- */
+double pkd_oracle_e4m3_to_double(uint8_t bits)
+{
+    int sign = (bits >> 7) & 1;
+    int e = (bits >> 3) & 0xf;
+    int m = bits & 0x7;
+    double v;
+    if (e == 0) v = ldexp((double)m, -9);                 /* 2^-6 * m / 8 */
+    else if (e == 15 && m == 7) v = NAN;
+    else v = ldexp(8.0 + (double)m, e - 10);              /* 2^(e-7) * (8+m) / 8 */
+    return sign ? -v : v;
+}
+
+static double g_e4m3_table[256];
+static pthread_once_t g_e4m3_once = PTHREAD_ONCE_INIT;
+static void build_e4m3_table(void)
+{
+    for (int i = 0; i < 256; ++i) g_e4m3_table[i] = pkd_oracle_e4m3_to_double((uint8_t)i);
+}
+static inline double e4m3d(uint8_t b) { return g_e4m3_table[b]; }
+
+/*
+ * float -> E4M3 by round-to-nearest-even onto the E4M3 grid, saturating to
+ * the largest finite magnitude (448) instead of overflowing; NaN stays NaN
+ * (0x7f).  Written from the grid: the representable magnitudes are
+ * (8+m)/8 * 2^(e-7) for e = 1..15 (m = 0..6 at e = 15) and m/8 * 2^-6.
+ */
+uint8_t pkd_oracle_float_to_e4m3(float x)
+{
+    if (x != x) return 0x7f;
+    uint8_t sign = (x < 0.0f || (x == 0.0f && 1.0f / x < 0.0f)) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (a >= 448.0) return sign | 0x7e;                   /* saturate */
+    /* exponent of the binade holding a; below 2^-6 the spacing is 2^-9 */
+    int e;
+    double step;
+    if (a < ldexp(1.0, -6)) {
+        e = 0;
+        step = ldexp(1.0, -9);
+    } else {
+        e = (int)floor(log2(a)) + 7;                      /* biased, 1..15 */
+        if (ldexp(1.0, e - 7) > a) e -= 1;                /* guard log2 rounding */
+        if (ldexp(1.0, e - 6) <= a) e += 1;
+        step = ldexp(1.0, e - 10);                        /* 2^(e-7) / 8 */
+    }
+    double n = a / step;                                  /* exact: step is a power of two */
+    double fl = floor(n);
+    double r = n - fl;
+    double k = fl;
+    if (r > 0.5 || (r == 0.5 && fmod(fl, 2.0) != 0.0)) k = fl + 1.0;
+    double v = k * step;                                  /* the rounded magnitude */
+#if PKD_ORACLE_MUTANT == 11     /* planted mistake: truncation instead of rounding */
+    v = fl * step;
+#endif
+    if (v >= 448.0) return sign | 0x7e;
+    if (v == 0.0) return sign;
+    /* re-encode v */
+    if (v < ldexp(1.0, -6)) return sign | (uint8_t)(v / ldexp(1.0, -9));
+    int ee = (int)floor(log2(v)) + 7;
+    if (ldexp(1.0, ee - 7) > v) ee -= 1;
+    if (ldexp(1.0, ee - 6) <= v) ee += 1;
+    int mm = (int)(v / ldexp(1.0, ee - 10)) - 8;
+    return sign | (uint8_t)((ee << 3) | mm);
+}
+
+/* Quantize n binary16 values: out[i] = e4m3(fp32(half(x[i])) / scale), the
+ * division in IEEE fp32 (round to nearest) and the E4M3 rounding as above. */
+void pkd_oracle_quantize_e4m3(const uint16_t *x, int n, float scale, uint8_t *out)
+{
+    pthread_once(&g_table_once, build_half_table);
+    for (int i = 0; i < n; ++i) {
+        float f = (float)h2d(x[i]);
+        float qv = f / scale;
+        out[i] = pkd_oracle_float_to_e4m3(qv);
+    }
+}
+
+/* ---------------------------------------------------------------------- */
 /* Problem description shared by the entry points below.                   */
 /* ---------------------------------------------------------------------- */
 typedef struct {
-    const uint16_t *q, *k_cache, *v_cache;
+    const uint16_t *q;
+    const void *k_cache, *v_cache;   /* binary16 words, or E4M3 bytes when kv_fp8 */
     const int32_t *block_tables, *context_lens;
     int num_seqs, num_q_heads, num_kv_heads, head_dim, block_size;
     int num_blocks, max_blocks_per_seq;
     double scale;
     int q_len;      /* query tokens per sequence (1: single-query decode) */
+    int kv_fp8;     /* 1: caches hold E4M3 bytes; value = e4m3(byte) * k_scale (v_scale) */
+    double k_scale, v_scale;
 } problem_t;
 
 /* Tokens that query jq of sequence b attends to: query jq sits at position
@@ -130,7 +216,7 @@ static int visible(const problem_t *P, int b, int jq)
 
 /* Address of the K (or V) row of logical token t of sequence b, kv head g.
  * Returns NULL when the block table entry is outside the pool. */
-static const uint16_t *kv_row(const problem_t *P, const uint16_t *cache, int b, int g, int t)
+static const void *kv_row(const problem_t *P, const void *cache, int b, int g, int t)
 {
     int logical_block = t / P->block_size;
     int slot = t % P->block_size;
@@ -143,7 +229,7 @@ static const uint16_t *kv_row(const problem_t *P, const uint16_t *cache, int b, 
     int p = P->block_tables[(size_t)b * P->max_blocks_per_seq + logical_block];
     if (p < 0 || p >= P->num_blocks) return NULL;
     size_t off = (((size_t)p * P->num_kv_heads + g) * P->block_size + slot) * P->head_dim;
-    return cache + off;
+    return (const char *)cache + off * (P->kv_fp8 ? 1 : 2);
 }
 
 static int kv_head_of(const problem_t *P, int h)
@@ -163,10 +249,16 @@ static int scores(const problem_t *P, int b, int jq, int h, int t0, int t1, doub
     int g = kv_head_of(P, h);
     const uint16_t *qv = P->q + (((size_t)b * P->q_len + jq) * P->num_q_heads + h) * P->head_dim;
     for (int t = t0; t < t1; ++t) {
-        const uint16_t *k = kv_row(P, P->k_cache, b, g, t);
+        const void *k = kv_row(P, P->k_cache, b, g, t);
         if (!k) return -1;
         double dot = 0.0;
-        for (int d = 0; d < P->head_dim; ++d) dot += h2d(qv[d]) * h2d(k[d]);
+        if (P->kv_fp8) {
+            const uint8_t *k8 = (const uint8_t *)k;
+            for (int d = 0; d < P->head_dim; ++d) dot += h2d(qv[d]) * (e4m3d(k8[d]) * P->k_scale);
+        } else {
+            const uint16_t *k16 = (const uint16_t *)k;
+            for (int d = 0; d < P->head_dim; ++d) dot += h2d(qv[d]) * h2d(k16[d]);
+        }
 #if PKD_ORACLE_MUTANT == 3      /* planted mistake: scale dropped */
         s[t - t0] = dot;
 #else
@@ -210,12 +302,22 @@ static int attend_row(const problem_t *P, int b, int jq, int h, double *w, doubl
     int g = kv_head_of(P, h);
     for (int t = 0; t < L; ++t) {
 #if PKD_ORACLE_MUTANT == 6      /* planted mistake: values read from the K cache */
-        const uint16_t *v = kv_row(P, P->k_cache, b, g, t);
+        const void *v = kv_row(P, P->k_cache, b, g, t);
 #else
-        const uint16_t *v = kv_row(P, P->v_cache, b, g, t);
+        const void *v = kv_row(P, P->v_cache, b, g, t);
 #endif
         if (!v) return -1;
-        for (int d = 0; d < D; ++d) out[d] += w[t] * h2d(v[d]);
+        if (P->kv_fp8) {
+            const uint8_t *v8 = (const uint8_t *)v;
+#if PKD_ORACLE_MUTANT == 10     /* planted mistake: the V scale is left out */
+            for (int d = 0; d < D; ++d) out[d] += w[t] * e4m3d(v8[d]);
+#else
+            for (int d = 0; d < D; ++d) out[d] += w[t] * (e4m3d(v8[d]) * P->v_scale);
+#endif
+        } else {
+            const uint16_t *v16 = (const uint16_t *)v;
+            for (int d = 0; d < D; ++d) out[d] += w[t] * h2d(v16[d]);
+        }
     }
     return 0;
 }
@@ -278,6 +380,8 @@ static int check_problem(const problem_t *P)
  * Returns 0; -1 if a used block-table entry is outside [0, num_blocks);
  * -2 on allocation failure; -3 on a bad argument.
  */
+static int attention_impl(problem_t P, const int32_t *rows, int num_rows, double *out, int num_threads);
+
 int pkd_oracle_attention_multi(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
                                const int32_t *block_tables, const int32_t *context_lens,
                                int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
@@ -285,9 +389,37 @@ int pkd_oracle_attention_multi(const uint16_t *q, const uint16_t *k_cache, const
                                double scale, const int32_t *rows, int num_rows, double *out,
                                int num_threads)
 {
-    pthread_once(&g_table_once, build_half_table);
     problem_t P = {q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads,
-                   num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, scale, q_len};
+                   num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, scale, q_len, 0, 1.0, 1.0};
+    return attention_impl(P, rows, num_rows, out, num_threads);
+}
+
+/*
+ * FP8 KV: the caches hold E4M3 bytes in the same [num_blocks][num_kv_heads]
+ * [block_size][head_dim] layout; element value = e4m3(byte) * k_scale for K,
+ * * v_scale for V (one scale per cache).  q, out and the rest as in
+ * pkd_oracle_attention_multi.  Source: CSDN answer "如何优化LLM推理引擎的内存
+ * 访问延迟？", section 4 (FP8 precision to shrink the KV footprint); the
+ * format and the per-cache scale are this library's plainest reading.
+ */
+int pkd_oracle_attention_fp8(const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                             const int32_t *block_tables, const int32_t *context_lens,
+                             int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
+                             int head_dim, int block_size, int num_blocks, int max_blocks_per_seq,
+                             double scale, double k_scale, double v_scale, const int32_t *rows,
+                             int num_rows, double *out, int num_threads)
+{
+    problem_t P = {q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads,
+                   num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, scale, q_len, 1,
+                   k_scale, v_scale};
+    return attention_impl(P, rows, num_rows, out, num_threads);
+}
+
+static int attention_impl(problem_t P, const int32_t *rows, int num_rows, double *out, int num_threads)
+{
+    pthread_once(&g_table_once, build_half_table);
+    pthread_once(&g_e4m3_once, build_e4m3_table);
+    const int num_seqs = P.num_seqs, q_len = P.q_len, num_q_heads = P.num_q_heads;
     int rc = check_problem(&P);
     if (rc) return rc;
     job_t J;
@@ -336,7 +468,7 @@ int pkd_oracle_weights(const uint16_t *q, const uint16_t *k_cache, const uint16_
 {
     pthread_once(&g_table_once, build_half_table);
     problem_t P = {q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads,
-                   num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, scale, 1};
+                   num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, scale, 1, 0, 1.0, 1.0};
     int rc = check_problem(&P);
     if (rc) return rc;
     if (b < 0 || b >= num_seqs || h < 0 || h >= num_q_heads) return -3;
@@ -361,7 +493,7 @@ int pkd_oracle_partitions(const uint16_t *q, const uint16_t *k_cache, const uint
 {
     pthread_once(&g_table_once, build_half_table);
     problem_t P = {q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads,
-                   num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, scale, 1};
+                   num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, scale, 1, 0, 1.0, 1.0};
     int rc = check_problem(&P);
     if (rc) return rc;
     if (partition_size <= 0 || max_partitions <= 0) return -3;
@@ -391,7 +523,7 @@ int pkd_oracle_partitions(const uint16_t *q, const uint16_t *k_cache, const uint
                 for (int t = t0; t < t1; ++t) {
                     double e = exp(s[t - t0] - m);
                     l += e;
-                    const uint16_t *v = kv_row(&P, v_cache, b, g, t);
+                    const uint16_t *v = (const uint16_t *)kv_row(&P, v_cache, b, g, t);
                     if (!v) { free(s); return -1; }
                     for (int d = 0; d < D; ++d) o[d] += e * h2d(v[d]);
                 }
@@ -480,6 +612,36 @@ int pkd_oracle_append(const uint16_t *k_new, const uint16_t *v_new, const int32_
                 k_cache[dst + d] = k_new[src + d];
                 v_cache[dst + d] = v_new[src + d];
             }
+        }
+    }
+    return status;
+}
+
+/* The cache write with FP8 caches: as pkd_oracle_append, each element of the
+ * new rows stored as pkd_oracle_quantize_e4m3 gives it (k_scale for K,
+ * v_scale for V).  Same return codes. */
+int pkd_oracle_append_fp8(const uint16_t *k_new, const uint16_t *v_new, const int32_t *block_tables,
+                          const int32_t *context_lens, uint8_t *k_cache, uint8_t *v_cache, int num_seqs,
+                          int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                          int max_blocks_per_seq, float k_scale, float v_scale)
+{
+    if (!k_new || !v_new || !block_tables || !context_lens || !k_cache || !v_cache) return -3;
+    if (num_seqs < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0 ||
+        max_blocks_per_seq <= 0 || !(k_scale > 0.0f) || !(v_scale > 0.0f))
+        return -3;
+    int status = 0;
+    for (int b = 0; b < num_seqs; ++b) {
+        int L = context_lens[b];
+        int logical_block = L / block_size;
+        int slot = L % block_size;
+        if (L < 0 || logical_block >= max_blocks_per_seq) { status = -1; continue; }
+        int p = block_tables[(size_t)b * max_blocks_per_seq + logical_block];
+        if (p < 0 || p >= num_blocks) { status = -1; continue; }
+        for (int g = 0; g < num_kv_heads; ++g) {
+            size_t dst = (((size_t)p * num_kv_heads + g) * block_size + slot) * head_dim;
+            size_t src = ((size_t)b * num_kv_heads + g) * head_dim;
+            pkd_oracle_quantize_e4m3(k_new + src, head_dim, k_scale, k_cache + dst);
+            pkd_oracle_quantize_e4m3(v_new + src, head_dim, v_scale, v_cache + dst);
         }
     }
     return status;

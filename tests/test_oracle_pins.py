@@ -365,12 +365,112 @@ def pin_multi_query_last_is_single_query(mutant=0):
     assert np.array_equal(got[:, -1], single)
 
 
+def torch_e4m3_to_f64(codes):
+    t = torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8))
+    return t.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def pin_e4m3_decoder(mutant=0):
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle.e4m3_to_double(codes, mutant=mutant)
+    ref = torch_e4m3_to_f64(codes)
+    nan = np.isnan(ref)
+    assert np.array_equal(nan, np.isnan(got)) and nan.sum() == 2      # 0x7f and 0xff
+    assert np.array_equal(ref[~nan], got[~nan])
+    assert got[0x7e] == 448.0 and got[0x01] == 2.0 ** -9 and got[0x38] == 1.0
+
+
+def pin_e4m3_rounding(mutant=0):
+    # every finite binary16 value, at two scales: nearest-even rounding of the
+    # fp32 quotient onto the E4M3 grid, compared with torch's conversion where
+    # it does not overflow; beyond, the oracle saturates to +-448
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    x = bits.view(np.float16)
+    fin = np.isfinite(x)
+    x = x[fin]
+    for scale in (1.0, 0.0625, 3.0):
+        got = oracle.quantize_e4m3(x, scale, mutant=mutant)
+        qf = torch.from_numpy(x.astype(np.float32)) / torch.tensor(scale, dtype=torch.float32)
+        inr = (qf.abs() < 464.0).numpy()
+        ref = qf.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        assert np.array_equal(got[inr], ref[inr])
+        big = ~inr
+        assert np.all(got[big] == np.where(qf.numpy()[big] < 0, 0xFE, 0x7E))
+    # ties to even at the smallest step: 0.5 and 1.5 units of 2^-9
+    t = oracle.float_to_e4m3(np.array([2.0 ** -10, 1.5 * 2.0 ** -9, 2.5 * 2.0 ** -9], np.float32), mutant=mutant)
+    assert t.tolist() == [0x00, 0x02, 0x02]
+
+
+def fp8_problem(seed, lens, q_len, Hq, Hkv, D, BS):
+    rng = np.random.default_rng(seed)
+    B = len(lens)
+    nbs = [-(-L // BS) for L in lens]
+    NB = sum(nbs) + 2
+    perm = rng.permutation(NB)[:sum(nbs)]
+    def codes(shape):  # any finite E4M3 code
+        c = rng.integers(0, 0x7f, size=shape, dtype=np.uint8)
+        return (c | (rng.integers(0, 2, size=shape, dtype=np.uint8) << 7)).astype(np.uint8)
+    k8 = codes((NB, Hkv, BS, D))
+    v8 = codes((NB, Hkv, BS, D))
+    lk = [codes((Hkv, L, D)) for L in lens]
+    lv = [codes((Hkv, L, D)) for L in lens]
+    bt = np.full((B, max(1, max(nbs))), -1, np.int32)
+    pos = 0
+    for b, L in enumerate(lens):
+        for i in range(nbs[b]):
+            p = int(perm[pos]); pos += 1
+            bt[b, i] = p
+            t0, t1 = i * BS, min(L, (i + 1) * BS)
+            k8[p, :, : t1 - t0] = lk[b][:, t0:t1]
+            v8[p, :, : t1 - t0] = lv[b][:, t0:t1]
+    q = rng.standard_normal((B, q_len, Hq, D)).astype(np.float16)
+    return dict(q=q, k8=k8, v8=v8, bt=bt, cl=np.array(lens, np.int32), lk=lk, lv=lv)
+
+
+def pin_fp8_attention_sdpa(mutant=0):
+    for seed, (lens, q_len, Hq, Hkv, D, BS, ks, vs) in enumerate([
+        ((37, 100, 5), 1, 8, 2, 32, 16, 0.05, 0.11),
+        ((20, 64), 3, 4, 4, 16, 8, 0.02, 0.3),
+    ]):
+        pr = fp8_problem(900 + seed, list(lens), q_len, Hq, Hkv, D, BS)
+        scale = 1.0 / math.sqrt(D)
+        got = oracle.attention_fp8(pr["q"], pr["k8"], pr["v8"], pr["bt"], pr["cl"], scale, ks, vs, mutant=mutant)
+        # reference: torch decodes the logical codes; SDPA with the causal mask
+        fp = dict(qm=pr["q"], cl=pr["cl"],
+                  lk=[torch_e4m3_to_f64(k) * ks for k in pr["lk"]],
+                  lv=[torch_e4m3_to_f64(v) * vs for v in pr["lv"]])
+        ref = causal_sdpa_reference(fp, scale, Hq, Hkv)
+        assert np.max(np.abs(got - ref)) <= TOL * max(1.0, np.max(np.abs(ref)))
+
+
+def pin_fp8_append(mutant=0):
+    lens, Hkv, D, BS = [5, 16, 0], 2, 16, 16
+    pr = fp8_problem(950, [L + 1 for L in lens], 1, 2, Hkv, D, BS)
+    rng = np.random.default_rng(951)
+    k_new = (rng.standard_normal((3, Hkv, D)) * 3).astype(np.float16)
+    v_new = (rng.standard_normal((3, Hkv, D)) * 3).astype(np.float16)
+    ks, vs = 0.03, 0.5
+    kc, vc = oracle.append_fp8(k_new, v_new, pr["bt"], np.array(lens, np.int32), pr["k8"], pr["v8"], ks, vs,
+                               mutant=mutant)
+    q = lambda x, sc: (torch.from_numpy(x.astype(np.float32)) / torch.tensor(sc, dtype=torch.float32)
+                       ).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    changed = np.zeros(kc.shape[:3], bool)
+    for b, L in enumerate(lens):
+        p = pr["bt"][b, L // BS]
+        changed[p, :, L % BS] = True
+        assert np.array_equal(kc[p, :, L % BS], q(k_new[b], ks))
+        assert np.array_equal(vc[p, :, L % BS], q(v_new[b], vs))
+    assert np.array_equal(kc[~changed], pr["k8"][~changed])
+    assert np.array_equal(vc[~changed], pr["v8"][~changed])
+
+
 PINS = [pin_half_decoder, pin_sdpa_contiguous, pin_permutation_invariance, pin_weights_sum_to_one,
         pin_identical_keys_mean_of_v, pin_scale_zero_mean_of_v, pin_single_token,
         pin_spike_every_position, pin_gqa_equals_repeated_mha, pin_context_zero,
         pin_nan_poison_ignored, pin_partition_merge, pin_partition_counts_scale_zero,
         pin_partition_max_is_max_score, pin_append_then_attend, pin_append_changes_one_row_per_head,
-        pin_multi_query_causal_sdpa, pin_multi_query_ignores_the_future, pin_multi_query_last_is_single_query]
+        pin_multi_query_causal_sdpa, pin_multi_query_ignores_the_future, pin_multi_query_last_is_single_query,
+        pin_e4m3_decoder, pin_e4m3_rounding, pin_fp8_attention_sdpa, pin_fp8_append]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -408,7 +508,7 @@ def test_bad_block_id_is_reported():
         run(pr, 0.3)
 
 
-MUTANTS = list(range(1, 10))
+MUTANTS = list(range(1, 12))
 
 
 @pytest.mark.parametrize("mutant", MUTANTS)
