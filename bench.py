@@ -201,7 +201,27 @@ def time_gpu(args, cfg, variant, dev, inp, steps, warmup, with_e2e=True, with_cl
                                       workspace=ws, error_word=ew, stream=stream)
 
     q_len = getattr(args, "q_len", 1)
-    if q_len > 1:
+    if getattr(args, "kv_fp8", False):
+        # E4M3 caches (one byte per element): the K/V stream halves
+        g = torch.Generator(device=dev).manual_seed(cfg.seed + 9)
+        k8 = workloads.rand_e4m3(inp.k_cache.shape, g, dev)
+        v8 = workloads.rand_e4m3(inp.v_cache.shape, g, dev)
+        kv16 = 2 * sum(lens) * inp.num_kv_heads * inp.head_dim * 2
+        algo -= kv16 // 2
+        qm = inp.q
+        if q_len > 1:
+            qm = workloads.randn_f16((inp.num_seqs, q_len, inp.num_q_heads, inp.head_dim), g, dev)
+            algo += (q_len - 1) * 2 * inp.num_seqs * inp.num_q_heads * inp.head_dim * 2
+        out = torch.empty_like(qm)
+        need = ops.paged_decode_multi_workspace_size(inp.num_seqs, q_len, inp.num_q_heads, inp.num_kv_heads,
+                                                     inp.head_dim, inp.block_size, inp.max_context_len, P)
+        ws = ops.alloc_workspace(need, dev)
+
+        def call():  # noqa: F811
+            ops.paged_decode_attention_fp8(qm, k8, v8, inp.block_tables, inp.context_lens, inp.scale,
+                                           0.05, 0.11, out=out, max_context_len=inp.max_context_len,
+                                           partition_size=P, workspace=ws, error_word=ew, stream=stream)
+    elif q_len > 1:
         # q_len new tokens per sequence (causal among them): the K/V stream is
         # the same, q and out grow by q_len
         g = torch.Generator(device=dev).manual_seed(cfg.seed + 5)
@@ -434,6 +454,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch (profiling runs)")
+    ap.add_argument("--kv-fp8", action="store_true",
+                    help="E4M3 K/V caches (one byte per element, per-cache scales)")
     ap.add_argument("--q-len", type=int, default=1,
                     help="query tokens per sequence (> 1: multi-token queries, causal among them)")
     args = ap.parse_args()
@@ -526,7 +548,7 @@ def main():
     mean_ms, value = aggregate_over_ranks(r["mean_ms"], r["algo_bytes"], ws, dev)
     achieved = r["algo_bytes"] / (r["mean_ms"] * 1e-3) / 1e9
     resolved = variant
-    if args.q_len > 1:
+    if args.q_len > 1 or args.kv_fp8:
         resolved = "tma_mma"
     elif variant == "auto":
         resolved = ops.variant_name(ops.paged_decode_auto_variant(
@@ -535,8 +557,10 @@ def main():
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(mean_ms, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f16 in, f32 arithmetic", "data": "synthetic",
-        "config": {"workload": describe(cfg) + (f", q_len={args.q_len} (causal)" if args.q_len > 1 else ""),
+        "scaling": "weak", "vs_baseline": None, "dtype": ("e4m3 KV, f16 q/out, f32 arithmetic" if args.kv_fp8 else "f16 in, f32 arithmetic"),
+        "data": "synthetic",
+        "config": {"workload": describe(cfg) + (f", q_len={args.q_len} (causal)" if args.q_len > 1 else "")
+                   + (", KV in E4M3 (1 byte/element)" if args.kv_fp8 else ""),
                    "variant": resolved,
                    "partition_size": r["partition_size"],
                    "us_per_call": round(mean_ms * 1e3, 2), "us_per_call_median": round(r["median_ms"] * 1e3, 2),

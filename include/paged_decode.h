@@ -261,6 +261,49 @@ size_t paged_decode_multi_workspace_size(int num_seqs, int q_len, int num_q_head
                                          int partition_size);
 
 /*
+ * paged_decode_attention_fp8 -- decode over FP8 (E4M3) KV caches: k_cache
+ * and v_cache hold one byte per element, same [num_blocks][num_kv_heads]
+ * [block_size][head_dim] layout, with value = e4m3(byte) * k_scale for K and
+ * * v_scale for V (E4M3: 1 sign, 4 exponent bits with bias 7, 3 mantissa
+ * bits, no infinities, largest magnitude 448).  Source: the CSDN answer
+ * "如何优化LLM推理引擎的内存访问延迟？", section 4 (FP8 precision to shrink
+ * the KV footprint); the byte format and the per-cache scale are this
+ * library's reading.  Halves the K/V bytes a step reads.
+ *
+ *   q, out         fp16, [num_seqs][q_len][num_q_heads][head_dim] (q_len = 1:
+ *                  single-query decode; q_len > 1: causal as in
+ *                  paged_decode_attention_multi)
+ *   k_cache, v_cache  device E4M3 bytes, 16-byte aligned
+ *   k_scale, v_scale  finite, > 0
+ *   other arguments as for paged_decode_attention_multi (workspace:
+ *   paged_decode_multi_workspace_size bytes when the context is split).
+ * The scores use the exact fp16 value of every code (all E4M3 values are
+ * fp16 values); the K scale multiplies the softmax scale, and the V scale the
+ * result.  Codes that are NaN (0x7f, 0xff) must not appear in used rows.
+ */
+pkd_status paged_decode_attention_fp8(const void* q, const void* k_cache, const void* v_cache,
+                                      const int32_t* block_tables, const int32_t* context_lens, void* out,
+                                      int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
+                                      int head_dim, int block_size, int num_blocks, int max_blocks_per_seq,
+                                      int max_context_len, float scale, float k_scale, float v_scale,
+                                      int partition_size, void* workspace, size_t workspace_bytes,
+                                      int* error_word, cudaStream_t stream);
+
+/*
+ * paged_kv_append_fp8 -- paged_kv_append into E4M3 caches: every element x
+ * of the new fp16 rows is stored as e4m3(fp32(x) / scale), the division in
+ * IEEE fp32 and the conversion round-to-nearest-even, saturating at +-448
+ * (k_scale for K, v_scale for V; finite, > 0).  head_dim a multiple of 16;
+ * k_cache / v_cache are E4M3 bytes.  Arguments and errors otherwise as for
+ * paged_kv_append.
+ */
+pkd_status paged_kv_append_fp8(const void* k_new, const void* v_new, const int32_t* block_tables,
+                               const int32_t* context_lens, void* k_cache, void* v_cache, int num_seqs,
+                               int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                               int max_blocks_per_seq, float k_scale, float v_scale, int* error_word,
+                               cudaStream_t stream);
+
+/*
  * paged_kv_append -- the cache write that precedes each decode step: stores
  * one new token's K and V rows per sequence into the paged cache, at the
  * sequence's next logical position.  With L = context_lens[b] (the length

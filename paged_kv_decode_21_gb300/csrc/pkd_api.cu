@@ -254,12 +254,15 @@ pkd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
                        int q_len, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                        int num_blocks, int max_blocks_per_seq, int max_context_len, float scale,
                        int partition_size, int variant, int prefetch_distance, void* workspace,
-                       size_t workspace_bytes, int* error_word, cudaStream_t stream) {
+                       size_t workspace_bytes, int* error_word, cudaStream_t stream, int kv_fp8 = 0,
+                       float k_scale = 1.f, float v_scale = 1.f) {
   Shape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq,
           max_context_len};
   pkd_status st = check_shape(s);
   if (st != PKD_OK) return st;
   if (q_len < 1) return PKD_ERR_SHAPE;
+  if (kv_fp8 && !(std::isfinite(k_scale) && std::isfinite(v_scale) && k_scale > 0.f && v_scale > 0.f))
+    return PKD_ERR_SHAPE;
   if (num_seqs == 0) return PKD_OK;
   st = check_inputs(q, k_cache, v_cache, block_tables, context_lens);
   if (st != PKD_OK) return st;
@@ -270,8 +273,8 @@ pkd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
   if (prefetch_distance < 0) return PKD_ERR_SHAPE;
   const int G = num_q_heads / num_kv_heads;
   const int q_chunks = query_chunks(q_len, G);
-  if (q_len > 1) {
-    // several query tokens per sequence: the tensor-core path only
+  if (q_len > 1 || kv_fp8) {
+    // several query tokens per sequence, or E4M3 caches: the tensor-core path only
     const int path = variant_path(variant);
     if (path != PKD_VARIANT_AUTO && path != PKD_VARIANT_TMA_MMA) return PKD_ERR_UNSUPPORTED;
     variant = PKD_VARIANT_TMA_MMA | (variant & PKD_FLAG_L2_EVICT_HINTS);
@@ -309,7 +312,9 @@ pkd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
   p.mode = 0;
   p.q_len = q_len;
   p.q_chunks = q_chunks;
-  p.scale_log2 = scale * 1.4426950408889634f;
+  // E4M3 caches: K = code * k_scale enters the scores, V = code * v_scale the output
+  p.scale_log2 = scale * (kv_fp8 ? k_scale : 1.f) * 1.4426950408889634f;
+  p.v_scale = kv_fp8 ? v_scale : 1.f;
   p.prefetch_distance = prefetch_distance == 0 ? kDefaultPrefetchDistance : prefetch_distance;
   const long long grid = (long long)num_seqs * num_kv_heads * q_chunks * np;
   variant = pick_auto(variant, G, grid, P);
@@ -325,7 +330,15 @@ pkd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
     p.max_logits = w.max_logits;
     p.exp_sums = w.exp_sums;
   }
-  st = launch_decode(variant_path(variant), head_dim, block_size, G, p, grid, stream);
+  if (kv_fp8) {
+    if (grid > 0x7fffffffLL) return PKD_ERR_SHAPE;
+    st = grid <= 0 ? PKD_OK
+                   : (pkd::launch_decode_tma_mma_fp8(head_dim, block_size, G, p, grid, stream) == cudaSuccess
+                          ? PKD_OK
+                          : PKD_ERR_LAUNCH);
+  } else {
+    st = launch_decode(variant_path(variant), head_dim, block_size, G, p, grid, stream);
+  }
   if (st != PKD_OK || !split) return st;
   // the merge sees q_len * Hq rows per sequence
   return launch_reduce(p.tmp_out, p.max_logits, p.exp_sums, context_lens, out, num_seqs, q_len * num_q_heads,
@@ -361,6 +374,19 @@ pkd_status paged_decode_attention_multi(const void* q, const void* k_cache, cons
                      num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, max_context_len,
                      scale, partition_size, PKD_VARIANT_TMA_MMA, 0, workspace, workspace_bytes,
                      error_word, stream);
+}
+
+pkd_status paged_decode_attention_fp8(const void* q, const void* k_cache, const void* v_cache,
+                                      const int32_t* block_tables, const int32_t* context_lens, void* out,
+                                      int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
+                                      int head_dim, int block_size, int num_blocks, int max_blocks_per_seq,
+                                      int max_context_len, float scale, float k_scale, float v_scale,
+                                      int partition_size, void* workspace, size_t workspace_bytes,
+                                      int* error_word, cudaStream_t stream) {
+  return decode_impl(q, k_cache, v_cache, block_tables, context_lens, out, num_seqs, q_len, num_q_heads,
+                     num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, max_context_len,
+                     scale, partition_size, PKD_VARIANT_TMA_MMA, 0, workspace, workspace_bytes, error_word,
+                     stream, 1, k_scale, v_scale);
 }
 
 size_t paged_decode_multi_workspace_size(int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
@@ -433,6 +459,7 @@ pkd_status paged_decode_partitions(const void* q, const void* k_cache, const voi
   p.mode = 1;
   p.q_len = 1;
   p.q_chunks = 1;
+  p.v_scale = 1.f;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.prefetch_distance = prefetch_distance == 0 ? kDefaultPrefetchDistance : prefetch_distance;
   const int G = num_q_heads / num_kv_heads;
@@ -496,6 +523,33 @@ pkd_status paged_kv_append(const void* k_new, const void* v_new, const int32_t* 
       static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), block_tables, context_lens,
       static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), num_seqs, num_kv_heads, chunks,
       block_size, num_blocks, max_blocks_per_seq, error_word);
+  return cudaGetLastError() == cudaSuccess ? PKD_OK : PKD_ERR_LAUNCH;
+}
+
+pkd_status paged_kv_append_fp8(const void* k_new, const void* v_new, const int32_t* block_tables,
+                               const int32_t* context_lens, void* k_cache, void* v_cache, int num_seqs,
+                               int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                               int max_blocks_per_seq, float k_scale, float v_scale, int* error_word,
+                               cudaStream_t stream) {
+  if (num_seqs < 0 || num_kv_heads <= 0 || head_dim <= 0 || head_dim % 16 != 0 || block_size <= 0 ||
+      num_blocks <= 0 || max_blocks_per_seq <= 0)
+    return PKD_ERR_SHAPE;
+  if (!(std::isfinite(k_scale) && std::isfinite(v_scale) && k_scale > 0.f && v_scale > 0.f))
+    return PKD_ERR_SHAPE;
+  if (num_seqs == 0) return PKD_OK;
+  if (!k_new || !v_new || !block_tables || !context_lens || !k_cache || !v_cache) return PKD_ERR_NULL;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(block_tables, 4) || !aligned(context_lens, 4) || (error_word && !aligned(error_word, 4)))
+    return PKD_ERR_ALIGN;
+  const int chunks = head_dim / 16;  // 16 output bytes per thread
+  const long long total = (long long)num_seqs * num_kv_heads * chunks;
+  int sms = sm_count();
+  if (sms <= 0) sms = 148;
+  const int grid = (int)std::min<long long>((total + 255) / 256, (long long)sms * 8);
+  pkd::paged_kv_append_fp8_kernel<<<grid, 256, 0, stream>>>(
+      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), block_tables, context_lens,
+      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), num_seqs, num_kv_heads, chunks, block_size,
+      num_blocks, max_blocks_per_seq, k_scale, v_scale, error_word);
   return cudaGetLastError() == cudaSuccess ? PKD_OK : PKD_ERR_LAUNCH;
 }
 

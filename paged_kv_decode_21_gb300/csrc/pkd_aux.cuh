@@ -100,6 +100,63 @@ __global__ void __launch_bounds__(256) paged_kv_append_kernel(
 }
 
 // ---------------------------------------------------------------------------
+// Paged KV append into E4M3 caches: as paged_kv_append_kernel, with each
+// element stored as e4m3(fp32(x) / scale) -- an IEEE fp32 division, then
+// round-to-nearest-even onto the E4M3 grid saturating at +-448
+// (cvt.rn.satfinite).  One thread writes 16 bytes (16 elements) of the K row
+// and of the V row.
+__device__ __forceinline__ uint32_t quant4_e4m3(const __half2 a, const __half2 b, float scale) {
+  const float2 fa = __half22float2(a), fb = __half22float2(b);
+  const float x0 = __fdiv_rn(fa.x, scale), x1 = __fdiv_rn(fa.y, scale);
+  const float x2 = __fdiv_rn(fb.x, scale), x3 = __fdiv_rn(fb.y, scale);
+  uint16_t lo, hi;
+  // the second source lands in the low byte
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(x1), "f"(x0));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(x3), "f"(x2));
+  return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
+__device__ __forceinline__ uint4 quant16_e4m3(const uint4 a, const uint4 b, float scale) {
+  auto h2 = [](uint32_t u) { return *reinterpret_cast<const __half2*>(&u); };
+  return make_uint4(quant4_e4m3(h2(a.x), h2(a.y), scale), quant4_e4m3(h2(a.z), h2(a.w), scale),
+                    quant4_e4m3(h2(b.x), h2(b.y), scale), quant4_e4m3(h2(b.z), h2(b.w), scale));
+}
+
+__global__ void __launch_bounds__(256) paged_kv_append_fp8_kernel(
+    const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
+    const int32_t* __restrict__ block_tables, const int32_t* __restrict__ context_lens,
+    uint4* __restrict__ k_cache, uint4* __restrict__ v_cache, int num_seqs, int num_kv_heads,
+    int chunks_per_row, int block_size, int num_blocks, int max_blocks_per_seq, float k_scale, float v_scale,
+    int* error_word) {
+  const long long total = (long long)num_seqs * num_kv_heads * chunks_per_row;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const long long row = i / chunks_per_row;  // b * Hkv + g
+    const int c = (int)(i - row * chunks_per_row);
+    const int b = (int)(row / num_kv_heads);
+    const int g = (int)(row - (long long)b * num_kv_heads);
+    // 16 fp16 inputs = two 16-byte loads, issued before the table walk
+    const uint4 k0 = __ldg(k_new + 2 * i), k1 = __ldg(k_new + 2 * i + 1);
+    const uint4 v0 = __ldg(v_new + 2 * i), v1 = __ldg(v_new + 2 * i + 1);
+    const int L = __ldg(context_lens + b);
+    const int lb = L / block_size;
+    if (L < 0 || lb >= max_blocks_per_seq) {
+      if (g == 0 && c == 0) record_error(error_word, kErrBadBlock);
+      continue;
+    }
+    const int p = __ldg(block_tables + (size_t)b * max_blocks_per_seq + lb);
+    if (p < 0 || p >= num_blocks) {
+      if (g == 0 && c == 0) record_error(error_word, kErrBadBlock);
+      continue;
+    }
+    const size_t dst = (((size_t)p * num_kv_heads + g) * block_size + (L - lb * block_size)) *
+                           (size_t)chunks_per_row + c;
+    k_cache[dst] = quant16_e4m3(k0, k1, k_scale);
+    v_cache[dst] = quant16_e4m3(v0, v1, v_scale);
+  }
+}
+
+// ---------------------------------------------------------------------------
 __global__ void validate_tables_kernel(const int32_t* block_tables, const int32_t* context_lens,
                                        int num_seqs, int max_blocks_per_seq, int block_size,
                                        int num_blocks, int* error_word) {

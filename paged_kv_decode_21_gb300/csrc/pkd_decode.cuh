@@ -65,6 +65,7 @@ struct DecodeParams {
   int mode;             // 0: final out when one partition, partials otherwise; 1: partials always
   int q_len;            // query tokens per sequence (1: single-query decode; > 1 tensor-core path only)
   int q_chunks;         // query chunks per (sequence, kv head) in the grid (1 when q_len == 1)
+  float v_scale;        // E4M3 caches: V value = code * v_scale (the K scale is folded into scale_log2)
   float scale_log2;     // softmax scale * log2(e)
   int prefetch_distance;
   int l2_hints;         // 1: evict_first on consuming loads/copies, evict_last on prefetches

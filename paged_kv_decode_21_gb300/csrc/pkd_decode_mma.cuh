@@ -83,6 +83,27 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Four E4M3 bytes -> two fp16 pairs: bytes (0, 1) -> lo, bytes (2, 3) -> hi,
+// the lower byte of each pair in the lower half (exact: every E4M3 value is
+// an fp16 value).
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t x, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\t"
+      "mov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(x));
+}
+
+// An ldmatrix.trans register of E4M3 data holds bytes (t0 d0, t0 d1, t1 d0,
+// t1 d1) for tokens t0 < t1 and dims d0 < d1; regroup to (t0 d0, t1 d0,
+// t0 d1, t1 d1) and convert: d0 -> (t0, t1) fp16 pair, d1 -> the same.
+__device__ __forceinline__ void e4m3_tpair(uint32_t x, uint32_t& d0, uint32_t& d1) {
+  uint32_t y;
+  asm("prmt.b32 %0, %1, 0, 0x3120;" : "=r"(y) : "r"(x));
+  e4m3x4_to_f16x2x2(y, d0, d1);
+}
+
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
@@ -116,8 +137,9 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* tmap) {
 constexpr int mma_query_chunk(int G) { return 16 / G; }
 
 // ---------------------------------------------------------------- layout
-// QC: query tokens per CTA (1 = single-query decode).
-template <int D, int BS, int G, int QC>
+// QC: query tokens per CTA (1 = single-query decode); KVB: bytes per K/V
+// element (2: fp16, 1: E4M3 with per-cache scales).
+template <int D, int BS, int G, int QC, int KVB = 2>
 struct MmaTraits {
   static_assert(D == 64 || D == 128, "head_dim");
   static_assert(BS == 16 || BS == 32, "block_size");
@@ -128,12 +150,18 @@ struct MmaTraits {
   static constexpr int NW = 4;
   static constexpr int THREADS = NW * 32;
   static constexpr int MIN_BLOCKS = 2;
+  static constexpr bool F8 = KVB == 1;
   static constexpr int KSTEPS = D / 16;       // QK k-steps and PV m-tiles
-  static constexpr int NBOX = D / 64;         // 64-column boxes per 16-row sub-tile
-  static constexpr int BOX_BYTES = 16 * 128;  // one swizzled box
+  // A box is 16 rows of BOX_ROWB bytes: 64 fp16 columns, or a whole E4M3 row
+  static constexpr int BOX_X = F8 ? D : 64;               // elements per box row
+  static constexpr int BOX_ROWB = BOX_X * KVB;            // 128, or 64 for E4M3 at D = 64
+  static constexpr int SWZ_MASK = BOX_ROWB == 128 ? 7 : 3;  // 128- or 64-byte swizzle
+  static constexpr int CHUNKS = BOX_ROWB / 16;            // 16-byte chunks per box row
+  static constexpr int NBOX = D / BOX_X;                  // boxes per 16-row sub-tile
+  static constexpr int BOX_BYTES = 16 * BOX_ROWB;         // one swizzled box
   static constexpr int SUB_BYTES = NBOX * BOX_BYTES;      // K (or V) of one sub-tile
   static constexpr int SLOT_BYTES = 2 * SUB_BYTES;        // K then V
-  static constexpr int TILE_BYTES = BS * D * 2;           // one (block, head) tile in HBM
+  static constexpr int TILE_BYTES = BS * D * KVB;         // one (block, head) tile in HBM
   // about 96 KiB of ring per CTA (two CTAs per SM)
   static constexpr int SW_RAW = (96 * 1024) / (NW * SLOT_BYTES);
   static constexpr int SW = SW_RAW > 8 ? 8 : (SW_RAW < 2 ? 2 : SW_RAW);
@@ -146,15 +174,18 @@ struct MmaTraits {
   // the swizzle needs 1024-byte aligned boxes: the kernel aligns the base
   static constexpr int SMEM_BYTES = 1024 + MAIN_BYTES + BAR_BYTES;
   static_assert(BOX_BYTES % 1024 == 0 && SLOT_BYTES % 1024 == 0, "boxes must stay 1024-byte aligned");
+  static_assert(!F8 || (D / 16) % 2 == 0, "E4M3 fragments come in pairs of 16-dim chunks");
   static_assert(MAIN_BYTES % 16 == 0, "barriers must stay 8-byte aligned");
 };
 
 // ---------------------------------------------------------------- kernel
-template <int D, int BS, int G, int QC>
-__global__ void __launch_bounds__(MmaTraits<D, BS, G, QC>::THREADS, MmaTraits<D, BS, G, QC>::MIN_BLOCKS)
+template <int D, int BS, int G, int QC, int KVB = 2>
+__global__ void __launch_bounds__(MmaTraits<D, BS, G, QC, KVB>::THREADS,
+                                  MmaTraits<D, BS, G, QC, KVB>::MIN_BLOCKS)
     paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                             const __grid_constant__ CUtensorMap tmap_v, const DecodeParams P) {
-  using T = MmaTraits<D, BS, G, QC>;
+  using T = MmaTraits<D, BS, G, QC, KVB>;
+  constexpr bool F8 = T::F8;
   constexpr int NW = T::NW, SW = T::SW, KS = T::KSTEPS, NT = T::NT, ROWS = T::ROWS;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // 1024-byte aligned base for the swizzled boxes
@@ -162,12 +193,14 @@ __global__ void __launch_bounds__(MmaTraits<D, BS, G, QC>::THREADS, MmaTraits<D,
   unsigned char* smem = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::MAIN_BYTES);
 
-  // work item: partition j fastest, then the query chunk, then (b, g)
+  // work item: query chunk fastest, then partition j, then (b, g).  The
+  // chunks of one (b, g, j) read the same K/V tiles; launched side by side,
+  // all but the first find them in L2.
   const int np_grid = P.max_partitions;
-  const int j = blockIdx.x % np_grid;
-  const int rest = blockIdx.x / np_grid;
-  const int qc = rest % P.q_chunks;
-  const int bg = rest / P.q_chunks;
+  const int qc = blockIdx.x % P.q_chunks;
+  const int rest = blockIdx.x / P.q_chunks;
+  const int j = rest % np_grid;
+  const int bg = rest / np_grid;
   const int g = bg % P.num_kv_heads;
   const int b = bg / P.num_kv_heads;
   const int L = P.context_lens[b];
@@ -196,10 +229,10 @@ __global__ void __launch_bounds__(MmaTraits<D, BS, G, QC>::THREADS, MmaTraits<D,
   const int t1 = min(min(t0 + PS, L), L - QL + jq0 + nq);
   const int nblk = t1 > t0 ? (t1 - t0 + BS - 1) / BS : 0;
   const int32_t* bt = P.block_tables + (size_t)b * P.max_blocks_per_seq + t0 / BS;
-  const size_t head_stride = (size_t)BS * D;
+  const size_t head_stride = (size_t)T::TILE_BYTES;  // bytes per (block, head) tile
   const size_t block_stride = (size_t)P.num_kv_heads * head_stride;
-  const __half* kbase = P.k_cache + (size_t)g * head_stride;
-  const __half* vbase = P.v_cache + (size_t)g * head_stride;
+  const char* kbase = reinterpret_cast<const char*>(P.k_cache) + (size_t)g * head_stride;
+  const char* vbase = reinterpret_cast<const char*>(P.v_cache) + (size_t)g * head_stride;
   const int pd = P.prefetch_distance;
   const L2Hints l2h = make_l2_hints(P.l2_hints != 0);
 
@@ -217,7 +250,11 @@ __global__ void __launch_bounds__(MmaTraits<D, BS, G, QC>::THREADS, MmaTraits<D,
   }
   const int lim_min = NT == 2 ? min(lim[0], lim[NT - 1]) : lim[0];
 
-  // Q as A fragments: qa[k] = {row r, row r+8} x {dims 16k + 2c, 16k + 8 + 2c}
+  // Q as A fragments: qa[k] = {row r, row r+8} x {k-slots 2c, 2c+1 | 8+2c, 9+2c}.
+  // fp16 K: slot j of step k is dim 16k + j.  E4M3 K: a lane's 4 bytes of a
+  // 16-dim chunk are dims 4c .. 4c+3, so slots (2c, 2c+1 | 8+2c, 9+2c) are
+  // dims 16k + (4c, 4c+1 | 4c+2, 4c+3); Q follows the same map.
+  constexpr int QHI = F8 ? 2 : 8, QMUL = F8 ? 4 : 2;
   uint32_t qa[KS][4];
 #pragma unroll
   for (int hf = 0; hf < 2; ++hf) {
@@ -226,8 +263,8 @@ __global__ void __launch_bounds__(MmaTraits<D, BS, G, QC>::THREADS, MmaTraits<D,
     const __half* qr = P.q + (live ? out_row(rr) * D : 0);
 #pragma unroll
     for (int k = 0; k < KS; ++k) {
-      qa[k][hf] = live ? *reinterpret_cast<const uint32_t*>(qr + 16 * k + 2 * c) : 0u;
-      qa[k][2 + hf] = live ? *reinterpret_cast<const uint32_t*>(qr + 16 * k + 8 + 2 * c) : 0u;
+      qa[k][hf] = live ? *reinterpret_cast<const uint32_t*>(qr + 16 * k + QMUL * c) : 0u;
+      qa[k][2 + hf] = live ? *reinterpret_cast<const uint32_t*>(qr + 16 * k + QHI + QMUL * c) : 0u;
     }
   }
   // O^T m-tile k, n-tile hf: [dim 16k + r | 16k + 8 + r] x [row 8hf + 2c | 8hf + 2c + 1]
@@ -248,11 +285,19 @@ __global__ void __launch_bounds__(MmaTraits<D, BS, G, QC>::THREADS, MmaTraits<D,
   // sub-tile, 16-byte chunk 2s + ((l >> 3) & 1) for step s; with the swizzle
   // the chunk offset of step s is ((2s & 7) ^ x) * 16, x = chunk bit ^ row % 8.
   uint32_t lm_off[4];
-  {
+  if constexpr (!F8) {
     const int row = (lane & 7) + 8 * (lane >> 4);
     const int x = ((lane >> 3) & 1) ^ (row & 7);
 #pragma unroll
     for (int i = 0; i < 4; ++i) lm_off[i] = row * 128 + (((2 * i) ^ x) << 4);
+  } else {
+    // E4M3: one ldmatrix.x4 covers chunks (2i, 2i+1) of 16 rows: lane l
+    // addresses row (l & 7) + 8 * ((l >> 3) & 1), chunk 2i + (l >> 4)
+    const int row = (lane & 7) + 8 * ((lane >> 3) & 1);
+    const int swz = ((row * T::BOX_ROWB) >> 7) & T::SWZ_MASK;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      lm_off[i] = row * T::BOX_ROWB + ((((2 * i + (lane >> 4)) & (T::CHUNKS - 1)) ^ swz) << 4);
   }
 
   uint64_t* full = bars + warp * SW;
@@ -288,8 +333,9 @@ __global__ void __launch_bounds__(MmaTraits<D, BS, G, QC>::THREADS, MmaTraits<D,
         mbar_arrive_expect_tx(&full[slot], T::SLOT_BYTES);
 #pragma unroll
         for (int hb = 0; hb < T::NBOX; ++hb) {
-          tma_load_3d(dst + hb * T::BOX_BYTES, &tmap_k, &full[slot], 64 * hb, y, ic_pb, l2h);
-          tma_load_3d(dst + T::SUB_BYTES + hb * T::BOX_BYTES, &tmap_v, &full[slot], 64 * hb, y, ic_pb, l2h);
+          tma_load_3d(dst + hb * T::BOX_BYTES, &tmap_k, &full[slot], T::BOX_X * hb, y, ic_pb, l2h);
+          tma_load_3d(dst + T::SUB_BYTES + hb * T::BOX_BYTES, &tmap_v, &full[slot], T::BOX_X * hb, y, ic_pb,
+                      l2h);
         }
       }
     }
@@ -326,27 +372,46 @@ __global__ void __launch_bounds__(MmaTraits<D, BS, G, QC>::THREADS, MmaTraits<D,
       if (valid < 16) {
         // rows past the CTA's tokens may hold anything (NaN included): zero the
         // V rows so that p = 0 times them stays 0; masked K rows get -inf below
-        for (int i = lane; i < (16 - valid) * T::NBOX * 8; i += 32) {
-          const int row = valid + i / (T::NBOX * 8);
-          const int rest8 = i % (T::NBOX * 8);
-          *reinterpret_cast<uint4*>(kslot + T::SUB_BYTES + (rest8 / 8) * T::BOX_BYTES + row * 128 +
-                                    (rest8 % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+        for (int i = lane; i < (16 - valid) * T::NBOX * T::CHUNKS; i += 32) {
+          const int row = valid + i / (T::NBOX * T::CHUNKS);
+          const int rest8 = i % (T::NBOX * T::CHUNKS);
+          *reinterpret_cast<uint4*>(kslot + T::SUB_BYTES + (rest8 / T::CHUNKS) * T::BOX_BYTES +
+                                    row * T::BOX_ROWB + (rest8 % T::CHUNKS) * 16) = make_uint4(0u, 0u, 0u, 0u);
         }
         fence_proxy_async_smem();  // ordered before the next tensor copy into this slot
         __syncwarp();
       }
       // ---- S = Q K^T: two n-tiles (tokens 0..7, 8..15)
       float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int k = 0; k < KS; ++k) {
-        uint32_t kb[4];
-        ldsm_x4(ks + (k / 4) * T::BOX_BYTES + lm_off[k % 4], kb);
+      auto qk = [&](int k, uint32_t b00, uint32_t b01, uint32_t b10, uint32_t b11) {
         if constexpr (NT == 1) {
-          mma_16816_top(s0, qa[k][0], qa[k][2], kb[0], kb[1]);
-          mma_16816_top(s1, qa[k][0], qa[k][2], kb[2], kb[3]);
+          mma_16816_top(s0, qa[k][0], qa[k][2], b00, b01);
+          mma_16816_top(s1, qa[k][0], qa[k][2], b10, b11);
         } else {
-          mma_16816(s0, qa[k], kb[0], kb[1]);
-          mma_16816(s1, qa[k], kb[2], kb[3]);
+          mma_16816(s0, qa[k], b00, b01);
+          mma_16816(s1, qa[k], b10, b11);
+        }
+      };
+      if constexpr (!F8) {
+#pragma unroll
+        for (int k = 0; k < KS; ++k) {
+          uint32_t kb[4];
+          ldsm_x4(ks + (k / 4) * T::BOX_BYTES + lm_off[k % 4], kb);
+          qk(k, kb[0], kb[1], kb[2], kb[3]);
+        }
+      } else {
+        // kb: (tokens 0-7, chunk 2i), (8-15, 2i), (0-7, 2i+1), (8-15, 2i+1)
+#pragma unroll
+        for (int i = 0; i < KS / 2; ++i) {
+          uint32_t kb[4];
+          ldsm_x4(ks + lm_off[i], kb);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t b00, b01, b10, b11;
+            e4m3x4_to_f16x2x2(kb[2 * h], b00, b01);
+            e4m3x4_to_f16x2x2(kb[2 * h + 1], b10, b11);
+            qk(2 * i + h, b00, b01, b10, b11);
+          }
         }
       }
       // ---- online softmax of rows r + 8hf over tokens 2c, 2c+1, 8+2c, 9+2c
@@ -410,12 +475,31 @@ __global__ void __launch_bounds__(MmaTraits<D, BS, G, QC>::THREADS, MmaTraits<D,
         pb[hf][1] = pack_half2(p2, p3);  // P^T[tokens 8+2c, 9+2c][row 8hf + r]
       }
       // ---- O^T += V^T P^T, one m-tile of 16 dims per step
+      if constexpr (!F8) {
 #pragma unroll
-      for (int k = 0; k < KS; ++k) {
-        uint32_t va[4];
-        ldsm_x4_trans(vs + (k / 4) * T::BOX_BYTES + lm_off[k % 4], va);
+        for (int k = 0; k < KS; ++k) {
+          uint32_t va[4];
+          ldsm_x4_trans(vs + (k / 4) * T::BOX_BYTES + lm_off[k % 4], va);
 #pragma unroll
-        for (int hf = 0; hf < NT; ++hf) mma_16816(o[k][hf], va, pb[hf][0], pb[hf][1]);
+          for (int hf = 0; hf < NT; ++hf) mma_16816(o[k][hf], va, pb[hf][0], pb[hf][1]);
+        }
+      } else {
+        // vt: (tokens 0-7, chunk 2i), (8-15, 2i), (0-7, 2i+1), (8-15, 2i+1), each
+        // register (token pair) x (dim pair); m-tile rows r and r + 8 are dims
+        // 2r and 2r + 1 of the chunk
+#pragma unroll
+        for (int i = 0; i < KS / 2; ++i) {
+          uint32_t vt[4];
+          ldsm_x4_trans(vs + lm_off[i], vt);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t va[4];
+            e4m3_tpair(vt[2 * h], va[0], va[1]);
+            e4m3_tpair(vt[2 * h + 1], va[2], va[3]);
+#pragma unroll
+            for (int hf = 0; hf < NT; ++hf) mma_16816(o[2 * i + h][hf], va, pb[hf][0], pb[hf][1]);
+          }
+        }
       }
     }
     __syncwarp();
@@ -447,15 +531,17 @@ __global__ void __launch_bounds__(MmaTraits<D, BS, G, QC>::THREADS, MmaTraits<D,
     }
     float* acc = mrg_acc + warp * ROWS * D;
     const int ra = 8 * hf + 2 * c;
+    // dims of m-tile rows r and r + 8: fp16 16k + r, 16k + 8 + r; E4M3 16k + 2r, 16k + 2r + 1
+    const int d_lo = F8 ? 2 * r : r, d_hi = F8 ? 2 * r + 1 : 8 + r;
 #pragma unroll
     for (int k = 0; k < KS; ++k) {
       if (ra < ROWS) {
-        acc[ra * D + 16 * k + r] = o[k][hf][0];
-        acc[ra * D + 16 * k + 8 + r] = o[k][hf][2];
+        acc[ra * D + 16 * k + d_lo] = o[k][hf][0];
+        acc[ra * D + 16 * k + d_hi] = o[k][hf][2];
       }
       if (ra + 1 < ROWS) {
-        acc[(ra + 1) * D + 16 * k + r] = o[k][hf][1];
-        acc[(ra + 1) * D + 16 * k + 8 + r] = o[k][hf][3];
+        acc[(ra + 1) * D + 16 * k + d_lo] = o[k][hf][1];
+        acc[(ra + 1) * D + 16 * k + d_hi] = o[k][hf][3];
       }
     }
   }
@@ -473,6 +559,7 @@ __global__ void __launch_bounds__(MmaTraits<D, BS, G, QC>::THREADS, MmaTraits<D,
       Z = fmaf(cw, mrg_l[w * 16 + rr], Z);
       O = fmaf(cw, mrg_acc[(w * ROWS + rr) * D + d], O);
     }
+    if constexpr (F8) O *= P.v_scale;  // V = code * v_scale
     const size_t row = out_row(rr);
     if (final_out) {
       P.out[row * D + d] = __float2half_rn(Z > 0.f ? O / Z : 0.f);  // Z = 0: the query saw no token

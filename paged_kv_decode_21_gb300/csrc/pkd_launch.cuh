@@ -63,5 +63,7 @@ cudaError_t launch_decode_tma_mma(int D, int BS, int G, const DecodeParams& p, l
                                   cudaStream_t stream);
 cudaError_t launch_decode_tma_mma_multi(int D, int BS, int G, const DecodeParams& p, long long grid,
                                         cudaStream_t stream);
+cudaError_t launch_decode_tma_mma_fp8(int D, int BS, int G, const DecodeParams& p, long long grid,
+                                      cudaStream_t stream);
 
 }  // namespace pkd

@@ -70,6 +70,11 @@ def lib():
         L.paged_decode_attention_multi.restype = I
         L.paged_decode_multi_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
         L.paged_decode_multi_workspace_size.restype = S
+        L.paged_decode_attention_fp8.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, F, F, I, P, S,
+                                                 P, P]
+        L.paged_decode_attention_fp8.restype = I
+        L.paged_kv_append_fp8.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, F, F, P, P]
+        L.paged_kv_append_fp8.restype = I
         L.paged_kv_append.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, P]
         L.paged_kv_append.restype = I
         L.pkd_selftest_bounded_wait.argtypes = [P, ctypes.c_ulonglong, P]
@@ -297,6 +302,68 @@ def paged_decode_attention_multi(q, k_cache, v_cache, block_tables, context_lens
                                             _ptr(error_word), _stream(stream))
     _check(st, "paged_decode_attention_multi")
     return out
+
+
+def _want_fp8_cache(t: torch.Tensor, name: str):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dim() != 4 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous 4-D CUDA tensor")
+    if t.element_size() != 1:
+        raise ValueError(f"{name} must hold one byte per element (uint8 or float8_e4m3fn)")
+
+
+def paged_decode_attention_fp8(q, k_cache, v_cache, block_tables, context_lens, scale, k_scale, v_scale,
+                               out=None, max_context_len=None, partition_size=0, workspace=None,
+                               error_word=None, stream=None) -> torch.Tensor:
+    """Decode over E4M3 caches (value = code * k_scale / v_scale); q is
+    [B][Hq][D] (single query) or [B][q_len][Hq][D] (causal multi-token)."""
+    single = q.dim() == 3
+    qm = q.unsqueeze(1) if single else q
+    _want(qm, "q", torch.float16, 4)
+    _want_fp8_cache(k_cache, "k_cache")
+    _want_fp8_cache(v_cache, "v_cache")
+    _want(block_tables, "block_tables", torch.int32, 2)
+    _want(context_lens, "context_lens", torch.int32, 1)
+    B, QL, Hq, D = qm.shape
+    NB, Hkv, BS, D2 = k_cache.shape
+    if D2 != D or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("k_cache / v_cache shape mismatch")
+    if block_tables.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("block_tables / context_lens batch mismatch")
+    if out is None:
+        out = torch.empty_like(q)
+    _want(out, "out", torch.float16, q.dim())
+    maxlen = _max_len(context_lens, max_context_len)
+    need = paged_decode_multi_workspace_size(B, QL, Hq, Hkv, D, BS, maxlen, partition_size)
+    if workspace is None:
+        workspace = alloc_workspace(need, q.device)
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().paged_decode_attention_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                          _ptr(context_lens), _ptr(out), B, QL, Hq, Hkv, D, BS, NB,
+                                          block_tables.shape[1], maxlen, float(scale), float(k_scale),
+                                          float(v_scale), int(partition_size), _ptr(workspace), wsb,
+                                          _ptr(error_word), _stream(stream))
+    _check(st, "paged_decode_attention_fp8")
+    return out
+
+
+def paged_kv_append_fp8(k_new, v_new, block_tables, context_lens, k_cache, v_cache, k_scale, v_scale,
+                        error_word=None, stream=None):
+    """Quantize each sequence's new K/V row (fp16 [B][Hkv][D]) to E4M3 and write it
+    at logical position context_lens[b] of the byte caches, in place."""
+    _want(k_new, "k_new", torch.float16, 3)
+    _want(v_new, "v_new", torch.float16, 3)
+    _want_fp8_cache(k_cache, "k_cache")
+    _want_fp8_cache(v_cache, "v_cache")
+    _want(block_tables, "block_tables", torch.int32, 2)
+    _want(context_lens, "context_lens", torch.int32, 1)
+    NB, Hkv, BS, D = k_cache.shape
+    B = context_lens.shape[0]
+    if tuple(k_new.shape) != (B, Hkv, D) or tuple(v_new.shape) != (B, Hkv, D):
+        raise ValueError("k_new / v_new must be [num_seqs][num_kv_heads][head_dim]")
+    st = lib().paged_kv_append_fp8(_ptr(k_new), _ptr(v_new), _ptr(block_tables), _ptr(context_lens),
+                                   _ptr(k_cache), _ptr(v_cache), B, Hkv, D, BS, NB, block_tables.shape[1],
+                                   float(k_scale), float(v_scale), _ptr(error_word), _stream(stream))
+    _check(st, "paged_kv_append_fp8")
 
 
 def paged_kv_append(k_new, v_new, block_tables, context_lens, k_cache, v_cache, error_word=None,

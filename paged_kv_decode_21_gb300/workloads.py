@@ -164,6 +164,20 @@ def randn_f16(shape, generator: torch.Generator, device) -> torch.Tensor:
     return out
 
 
+def rand_e4m3(shape, generator: torch.Generator, device, exp_lo: int = 4, exp_hi: int = 10) -> torch.Tensor:
+    """Random E4M3 bit patterns (uint8): random sign and mantissa, biased
+    exponent uniform in [exp_lo, exp_hi] (magnitudes 2^(exp_lo-7) .. 2^(exp_hi-6)),
+    never a NaN code.  A bit-pattern generator: no rounding or scaling."""
+    n = 1
+    for x in shape:
+        n *= int(x)
+    bits = torch.randint(0, 1 << 16, (n,), generator=generator, device=device, dtype=torch.int32)
+    sign = (bits & 1) << 7
+    mant = (bits >> 1) & 7
+    expo = exp_lo + ((bits >> 4) % (exp_hi - exp_lo + 1))
+    return (sign | (expo << 3) | mant).to(torch.uint8).view(*shape)
+
+
 def make_inputs(cfg: DecodeConfig, device="cpu", context_lens: Optional[torch.Tensor] = None,
                 max_blocks_per_seq: Optional[int] = None) -> DecodeInputs:
     """Draw every tensor of ``cfg`` with its seed; q/k/v are drawn on ``device``."""
