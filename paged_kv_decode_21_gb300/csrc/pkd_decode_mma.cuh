@@ -150,6 +150,7 @@ struct MmaTraits {
   static constexpr int NW = 4;
   static constexpr int THREADS = NW * 32;
   static constexpr int MIN_BLOCKS = 2;
+  static constexpr int QK_CHAINS = 2;         // independent accumulator chains per QK n-tile
   static constexpr bool F8 = KVB == 1;
   static constexpr int KSTEPS = D / 16;       // QK k-steps and PV m-tiles
   // A box is 16 rows of BOX_ROWB bytes: 64 fp16 columns, or a whole E4M3 row
@@ -381,15 +382,22 @@ __global__ void __launch_bounds__(MmaTraits<D, BS, G, QC, KVB>::THREADS,
         fence_proxy_async_smem();  // ordered before the next tensor copy into this slot
         __syncwarp();
       }
-      // ---- S = Q K^T: two n-tiles (tokens 0..7, 8..15)
-      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+      // ---- S = Q K^T: two n-tiles (tokens 0..7, 8..15); the k-steps alternate
+      // between QK_CHAINS accumulators so that dependent MMAs do not form one
+      // long chain
+      constexpr int QC_ = T::QK_CHAINS;
+      float sa[QC_][4], sb[QC_][4];
+#pragma unroll
+      for (int ch = 0; ch < QC_; ++ch)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sa[ch][e] = sb[ch][e] = 0.f;
       auto qk = [&](int k, uint32_t b00, uint32_t b01, uint32_t b10, uint32_t b11) {
         if constexpr (NT == 1) {
-          mma_16816_top(s0, qa[k][0], qa[k][2], b00, b01);
-          mma_16816_top(s1, qa[k][0], qa[k][2], b10, b11);
+          mma_16816_top(sa[k % QC_], qa[k][0], qa[k][2], b00, b01);
+          mma_16816_top(sb[k % QC_], qa[k][0], qa[k][2], b10, b11);
         } else {
-          mma_16816(s0, qa[k], b00, b01);
-          mma_16816(s1, qa[k], b10, b11);
+          mma_16816(sa[k % QC_], qa[k], b00, b01);
+          mma_16816(sb[k % QC_], qa[k], b10, b11);
         }
       };
       if constexpr (!F8) {
@@ -412,6 +420,17 @@ __global__ void __launch_bounds__(MmaTraits<D, BS, G, QC, KVB>::THREADS,
             e4m3x4_to_f16x2x2(kb[2 * h + 1], b10, b11);
             qk(2 * i + h, b00, b01, b10, b11);
           }
+        }
+      }
+      float s0[4], s1[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        s0[e] = sa[0][e];
+        s1[e] = sb[0][e];
+#pragma unroll
+        for (int ch = 1; ch < QC_; ++ch) {
+          s0[e] += sa[ch][e];
+          s1[e] += sb[ch][e];
         }
       }
       // ---- online softmax of rows r + 8hf over tokens 2c, 2c+1, 8+2c, 9+2c
