@@ -447,7 +447,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=list(workloads.CONFIGS))
     ap.add_argument("--variant", default="auto",
-                    help="auto|no_prefetch|l2_prefetch|tma_staged, optionally +l2_hints (L2 eviction priorities)")
+                    help="auto|no_prefetch|l2_prefetch|tma_staged|tma_mma, optionally +l2_hints "
+                         "(L2 eviction priorities)")
     ap.add_argument("--partition-size", type=int, default=None)
     ap.add_argument("--prefetch-distance", type=int, default=0)
     ap.add_argument("--sweep", action="store_true", help="every workload x variant, one line each")

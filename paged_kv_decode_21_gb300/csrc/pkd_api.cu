@@ -157,18 +157,31 @@ pkd_status launch_reduce(const float* tmp_out, const float* max_logits, const fl
   const size_t smem = (size_t)max_num_partitions * sizeof(float);
   if (smem > 48 * 1024) return PKD_ERR_SHAPE;
   __half* o = static_cast<__half*>(out);
+  // Programmatic dependent launch: the merge may become resident while the
+  // decode grid's last CTAs still run; its griddepcontrol.wait holds it until
+  // that grid has completed and its partials are visible.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e;
   if (head_dim == 128) {
-    pkd::paged_decode_reduce_kernel<128><<<(unsigned)grid, 128, smem, stream>>>(
-        tmp_out, max_logits, exp_sums, context_lens, o, num_q_heads, partition_size,
-        max_num_partitions, min_merge);
+    cfg.blockDim = dim3(128);
+    e = cudaLaunchKernelEx(&cfg, pkd::paged_decode_reduce_kernel<128>, tmp_out, max_logits, exp_sums,
+                           context_lens, o, num_q_heads, partition_size, max_num_partitions, min_merge);
   } else if (head_dim == 64) {
-    pkd::paged_decode_reduce_kernel<64><<<(unsigned)grid, 64, smem, stream>>>(
-        tmp_out, max_logits, exp_sums, context_lens, o, num_q_heads, partition_size,
-        max_num_partitions, min_merge);
+    cfg.blockDim = dim3(64);
+    e = cudaLaunchKernelEx(&cfg, pkd::paged_decode_reduce_kernel<64>, tmp_out, max_logits, exp_sums,
+                           context_lens, o, num_q_heads, partition_size, max_num_partitions, min_merge);
   } else {
     return PKD_ERR_UNSUPPORTED;
   }
-  return cudaGetLastError() == cudaSuccess ? PKD_OK : PKD_ERR_LAUNCH;
+  return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? PKD_OK : PKD_ERR_LAUNCH;
 }
 
 pkd_status check_inputs(const void* q, const void* k_cache, const void* v_cache,

@@ -15,6 +15,9 @@ __global__ void __launch_bounds__(D) paged_decode_reduce_kernel(
     const float* __restrict__ exp_sums, const int32_t* __restrict__ context_lens, __half* out,
     int num_q_heads, int partition_size, int max_partitions, int min_partitions_to_merge) {
   extern __shared__ float wsm[];  // [max_partitions] weights, then [1] 1/Z
+  // launched as a programmatic dependent of the decode grid: wait until that
+  // grid has completed and its partials are visible (a no-op otherwise)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int row = blockIdx.x;     // b * Hq + h
   const int b = row / num_q_heads;
   const int L = context_lens[b];
