@@ -396,6 +396,8 @@ __global__ void __launch_bounds__(DecodeTraits<D, BS, G, VARIANT>::THREADS,
   const int bg = blockIdx.x / np_grid;
   const int g = bg % P.num_kv_heads;
   const int b = bg / P.num_kv_heads;
+  // the split-K merge (a programmatic dependent) may launch once every CTA has started
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int L = P.context_lens[b];
   const int PS = P.partition_size;
   const int np_b = (L + PS - 1) / PS;
