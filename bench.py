@@ -396,6 +396,22 @@ def cpu_oracle_rate(inp, target_s=10.0, max_passes=50):
     return algo * passes / t / 1e9, cores, sample, t / passes
 
 
+def cpu_oracle_rate_1thread(inp, nseq=4):
+    """The oracle on one host thread, over all query rows of the first `nseq`
+    sequences (a bounded sample of the same workload); returns (GB/s, sample)."""
+    import oracle
+    cpu = inp.to("cpu")
+    nseq = max(1, min(nseq, cpu.num_seqs))
+    lens = cpu.context_lens.tolist()[:nseq]
+    algo = traffic.algorithmic_bytes(lens, cpu.num_q_heads, cpu.num_kv_heads, cpu.head_dim)
+    rows = [b * cpu.num_q_heads + h for b in range(nseq) for h in range(cpu.num_q_heads)]
+    t0 = time.perf_counter()
+    oracle.attention(cpu.q, cpu.k_cache, cpu.v_cache, cpu.block_tables, cpu.context_lens, cpu.scale,
+                     rows=rows, threads=1)
+    t = time.perf_counter() - t0
+    return algo / t / 1e9, f"all query rows of {nseq} sequences ({algo / 1e6:.1f} MB) on 1 thread, {t:.2f} s"
+
+
 def make_workload(name, dev, batch=None):
     import dataclasses
     cfg = workloads.CONFIGS[name]
@@ -593,7 +609,9 @@ def main():
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         v, cores, sample, _ = cpu_oracle_rate(inp)
+        v1, sample1 = cpu_oracle_rate_1thread(inp)
         line["cpu_baseline"] = {"value": round(v, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                "value_1_thread": round(v1, 3), "sample_1_thread": sample1,
                                 "sample": sample}
     if rank == 0:
         print(json.dumps(line), flush=True)
