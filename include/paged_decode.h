@@ -92,6 +92,18 @@ typedef enum {
  *       Asynchronous KV Cache Prefetching".  Results are unchanged.
  */
 #define PKD_FLAG_L2_EVICT_HINTS 0x100
+/*
+ *   PKD_FLAG_LONGEST_FIRST  hand the decode grid's work out longest sequence
+ *       first: a one-CTA-per-128-sequences kernel ranks the sequences by
+ *       context length (ties by index) into the workspace, and the tensor-core
+ *       decode grid walks the ranks, so the last CTAs to start hold the
+ *       shortest work and the tail of a ragged batch shortens.  Results are
+ *       unchanged.  Tensor-core path only, batches of 2..4096 sequences;
+ *       elsewhere it is ignored.  The workspace grows by the order
+ *       (paged_decode_workspace_size counts it, after the split partials);
+ *       a workspace without that room runs the plain order.
+ */
+#define PKD_FLAG_LONGEST_FIRST 0x200
 
 /*
  * paged_decode_attention -- the whole operation, one partition per
@@ -127,13 +139,18 @@ pkd_status paged_decode_attention(const void* q, const void* k_cache, const void
  *                   block_size).  A sequence longer than one partition is
  *                   computed by one CTA per (sequence, kv head, partition)
  *                   and merged by the split-K reduce; shorter ones are
- *                   written directly.
+ *                   written directly.  The automatic choice splits only
+ *                   grids of fewer than two waves of (sequence, kv head)
+ *                   units, and walks unsplit grids of one to six waves
+ *                   longest first (PKD_FLAG_LONGEST_FIRST) when the
+ *                   workspace has room for the order.
  *   variant         pkd_variant, optionally ORed with PKD_FLAG_* bits
  *   prefetch_distance  how many of a warp's iterations ahead the L2 prefetch
  *                   runs (0 = default, 1); ignored by PKD_VARIANT_NO_PREFETCH
  *   workspace, workspace_bytes  device scratch of at least
  *                   paged_decode_workspace_size(...) bytes, 256-byte aligned
- *                   (may be NULL when no sequence is split)
+ *                   (may be NULL when no sequence is split; the automatic
+ *                   order then falls back to the plain one)
  *   error_word      device int or NULL; see "Errors" above
  * Calls that share a workspace must not overlap on the GPU.
  */
@@ -160,7 +177,9 @@ int paged_decode_auto_partition_size(int num_seqs, int num_q_heads, int num_kv_h
  * above): the fp32
  * partials [num_seqs][num_q_heads][NP][head_dim] and the per-partition
  * max and sum [num_seqs][num_q_heads][NP], NP = ceil(max_context_len /
- * partition_size), each region 256-byte aligned.  0 when nothing splits.
+ * partition_size), then, for partition_size 0 or PKD_FLAG_LONGEST_FIRST,
+ * the longest-first order (num_seqs int32), each region 256-byte aligned.
+ * 0 when nothing splits and no order is kept.
  */
 /*
  * paged_decode_auto_variant -- the variant value (data path ORed with
@@ -169,7 +188,8 @@ int paged_decode_auto_partition_size(int num_seqs, int num_q_heads, int num_kv_h
  * automatic, -1 = unsplit, or a partition).  It is TMA_MMA, except for group
  * size 1 with at most 512 tokens per CTA and between 1 and 16 CTAs per SM,
  * where it is NO_PREFETCH (plain loads: a warp handles too few blocks for a
- * shared-memory ring to pay off).
+ * shared-memory ring to pay off).  With partition_size 0, TMA_MMA carries
+ * PKD_FLAG_LONGEST_FIRST where the automatic choice orders the batch.
  * Returns -2 on an invalid shape or partition size.
  */
 int paged_decode_auto_variant(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
@@ -245,7 +265,9 @@ pkd_status paged_decode_validate_tables(const int32_t* block_tables, const int32
  *   CTA serves 16 / G query tokens of one (sequence, kv head, partition), so
  *   every K/V tile is read once per group of 16 / G query tokens.
  *   workspace      required when the context is split
- *                  (paged_decode_multi_workspace_size bytes, 256-byte aligned)
+ *                  (paged_decode_multi_workspace_size bytes, 256-byte aligned);
+ *                  with partition_size 0 it also keeps the longest-first
+ *                  order (NULL then runs the plain order)
  */
 pkd_status paged_decode_attention_multi(const void* q, const void* k_cache, const void* v_cache,
                                         const int32_t* block_tables, const int32_t* context_lens,

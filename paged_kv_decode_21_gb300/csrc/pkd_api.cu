@@ -16,7 +16,11 @@ constexpr unsigned long long kWaitBudgetNs = 100ull * 1000ull * 1000ull;  // 100
 constexpr int kDefaultPrefetchDistance = 1;  // measured best or tied on every workload
 constexpr int kMinAutoPartition = 512;
 constexpr int kMaxAutoPartition = 2048;
-constexpr int kTargetWaves = 6;      // split when the grid would cover fewer waves than this
+constexpr int kSplitWaves = 2;       // split when the (sequence, kv head) units cover fewer waves than this,
+constexpr int kTargetWaves = 6;      // into enough partitions for this many waves;
+constexpr int kLongContext = 8192;   // contexts this long split below kTargetWaves waves
+constexpr int kOrderMaxWaves = 6;    // unsplit grids below this many waves walk longest first,
+constexpr int kOrderMinContext = 1024;  // when their contexts reach this many tokens
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -51,7 +55,8 @@ int sm_count() {
 int variant_path(int variant) { return variant & 0xff; }
 bool variant_ok(int variant) {
   const int path = variant_path(variant);
-  return variant >= 0 && path <= PKD_VARIANT_TMA_MMA && (variant & ~0xff & ~PKD_FLAG_L2_EVICT_HINTS) == 0;
+  return variant >= 0 && path <= PKD_VARIANT_TMA_MMA &&
+         (variant & ~0xff & ~PKD_FLAG_L2_EVICT_HINTS & ~PKD_FLAG_LONGEST_FIRST) == 0;
 }
 
 int resolve_variant(int variant) {
@@ -90,20 +95,34 @@ int ctas_per_sm(int variant, int group) {
   return (resolve_variant(variant) == PKD_VARIANT_TMA_STAGED && group >= 2 && group <= 5) ? 3 : 2;
 }
 
+// Resident CTAs of one wave for a data path and group size.
+long long wave_ctas(int variant, int group) {
+  int sms = sm_count();
+  if (sms <= 0) sms = 148;
+  return (long long)sms * ctas_per_sm(variant, group);
+}
+
 // Partition size for the automatic split, or -1 for none.  A shape is split
-// only when its (sequence, kv head) units would give the GPU fewer than
-// kTargetWaves waves of resident CTAs; the partition is then the largest
-// power of two (at most kMaxAutoPartition, at least kMinAutoPartition tokens)
-// that yields enough CTAs.  Powers of two keep partition boundaries aligned
-// with the blocks of every sequence.
+// when its (sequence, kv head) units would give the GPU fewer than
+// kSplitWaves waves of resident CTAs, or, for contexts of kLongContext
+// tokens and more, fewer than kTargetWaves waves; the partition is then the
+// largest power of two (at most kMaxAutoPartition, at least
+// kMinAutoPartition tokens) that yields kTargetWaves waves.  Powers of two
+// keep partition boundaries aligned with the blocks of every sequence.
+// Shorter contexts from two waves up run unsplit: there the merge pass and
+// the shorter CTAs cost more than the tail they save (GQA 4:1 at 3.4 waves:
+// 168 us unsplit against 180 us at P = 1024), and a ragged batch's tail is
+// shortened by walking it longest first instead (auto_order).  Long ones
+// split cheaply, and a grid of a few waves of very long CTAs leaves the
+// latency-bound E4M3 kernel a costly last wave (GQA 7:1, 8192 tokens: 358
+// us at P = 2048 against 394 us unsplit).
 int auto_partition(const Shape& s, int variant = PKD_VARIANT_AUTO, int q_chunks = 1) {
   const long long units = (long long)s.num_seqs * s.num_kv_heads * q_chunks;
   if (units <= 0 || s.max_context_len <= kMinAutoPartition) return -1;
-  int sms = sm_count();
-  if (sms <= 0) sms = 148;
-  const long long want =
-      (long long)kTargetWaves * sms * ctas_per_sm(variant, s.num_q_heads / s.num_kv_heads);
-  if (units >= want) return -1;
+  const long long wave = wave_ctas(variant, s.num_q_heads / s.num_kv_heads);
+  const long long split_below = (s.max_context_len >= kLongContext ? kTargetWaves : kSplitWaves) * wave;
+  if (units >= split_below) return -1;
+  const long long want = kTargetWaves * wave;
   const long long np = (want + units - 1) / units;
   const long long per = (s.max_context_len + np - 1) / np;
   long long p = kMinAutoPartition;
@@ -118,6 +137,28 @@ struct Workspace {
   float* exp_sums;
   size_t bytes;
 };
+
+// Bytes of the longest-first order (one int32 per sequence) appended to a workspace.
+size_t order_bytes(int num_seqs) { return round_up((size_t)num_seqs * sizeof(int32_t), 256); }
+
+// Whether the automatic split also walks the batch longest first: an unsplit
+// grid of one to kOrderMaxWaves waves, where the last wave's short CTAs
+// decide the tail, of contexts long enough that the order kernel's few
+// microseconds are paid back.  Lengths of equal sequences leave the order
+// harmless (about 1% at 3-7 waves); ragged ones gain up to 1.1x.
+bool auto_order(const Shape& s, int variant, int q_chunks, int partition) {
+  const long long units = (long long)s.num_seqs * s.num_kv_heads * q_chunks;
+  const long long wave = wave_ctas(variant, s.num_q_heads / s.num_kv_heads);
+  return partition <= 0 && s.num_seqs >= 2 && s.num_seqs <= pkd::kOrderMaxSeqs &&
+         s.max_context_len >= kOrderMinContext && units >= wave && units < kOrderMaxWaves * wave;
+}
+
+// Whether a launch walks the sequences longest first: asked for by flag, on
+// the tensor-core path, for batches whose lengths fit the order kernel.
+bool want_order(int variant, int resolved_path, int num_seqs) {
+  return (variant & PKD_FLAG_LONGEST_FIRST) && resolved_path == PKD_VARIANT_TMA_MMA && num_seqs > 1 &&
+         num_seqs <= pkd::kOrderMaxSeqs;
+}
 
 Workspace layout(void* base, int num_seqs, int num_q_heads, int head_dim, int np) {
   const size_t rows = (size_t)num_seqs * num_q_heads * np;
@@ -233,8 +274,12 @@ int paged_decode_auto_variant(int num_seqs, int num_q_heads, int num_kv_heads, i
   const bool split = P > 0 && max_context_len > P;
   const long long np = split ? (max_context_len + P - 1) / P : 1;
   const long long tokens = split ? P : (long long)round_up((size_t)(max_context_len > 0 ? max_context_len : 1), 32);
-  return pick_auto(PKD_VARIANT_AUTO, num_q_heads / num_kv_heads, (long long)num_seqs * num_kv_heads * np,
-                   tokens);
+  const int v = pick_auto(PKD_VARIANT_AUTO, num_q_heads / num_kv_heads, (long long)num_seqs * num_kv_heads * np,
+                          tokens);
+  if (partition_size == 0 && v == PKD_VARIANT_TMA_MMA && auto_order(s, v, 1, P) &&
+      want_order(PKD_FLAG_LONGEST_FIRST, v, num_seqs))
+    return v | PKD_FLAG_LONGEST_FIRST;
+  return v;
 }
 
 size_t paged_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
@@ -244,9 +289,11 @@ size_t paged_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_hea
   if (check_shape(s) != PKD_OK) return 0;
   if (!variant_ok(variant)) return 0;
   int P = partition_size == 0 ? auto_partition(s, variant) : partition_size;
-  if (P <= 0 || max_context_len <= P) return 0;
-  const int np = (max_context_len + P - 1) / P;
-  return layout(nullptr, num_seqs, num_q_heads, head_dim, np).bytes;
+  size_t bytes = 0;
+  if (P > 0 && max_context_len > P)
+    bytes = layout(nullptr, num_seqs, num_q_heads, head_dim, (max_context_len + P - 1) / P).bytes;
+  if ((variant & PKD_FLAG_LONGEST_FIRST) || partition_size == 0) bytes += order_bytes(num_seqs);
+  return bytes;
 }
 
 }  // extern "C"
@@ -286,15 +333,18 @@ pkd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
   if (prefetch_distance < 0) return PKD_ERR_SHAPE;
   const int G = num_q_heads / num_kv_heads;
   const int q_chunks = query_chunks(q_len, G);
+  const int flags = variant & ~0xff;
   if (q_len > 1 || kv_fp8) {
     // several query tokens per sequence, or E4M3 caches: the tensor-core path only
     const int path = variant_path(variant);
     if (path != PKD_VARIANT_AUTO && path != PKD_VARIANT_TMA_MMA) return PKD_ERR_UNSUPPORTED;
-    variant = PKD_VARIANT_TMA_MMA | (variant & PKD_FLAG_L2_EVICT_HINTS);
+    variant = PKD_VARIANT_TMA_MMA | flags;
   }
   int P;
+  int flags_eff = flags;
   if (partition_size == 0) {
     P = auto_partition(s, variant, q_chunks);
+    if (auto_order(s, variant, q_chunks, P)) flags_eff |= PKD_FLAG_LONGEST_FIRST;
   } else if (partition_size == -1) {
     P = -1;
   } else {
@@ -333,6 +383,7 @@ pkd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
   variant = pick_auto(variant, G, grid, P);
   p.l2_hints = (variant & PKD_FLAG_L2_EVICT_HINTS) ? 1 : 0;
   p.timeout_ns = kWaitBudgetNs;
+  size_t used = 0;
   if (split) {
     // partial rows are (sequence, query token, head)
     if (!workspace) return PKD_ERR_WORKSPACE;
@@ -342,6 +393,16 @@ pkd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
     p.tmp_out = w.tmp_out;
     p.max_logits = w.max_logits;
     p.exp_sums = w.exp_sums;
+    used = w.bytes;
+  }
+  // the order sits after the partials; it only reschedules, so a workspace
+  // without room for it runs the plain grid order instead
+  if (grid > 0 && want_order(flags_eff, variant_path(variant), num_seqs) && workspace &&
+      aligned(workspace, 256) && workspace_bytes >= used + order_bytes(num_seqs)) {
+    int32_t* order = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(workspace) + used);
+    pkd::seq_order_kernel<<<(num_seqs + 127) / 128, 128, 0, stream>>>(context_lens, num_seqs, order);
+    if (cudaGetLastError() != cudaSuccess) return PKD_ERR_LAUNCH;
+    p.seq_order = order;
   }
   if (kv_fp8) {
     if (grid > 0x7fffffffLL) return PKD_ERR_SHAPE;
@@ -409,9 +470,11 @@ size_t paged_decode_multi_workspace_size(int num_seqs, int q_len, int num_q_head
   if (check_shape(s) != PKD_OK || q_len < 1) return 0;
   const int qch = query_chunks(q_len, num_q_heads / num_kv_heads);
   int P = partition_size == 0 ? auto_partition(s, PKD_VARIANT_TMA_MMA, qch) : partition_size;
-  if (P <= 0 || max_context_len <= P) return 0;
-  const int np = (max_context_len + P - 1) / P;
-  return layout(nullptr, num_seqs * q_len, num_q_heads, head_dim, np).bytes;
+  size_t bytes = 0;
+  if (P > 0 && max_context_len > P)
+    bytes = layout(nullptr, num_seqs * q_len, num_q_heads, head_dim, (max_context_len + P - 1) / P).bytes;
+  if (partition_size == 0) bytes += order_bytes(num_seqs);  // the automatic split may order the batch
+  return bytes;
 }
 
 pkd_status paged_decode_attention(const void* q, const void* k_cache, const void* v_cache,

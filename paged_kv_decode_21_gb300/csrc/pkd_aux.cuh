@@ -160,6 +160,36 @@ __global__ void __launch_bounds__(256) paged_kv_append_fp8_kernel(
 }
 
 // ---------------------------------------------------------------------------
+// Longest-first order of the sequences: seq_order[r] is the sequence of rank
+// r when the sequences are sorted by decreasing context length (ties by
+// index), so a decode grid that walks ranks hands its longest work out
+// first and ends on short work.  Each CTA holds all lengths in shared memory
+// and ranks 128 of the sequences against them, four lengths per step.  The
+// decode grid reading the order is launched as its programmatic dependent.
+constexpr int kOrderMaxSeqs = 4096;  // lengths held in shared memory (16 KiB)
+__global__ void __launch_bounds__(128) seq_order_kernel(const int32_t* __restrict__ context_lens, int num_seqs,
+                                                        int32_t* __restrict__ seq_order) {
+  __shared__ __align__(16) int32_t lens[kOrderMaxSeqs + 4];
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int padded = (num_seqs + 3) & ~3;
+  for (int i = threadIdx.x; i < padded; i += blockDim.x)
+    lens[i] = i < num_seqs ? max(context_lens[i], 0) : -1;  // padding ranks below every sequence
+  __syncthreads();
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= num_seqs) return;
+  const int L = lens[b];
+  int rank = 0;
+  for (int i = 0; i < padded; i += 4) {
+    const int4 v = *reinterpret_cast<const int4*>(lens + i);
+    rank += (v.x > L) | ((v.x == L) & (i < b));
+    rank += (v.y > L) | ((v.y == L) & (i + 1 < b));
+    rank += (v.z > L) | ((v.z == L) & (i + 2 < b));
+    rank += (v.w > L) | ((v.w == L) & (i + 3 < b));
+  }
+  seq_order[rank] = b;
+}
+
+// ---------------------------------------------------------------------------
 __global__ void validate_tables_kernel(const int32_t* block_tables, const int32_t* context_lens,
                                        int num_seqs, int max_blocks_per_seq, int block_size,
                                        int num_blocks, int* error_word) {

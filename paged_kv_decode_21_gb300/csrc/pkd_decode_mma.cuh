@@ -206,10 +206,17 @@ __global__ void __launch_bounds__(MmaTraits<D, BS, G, QC, KVB>::THREADS,
   const int j = rest % np_grid;
   const int bg = rest / np_grid;
   const int g = bg % P.num_kv_heads;
-  const int b = bg / P.num_kv_heads;
   // a dependent grid (the split-K merge) may launch once every CTA of this
   // grid has started; it waits for this grid's completion itself
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // with a longest-first order the grid walks ranks; it is the programmatic
+  // dependent of the kernel writing the order and waits for it here (without
+  // a prerequisite grid the wait returns at once)
+  int b = bg / P.num_kv_heads;
+  if (P.seq_order) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    b = P.seq_order[b];
+  }
   const int L = P.context_lens[b];
   const int QL = P.q_len;
   const int jq0 = qc * QC;               // first query token of this CTA

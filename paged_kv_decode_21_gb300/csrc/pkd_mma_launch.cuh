@@ -63,7 +63,24 @@ cudaError_t launch_qc(const CUtensorMap& mk, const CUtensorMap& mv, const Decode
   auto* fn = paged_decode_mma_kernel<D, BS, G, QC, KVB>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  fn<<<(unsigned)grid, T::THREADS, T::SMEM_BYTES, stream>>>(mk, mv, p);
+  if (!p.seq_order) {
+    fn<<<(unsigned)grid, T::THREADS, T::SMEM_BYTES, stream>>>(mk, mv, p);
+    return cudaGetLastError();
+  }
+  // a programmatic dependent of the order kernel: the CTAs become resident
+  // while it runs and wait for its order with griddepcontrol.wait
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(T::THREADS);
+  cfg.dynamicSmemBytes = T::SMEM_BYTES;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, fn, mk, mv, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

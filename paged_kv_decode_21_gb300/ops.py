@@ -156,17 +156,21 @@ def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scal
 
 
 FLAG_L2_EVICT_HINTS = 0x100
+FLAG_LONGEST_FIRST = 0x200
+
+
+FLAGS = {"l2_hints": FLAG_L2_EVICT_HINTS, "longest_first": FLAG_LONGEST_FIRST}
 
 
 def _variant(variant) -> int:
-    """A data-path name ("tma_staged", optionally "+l2_hints") or its integer code."""
+    """A data-path name ("tma_staged", optionally "+l2_hints", "+longest_first") or its integer code."""
     if isinstance(variant, str):
-        name, _, flag = variant.partition("+")
+        name, *flags = variant.split("+")
         code = VARIANTS[name]
-        if flag:
-            if flag != "l2_hints":
+        for flag in flags:
+            if flag not in FLAGS:
                 raise ValueError(f"unknown variant flag {flag!r}")
-            code |= FLAG_L2_EVICT_HINTS
+            code |= FLAGS[flag]
         return code
     return int(variant)
 
@@ -197,8 +201,7 @@ def paged_decode_auto_variant(num_seqs, num_q_heads, num_kv_heads, head_dim, blo
 def variant_name(v: int) -> str:
     """Name of a variant value, e.g. 'tma_staged+l2_hints'."""
     names = {n: k for k, n in VARIANTS.items()}
-    base = names[v & 0xff]
-    return base + ("+l2_hints" if v & FLAG_L2_EVICT_HINTS else "")
+    return names[v & 0xff] + "".join("+" + f for f, bit in FLAGS.items() if v & bit)
 
 
 def alloc_workspace(nbytes: int, device) -> Optional[torch.Tensor]:

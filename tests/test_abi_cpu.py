@@ -73,7 +73,12 @@ def test_shape_checks(L):
 
 def test_variant_flags(L):
     assert call_ex(L, var=0x100 | 3, D=96) == 3        # flag accepted; fails later on head_dim
-    assert call_ex(L, var=0x200 | 3) == 2              # unknown flag bit
+    assert call_ex(L, var=0x400 | 3) == 2              # unknown flag bit
+    assert call_ex(L, var=0x200 | 4, D=96) == 3        # the longest-first flag is known
+    # the order (one int32 per sequence, 256-byte aligned) follows the split partials
+    base = L.paged_decode_workspace_size(2, 8, 2, 128, 16, 100, 32, 4)
+    assert L.paged_decode_workspace_size(2, 8, 2, 128, 16, 100, 32, 0x200 | 4) == base + 256
+    assert L.paged_decode_workspace_size(300, 8, 2, 128, 16, 100, -1, 0x200 | 4) == 1280
     assert call_ex(L, var=4, D=96) == 3                # the tensor-core path is a known variant
     assert call_ex(L, var=5) == 2                      # past the last variant
     assert L.paged_decode_workspace_size(2, 8, 2, 128, 16, 100, 32, 0x100 | 2) > 0
@@ -150,6 +155,13 @@ def test_auto_variant_policy(L):
     assert av(64, 32, 8, 128, 16, 512) == staged        # GQA always staged
     assert av(64, 32, 32, 128, 16, 512, -1) == plain
     assert av(64, 32, 32, 128, 16, 4096, 256) == staged  # 16384 CTAs
+    # unsplit grids of one to six waves of units walk the batch longest first
+    ordered = staged | ops.FLAG_LONGEST_FIRST
+    assert av(128, 32, 8, 128, 16, 4096) == ordered      # 1024 units: 3.5 waves
+    assert av(128, 32, 8, 128, 16, 4096, -1) == staged   # an explicit partition keeps the grid order
+    assert av(128, 32, 8, 128, 16, 512) == staged        # short contexts: the order is not paid back
+    assert av(1024, 32, 8, 128, 16, 4096) == staged      # 8192 units: many waves
+    assert ops.variant_name(ordered) == "tma_mma+longest_first"
     assert ops.variant_name(staged) == "tma_mma"
     assert ops.variant_name(ops.VARIANTS["tma_staged"] | ops.FLAG_L2_EVICT_HINTS) == "tma_staged+l2_hints"
     with pytest.raises(ops.PagedDecodeError):

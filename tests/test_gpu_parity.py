@@ -307,3 +307,43 @@ def test_full_config_sampled(name):
         assert ops.pkd_read_device_error(ew) == 0
         got = out.view(-1, cfg.head_dim)[torch.from_numpy(rows).long().cuda()]
         assert_close(got, ref, f"{name} {variant}")
+
+
+# --------------------------------------------------------------------------- longest-first order
+@pytest.mark.parametrize("partition", [-1, 64, 0])
+@pytest.mark.parametrize("lens,Hq,Hkv", [([300, 17, 5000, 0, 129, 64, 2048, 1], 32, 8),
+                                         ([700, 31, 2, 900, 90], 28, 4),
+                                         ([1000] * 5 + [3], 8, 8)])
+def test_longest_first_order_is_bitwise_neutral(lens, Hq, Hkv, partition):
+    # the order only changes which CTA starts when: every CTA computes the same
+    inp = workloads.make_custom(len(lens), Hq, Hkv, 128, 16, lens, seed=len(lens) + Hq, device="cuda")
+    ew = errword()
+    a = run_ex(inp, "tma_mma", partition)
+    b = run_ex(inp, "tma_mma+longest_first", partition, error_word=ew)
+    assert ops.pkd_read_device_error(ew) == 0
+    assert torch.equal(a, b)
+    assert_close(b, oracle_out(inp), f"longest first P={partition}")
+
+
+def test_longest_first_full_size_ragged_sampled():
+    cfg = workloads.CONFIGS["llama3_8b_gqa4"]
+    inp = workloads.make_inputs(cfg, device="cuda")
+    a = run_ex(inp, "tma_mma", -1)
+    b = run_ex(inp, "tma_mma+longest_first", -1)
+    assert torch.equal(a, b)
+    rows = sample_rows(cfg.num_seqs, cfg.num_q_heads, 64, seed=13)
+    got = b.view(-1, cfg.head_dim)[torch.from_numpy(rows).long().cuda()]
+    assert_close(got, oracle_out(inp, rows=rows), "llama3_8b_gqa4 longest first")
+
+
+def test_longest_first_order_kernel_ranks_by_length():
+    # the order the grid walks: decreasing length, ties by index
+    lens = [5, 9, 9, 0, 12, 5, 1]
+    inp = workloads.make_custom(len(lens), 4, 4, 64, 16, lens, seed=3, device="cuda")
+    need = ops.paged_decode_workspace_size(len(lens), 4, 4, 64, 16, max(lens), -1, "tma_mma+longest_first")
+    ws = ops.alloc_workspace(need, "cuda")
+    ws.fill_(0xFF)
+    run_ex(inp, "tma_mma+longest_first", -1, workspace=ws)
+    torch.cuda.synchronize()
+    order = ws[:4 * len(lens)].view(torch.int32).cpu().tolist()
+    assert order == sorted(range(len(lens)), key=lambda b: (-lens[b], b))
