@@ -188,10 +188,21 @@ def time_gpu(args, cfg, variant, dev, inp, steps, warmup, with_e2e=True, with_cl
     need = ops.paged_decode_workspace_size(inp.num_seqs, inp.num_q_heads, inp.num_kv_heads,
                                            inp.head_dim, inp.block_size, inp.max_context_len, P, var)
     ws = ops.alloc_workspace(need, dev)
-    eff_P = P if P != 0 else ops.paged_decode_auto_partition_size(
-        inp.num_seqs, inp.num_q_heads, inp.num_kv_heads, inp.head_dim, inp.block_size,
-        inp.max_context_len, var)
-    split = eff_P > 0 and inp.max_context_len > eff_P
+    q_len = getattr(args, "q_len", 1)
+    kv_fp8 = getattr(args, "kv_fp8", False)
+    if P == 0 and (variant == "auto" or q_len > 1 or kv_fp8):
+        # the library's own plan for the automatic split: partition, order, launches
+        launches, eff_P, ordered = ops.paged_decode_auto_plan(
+            inp.num_seqs, q_len, inp.num_q_heads, inp.num_kv_heads, inp.head_dim, inp.block_size,
+            inp.max_context_len, kv_fp8)
+        split = eff_P > 0
+    else:
+        eff_P = P if P != 0 else ops.paged_decode_auto_partition_size(
+            inp.num_seqs, inp.num_q_heads, inp.num_kv_heads, inp.head_dim, inp.block_size,
+            inp.max_context_len, var)
+        split = eff_P > 0 and inp.max_context_len > eff_P
+        ordered = "longest_first" in variant and inp.num_seqs >= 2 and variant.startswith("tma_mma")
+        launches = 1 + int(split) + int(ordered)
     out = torch.empty_like(inp.q)
     ew = torch.zeros(1, dtype=torch.int32, device=dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -204,8 +215,7 @@ def time_gpu(args, cfg, variant, dev, inp, steps, warmup, with_e2e=True, with_cl
                                       variant=variant, prefetch_distance=args.prefetch_distance,
                                       workspace=ws, error_word=ew, stream=stream)
 
-    q_len = getattr(args, "q_len", 1)
-    if getattr(args, "kv_fp8", False):
+    if kv_fp8:
         # E4M3 caches (one byte per element): the K/V stream halves
         g = torch.Generator(device=dev).manual_seed(cfg.seed + 9)
         k8 = workloads.rand_e4m3(inp.k_cache.shape, g, dev)
@@ -276,8 +286,8 @@ def time_gpu(args, cfg, variant, dev, inp, steps, warmup, with_e2e=True, with_cl
     errbits = ops.pkd_read_device_error(ew)
     res = {
         "algo_bytes": algo, "mean_ms": statistics.mean(times_ms), "median_ms": statistics.median(times_ms),
-        "min_ms": min(times_ms), "wall_s": t_wall, "launches_per_call": 2 if split else 1,
-        "partition_size": eff_P if split else -1, "device_error": errbits,
+        "min_ms": min(times_ms), "wall_s": t_wall, "launches_per_call": launches,
+        "partition_size": eff_P if split else -1, "longest_first": ordered, "device_error": errbits,
         "clocks": sampler.summary() if sampler else None,
         "l2": (f"an L2 flush (2x L2 write) before every timed call; inputs {algo / 1e6:.0f} MB" if use_flush
                else f"inputs larger than L2 ({algo / 1e9:.2f} GB against {l2 / 1e6:.0f} MB): calls back to "
@@ -479,6 +489,8 @@ def main():
     ap.add_argument("--fig4-variants", default="no_prefetch,l2_prefetch,tma_staged,tma_mma,auto")
     ap.add_argument("--fig4-batches", default="1,4,16,64,128,256")
     ap.add_argument("--fig4-contexts", default="512,1024,2048,4096,8192")
+    ap.add_argument("--fig4-ragged", action="store_true",
+                    help="per-sequence contexts drawn from U[context/8, context] (seeded) instead of all equal")
     ap.add_argument("--append", action="store_true",
                     help="time paged_kv_append alone and in front of the decode call, on --config")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -514,9 +526,14 @@ def main():
         base = workloads.CONFIGS[args.fig4_config]
         for L in [int(x) for x in args.fig4_contexts.split(",")]:
             for B in [int(x) for x in args.fig4_batches.split(",")]:
-                cfg = dataclasses.replace(base, name=f"{base.name}_b{B}_L{L}", num_seqs=B,
-                                          context_lens=(L,) * B, len_range=None, num_blocks=None,
-                                          partition_size=0)
+                if args.fig4_ragged:
+                    cfg = dataclasses.replace(base, name=f"{base.name}_b{B}_L{L}r", num_seqs=B,
+                                              context_lens=None, len_range=(max(1, L // 8), L),
+                                              num_blocks=None, partition_size=0)
+                else:
+                    cfg = dataclasses.replace(base, name=f"{base.name}_b{B}_L{L}", num_seqs=B,
+                                              context_lens=(L,) * B, len_range=None, num_blocks=None,
+                                              partition_size=0)
                 inp = workloads.make_inputs(cfg, device=dev)
                 res = {}
                 for variant in ["no_prefetch"] + [v for v in args.fig4_variants.split(",")
@@ -527,11 +544,13 @@ def main():
                     res[variant] = r
                 base_us = res["no_prefetch"]["mean_ms"] * 1e3
                 line = {"shape": f"{cfg.num_q_heads}q/{cfg.num_kv_heads}kv", "batch": B, "context": L,
+                        "ragged": bool(args.fig4_ragged),
                         "algo_bytes": res["auto"]["algo_bytes"],
                         "partition_size": res["auto"]["partition_size"],
+                        "longest_first": res["auto"]["longest_first"],
                         "auto_variant": ops.variant_name(ops.paged_decode_auto_variant(
                             B, cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim, cfg.block_size, L,
-                            res["auto"]["partition_size"]))}
+                            cfg.partition_size or 0))}
                 for variant, r in res.items():
                     us = r["mean_ms"] * 1e3
                     gbs = r["algo_bytes"] / (r["mean_ms"] * 1e-3) / 1e9
@@ -579,11 +598,12 @@ def main():
     achieved = r["algo_bytes"] / (r["mean_ms"] * 1e-3) / 1e9
     resolved = variant
     if args.q_len > 1 or args.kv_fp8:
-        resolved = "tma_mma"
+        resolved = "tma_mma" + ("+longest_first" if r["longest_first"] else "")
     elif variant == "auto":
+        P_req = args.partition_size if args.partition_size is not None else (cfg.partition_size or 0)
         resolved = ops.variant_name(ops.paged_decode_auto_variant(
             cfg.num_seqs, cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim, cfg.block_size,
-            inp.max_context_len, r["partition_size"]))
+            inp.max_context_len, P_req))
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(mean_ms, 5), "higher_is_better": True,

@@ -277,6 +277,21 @@ pkd_status paged_decode_attention_multi(const void* q, const void* k_cache, cons
                                         int partition_size, void* workspace, size_t workspace_bytes,
                                         int* error_word, cudaStream_t stream);
 
+/*
+ * paged_decode_auto_plan -- what a call with partition_size 0 runs on the
+ * current device: paged_decode_attention_ex with PKD_VARIANT_AUTO (q_len 1,
+ * kv_fp8 0), paged_decode_attention_multi (q_len > 1) or
+ * paged_decode_attention_fp8 (kv_fp8 1).  Writes *partition_size (the
+ * partition, or -1 when unsplit) and *longest_first (1 when the batch is
+ * walked longest first, given a workspace of the size the *_workspace_size
+ * functions return); either pointer may be NULL.  Returns the kernel launches
+ * the call makes (the decode grid, plus the split-K merge, plus the order
+ * kernel; 0 for an empty batch), or -2 on an invalid shape.
+ */
+int paged_decode_auto_plan(int num_seqs, int q_len, int num_q_heads, int num_kv_heads, int head_dim,
+                           int block_size, int max_context_len, int kv_fp8, int* partition_size,
+                           int* longest_first);
+
 /* Workspace bytes paged_decode_attention_multi needs (0 = none). */
 size_t paged_decode_multi_workspace_size(int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
                                          int head_dim, int block_size, int max_context_len,

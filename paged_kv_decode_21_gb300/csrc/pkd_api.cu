@@ -308,6 +308,51 @@ int query_chunks(int q_len, int G) {
   return (q_len + qc - 1) / qc;
 }
 
+// The launch plan of one decode call.
+struct CallPlan {
+  int P;           // tokens per partition (the whole context, rounded up to 32, when unsplit)
+  int np;          // partitions in the grid (1 when unsplit)
+  bool split;      // the split-K merge runs
+  long long grid;  // decode CTAs
+  int variant;     // the data path it runs, with the PKD_FLAG_* bits that apply
+  bool order;      // the batch is walked longest first (when the workspace has room)
+};
+
+// The partition, grid, data path and order a call with these arguments runs
+// (the shape already checked).
+pkd_status plan_call(const Shape& s, int q_len, int variant, int partition_size, int kv_fp8, CallPlan* out) {
+  const int G = s.num_q_heads / s.num_kv_heads;
+  const int q_chunks = query_chunks(q_len, G);
+  const int flags = variant & ~0xff;
+  if (q_len > 1 || kv_fp8) {
+    // several query tokens per sequence, or E4M3 caches: the tensor-core path only
+    const int path = variant_path(variant);
+    if (path != PKD_VARIANT_AUTO && path != PKD_VARIANT_TMA_MMA) return PKD_ERR_UNSUPPORTED;
+    variant = PKD_VARIANT_TMA_MMA | flags;
+  }
+  int P;
+  int flags_eff = flags;
+  if (partition_size == 0) {
+    P = auto_partition(s, variant, q_chunks);
+    if (auto_order(s, variant, q_chunks, P)) flags_eff |= PKD_FLAG_LONGEST_FIRST;
+  } else if (partition_size == -1) {
+    P = -1;
+  } else {
+    if (partition_size < 0 || partition_size % 32 != 0 || partition_size % s.block_size != 0)
+      return PKD_ERR_SHAPE;
+    P = partition_size;
+  }
+  out->split = P > 0 && s.max_context_len > P;
+  out->np = out->split ? (s.max_context_len + P - 1) / P : 1;
+  if (!out->split) P = s.max_context_len > 0 ? (int)round_up((size_t)s.max_context_len, 32) : 32;
+  out->P = P;
+  out->grid = (long long)s.num_seqs * s.num_kv_heads * q_chunks * out->np;
+  const int v = pick_auto(variant, G, out->grid, P);
+  out->order = out->grid > 0 && want_order(flags_eff, variant_path(v), s.num_seqs);
+  out->variant = (v & ~PKD_FLAG_LONGEST_FIRST) | (out->order ? PKD_FLAG_LONGEST_FIRST : 0);
+  return PKD_OK;
+}
+
 // Decode of q_len query tokens per sequence (q_len = 1: single-query decode).
 pkd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
                        const int32_t* block_tables, const int32_t* context_lens, void* out, int num_seqs,
@@ -333,29 +378,13 @@ pkd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
   if (prefetch_distance < 0) return PKD_ERR_SHAPE;
   const int G = num_q_heads / num_kv_heads;
   const int q_chunks = query_chunks(q_len, G);
-  const int flags = variant & ~0xff;
-  if (q_len > 1 || kv_fp8) {
-    // several query tokens per sequence, or E4M3 caches: the tensor-core path only
-    const int path = variant_path(variant);
-    if (path != PKD_VARIANT_AUTO && path != PKD_VARIANT_TMA_MMA) return PKD_ERR_UNSUPPORTED;
-    variant = PKD_VARIANT_TMA_MMA | flags;
-  }
-  int P;
-  int flags_eff = flags;
-  if (partition_size == 0) {
-    P = auto_partition(s, variant, q_chunks);
-    if (auto_order(s, variant, q_chunks, P)) flags_eff |= PKD_FLAG_LONGEST_FIRST;
-  } else if (partition_size == -1) {
-    P = -1;
-  } else {
-    if (partition_size < 0 || partition_size % 32 != 0 || partition_size % block_size != 0)
-      return PKD_ERR_SHAPE;
-    P = partition_size;
-  }
-  const bool split = P > 0 && max_context_len > P;
-  int np = 1;
-  if (split) np = (max_context_len + P - 1) / P;
-  else P = max_context_len > 0 ? (int)round_up((size_t)max_context_len, 32) : 32;
+  CallPlan plan;
+  st = plan_call(s, q_len, variant, partition_size, kv_fp8, &plan);
+  if (st != PKD_OK) return st;
+  const int P = plan.P, np = plan.np;
+  const bool split = plan.split;
+  const long long grid = plan.grid;
+  variant = plan.variant;
 
   pkd::DecodeParams p{};
   p.q = static_cast<const __half*>(q);
@@ -379,8 +408,6 @@ pkd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
   p.scale_log2 = scale * (kv_fp8 ? k_scale : 1.f) * 1.4426950408889634f;
   p.v_scale = kv_fp8 ? v_scale : 1.f;
   p.prefetch_distance = prefetch_distance == 0 ? kDefaultPrefetchDistance : prefetch_distance;
-  const long long grid = (long long)num_seqs * num_kv_heads * q_chunks * np;
-  variant = pick_auto(variant, G, grid, P);
   p.l2_hints = (variant & PKD_FLAG_L2_EVICT_HINTS) ? 1 : 0;
   p.timeout_ns = kWaitBudgetNs;
   size_t used = 0;
@@ -397,7 +424,7 @@ pkd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
   }
   // the order sits after the partials; it only reschedules, so a workspace
   // without room for it runs the plain grid order instead
-  if (grid > 0 && want_order(flags_eff, variant_path(variant), num_seqs) && workspace &&
+  if (grid > 0 && plan.order && workspace &&
       aligned(workspace, 256) && workspace_bytes >= used + order_bytes(num_seqs)) {
     int32_t* order = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(workspace) + used);
     pkd::seq_order_kernel<<<(num_seqs + 127) / 128, 128, 0, stream>>>(context_lens, num_seqs, order);
@@ -461,6 +488,19 @@ pkd_status paged_decode_attention_fp8(const void* q, const void* k_cache, const 
                      num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, max_context_len,
                      scale, partition_size, PKD_VARIANT_TMA_MMA, 0, workspace, workspace_bytes, error_word,
                      stream, 1, k_scale, v_scale);
+}
+
+int paged_decode_auto_plan(int num_seqs, int q_len, int num_q_heads, int num_kv_heads, int head_dim,
+                           int block_size, int max_context_len, int kv_fp8, int* partition_size,
+                           int* longest_first) {
+  Shape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, 1, 1 << 30, max_context_len};
+  if (check_shape(s) != PKD_OK || q_len < 1) return -2;
+  CallPlan plan;
+  if (plan_call(s, q_len, PKD_VARIANT_AUTO, 0, kv_fp8, &plan) != PKD_OK) return -2;
+  if (partition_size) *partition_size = plan.split ? plan.P : -1;
+  if (longest_first) *longest_first = plan.order ? 1 : 0;
+  if (num_seqs == 0 || plan.grid == 0) return 0;
+  return 1 + (plan.split ? 1 : 0) + (plan.order ? 1 : 0);
 }
 
 size_t paged_decode_multi_workspace_size(int num_seqs, int q_len, int num_q_heads, int num_kv_heads,

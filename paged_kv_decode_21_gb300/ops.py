@@ -68,6 +68,9 @@ def lib():
         L.paged_decode_attention_multi.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, I, P, S,
                                                    P, P]
         L.paged_decode_attention_multi.restype = I
+        L.paged_decode_auto_plan.argtypes = [I, I, I, I, I, I, I, I, ctypes.POINTER(ctypes.c_int),
+                                             ctypes.POINTER(ctypes.c_int)]
+        L.paged_decode_auto_plan.restype = I
         L.paged_decode_multi_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
         L.paged_decode_multi_workspace_size.restype = S
         L.paged_decode_attention_fp8.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, F, F, I, P, S,
@@ -196,6 +199,17 @@ def paged_decode_auto_variant(num_seqs, num_q_heads, num_kv_heads, head_dim, blo
     if v < 0:
         raise PagedDecodeError(2, "paged_decode_auto_variant")
     return v
+
+
+def paged_decode_auto_plan(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len,
+                           kv_fp8=False):
+    """What a call with partition_size 0 runs: (launches, partition or -1, longest_first)."""
+    part, order = ctypes.c_int(0), ctypes.c_int(0)
+    n = lib().paged_decode_auto_plan(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size,
+                                     max_context_len, int(bool(kv_fp8)), ctypes.byref(part), ctypes.byref(order))
+    if n < 0:
+        raise PagedDecodeError(2, "paged_decode_auto_plan")
+    return n, part.value, bool(order.value)
 
 
 def variant_name(v: int) -> str:

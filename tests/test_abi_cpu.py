@@ -168,6 +168,23 @@ def test_auto_variant_policy(L):
         av(64, 32, 32, 128, 16, 512, 100)               # partition not a multiple of 32
 
 
+def test_auto_plan_matches_policy(L):
+    from paged_kv_decode_21_gb300 import ops
+    plan = ops.paged_decode_auto_plan
+    assert plan(64, 1, 32, 32, 128, 16, 2048) == (1, -1, False)      # MHA bench shape: one launch
+    assert plan(128, 1, 32, 8, 128, 16, 4096) == (2, -1, True)       # order + decode
+    assert plan(128, 1, 32, 8, 128, 16, 4096, kv_fp8=True) == (2, -1, True)
+    n, part, order = plan(32, 1, 40, 8, 128, 16, 32768)              # 256 units: split + merge
+    assert n == 2 and part > 0 and not order
+    n, part, order = plan(256, 1, 28, 4, 128, 16, 8192)              # long contexts below six waves split
+    assert n == 2 and part == 2048 and not order
+    # multi-token queries count query chunks as units: 16 / G tokens per CTA
+    assert plan(128, 4, 32, 8, 128, 16, 4096)[0] in (2, 3)
+    assert plan(0, 1, 32, 8, 128, 16, 4096) == (0, -1, False)
+    with pytest.raises(ops.PagedDecodeError):
+        plan(2, 0, 8, 2, 128, 16, 100)
+
+
 def test_empty_batch_is_a_no_op(L):
     assert call_ex(L, B=0) == 0
 
