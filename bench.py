@@ -549,8 +549,8 @@ def main():
                         "partition_size": res["auto"]["partition_size"],
                         "longest_first": res["auto"]["longest_first"],
                         "auto_variant": ops.variant_name(ops.paged_decode_auto_variant(
-                            B, cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim, cfg.block_size, L,
-                            cfg.partition_size or 0))}
+                            B, cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim, cfg.block_size,
+                            inp.max_context_len, cfg.partition_size or 0))}
                 for variant, r in res.items():
                     us = r["mean_ms"] * 1e3
                     gbs = r["algo_bytes"] / (r["mean_ms"] * 1e-3) / 1e9
