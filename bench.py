@@ -75,12 +75,13 @@ def kernel_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def kernel_name(cfg: workloads.DecodeConfig, variant: str) -> str:
+def kernel_name(cfg: workloads.DecodeConfig, variant: str, kv_fp8: bool = False) -> str:
     """The decode kernel a resolved variant launches for a shape."""
     path = variant.split("+")[0]
     shape = f"{cfg.head_dim},{cfg.block_size},{cfg.group}"
     if path == "tma_mma":
-        return f"paged_decode_mma_kernel<{shape},1,2>"
+        # E4M3 caches: bytes per element 1; grids of 3+ waves of four CTAs per SM add CPS = 4
+        return f"paged_decode_mma_kernel<{shape},1,{1 if kv_fp8 else 2}>"
     if path == "tma_staged" and cfg.group >= 6:
         return f"paged_decode_ws_kernel<{shape}>"
     return f"paged_decode_kernel<{shape},{variant}>"
@@ -621,7 +622,7 @@ def main():
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "traffic": ncu_traffic(cfg.name, resolved),
-                     "kernel": kernel_name(cfg, resolved)},
+                     "kernel": kernel_name(cfg, resolved, args.kv_fp8)},
         "gpu_launches": r["launches_per_call"] * args.steps,
         "clocks": r["clocks"],
         "e2e": r.get("e2e"),

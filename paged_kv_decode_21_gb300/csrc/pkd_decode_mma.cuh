@@ -138,8 +138,9 @@ constexpr int mma_query_chunk(int G) { return 16 / G; }
 
 // ---------------------------------------------------------------- layout
 // QC: query tokens per CTA (1 = single-query decode); KVB: bytes per K/V
-// element (2: fp16, 1: E4M3 with per-cache scales).
-template <int D, int BS, int G, int QC, int KVB = 2>
+// element (2: fp16, 1: E4M3 with per-cache scales); CPS: resident CTAs per
+// SM the build targets (0: the cache type's default).
+template <int D, int BS, int G, int QC, int KVB = 2, int CPS = 0>
 struct MmaTraits {
   static_assert(D == 64 || D == 128, "head_dim");
   static_assert(BS == 16 || BS == 32, "block_size");
@@ -152,9 +153,12 @@ struct MmaTraits {
   // Two CTAs per SM with 96 KiB rings for fp16.  E4M3 halves the bytes per
   // token, so the same warps must retire twice the tokens: three CTAs per SM
   // with 64 KiB rings (4 KiB slots, 4 per warp) measured 1.24-1.29x faster.
-  static constexpr int MIN_BLOCKS = KVB == 1 ? 3 : 2;
-  static constexpr int RING_KIB = KVB == 1 ? 64 : 96;
-  static constexpr int QK_CHAINS = 2;         // independent accumulator chains per QK n-tile
+  // Single-query E4M3 grids of many waves go to four CTAs per SM (48 KiB
+  // rings, one QK chain so the state fits in 128 registers): 2-7% faster
+  // there, but slower where a few waves of long CTAs bound the grid.
+  static constexpr int MIN_BLOCKS = CPS ? CPS : (KVB == 1 ? 3 : 2);
+  static constexpr int RING_KIB = MIN_BLOCKS >= 4 ? 48 : (MIN_BLOCKS == 3 ? 64 : 96);
+  static constexpr int QK_CHAINS = MIN_BLOCKS >= 4 ? 1 : 2;  // independent accumulator chains per QK n-tile
   static constexpr bool F8 = KVB == 1;
   static constexpr int KSTEPS = D / 16;       // QK k-steps and PV m-tiles
   // A box is 16 rows of BOX_ROWB bytes: 64 fp16 columns, or a whole E4M3 row
@@ -183,12 +187,12 @@ struct MmaTraits {
 };
 
 // ---------------------------------------------------------------- kernel
-template <int D, int BS, int G, int QC, int KVB = 2>
-__global__ void __launch_bounds__(MmaTraits<D, BS, G, QC, KVB>::THREADS,
-                                  MmaTraits<D, BS, G, QC, KVB>::MIN_BLOCKS)
+template <int D, int BS, int G, int QC, int KVB = 2, int CPS = 0>
+__global__ void __launch_bounds__(MmaTraits<D, BS, G, QC, KVB, CPS>::THREADS,
+                                  MmaTraits<D, BS, G, QC, KVB, CPS>::MIN_BLOCKS)
     paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                             const __grid_constant__ CUtensorMap tmap_v, const DecodeParams P) {
-  using T = MmaTraits<D, BS, G, QC, KVB>;
+  using T = MmaTraits<D, BS, G, QC, KVB, CPS>;
   constexpr bool F8 = T::F8;
   constexpr int NW = T::NW, SW = T::SW, KS = T::KSTEPS, NT = T::NT, ROWS = T::ROWS;
   extern __shared__ __align__(1024) unsigned char smem_raw[];

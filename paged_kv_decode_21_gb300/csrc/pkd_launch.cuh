@@ -65,5 +65,9 @@ cudaError_t launch_decode_tma_mma_multi(int D, int BS, int G, const DecodeParams
                                         cudaStream_t stream);
 cudaError_t launch_decode_tma_mma_fp8(int D, int BS, int G, const DecodeParams& p, long long grid,
                                       cudaStream_t stream);
+// Single-query decode over E4M3 caches at four CTAs per SM, for grids of
+// many waves (pkd_inst_tma_mma_fp8_w4.cu).
+cudaError_t launch_decode_tma_mma_fp8_w4(int D, int BS, int G, const DecodeParams& p, long long grid,
+                                         cudaStream_t stream);
 
 }  // namespace pkd

@@ -56,11 +56,11 @@ inline cudaError_t make_maps(const DecodeParams& p, int D, int BS, int kvb, CUte
   return make_map(mv, p.v_cache, D, p.num_kv_heads * BS, p.num_blocks, kvb);
 }
 
-template <int D, int BS, int G, int QC, int KVB>
+template <int D, int BS, int G, int QC, int KVB, int CPS>
 cudaError_t launch_qc(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeParams& p, long long grid,
                       cudaStream_t stream) {
-  using T = MmaTraits<D, BS, G, QC, KVB>;
-  auto* fn = paged_decode_mma_kernel<D, BS, G, QC, KVB>;
+  using T = MmaTraits<D, BS, G, QC, KVB, CPS>;
+  auto* fn = paged_decode_mma_kernel<D, BS, G, QC, KVB, CPS>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   if (!p.seq_order) {
@@ -85,23 +85,24 @@ cudaError_t launch_qc(const CUtensorMap& mk, const CUtensorMap& mv, const Decode
 }
 
 // Dispatch over the compiled (head_dim, block_size, group) set; QCOF maps a
-// group size to the query tokens per CTA of the instantiation.
-template <template <int> class QCOF, int KVB = 2>
+// group size to the query tokens per CTA of the instantiation, CPS selects
+// the resident CTAs per SM (0: the cache type's default).
+template <template <int> class QCOF, int KVB = 2, int CPS = 0>
 cudaError_t launch_all(int D, int BS, int G, const DecodeParams& p, long long grid, cudaStream_t stream) {
   CUtensorMap mk, mv;
   cudaError_t e = make_maps(p, D, BS, KVB, &mk, &mv);
   if (e != cudaSuccess) return e;
-#define PKD_CASE_G(D_, BS_)                                                                   \
-  switch (G) {                                                                                \
-    case 1: return launch_qc<D_, BS_, 1, QCOF<1>::value, KVB>(mk, mv, p, grid, stream);      \
-    case 2: return launch_qc<D_, BS_, 2, QCOF<2>::value, KVB>(mk, mv, p, grid, stream);      \
-    case 3: return launch_qc<D_, BS_, 3, QCOF<3>::value, KVB>(mk, mv, p, grid, stream);      \
-    case 4: return launch_qc<D_, BS_, 4, QCOF<4>::value, KVB>(mk, mv, p, grid, stream);      \
-    case 5: return launch_qc<D_, BS_, 5, QCOF<5>::value, KVB>(mk, mv, p, grid, stream);      \
-    case 6: return launch_qc<D_, BS_, 6, QCOF<6>::value, KVB>(mk, mv, p, grid, stream);      \
-    case 7: return launch_qc<D_, BS_, 7, QCOF<7>::value, KVB>(mk, mv, p, grid, stream);      \
-    case 8: return launch_qc<D_, BS_, 8, QCOF<8>::value, KVB>(mk, mv, p, grid, stream);      \
-    default: return cudaErrorInvalidValue;                                                    \
+#define PKD_CASE_G(D_, BS_)                                                                  \
+  switch (G) {                                                                               \
+    case 1: return launch_qc<D_, BS_, 1, QCOF<1>::value, KVB, CPS>(mk, mv, p, grid, stream); \
+    case 2: return launch_qc<D_, BS_, 2, QCOF<2>::value, KVB, CPS>(mk, mv, p, grid, stream); \
+    case 3: return launch_qc<D_, BS_, 3, QCOF<3>::value, KVB, CPS>(mk, mv, p, grid, stream); \
+    case 4: return launch_qc<D_, BS_, 4, QCOF<4>::value, KVB, CPS>(mk, mv, p, grid, stream); \
+    case 5: return launch_qc<D_, BS_, 5, QCOF<5>::value, KVB, CPS>(mk, mv, p, grid, stream); \
+    case 6: return launch_qc<D_, BS_, 6, QCOF<6>::value, KVB, CPS>(mk, mv, p, grid, stream); \
+    case 7: return launch_qc<D_, BS_, 7, QCOF<7>::value, KVB, CPS>(mk, mv, p, grid, stream); \
+    case 8: return launch_qc<D_, BS_, 8, QCOF<8>::value, KVB, CPS>(mk, mv, p, grid, stream); \
+    default: return cudaErrorInvalidValue;                                                   \
   }
   if (D == 128 && BS == 16) { PKD_CASE_G(128, 16) }
   if (D == 128 && BS == 32) { PKD_CASE_G(128, 32) }

@@ -154,3 +154,23 @@ def test_fp8_full_size_gqa_sampled():
     expect = ref(inp, inp.q, k8, v8, rows=rows)
     got = out.view(-1, cfg.head_dim)[torch.from_numpy(rows).long().cuda()]
     assert_close(got, expect, "qwen25_7b_gqa7 fp8")
+
+
+@pytest.mark.parametrize("shape", [
+    # (D, BS, Hq, Hkv, B, length range): single-query grids of >= 3 waves of four CTAs per
+    # SM (>= 1824 CTAs on 152 SMs), which run the four-per-SM build
+    (128, 16, 32, 32, 64, (200, 300)),
+    (128, 16, 32, 8, 256, (100, 500)),
+    (128, 16, 28, 4, 512, (1, 480)),
+    (64, 32, 16, 16, 128, (150, 220)),
+])
+def test_fp8_wide_grid_four_per_sm_build(shape):
+    D, BS, Hq, Hkv, B, (lo, hi) = shape
+    lens = torch.randint(lo, hi + 1, (B,), generator=torch.Generator().manual_seed(B + Hq)).tolist()
+    inp, q, k8, v8 = make(lens, Hq, Hkv, D, BS, seed=B + D)
+    ew = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = run(inp, q, k8, v8, 0, error_word=ew)
+    assert ops.pkd_read_device_error(ew) == 0
+    rows = sample_rows(B, Hq, 256, seed=B)
+    got = out.view(-1, D)[torch.from_numpy(rows).long().cuda()]
+    assert_close(got, ref(inp, q, k8, v8, rows=rows), f"wide fp8 {shape}")
