@@ -94,13 +94,17 @@ int pick_auto(int variant, int group, long long grid, long long tokens_per_cta) 
   return PKD_VARIANT_TMA_MMA;
 }
 
-// Resident CTAs per SM the kernel of a data path and group size is built for
-// (mirrors DecodeTraits::MIN_BLOCKS).
+// CTAs per SM of the split and order policy's wave unit for a data path and
+// group size: the CUDA-core kernels' residency (DecodeTraits::MIN_BLOCKS),
+// and two for the tensor-core path, the residency its thresholds were
+// measured at (it now runs three or four per SM).
 int ctas_per_sm(int variant, int group) {
   return (resolve_variant(variant) == PKD_VARIANT_TMA_STAGED && group >= 2 && group <= 5) ? 3 : 2;
 }
 
-// Resident CTAs of one wave for a data path and group size.
+// The wave unit of the split and order policy: ctas_per_sm of the data path
+// (two CTAs per SM for the tensor-core path, the residency its thresholds
+// were measured at) times the SM count.
 long long wave_ctas(int variant, int group) {
   int sms = sm_count();
   if (sms <= 0) sms = 148;

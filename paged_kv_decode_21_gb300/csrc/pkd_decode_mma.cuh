@@ -150,13 +150,15 @@ struct MmaTraits {
   static constexpr int NT = ROWS > 8 ? 2 : 1;  // 8-row halves in use (P.V n-tiles)
   static constexpr int NW = 4;
   static constexpr int THREADS = NW * 32;
-  // Two CTAs per SM with 96 KiB rings for fp16.  E4M3 halves the bytes per
-  // token, so the same warps must retire twice the tokens: three CTAs per SM
-  // with 64 KiB rings (4 KiB slots, 4 per warp) measured 1.24-1.29x faster.
-  // Single-query E4M3 grids of many waves go to four CTAs per SM (48 KiB
-  // rings, one QK chain so the state fits in 128 registers): 2-7% faster
-  // there, but slower where a few waves of long CTAs bound the grid.
-  static constexpr int MIN_BLOCKS = CPS ? CPS : (KVB == 1 ? 3 : 2);
+  // Three CTAs per SM with 64 KiB rings: more warps to hide the latency of
+  // the ldmatrix -> mma -> softmax chains.  Against two CTAs with 96 KiB
+  // rings this measured 1.24-1.29x faster with E4M3 caches (half the bytes
+  // per token, so twice the tokens per warp) and, with fp16, up to 1.02x on
+  // single-query decode and 1.05-1.21x on multi-token queries.  Single-query
+  // E4M3 grids of many waves go to four CTAs per SM (48 KiB rings, one QK
+  // chain so the state fits in 128 registers): 2-9% faster there, but slower
+  // where a few waves of long CTAs bound the grid.
+  static constexpr int MIN_BLOCKS = CPS ? CPS : 3;
   static constexpr int RING_KIB = MIN_BLOCKS >= 4 ? 48 : (MIN_BLOCKS == 3 ? 64 : 96);
   static constexpr int QK_CHAINS = MIN_BLOCKS >= 4 ? 1 : 2;  // independent accumulator chains per QK n-tile
   static constexpr bool F8 = KVB == 1;
