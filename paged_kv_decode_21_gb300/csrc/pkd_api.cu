@@ -182,6 +182,59 @@ Workspace layout(void* base, int num_seqs, int num_q_heads, int head_dim, int np
   return w;
 }
 
+// Query chunks per (sequence, kv head) of q_len query tokens: the
+// multi-token kernel serves 16 / G query tokens per CTA.
+int query_chunks(int q_len, int G) {
+  if (q_len <= 1) return 1;
+  const int qc = 16 / G;
+  return (q_len + qc - 1) / qc;
+}
+
+// The launch plan of one decode call.
+struct CallPlan {
+  int P;           // tokens per partition (the whole context, rounded up to 32, when unsplit)
+  int np;          // partitions in the grid (1 when unsplit)
+  bool split;      // the split-K merge runs
+  long long grid;  // decode CTAs
+  int variant;     // the data path it runs, with the PKD_FLAG_* bits that apply
+  bool order;      // the batch is walked longest first (when the workspace has room)
+};
+
+// The partition, grid, data path and order a call with these arguments runs
+// (the shape already checked).
+pkd_status plan_call(const Shape& s, int q_len, int variant, int partition_size, int kv_fp8, CallPlan* out) {
+  const int G = s.num_q_heads / s.num_kv_heads;
+  const int q_chunks = query_chunks(q_len, G);
+  const int flags = variant & ~0xff;
+  if (q_len > 1 || kv_fp8) {
+    // several query tokens per sequence, or E4M3 caches: the tensor-core path only
+    const int path = variant_path(variant);
+    if (path != PKD_VARIANT_AUTO && path != PKD_VARIANT_TMA_MMA) return PKD_ERR_UNSUPPORTED;
+    variant = PKD_VARIANT_TMA_MMA | flags;
+  }
+  int P;
+  int flags_eff = flags;
+  if (partition_size == 0) {
+    P = auto_partition(s, variant, q_chunks);
+    if (auto_order(s, variant, q_chunks, P)) flags_eff |= PKD_FLAG_LONGEST_FIRST;
+  } else if (partition_size == -1) {
+    P = -1;
+  } else {
+    if (partition_size < 0 || partition_size % 32 != 0 || partition_size % s.block_size != 0)
+      return PKD_ERR_SHAPE;
+    P = partition_size;
+  }
+  out->split = P > 0 && s.max_context_len > P;
+  out->np = out->split ? (s.max_context_len + P - 1) / P : 1;
+  if (!out->split) P = s.max_context_len > 0 ? (int)round_up((size_t)s.max_context_len, 32) : 32;
+  out->P = P;
+  out->grid = (long long)s.num_seqs * s.num_kv_heads * q_chunks * out->np;
+  const int v = pick_auto(variant, G, out->grid, P);
+  out->order = out->grid > 0 && want_order(flags_eff, variant_path(v), s.num_seqs);
+  out->variant = (v & ~PKD_FLAG_LONGEST_FIRST) | (out->order ? PKD_FLAG_LONGEST_FIRST : 0);
+  return PKD_OK;
+}
+
 pkd_status launch_decode(int variant, int D, int BS, int G, const pkd::DecodeParams& p,
                          long long grid, cudaStream_t stream) {
   if (grid <= 0) return PKD_OK;
@@ -275,20 +328,10 @@ int paged_decode_auto_partition_size(int num_seqs, int num_q_heads, int num_kv_h
 int paged_decode_auto_variant(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                               int block_size, int max_context_len, int partition_size) {
   Shape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, 1, 1 << 30, max_context_len};
-  if (check_shape(s) != PKD_OK) return -2;
-  if (partition_size < -1 || (partition_size > 0 && (partition_size % 32 != 0 ||
-                                                     partition_size % block_size != 0)))
-    return -2;
-  int P = partition_size == 0 ? auto_partition(s) : partition_size;
-  const bool split = P > 0 && max_context_len > P;
-  const long long np = split ? (max_context_len + P - 1) / P : 1;
-  const long long tokens = split ? P : (long long)round_up((size_t)(max_context_len > 0 ? max_context_len : 1), 32);
-  const int v = pick_auto(PKD_VARIANT_AUTO, num_q_heads / num_kv_heads, (long long)num_seqs * num_kv_heads * np,
-                          tokens);
-  if (partition_size == 0 && v == PKD_VARIANT_TMA_MMA && auto_order(s, v, 1, P) &&
-      want_order(PKD_FLAG_LONGEST_FIRST, v, num_seqs))
-    return v | PKD_FLAG_LONGEST_FIRST;
-  return v;
+  if (check_shape(s) != PKD_OK || partition_size < -1) return -2;
+  CallPlan plan;
+  if (plan_call(s, 1, PKD_VARIANT_AUTO, partition_size, 0, &plan) != PKD_OK) return -2;
+  return plan.variant;
 }
 
 size_t paged_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
@@ -309,58 +352,6 @@ size_t paged_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_hea
 
 namespace {
 
-// Query chunks per (sequence, kv head) of q_len query tokens: the
-// multi-token kernel serves 16 / G query tokens per CTA.
-int query_chunks(int q_len, int G) {
-  if (q_len <= 1) return 1;
-  const int qc = 16 / G;
-  return (q_len + qc - 1) / qc;
-}
-
-// The launch plan of one decode call.
-struct CallPlan {
-  int P;           // tokens per partition (the whole context, rounded up to 32, when unsplit)
-  int np;          // partitions in the grid (1 when unsplit)
-  bool split;      // the split-K merge runs
-  long long grid;  // decode CTAs
-  int variant;     // the data path it runs, with the PKD_FLAG_* bits that apply
-  bool order;      // the batch is walked longest first (when the workspace has room)
-};
-
-// The partition, grid, data path and order a call with these arguments runs
-// (the shape already checked).
-pkd_status plan_call(const Shape& s, int q_len, int variant, int partition_size, int kv_fp8, CallPlan* out) {
-  const int G = s.num_q_heads / s.num_kv_heads;
-  const int q_chunks = query_chunks(q_len, G);
-  const int flags = variant & ~0xff;
-  if (q_len > 1 || kv_fp8) {
-    // several query tokens per sequence, or E4M3 caches: the tensor-core path only
-    const int path = variant_path(variant);
-    if (path != PKD_VARIANT_AUTO && path != PKD_VARIANT_TMA_MMA) return PKD_ERR_UNSUPPORTED;
-    variant = PKD_VARIANT_TMA_MMA | flags;
-  }
-  int P;
-  int flags_eff = flags;
-  if (partition_size == 0) {
-    P = auto_partition(s, variant, q_chunks);
-    if (auto_order(s, variant, q_chunks, P)) flags_eff |= PKD_FLAG_LONGEST_FIRST;
-  } else if (partition_size == -1) {
-    P = -1;
-  } else {
-    if (partition_size < 0 || partition_size % 32 != 0 || partition_size % s.block_size != 0)
-      return PKD_ERR_SHAPE;
-    P = partition_size;
-  }
-  out->split = P > 0 && s.max_context_len > P;
-  out->np = out->split ? (s.max_context_len + P - 1) / P : 1;
-  if (!out->split) P = s.max_context_len > 0 ? (int)round_up((size_t)s.max_context_len, 32) : 32;
-  out->P = P;
-  out->grid = (long long)s.num_seqs * s.num_kv_heads * q_chunks * out->np;
-  const int v = pick_auto(variant, G, out->grid, P);
-  out->order = out->grid > 0 && want_order(flags_eff, variant_path(v), s.num_seqs);
-  out->variant = (v & ~PKD_FLAG_LONGEST_FIRST) | (out->order ? PKD_FLAG_LONGEST_FIRST : 0);
-  return PKD_OK;
-}
 
 // Decode of q_len query tokens per sequence (q_len = 1: single-query decode).
 pkd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
