@@ -93,15 +93,18 @@ typedef enum {
  */
 #define PKD_FLAG_L2_EVICT_HINTS 0x100
 /*
- *   PKD_FLAG_LONGEST_FIRST  hand the decode grid's work out longest sequence
- *       first: a one-CTA-per-128-sequences kernel ranks the sequences by
- *       context length (ties by index) into the workspace, and the tensor-core
- *       decode grid walks the ranks, so the last CTAs to start hold the
- *       shortest work and the tail of a ragged batch shortens.  Results are
- *       unchanged.  Tensor-core path only, batches of 2..4096 sequences;
- *       elsewhere it is ignored.  The workspace grows by the order
- *       (paged_decode_workspace_size counts it, after the split partials);
- *       a workspace without that room runs the plain order.
+ *   PKD_FLAG_LONGEST_FIRST  hand the decode grid's work out longest first:
+ *       a kernel of one CTA per 128 sequences orders the grid's pieces
+ *       (partition j of sequence b) into the workspace: the full partitions,
+ *       then each sequence's last partition by decreasing length, then the
+ *       empty ones.  The tensor-core decode grid walks that order, so the
+ *       last CTAs to start hold the shortest work and the tail of a ragged
+ *       batch shortens.  Unsplit, this is the sequences by decreasing
+ *       length.  Results are unchanged.  Tensor-core path only, batches of
+ *       2..4096 sequences; elsewhere it is ignored.  The workspace grows by
+ *       the order, one int32 per piece (paged_decode_workspace_size counts
+ *       it, after the split partials); a workspace without that room runs
+ *       the plain order.
  */
 #define PKD_FLAG_LONGEST_FIRST 0x200
 
@@ -178,7 +181,8 @@ int paged_decode_auto_partition_size(int num_seqs, int num_q_heads, int num_kv_h
  * partials [num_seqs][num_q_heads][NP][head_dim] and the per-partition
  * max and sum [num_seqs][num_q_heads][NP], NP = ceil(max_context_len /
  * partition_size), then, for partition_size 0 or PKD_FLAG_LONGEST_FIRST,
- * the longest-first order (num_seqs int32), each region 256-byte aligned.
+ * the longest-first order (num_seqs x NP int32, NP = 1 unsplit), each region
+ * 256-byte aligned.
  * 0 when nothing splits and no order is kept.
  */
 /*

@@ -147,8 +147,16 @@ struct Workspace {
   size_t bytes;
 };
 
-// Bytes of the longest-first order (one int32 per sequence) appended to a workspace.
-size_t order_bytes(int num_seqs) { return round_up((size_t)num_seqs * sizeof(int32_t), 256); }
+// Bytes of the longest-first order (one int32 per piece: sequences x partitions
+// of the grid) appended to a workspace.
+size_t order_bytes(int num_seqs, int np = 1) {
+  return round_up((size_t)num_seqs * (size_t)(np > 0 ? np : 1) * sizeof(int32_t), 256);
+}
+
+// Partitions of the grid for a partition choice (1 when unsplit).
+int grid_partitions(int max_context_len, int P) {
+  return (P > 0 && max_context_len > P) ? (max_context_len + P - 1) / P : 1;
+}
 
 // Whether the automatic split also walks the batch longest first: an unsplit
 // grid of one to kOrderMaxWaves waves, where the last wave's short CTAs
@@ -344,7 +352,8 @@ size_t paged_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_hea
   size_t bytes = 0;
   if (P > 0 && max_context_len > P)
     bytes = layout(nullptr, num_seqs, num_q_heads, head_dim, (max_context_len + P - 1) / P).bytes;
-  if ((variant & PKD_FLAG_LONGEST_FIRST) || partition_size == 0) bytes += order_bytes(num_seqs);
+  if ((variant & PKD_FLAG_LONGEST_FIRST) || partition_size == 0)
+    bytes += order_bytes(num_seqs, grid_partitions(max_context_len, P));
   return bytes;
 }
 
@@ -425,11 +434,11 @@ pkd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
   // the order sits after the partials; it only reschedules, so a workspace
   // without room for it runs the plain grid order instead
   if (grid > 0 && plan.order && workspace &&
-      aligned(workspace, 256) && workspace_bytes >= used + order_bytes(num_seqs)) {
+      aligned(workspace, 256) && workspace_bytes >= used + order_bytes(num_seqs, np)) {
     int32_t* order = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(workspace) + used);
-    pkd::seq_order_kernel<<<(num_seqs + 127) / 128, 128, 0, stream>>>(context_lens, num_seqs, order);
+    pkd::piece_order_kernel<<<(num_seqs + 127) / 128, 128, 0, stream>>>(context_lens, num_seqs, P, np, order);
     if (cudaGetLastError() != cudaSuccess) return PKD_ERR_LAUNCH;
-    p.seq_order = order;
+    p.piece_order = order;
   }
   if (kv_fp8) {
     if (grid > 0x7fffffffLL) return PKD_ERR_SHAPE;
@@ -518,7 +527,8 @@ size_t paged_decode_multi_workspace_size(int num_seqs, int q_len, int num_q_head
   size_t bytes = 0;
   if (P > 0 && max_context_len > P)
     bytes = layout(nullptr, num_seqs * q_len, num_q_heads, head_dim, (max_context_len + P - 1) / P).bytes;
-  if (partition_size == 0) bytes += order_bytes(num_seqs);  // the automatic split may order the batch
+  if (partition_size == 0)  // the automatic split may order the batch
+    bytes += order_bytes(num_seqs, grid_partitions(max_context_len, P));
   return bytes;
 }
 

@@ -160,33 +160,54 @@ __global__ void __launch_bounds__(256) paged_kv_append_fp8_kernel(
 }
 
 // ---------------------------------------------------------------------------
-// Longest-first order of the sequences: seq_order[r] is the sequence of rank
-// r when the sequences are sorted by decreasing context length (ties by
-// index), so a decode grid that walks ranks hands its longest work out
-// first and ends on short work.  Each CTA holds all lengths in shared memory
-// and ranks 128 of the sequences against them, four lengths per step.  The
-// decode grid reading the order is launched as its programmatic dependent.
-constexpr int kOrderMaxSeqs = 4096;  // lengths held in shared memory (16 KiB)
-__global__ void __launch_bounds__(128) seq_order_kernel(const int32_t* __restrict__ context_lens, int num_seqs,
-                                                        int32_t* __restrict__ seq_order) {
-  __shared__ __align__(16) int32_t lens[kOrderMaxSeqs + 4];
+// Longest-first order of the grid's pieces.  A piece is partition j of
+// sequence b, (b, j) for j < NP; its tokens are min(PS, L_b - j PS), none
+// past the context.  piece_order[p] = b * NP + j lists every piece once:
+//   1. the full pieces (all but each sequence's last), by sequence and j;
+//   2. each sequence's last piece, by decreasing tokens (ties by sequence);
+//   3. the empty pieces (past a sequence's context), by sequence and j.
+// A decode grid that walks p hands its longest work out first and ends on
+// the shortest.  Unsplit (NP = 1) the pieces are the sequences, sorted by
+// decreasing length.  Each CTA holds every sequence's piece count and last
+// piece in shared memory and places the pieces of 128 sequences.  The decode
+// grid reading the order is launched as its programmatic dependent.
+constexpr int kOrderMaxSeqs = 4096;  // sequences held in shared memory (2 x 16 KiB)
+__global__ void __launch_bounds__(128) piece_order_kernel(const int32_t* __restrict__ context_lens, int num_seqs,
+                                                          int partition_size, int num_partitions,
+                                                          int32_t* __restrict__ piece_order) {
+  __shared__ int32_t s_np[kOrderMaxSeqs];    // pieces with tokens
+  __shared__ int32_t s_last[kOrderMaxSeqs];  // tokens of the last of them
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int padded = (num_seqs + 3) & ~3;
-  for (int i = threadIdx.x; i < padded; i += blockDim.x)
-    lens[i] = i < num_seqs ? max(context_lens[i], 0) : -1;  // padding ranks below every sequence
+  const int PS = partition_size, NP = num_partitions;
+  for (int i = threadIdx.x; i < num_seqs; i += blockDim.x) {
+    const int L = max(context_lens[i], 0);
+    const int n = min((L + PS - 1) / PS, NP);
+    s_np[i] = n;
+    s_last[i] = n > 0 ? L - (n - 1) * PS : 0;
+  }
   __syncthreads();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= num_seqs) return;
-  const int L = lens[b];
-  int rank = 0;
-  for (int i = 0; i < padded; i += 4) {
-    const int4 v = *reinterpret_cast<const int4*>(lens + i);
-    rank += (v.x > L) | ((v.x == L) & (i < b));
-    rank += (v.y > L) | ((v.y == L) & (i + 1 < b));
-    rank += (v.z > L) | ((v.z == L) & (i + 2 < b));
-    rank += (v.w > L) | ((v.w == L) & (i + 3 < b));
+  const int n_b = s_np[b], last_b = s_last[b];
+  int full = 0, full_before = 0, lasts = 0, last_rank = 0, empty_before = 0;
+  for (int i = 0; i < num_seqs; ++i) {
+    const int n = s_np[i];
+    const int f = n > 0 ? n - 1 : 0;
+    full += f;
+    lasts += n > 0;
+    if (i < b) {
+      full_before += f;
+      empty_before += NP - n;
+    }
+    if (n > 0) {
+      const int li = s_last[i];
+      last_rank += (li > last_b) | ((li == last_b) & (i < b));
+    }
   }
-  seq_order[rank] = b;
+  const int base = b * NP;
+  for (int j = 0; j + 1 < n_b; ++j) piece_order[full_before + j] = base + j;
+  if (n_b > 0) piece_order[full + last_rank] = base + n_b - 1;
+  for (int j = n_b; j < NP; ++j) piece_order[full + lasts + empty_before + (j - n_b)] = base + j;
 }
 
 // ---------------------------------------------------------------------------

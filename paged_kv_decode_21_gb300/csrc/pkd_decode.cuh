@@ -70,7 +70,7 @@ struct DecodeParams {
   int prefetch_distance;
   int l2_hints;         // 1: evict_first on consuming loads/copies, evict_last on prefetches
   unsigned long long timeout_ns;
-  const int32_t* seq_order;  // nullable: grid rank -> sequence (longest first); tensor-core path only
+  const int32_t* piece_order;  // nullable: grid piece p -> b * NP + j (longest first); tensor-core path only
 };
 
 template <int D, int BS, int G, int VARIANT>

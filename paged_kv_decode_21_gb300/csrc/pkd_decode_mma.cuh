@@ -209,19 +209,24 @@ __global__ void __launch_bounds__(MmaTraits<D, BS, G, QC, KVB, CPS>::THREADS,
   const int np_grid = P.max_partitions;
   const int qc = blockIdx.x % P.q_chunks;
   const int rest = blockIdx.x / P.q_chunks;
-  const int j = rest % np_grid;
-  const int bg = rest / np_grid;
-  const int g = bg % P.num_kv_heads;
   // a dependent grid (the split-K merge) may launch once every CTA of this
   // grid has started; it waits for this grid's completion itself
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  // with a longest-first order the grid walks ranks; it is the programmatic
-  // dependent of the kernel writing the order and waits for it here (without
-  // a prerequisite grid the wait returns at once)
-  int b = bg / P.num_kv_heads;
-  if (P.seq_order) {
+  int j, b, g;
+  if (P.piece_order) {
+    // longest first: the grid walks pieces p (all kv heads of a piece side by
+    // side); it is the programmatic dependent of the kernel writing the
+    // order and waits for it here
+    g = rest % P.num_kv_heads;
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    b = P.seq_order[b];
+    const int piece = P.piece_order[rest / P.num_kv_heads];
+    b = piece / np_grid;
+    j = piece % np_grid;
+  } else {
+    j = rest % np_grid;
+    const int bg = rest / np_grid;
+    g = bg % P.num_kv_heads;
+    b = bg / P.num_kv_heads;
   }
   const int L = P.context_lens[b];
   const int QL = P.q_len;

@@ -63,7 +63,7 @@ cudaError_t launch_qc(const CUtensorMap& mk, const CUtensorMap& mv, const Decode
   auto* fn = paged_decode_mma_kernel<D, BS, G, QC, KVB, CPS>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  if (!p.seq_order) {
+  if (!p.piece_order) {
     fn<<<(unsigned)grid, T::THREADS, T::SMEM_BYTES, stream>>>(mk, mv, p);
     return cudaGetLastError();
   }

@@ -347,3 +347,26 @@ def test_longest_first_order_kernel_ranks_by_length():
     torch.cuda.synchronize()
     order = ws[:4 * len(lens)].view(torch.int32).cpu().tolist()
     assert order == sorted(range(len(lens)), key=lambda b: (-lens[b], b))
+
+
+def test_longest_first_piece_order_of_a_split_grid():
+    # partition 64: full pieces by sequence, then last pieces by decreasing length, then empties
+    lens = [130, 0, 64, 200, 7, 129]
+    P, NP = 64, 4
+    inp = workloads.make_custom(len(lens), 4, 4, 64, 16, lens, seed=5, device="cuda")
+    need = ops.paged_decode_workspace_size(len(lens), 4, 4, 64, 16, max(lens), P, "tma_mma+longest_first")
+    ws = ops.alloc_workspace(need, "cuda")
+    ws.fill_(0xFF)
+    out = run_ex(inp, "tma_mma+longest_first", P, workspace=ws)
+    assert_close(out, oracle_out(inp), "piece order")
+    torch.cuda.synchronize()
+    # the order follows the split partials in the workspace
+    rows = len(lens) * 4 * NP
+    off = -(-rows * 64 * 4 // 256) * 256 + 2 * (-(-rows * 4 // 256) * 256)
+    got = ws[off:off + 4 * len(lens) * NP].view(torch.int32).cpu().tolist()
+    n = [min(-(-L // P), NP) for L in lens]
+    last = [L - (k - 1) * P if k else 0 for L, k in zip(lens, n)]
+    full = [b * NP + j for b in range(len(lens)) for j in range(n[b] - 1)]
+    lasts = [b * NP + n[b] - 1 for b in sorted((b for b in range(len(lens)) if n[b]), key=lambda b: (-last[b], b))]
+    empties = [b * NP + j for b in range(len(lens)) for j in range(n[b], NP)]
+    assert got == full + lasts + empties
