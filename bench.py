@@ -13,9 +13,10 @@ Timing: W warm-up calls, then K timed calls, each bracketed by CUDA events
 on the launching stream.  A workload whose algorithmic bytes exceed 4x the
 L2 size runs its calls back to back: the inputs are larger than L2, and a
 call's first reads are the blocks the previous call read first, long
-evicted.  Smaller workloads get an L2 flush (a 2x-L2 buffer write) before
-every call.  (A flush leaves L2 full of dirty lines whose write-back lands
-inside the next call; measured at about 5% of the MHA call.)  value =
+evicted.  Smaller workloads get an L2 flush before every call: a read of a
+buffer twice the L2 size, which leaves only clean lines behind.  (A write
+flush would leave L2 full of dirty lines whose write-back lands inside the
+next call: about 5% of the MHA call, more of a short one.)  value =
 algorithmic bytes (K and V rows used, Q, out) per call / mean call time.
 """
 from __future__ import annotations
@@ -178,6 +179,18 @@ def aggregate_over_ranks(mean_ms: float, algo_bytes: int, world_size: int, devic
     return mean_ms, world_size * algo_bytes / (mean_ms * 1e-3) / 1e9
 
 
+class L2Flush:
+    """Evicts L2 by reading a buffer of twice its size (clean lines only: no
+    write-back of the flush can land inside the next timed call)."""
+
+    def __init__(self, dev, l2):
+        self.buf = torch.ones(max(2 * l2, 256 << 20) // 4, dtype=torch.int32, device=dev)
+        self.sink = torch.empty((), dtype=torch.int64, device=dev)
+
+    def __call__(self):
+        torch.sum(self.buf, dtype=torch.int64, out=self.sink)
+
+
 def time_gpu(args, cfg, variant, dev, inp, steps, warmup, with_e2e=True, with_clocks=True):
     """Kernel-resident timing (+ optional end-to-end leg) of one workload and variant."""
     from paged_kv_decode_21_gb300 import ops
@@ -207,7 +220,7 @@ def time_gpu(args, cfg, variant, dev, inp, steps, warmup, with_e2e=True, with_cl
     out = torch.empty_like(inp.q)
     ew = torch.zeros(1, dtype=torch.int32, device=dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev, l2)
 
     def call():
         ops.paged_decode_attention_ex(inp.q, inp.k_cache, inp.v_cache, inp.block_tables,
@@ -257,7 +270,7 @@ def time_gpu(args, cfg, variant, dev, inp, steps, warmup, with_e2e=True, with_cl
 
     def maybe_flush():
         if use_flush:
-            flush.zero_()
+            flush()
 
     for _ in range(warmup):
         maybe_flush()
@@ -290,7 +303,7 @@ def time_gpu(args, cfg, variant, dev, inp, steps, warmup, with_e2e=True, with_cl
         "min_ms": min(times_ms), "wall_s": t_wall, "launches_per_call": launches,
         "partition_size": eff_P if split else -1, "longest_first": ordered, "device_error": errbits,
         "clocks": sampler.summary() if sampler else None,
-        "l2": (f"an L2 flush (2x L2 write) before every timed call; inputs {algo / 1e6:.0f} MB" if use_flush
+        "l2": (f"an L2 flush (2x L2 read) before every timed call; inputs {algo / 1e6:.0f} MB" if use_flush
                else f"inputs larger than L2 ({algo / 1e9:.2f} GB against {l2 / 1e6:.0f} MB): calls back to "
                     "back, no flush"),
     }
@@ -316,7 +329,7 @@ def time_append(cfg, inp, dev, steps, warmup, peak):
                                            inp.max_context_len, 0, 0)
     ws = ops.alloc_workspace(need, dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev, l2)
 
     def append():
         ops.paged_kv_append(k_new, v_new, inp.block_tables, pos, inp.k_cache, inp.v_cache,
@@ -334,13 +347,13 @@ def time_append(cfg, inp, dev, steps, warmup, peak):
 
     def timed(fn):
         for _ in range(warmup):
-            flush.zero_()
+            flush()
             fn()
         torch.cuda.synchronize(dev)
         st = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
         en = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
         for i in range(steps):
-            flush.zero_()
+            flush()
             st[i].record(stream)
             fn()
             en[i].record(stream)
@@ -360,7 +373,7 @@ def time_append(cfg, inp, dev, steps, warmup, peak):
             "append_frac_of_peak": round(app_bytes / (t_app * 1e-6) / 1e9 / peak, 4),
             "decode_us": round(t_dec, 2), "append_then_decode_us": round(t_both, 2),
             "device_error": ops.pkd_read_device_error(ew),
-            "l2": "an L2 flush (2x L2 write) before every timed call"}
+            "l2": "an L2 flush (2x L2 read) before every timed call"}
 
 
 def time_e2e(call, inp, out, stream, dev, algo, steps):
