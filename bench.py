@@ -188,7 +188,7 @@ class L2Flush:
         self.sink = torch.empty((), dtype=torch.int64, device=dev)
 
     def __call__(self):
-        torch.sum(self.buf, dtype=torch.int64, out=self.sink)
+        torch.sum(self.buf, dim=0, dtype=torch.int64, out=self.sink)
 
 
 def time_gpu(args, cfg, variant, dev, inp, steps, warmup, with_e2e=True, with_clocks=True):
