@@ -39,3 +39,12 @@ def test_warmup_floor_is_enforced():
     r = run_bench("--impl", "reference", "--steps", "1", "--warmup", "2", timeout=120)
     assert r.returncode != 0
     assert "warmup" in r.stderr
+
+
+def test_l2_flush_reads_its_buffer():
+    # the flush is a full read of a buffer (no writes): it must run without a GPU too
+    import torch
+    import bench
+    f = bench.L2Flush(torch.device("cpu"), 1 << 16)
+    f()
+    assert int(f.sink) == f.buf.numel()
