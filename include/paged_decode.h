@@ -189,11 +189,9 @@ int paged_decode_auto_partition_size(int num_seqs, int num_q_heads, int num_kv_h
  * paged_decode_auto_variant -- the variant value (data path ORed with
  * PKD_FLAG_* bits) that PKD_VARIANT_AUTO runs for this shape, on the current
  * device, given partition_size as passed to paged_decode_attention_ex (0 =
- * automatic, -1 = unsplit, or a partition).  It is TMA_MMA, except for group
- * size 1 with at most 512 tokens per CTA and between 1 and 16 CTAs per SM,
- * where it is NO_PREFETCH (plain loads: a warp handles too few blocks for a
- * shared-memory ring to pay off).  With partition_size 0, TMA_MMA carries
- * PKD_FLAG_LONGEST_FIRST where the automatic choice orders the batch.
+ * automatic, -1 = unsplit, or a partition).  It is TMA_MMA; with
+ * partition_size 0 it carries PKD_FLAG_LONGEST_FIRST where the automatic
+ * choice orders the batch.
  * Returns -2 on an invalid shape or partition size.
  */
 int paged_decode_auto_variant(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,

@@ -69,28 +69,19 @@ int resolve_variant(int variant) {
   return variant == PKD_VARIANT_AUTO ? PKD_VARIANT_TMA_MMA : variant;
 }
 
-// What the automatic variant runs for one launch: the data path and whether
-// the L2 eviction priorities are on.  The tensor-core path (swizzled tensor
-// copies into a ring, mma for both products) is the fastest wherever a CTA
-// streams a long run of blocks, at every group size, and when the grid is
-// smaller than the GPU (each CTA's latency is exposed); the eviction
-// priorities measured neutral on it, so they stay off.  One case goes to
-// plain 16-byte loads: group size 1 with at most kShortCtaTokens tokens per
-// CTA and between 1 and kShortCtaMaxWaves CTAs per SM.  There a warp handles
-// only a few blocks, a ring's fill time is not paid back, and the batch x
-// context sweep measured the plain loads 5-15% faster (at 4096+ such CTAs
-// they tie, and beyond that the ring is ahead again).  At group sizes >= 2
-// the tensor-core path wins even there: the plain-load path is issue-bound.
-constexpr int kShortCtaTokens = 512;
-constexpr int kShortCtaMaxWaves = 16;
-
+// What the automatic variant runs for one launch: the tensor-core path
+// (swizzled tensor copies into a ring, mma for both products), without the
+// L2 eviction priorities, which measured neutral on it.  It is the fastest
+// path at every point of the batch x context sweep, uniform and ragged.
+// (Plain 16-byte loads used to be picked for group size 1 with at most 512
+// tokens per CTA and 1-16 CTAs per SM; with three CTAs per SM, and L2
+// flushed without dirty lines, the tensor-core path is 0-7% faster there
+// too.)
 int pick_auto(int variant, int group, long long grid, long long tokens_per_cta) {
+  (void)group;
+  (void)grid;
+  (void)tokens_per_cta;
   if (variant_path(variant) != PKD_VARIANT_AUTO) return variant;
-  int sms = sm_count();
-  if (sms <= 0) sms = 148;
-  if (group == 1 && tokens_per_cta <= kShortCtaTokens && grid >= sms &&
-      grid <= (long long)kShortCtaMaxWaves * sms)
-    return PKD_VARIANT_NO_PREFETCH;
   return PKD_VARIANT_TMA_MMA;
 }
 

@@ -146,14 +146,14 @@ def test_auto_variant_policy(L):
     # thresholds, so they hold for 152 as well
     av = ops.paged_decode_auto_variant
     staged = ops.VARIANTS["tma_mma"]
-    plain = ops.VARIANTS["no_prefetch"]
+    # the tensor-core path at every shape, short CTAs included
     assert av(64, 32, 32, 128, 16, 2048) == staged      # long CTAs
-    assert av(64, 32, 32, 128, 16, 512) == plain        # 2048 CTAs of 512 tokens
-    assert av(16, 32, 32, 128, 16, 2048) == plain       # split at 512: 2048 CTAs
+    assert av(64, 32, 32, 128, 16, 512) == staged       # 2048 CTAs of 512 tokens
+    assert av(16, 32, 32, 128, 16, 2048) == staged      # split at 512: 2048 CTAs
     assert av(256, 32, 32, 128, 16, 512) == staged      # 8192 CTAs: many waves
     assert av(1, 32, 32, 128, 16, 1024) == staged       # fewer CTAs than SMs
-    assert av(64, 32, 8, 128, 16, 512) == staged        # GQA always staged
-    assert av(64, 32, 32, 128, 16, 512, -1) == plain
+    assert av(64, 32, 8, 128, 16, 512) == staged
+    assert av(64, 32, 32, 128, 16, 512, -1) == staged
     assert av(64, 32, 32, 128, 16, 4096, 256) == staged  # 16384 CTAs
     # unsplit grids of one to six waves of units walk the batch longest first
     ordered = staged | ops.FLAG_LONGEST_FIRST

@@ -32,7 +32,7 @@ def _worker(rank, world, port, results):
 def test_two_replicas_take_the_slowest_rank():
     world = 2
     port = _free_port()
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:
         results = mgr.dict()
         mp.start_processes(_worker, args=(world, port, results), nprocs=world, start_method="spawn")
         res = dict(results)
