@@ -76,13 +76,15 @@ def kernel_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def kernel_name(cfg: workloads.DecodeConfig, variant: str, kv_fp8: bool = False) -> str:
-    """The decode kernel a resolved variant launches for a shape."""
+def kernel_name(cfg: workloads.DecodeConfig, variant: str, kv_fp8: bool = False, wide: bool = False) -> str:
+    """The decode kernel a resolved variant launches for a shape (template arguments: head
+    dim, block size, group, query tokens per CTA, bytes per K/V element, CTAs per SM with 0
+    for the default three)."""
     path = variant.split("+")[0]
     shape = f"{cfg.head_dim},{cfg.block_size},{cfg.group}"
     if path == "tma_mma":
-        # E4M3 caches: bytes per element 1; grids of 3+ waves of four CTAs per SM add CPS = 4
-        return f"paged_decode_mma_kernel<{shape},1,{1 if kv_fp8 else 2}>"
+        # single-query E4M3 grids of 3+ waves of four CTAs per SM run the four-per-SM build
+        return f"paged_decode_mma_kernel<{shape},1,{1 if kv_fp8 else 2},{4 if (kv_fp8 and wide) else 0}>"
     if path == "tma_staged" and cfg.group >= 6:
         return f"paged_decode_ws_kernel<{shape}>"
     return f"paged_decode_kernel<{shape},{variant}>"
@@ -217,6 +219,9 @@ def time_gpu(args, cfg, variant, dev, inp, steps, warmup, with_e2e=True, with_cl
         split = eff_P > 0 and inp.max_context_len > eff_P
         ordered = "longest_first" in variant and inp.num_seqs >= 2 and variant.startswith("tma_mma")
         launches = 1 + int(split) + int(ordered)
+    # decode CTAs: (sequence, kv head, query chunk of 16 / G tokens, partition)
+    q_chunks = 1 if q_len <= 1 else -(-q_len // (16 // cfg.group))
+    grid = inp.num_seqs * inp.num_kv_heads * q_chunks * (-(-inp.max_context_len // eff_P) if split and eff_P > 0 else 1)
     out = torch.empty_like(inp.q)
     ew = torch.zeros(1, dtype=torch.int32, device=dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -300,7 +305,7 @@ def time_gpu(args, cfg, variant, dev, inp, steps, warmup, with_e2e=True, with_cl
     errbits = ops.pkd_read_device_error(ew)
     res = {
         "algo_bytes": algo, "mean_ms": statistics.mean(times_ms), "median_ms": statistics.median(times_ms),
-        "min_ms": min(times_ms), "wall_s": t_wall, "launches_per_call": launches,
+        "min_ms": min(times_ms), "wall_s": t_wall, "launches_per_call": launches, "grid": grid,
         "partition_size": eff_P if split else -1, "longest_first": ordered, "device_error": errbits,
         "clocks": sampler.summary() if sampler else None,
         "l2": (f"an L2 flush (2x L2 read) before every timed call; inputs {algo / 1e6:.0f} MB" if use_flush
@@ -635,7 +640,8 @@ def main():
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "traffic": ncu_traffic(cfg.name, resolved),
-                     "kernel": kernel_name(cfg, resolved, args.kv_fp8)},
+                     "kernel": kernel_name(cfg, resolved, args.kv_fp8,
+                                           wide=args.q_len == 1 and r["grid"] >= 3 * 4 * torch.cuda.get_device_properties(dev).multi_processor_count)},
         "gpu_launches": r["launches_per_call"] * args.steps,
         "clocks": r["clocks"],
         "e2e": r.get("e2e"),
