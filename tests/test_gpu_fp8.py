@@ -174,3 +174,19 @@ def test_fp8_wide_grid_four_per_sm_build(shape):
     rows = sample_rows(B, Hq, 256, seed=B)
     got = out.view(-1, D)[torch.from_numpy(rows).long().cuda()]
     assert_close(got, ref(inp, q, k8, v8, rows=rows), f"wide fp8 {shape}")
+
+
+def test_fp8_automatic_order_is_bitwise_neutral():
+    # 1024 (sequence, kv head) units of ragged length: the automatic split keeps the grid
+    # unsplit and walks it longest first; the order only reschedules CTAs
+    B, Hq, Hkv = 128, 32, 8
+    lens = torch.randint(512, 4097, (B,), generator=torch.Generator().manual_seed(21)).tolist()
+    inp, q, k8, v8 = make(lens, Hq, Hkv, 128, 16, seed=21)
+    n, part, ordered = ops.paged_decode_auto_plan(B, 1, Hq, Hkv, 128, 16, inp.max_context_len, kv_fp8=True)
+    assert ordered and part == -1 and n == 2
+    a = run(inp, q, k8, v8, 0)
+    b = run(inp, q, k8, v8, -1)
+    assert torch.equal(a, b)
+    rows = sample_rows(B, Hq, 128, seed=21)
+    got = a.view(-1, 128)[torch.from_numpy(rows).long().cuda()]
+    assert_close(got, ref(inp, q, k8, v8, rows=rows), "fp8 longest first")

@@ -140,3 +140,18 @@ def test_multi_query_full_size_gqa_sampled():
     ref = oracle_multi(inp, q, rows=rows)
     got = out.view(-1, cfg.head_dim)[torch.from_numpy(rows).long().cuda()]
     assert_close(got, ref, "llama3_8b_gqa4 q_len=4")
+
+
+def test_multi_query_automatic_order_is_bitwise_neutral():
+    # ragged batch whose unsplit grid the automatic split walks longest first
+    B, Hq, Hkv, q_len = 128, 32, 8, 2
+    lens = torch.randint(1024, 4097, (B,), generator=torch.Generator().manual_seed(23)).tolist()
+    inp, q = make(lens, q_len, Hq, Hkv, 128, 16, seed=23)
+    n, part, ordered = ops.paged_decode_auto_plan(B, q_len, Hq, Hkv, 128, 16, inp.max_context_len)
+    assert ordered and part == -1
+    a = run_multi(inp, q, 0)
+    b = run_multi(inp, q, -1)
+    assert torch.equal(a, b)
+    rows = sample_rows(B * q_len, Hq, 96, seed=23)
+    got = a.view(-1, 128)[torch.from_numpy(rows).long().cuda()]
+    assert_close(got, oracle_multi(inp, q, rows=rows), "multi longest first")
