@@ -211,3 +211,35 @@ def test_auto_partition_policy(L):
     for variant in (1, 2, 3):
         p1 = L.paged_decode_auto_partition_size(2, 8, 1, 128, 16, 32768, variant)
         assert 0 < p1 and p1 % 32 == 0
+
+
+def test_workspace_sizes_cover_every_plan(L):
+    # For random shapes, partitions and flags, a workspace of exactly the reported size is
+    # never refused (PKD_ERR_WORKSPACE = 5); without a GPU the call then fails at launch
+    # (PKD_ERR_LAUNCH = 6) or on the device query (PKD_ERR_CUDA = 8), after every host check.
+    import random
+    rng = random.Random(7)
+    ws_ptr = ctypes.c_void_p(1 << 20)
+    for _ in range(300):
+        Hkv = rng.choice([1, 2, 4, 8])
+        G = rng.randint(1, 8)
+        D = rng.choice([64, 128])
+        BS = rng.choice([16, 32])
+        B = rng.randint(1, 300)
+        maxlen = rng.randint(1, 20000)
+        MB = -(-maxlen // BS) + rng.randint(0, 3)
+        P = rng.choice([0, 0, -1, 32 * BS // 16 * rng.randint(1, 64)])
+        var = rng.choice([0, 4, 4 | 0x200, 3, 0x100 | 4])
+        need = L.paged_decode_workspace_size(B, G * Hkv, Hkv, D, BS, maxlen, P, var)
+        st = L.paged_decode_attention_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, B, G * Hkv, Hkv, D, BS, 64, MB, maxlen,
+                                         ctypes.c_float(0.1), P, var, 0, ws_ptr if need else None, need, None, None)
+        assert st in (6, 8), (B, G, Hkv, D, BS, maxlen, P, var, need, st)
+        q_len = rng.randint(1, 9)
+        needm = L.paged_decode_multi_workspace_size(B, q_len, G * Hkv, Hkv, D, BS, maxlen, P)
+        stm = L.paged_decode_attention_multi(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, B, q_len, G * Hkv, Hkv, D, BS, 64, MB,
+                                             maxlen, ctypes.c_float(0.1), P, ws_ptr if needm else None, needm, None, None)
+        assert stm in (6, 8), (B, q_len, G, Hkv, D, BS, maxlen, P, needm, stm)
+        stf = L.paged_decode_attention_fp8(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, B, q_len, G * Hkv, Hkv, D, BS, 64, MB,
+                                           maxlen, ctypes.c_float(0.1), ctypes.c_float(0.5), ctypes.c_float(0.5), P,
+                                           ws_ptr if needm else None, needm, None, None)
+        assert stf in (6, 8), (B, q_len, G, Hkv, D, BS, maxlen, P, needm, stf)
