@@ -30,6 +30,7 @@ import subprocess
 import sys
 import threading
 import time
+import types
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
@@ -313,7 +314,11 @@ def time_gpu(args, cfg, variant, dev, inp, steps, warmup, with_e2e=True, with_cl
                     "back, no flush"),
     }
     if with_e2e:
-        res["e2e"] = time_e2e(call, inp, out, stream, dev, algo, max(3, min(20, steps // 10)))
+        e2e_steps = max(3, min(20, steps // 10))
+        if variant == "auto" and q_len == 1 and not kv_fp8 and P == 0:
+            res["e2e"] = time_e2e_host_api(inp, stream, dev, algo, e2e_steps)
+        else:
+            res["e2e"] = time_e2e(call, inp, out, stream, dev, algo, e2e_steps)
     return res
 
 
@@ -379,6 +384,48 @@ def time_append(cfg, inp, dev, steps, warmup, peak):
             "decode_us": round(t_dec, 2), "append_then_decode_us": round(t_both, 2),
             "device_error": ops.pkd_read_device_error(ew),
             "l2": "an L2 flush (2x L2 read) before every timed call"}
+
+
+def time_e2e_host_api(inp, stream, dev, algo, steps):
+    """The library's host-buffer call, paged_decode_attention_host: every step
+    copies q, the tables and lengths to the device, reads the cache blocks the
+    tables reference from pinned host memory (a gather over the host link),
+    decodes, and copies the output back.  Events bracket the whole call."""
+    from paged_kv_decode_21_gb300 import ops
+    names = ["q", "k_cache", "v_cache", "block_tables", "context_lens"]
+    host = {n: getattr(inp, n).cpu().pin_memory() for n in names}
+    out_h = torch.empty(inp.q.shape, dtype=inp.q.dtype).pin_memory()
+    need = ops.paged_decode_workspace_size(inp.num_seqs, inp.num_q_heads, inp.num_kv_heads, inp.head_dim,
+                                           inp.block_size, inp.max_context_len, 0, "auto")
+    ws = ops.alloc_workspace(need, dev)
+    lens = host["context_lens"].tolist()
+    used_blocks = sum(-(-max(L, 0) // inp.block_size) for L in lens)
+    block_bytes = inp.num_kv_heads * inp.block_size * inp.head_dim * 2
+    h2d = (host["q"].numel() * 2 + host["block_tables"].numel() * 4 + host["context_lens"].numel() * 4
+           + 2 * used_blocks * block_bytes)
+    d2h = out_h.numel() * out_h.element_size()
+    devbuf = types.SimpleNamespace(q=inp.q, k_cache=inp.k_cache, v_cache=inp.v_cache, block_tables=inp.block_tables,
+                                   context_lens=inp.context_lens, out=torch.empty_like(inp.q))
+
+    def call():
+        ops.paged_decode_attention_host(host["q"], host["k_cache"], host["v_cache"], host["block_tables"],
+                                        host["context_lens"], out_h, devbuf, inp.scale,
+                                        max_context_len=inp.max_context_len, used_blocks_only=True,
+                                        workspace=ws, stream=stream)
+
+    st = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    en = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    call()
+    torch.cuda.synchronize(dev)
+    for i in range(steps):
+        st[i].record(stream)
+        call()
+        en[i].record(stream)
+    torch.cuda.synchronize(dev)
+    ms = statistics.mean(s.elapsed_time(e) for s, e in zip(st, en))
+    return {"value": round(algo / (ms * 1e-3) / 1e9, 2), "unit": "GB/s", "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "api": "paged_decode_attention_host (used blocks only)"}
 
 
 def time_e2e(call, inp, out, stream, dev, algo, steps):

@@ -133,6 +133,41 @@ pkd_status paged_decode_attention(const void* q, const void* k_cache, const void
                                   int max_context_len, float scale, cudaStream_t stream);
 
 /*
+ * paged_decode_attention_host -- the whole operation from host buffers: the
+ * inputs are copied to the caller's device buffers, the automatic decode
+ * (as paged_decode_attention_ex with PKD_VARIANT_AUTO and partition_size 0)
+ * runs on them, and out is copied back; every step is asynchronous on
+ * `stream`, and the host `out` holds the result once the stream has
+ * reached this point.
+ *
+ *   q, k_cache, v_cache, block_tables, context_lens, out
+ *                  host buffers, layouts as above; page-locked (cudaHostAlloc
+ *                  or cudaHostRegister) for the copies to be asynchronous
+ *   q_dev, k_cache_dev, v_cache_dev, block_tables_dev, context_lens_dev, out_dev
+ *                  device buffers of the same sizes (owned by the caller)
+ *   used_blocks_only  non-zero: K and V cross the host link only for the
+ *                  blocks the tables reference (context_lens[b] tokens of
+ *                  sequence b, read in place from the mapped host pools by
+ *                  a gather kernel); blocks of k_cache_dev / v_cache_dev that
+ *                  no sequence references keep their old contents.  When the
+ *                  host pools are not mapped into the device's address space,
+ *                  or with 0, each pool is copied whole.
+ *   workspace, workspace_bytes, error_word: as for paged_decode_attention_ex
+ *                  (paged_decode_workspace_size with partition_size 0 and
+ *                  PKD_VARIANT_AUTO); error_word is device memory
+ * Other arguments as for paged_decode_attention_ex.  Returns PKD_ERR_CUDA if
+ * a copy cannot be enqueued.
+ */
+pkd_status paged_decode_attention_host(const void* q, const void* k_cache, const void* v_cache,
+                                       const int32_t* block_tables, const int32_t* context_lens, void* out,
+                                       void* q_dev, void* k_cache_dev, void* v_cache_dev,
+                                       int32_t* block_tables_dev, int32_t* context_lens_dev, void* out_dev,
+                                       int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                       int block_size, int num_blocks, int max_blocks_per_seq,
+                                       int max_context_len, float scale, int used_blocks_only, void* workspace,
+                                       size_t workspace_bytes, int* error_word, cudaStream_t stream);
+
+/*
  * paged_decode_attention_ex -- as paged_decode_attention, with control over
  * the context split and the data path.
  *

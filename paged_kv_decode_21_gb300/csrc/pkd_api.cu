@@ -523,6 +523,65 @@ size_t paged_decode_multi_workspace_size(int num_seqs, int q_len, int num_q_head
   return bytes;
 }
 
+pkd_status paged_decode_attention_host(const void* q, const void* k_cache, const void* v_cache,
+                                       const int32_t* block_tables, const int32_t* context_lens, void* out,
+                                       void* q_dev, void* k_cache_dev, void* v_cache_dev,
+                                       int32_t* block_tables_dev, int32_t* context_lens_dev, void* out_dev,
+                                       int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                       int block_size, int num_blocks, int max_blocks_per_seq,
+                                       int max_context_len, float scale, int used_blocks_only, void* workspace,
+                                       size_t workspace_bytes, int* error_word, cudaStream_t stream) {
+  Shape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq,
+          max_context_len};
+  pkd_status st = check_shape(s);
+  if (st != PKD_OK) return st;
+  if (num_seqs == 0) return PKD_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out || !q_dev || !k_cache_dev ||
+      !v_cache_dev || !block_tables_dev || !context_lens_dev || !out_dev)
+    return PKD_ERR_NULL;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(out_dev, 16) || !aligned(k_cache_dev, 16) || !aligned(v_cache_dev, 16))
+    return PKD_ERR_ALIGN;
+  const size_t q_bytes = (size_t)num_seqs * num_q_heads * head_dim * 2;
+  const size_t block_bytes = (size_t)num_kv_heads * block_size * head_dim * 2;
+  const size_t pool_bytes = (size_t)num_blocks * block_bytes;
+  const size_t bt_bytes = (size_t)num_seqs * max_blocks_per_seq * sizeof(int32_t);
+  const size_t cl_bytes = (size_t)num_seqs * sizeof(int32_t);
+  // the small inputs: one copy each
+  if (cudaMemcpyAsync(q_dev, q, q_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+      cudaMemcpyAsync(block_tables_dev, block_tables, bt_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+      cudaMemcpyAsync(context_lens_dev, context_lens, cl_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    return PKD_ERR_CUDA;
+  // the pools: the used blocks read in place from mapped host memory, or
+  // (not mapped, or asked for) one copy of each whole pool
+  void* k_map = nullptr;
+  void* v_map = nullptr;
+  const bool gather = used_blocks_only && cudaHostGetDevicePointer(&k_map, const_cast<void*>(k_cache), 0) == cudaSuccess &&
+                      cudaHostGetDevicePointer(&v_map, const_cast<void*>(v_cache), 0) == cudaSuccess;
+  if (!gather) {
+    (void)cudaGetLastError();  // a failed mapping query is not an error of this call
+    if (cudaMemcpyAsync(k_cache_dev, k_cache, pool_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+        cudaMemcpyAsync(v_cache_dev, v_cache, pool_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+      return PKD_ERR_CUDA;
+  } else {
+    const int mb = std::min(max_blocks_per_seq, (max_context_len + block_size - 1) / block_size);
+    if (mb > 0) {
+      if (num_seqs > 65535) return PKD_ERR_SHAPE;
+      pkd::gather_used_blocks_kernel<<<dim3((unsigned)mb, (unsigned)num_seqs), 256, 0, stream>>>(
+          static_cast<const uint4*>(k_map), static_cast<const uint4*>(v_map), static_cast<uint4*>(k_cache_dev),
+          static_cast<uint4*>(v_cache_dev), block_tables_dev, context_lens_dev, max_blocks_per_seq, block_size,
+          num_blocks, (long long)(block_bytes / 16), error_word);
+      if (cudaGetLastError() != cudaSuccess) return PKD_ERR_LAUNCH;
+    }
+  }
+  st = decode_impl(q_dev, k_cache_dev, v_cache_dev, block_tables_dev, context_lens_dev, out_dev, num_seqs, 1,
+                   num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq,
+                   max_context_len, scale, 0, PKD_VARIANT_AUTO, 0, workspace, workspace_bytes, error_word, stream);
+  if (st != PKD_OK) return st;
+  return cudaMemcpyAsync(out, out_dev, q_bytes, cudaMemcpyDeviceToHost, stream) == cudaSuccess ? PKD_OK
+                                                                                               : PKD_ERR_CUDA;
+}
+
 pkd_status paged_decode_attention(const void* q, const void* k_cache, const void* v_cache,
                                   const int32_t* block_tables, const int32_t* context_lens, void* out,
                                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,

@@ -160,6 +160,37 @@ __global__ void __launch_bounds__(256) paged_kv_append_fp8_kernel(
 }
 
 // ---------------------------------------------------------------------------
+// Gather of the used cache blocks from host memory: CTA (k, b) copies
+// physical block block_tables[b][k] of K and of V (all kv heads: one
+// contiguous run of chunks_per_block 16-byte chunks each) from the
+// device-mapped host pools into the device pools, for k < ceil(L_b / BS).
+// The host pools are read in place over the host link (16-byte loads), so
+// only the blocks the tables reference cross it.  A block two sequences
+// share is copied twice, with the same bytes.  Entries outside
+// [0, num_blocks) are skipped and recorded as kErrBadBlock.
+__global__ void __launch_bounds__(256) gather_used_blocks_kernel(
+    const uint4* __restrict__ k_src, const uint4* __restrict__ v_src, uint4* __restrict__ k_dst,
+    uint4* __restrict__ v_dst, const int32_t* __restrict__ block_tables,
+    const int32_t* __restrict__ context_lens, int max_blocks_per_seq, int block_size, int num_blocks,
+    long long chunks_per_block, int* error_word) {
+  const int k = blockIdx.x, b = blockIdx.y;
+  const int L = context_lens[b];
+  if (L <= 0 || (long long)k * block_size >= L || k >= max_blocks_per_seq) return;
+  const int p = block_tables[(size_t)b * max_blocks_per_seq + k];
+  if (p < 0 || p >= num_blocks) {
+    if (threadIdx.x == 0) record_error(error_word, kErrBadBlock);
+    return;
+  }
+  const size_t base = (size_t)p * (size_t)chunks_per_block;
+  for (long long i = threadIdx.x; i < chunks_per_block; i += blockDim.x) {
+    const uint4 kv = k_src[base + i];
+    const uint4 vv = v_src[base + i];
+    k_dst[base + i] = kv;
+    v_dst[base + i] = vv;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Longest-first order of the grid's pieces.  A piece is partition j of
 // sequence b, (b, j) for j < NP; its tokens are min(PS, L_b - j PS), none
 // past the context.  piece_order[p] = b * NP + j lists every piece once:

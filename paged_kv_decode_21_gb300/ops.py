@@ -68,6 +68,8 @@ def lib():
         L.paged_decode_attention_multi.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, I, P, S,
                                                    P, P]
         L.paged_decode_attention_multi.restype = I
+        L.paged_decode_attention_host.argtypes = [P] * 12 + [I] * 8 + [F, I, P, S, P, P]
+        L.paged_decode_attention_host.restype = I
         L.paged_decode_auto_plan.argtypes = [I, I, I, I, I, I, I, I, ctypes.POINTER(ctypes.c_int),
                                              ctypes.POINTER(ctypes.c_int)]
         L.paged_decode_auto_plan.restype = I
@@ -251,6 +253,30 @@ def paged_decode_attention_ex(q, k_cache, v_cache, block_tables, context_lens, s
                                          int(prefetch_distance), _ptr(workspace), wbytes,
                                          _ptr(error_word), _stream(stream))
     _check(st, "paged_decode_attention_ex")
+    return out
+
+
+def paged_decode_attention_host(q, k_cache, v_cache, block_tables, context_lens, out, dev, scale,
+                                max_context_len=None, used_blocks_only=True, workspace=None, error_word=None,
+                                stream=None) -> torch.Tensor:
+    """The whole operation from host tensors (page-locked for asynchronous copies): inputs are
+    copied into the device tensors of ``dev`` (a DecodeInputs-like object with q, k_cache,
+    v_cache, block_tables, context_lens) and ``out`` (host) receives the result once the stream
+    has run.  Returns ``out``."""
+    B, Hq, D = q.shape
+    NB, Hkv, BS, _ = k_cache.shape
+    MB = block_tables.shape[1]
+    ml = int(max_context_len) if max_context_len is not None else (int(context_lens.max()) if B else 0)
+    out_dev = dev.out if getattr(dev, "out", None) is not None else torch.empty_like(dev.q)
+    if workspace is None:
+        workspace = alloc_workspace(paged_decode_workspace_size(B, Hq, Hkv, D, BS, ml, 0, "auto"), dev.q.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().paged_decode_attention_host(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens), _ptr(out),
+        _ptr(dev.q), _ptr(dev.k_cache), _ptr(dev.v_cache), _ptr(dev.block_tables), _ptr(dev.context_lens),
+        _ptr(out_dev), B, Hq, Hkv, D, BS, NB, MB, ml, float(scale), int(bool(used_blocks_only)),
+        _ptr(workspace), wbytes, _ptr(error_word), _stream(stream))
+    _check(st, "paged_decode_attention_host")
     return out
 
 

@@ -243,3 +243,14 @@ def test_workspace_sizes_cover_every_plan(L):
                                            maxlen, ctypes.c_float(0.1), ctypes.c_float(0.5), ctypes.c_float(0.5), P,
                                            ws_ptr if needm else None, needm, None, None)
         assert stf in (6, 8), (B, q_len, G, Hkv, D, BS, maxlen, P, needm, stf)
+
+
+def test_host_entry_argument_checks(L):
+    def call(*, ptrs=(FAKE,) * 12, B=2, D=128, ws=None, wsb=0):
+        return L.paged_decode_attention_host(*ptrs, B, 8, 2, D, 16, 64, 8, 100, ctypes.c_float(0.1), 1, ws, wsb,
+                                             None, None)
+    assert call(B=0) == 0                                   # empty batch: a no-op
+    assert call(ptrs=(None,) + (FAKE,) * 11) == 1           # a host buffer missing
+    assert call(ptrs=(FAKE,) * 6 + (None,) + (FAKE,) * 5) == 1  # a device buffer missing
+    assert call(ptrs=(MISALIGNED,) + (FAKE,) * 11) == 4
+    assert call(D=96) == 3
