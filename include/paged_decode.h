@@ -67,7 +67,10 @@ typedef enum {
 } pkd_status;
 
 /* Bits of the device error word. */
-#define PKD_DEVERR_BAD_BLOCK 1u /* a used block-table entry was outside [0, num_blocks) */
+#define PKD_DEVERR_BAD_BLOCK 1u /* a used block-table entry was outside [0, num_blocks), or a
+                                   context length ran past its block-table row (the kernels
+                                   then read only the row's blocks; that sequence's output is
+                                   undefined, and nothing outside the inputs is read) */
 #define PKD_DEVERR_TIMEOUT 2u   /* a bounded wait on a shared-memory barrier ran out */
 
 /* How K/V tiles reach the arithmetic.  All variants give the same result. */

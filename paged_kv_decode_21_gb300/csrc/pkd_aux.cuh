@@ -21,7 +21,8 @@ __global__ void __launch_bounds__(D) paged_decode_reduce_kernel(
   const int row = blockIdx.x;     // b * Hq + h
   const int b = row / num_q_heads;
   const int L = context_lens[b];
-  const int np = (L + partition_size - 1) / partition_size;
+  // partitions the first kernel wrote (none past its grid)
+  const int np = min((L + partition_size - 1) / partition_size, max_partitions);
   // min_partitions_to_merge > 0: those sequences were written by the
   // partition kernel itself; 0 merges every sequence (empty ones get zeros)
   if (min_partitions_to_merge > 0 && np <= min_partitions_to_merge) return;

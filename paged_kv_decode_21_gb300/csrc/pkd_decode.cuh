@@ -120,6 +120,20 @@ __device__ __forceinline__ void record_error(int* err, uint32_t bits) {
   if (err) atomicOr(reinterpret_cast<unsigned*>(err), bits);
 }
 
+// Sequence b's length as the decode kernels read it.  A length past the
+// block-table row (max_blocks_per_seq * BS tokens) is cut to the row and
+// reported as kErrBadBlock, so no table entry past the row is ever read.
+template <int BS>
+__device__ __forceinline__ int row_clamped_len(const DecodeParams& P, int b) {
+  const int L = P.context_lens[b];
+  const int row = P.max_blocks_per_seq * BS;
+  if (L > row) {
+    record_error(P.error_word, kErrBadBlock);
+    return row;
+  }
+  return L;
+}
+
 __device__ __forceinline__ uint4 ldg_stream(const void* p) {
   // 16-byte global load; the KV stream is read once, so do not allocate in L1
   uint4 r;
@@ -399,9 +413,11 @@ __global__ void __launch_bounds__(DecodeTraits<D, BS, G, VARIANT>::THREADS,
   const int b = bg / P.num_kv_heads;
   // the split-K merge (a programmatic dependent) may launch once every CTA has started
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int L = P.context_lens[b];
+  const int L = row_clamped_len<BS>(P, b);
   const int PS = P.partition_size;
-  const int np_b = (L + PS - 1) / PS;
+  // partitions of the sequence inside the grid (a length past max_context_len
+  // is read up to the grid's last partition)
+  const int np_b = min((L + PS - 1) / PS, np_grid);
   const bool final_out = (P.mode == 0) && np_b <= 1;
   const int h0 = g * G;
 

@@ -228,12 +228,12 @@ __global__ void __launch_bounds__(MmaTraits<D, BS, G, QC, KVB, CPS>::THREADS,
     g = bg % P.num_kv_heads;
     b = bg / P.num_kv_heads;
   }
-  const int L = P.context_lens[b];
+  const int L = row_clamped_len<BS>(P, b);
   const int QL = P.q_len;
   const int jq0 = qc * QC;               // first query token of this CTA
   const int nq = min(QC, QL - jq0);      // its query tokens (>= 1)
   const int PS = P.partition_size;
-  const int np_b = (L + PS - 1) / PS;
+  const int np_b = min((L + PS - 1) / PS, np_grid);  // partitions inside the grid
   const bool final_out = (P.mode == 0) && np_b <= 1;
   const int h0 = g * G;
   const int Hq = P.num_q_heads;

@@ -72,9 +72,9 @@ __global__ void __launch_bounds__(WsTraits<D, BS, G>::THREADS, WsTraits<D, BS, G
   const int b = bg / P.num_kv_heads;
   // the split-K merge (a programmatic dependent) may launch once every CTA has started
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int L = P.context_lens[b];
+  const int L = row_clamped_len<BS>(P, b);
   const int PS = P.partition_size;
-  const int np_b = (L + PS - 1) / PS;
+  const int np_b = min((L + PS - 1) / PS, np_grid);  // partitions inside the grid
   const bool final_out = (P.mode == 0) && np_b <= 1;
   const int h0 = g * G;
   if (L <= 0) {

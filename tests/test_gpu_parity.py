@@ -370,3 +370,21 @@ def test_longest_first_piece_order_of_a_split_grid():
     lasts = [b * NP + n[b] - 1 for b in sorted((b for b in range(len(lens)) if n[b]), key=lambda b: (-last[b], b))]
     empties = [b * NP + j for b in range(len(lens)) for j in range(n[b], NP)]
     assert got == full + lasts + empties
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("partition", [-1, 64])
+def test_length_past_the_table_row_is_reported_and_contained(variant, partition):
+    # sequence 1 claims more tokens than its block-table row holds: the kernels read only the
+    # row, report PKD_DEVERR_BAD_BLOCK, and the other sequences are unaffected
+    lens = [100, 60, 37]
+    inp = workloads.make_custom(len(lens), 8, 2, 128, 16, lens, seed=41, device="cuda", max_blocks_per_seq=7)
+    ref = oracle_out(inp)
+    bad = inp.context_lens.clone()
+    bad[1] = 10_000
+    ew = errword()
+    out = ops.paged_decode_attention_ex(inp.q, inp.k_cache, inp.v_cache, inp.block_tables, bad, inp.scale,
+                                        max_context_len=112, partition_size=partition, variant=variant,
+                                        error_word=ew)
+    assert ops.pkd_read_device_error(ew) & ops.DEVERR_BAD_BLOCK
+    assert_close(out[[0, 2]], ref[[0, 2]], "sequences with valid lengths")
