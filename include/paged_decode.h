@@ -79,9 +79,10 @@ typedef enum {
   PKD_VARIANT_NO_PREFETCH = 1, /* each warp loads its current blocks (16-byte loads) */
   PKD_VARIANT_L2_PREFETCH = 2, /* as 1, plus cp.async.bulk.prefetch.L2 of blocks ahead */
   PKD_VARIANT_TMA_STAGED = 3,  /* bulk copies into a shared-memory ring, plus L2 prefetch */
-  PKD_VARIANT_TMA_MMA = 4      /* 128-byte-swizzled tensor copies into a shared-memory ring, plus
-                                  L2 prefetch; Q.K^T and P.V on the tensor cores (mma, fp16
-                                  operands, fp32 accumulation; p rounded to fp16 for P.V) */
+  PKD_VARIANT_TMA_MMA = 4      /* 128-byte-swizzled tensor copies into a shared-memory ring (L2
+                                  prefetch beyond it with prefetch_distance >= 1); Q.K^T and P.V
+                                  on the tensor cores (mma, fp16 operands, fp32 accumulation; p
+                                  rounded to fp16 for P.V) */
 } pkd_variant;
 
 /*
@@ -187,7 +188,10 @@ pkd_status paged_decode_attention_host(const void* q, const void* k_cache, const
  *                   workspace has room for the order.
  *   variant         pkd_variant, optionally ORed with PKD_FLAG_* bits
  *   prefetch_distance  how many of a warp's iterations ahead the L2 prefetch
- *                   runs (0 = default, 1); ignored by PKD_VARIANT_NO_PREFETCH
+ *                   runs; 0 = the data path's default: 1 for the CUDA-core
+ *                   paths, none for PKD_VARIANT_TMA_MMA (its ring of tensor
+ *                   copies already runs ahead; an L2 prefetch beyond it
+ *                   measured slower); ignored by PKD_VARIANT_NO_PREFETCH
  *   workspace, workspace_bytes  device scratch of at least
  *                   paged_decode_workspace_size(...) bytes, 256-byte aligned
  *                   (may be NULL when no sequence is split; the automatic

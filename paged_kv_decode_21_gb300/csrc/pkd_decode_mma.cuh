@@ -13,10 +13,13 @@
 // tensor map views a cache as [num_blocks][num_kv_heads * block_size][D]).
 // A box is 16 rows x 64 halves (128 bytes) with the 128-byte swizzle, so the
 // 16-byte chunk j of row r lands at chunk j ^ (r % 8): the eight rows an
-// ldmatrix reads in one phase fall in eight different bank groups.  Tiles
-// beyond the ring are prefetched into L2 (cp.async.bulk.prefetch.L2), the
-// pairing of SRAM staging with L2 prefetch that the blog post "KV Cache
-// Prefetching：三层预取如何隐藏 KV 访问延迟" suggests (section 2.3).
+// ldmatrix reads in one phase fall in eight different bank groups.  The ring
+// is itself an asynchronous prefetch of the warp's next sub-tiles into SRAM;
+// with prefetch_distance >= 1, whole tiles beyond it are also prefetched into
+// L2 (cp.async.bulk.prefetch.L2), the pairing of SRAM staging with L2
+// prefetch that the blog post "KV Cache Prefetching：三层预取如何隐藏 KV 访问延迟"
+// suggests (section 2.3).  That extra prefetch measured slower on GB300, so
+// it is off by default.
 //
 // Arithmetic per 16-token sub-tile, with mma.m16n8k16 (fp16 operands, fp32
 // accumulators), c = lane % 4 and r = lane / 4:
