@@ -79,10 +79,16 @@ typedef enum {
   PKD_VARIANT_NO_PREFETCH = 1, /* each warp loads its current blocks (16-byte loads) */
   PKD_VARIANT_L2_PREFETCH = 2, /* as 1, plus cp.async.bulk.prefetch.L2 of blocks ahead */
   PKD_VARIANT_TMA_STAGED = 3,  /* bulk copies into a shared-memory ring, plus L2 prefetch */
-  PKD_VARIANT_TMA_MMA = 4      /* 128-byte-swizzled tensor copies into a shared-memory ring (L2
+  PKD_VARIANT_TMA_MMA = 4,     /* 128-byte-swizzled tensor copies into a shared-memory ring (L2
                                   prefetch beyond it with prefetch_distance >= 1); Q.K^T and P.V
                                   on the tensor cores (mma, fp16 operands, fp32 accumulation; p
                                   rounded to fp16 for P.V) */
+  PKD_VARIANT_TCGEN05 = 5      /* the same copies into a two-stage ring of 64-token tiles; Q.K^T
+                                  and P.V as tcgen05 MMAs with S and O in tensor memory, one
+                                  softmax thread per query row; up to 64 query rows (query
+                                  tokens x group heads) share one read of the K/V tiles (fp16
+                                  caches, head_dim 128 only: PKD_ERR_UNSUPPORTED otherwise; no
+                                  L2 prefetch) */
 } pkd_variant;
 
 /*
@@ -305,9 +311,12 @@ pkd_status paged_decode_validate_tables(const int32_t* block_tables, const int32
  *   q, out         device fp16 [num_seqs][q_len][num_q_heads][head_dim]
  *   q_len          >= 1 (1 gives single-query decode)
  *   other arguments as for paged_decode_attention_ex; context_lens[b] counts
- *   the new tokens.  Runs the tensor-core path (PKD_VARIANT_TMA_MMA): each
- *   CTA serves 16 / G query tokens of one (sequence, kv head, partition), so
- *   every K/V tile is read once per group of 16 / G query tokens.
+ *   the new tokens.  Runs a tensor-core path (PKD_VARIANT_AUTO of
+ *   paged_decode_attention_multi_ex): where the rows of a (sequence, kv
+ *   head), q_len x G, fit one 16-row tile or the caches are not fp16 with
+ *   head_dim 128, PKD_VARIANT_TMA_MMA, whose CTAs serve 16 / G query tokens
+ *   each; otherwise PKD_VARIANT_TCGEN05, whose CTAs serve 64 / G, so every
+ *   K/V tile is read once per group of 64 / G query tokens.
  *   workspace      required when the context is split
  *                  (paged_decode_multi_workspace_size bytes, 256-byte aligned);
  *                  with partition_size 0 it also keeps the longest-first
@@ -320,6 +329,38 @@ pkd_status paged_decode_attention_multi(const void* q, const void* k_cache, cons
                                         int max_blocks_per_seq, int max_context_len, float scale,
                                         int partition_size, void* workspace, size_t workspace_bytes,
                                         int* error_word, cudaStream_t stream);
+
+/*
+ * paged_decode_attention_multi_ex -- paged_decode_attention_multi with the
+ * data path chosen by the caller: variant PKD_VARIANT_AUTO (the choice
+ * paged_decode_attention_multi makes), PKD_VARIANT_TMA_MMA or
+ * PKD_VARIANT_TCGEN05, optionally ORed with PKD_FLAG_* bits
+ * (PKD_ERR_UNSUPPORTED for the CUDA-core paths when q_len > 1).  Both
+ * tensor-core paths give the same result up to fp32 rounding order.
+ */
+pkd_status paged_decode_attention_multi_ex(const void* q, const void* k_cache, const void* v_cache,
+                                           const int32_t* block_tables, const int32_t* context_lens,
+                                           void* out, int num_seqs, int q_len, int num_q_heads,
+                                           int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                           int max_blocks_per_seq, int max_context_len, float scale,
+                                           int partition_size, int variant, void* workspace,
+                                           size_t workspace_bytes, int* error_word, cudaStream_t stream);
+
+/*
+ * paged_decode_call_plan -- the launch plan of a decode call on the current
+ * device: q_len query tokens per sequence, kv_fp8 1 for E4M3 caches, and the
+ * partition_size and variant the call is given.  Writes *partition_out (the
+ * partition, or -1 when unsplit), *longest_first (1 when the batch is walked
+ * longest first, given a workspace of the size the *_workspace_size
+ * functions return), *variant_out (the data path with the PKD_FLAG_* bits
+ * that apply) and *grid_out (decode CTAs); any pointer may be NULL.
+ * Returns the kernel launches (decode grid, split-K merge, order kernel; 0
+ * for an empty batch), or -2 for a shape, partition or variant the call
+ * would refuse.
+ */
+int paged_decode_call_plan(int num_seqs, int q_len, int num_q_heads, int num_kv_heads, int head_dim,
+                           int block_size, int max_context_len, int kv_fp8, int partition_size, int variant,
+                           int* partition_out, int* longest_first, int* variant_out, long long* grid_out);
 
 /*
  * paged_decode_auto_plan -- what a call with partition_size 0 runs on the
@@ -336,7 +377,8 @@ int paged_decode_auto_plan(int num_seqs, int q_len, int num_q_heads, int num_kv_
                            int block_size, int max_context_len, int kv_fp8, int* partition_size,
                            int* longest_first);
 
-/* Workspace bytes paged_decode_attention_multi needs (0 = none). */
+/* Workspace bytes paged_decode_attention_multi, paged_decode_attention_multi_ex
+   (every variant) and paged_decode_attention_fp8 need (0 = none). */
 size_t paged_decode_multi_workspace_size(int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
                                          int head_dim, int block_size, int max_context_len,
                                          int partition_size);

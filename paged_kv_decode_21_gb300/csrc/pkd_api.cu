@@ -9,6 +9,7 @@
 #include "../../include/paged_decode.h"
 #include "pkd_aux.cuh"
 #include "pkd_launch.cuh"
+#include "pkd_tc_launch.h"
 
 namespace {
 
@@ -20,7 +21,8 @@ constexpr unsigned long long kWaitBudgetNs = 100ull * 1000ull * 1000ull;  // 100
 // sub-tiles ahead into shared memory, and a prefetch beyond the ring measured
 // 0-1.4% slower with fp16 caches (distance 1; 2-4 lose 1-18% more) and 3-4%
 // slower with E4M3.
-int default_prefetch_distance(int path) { return path == PKD_VARIANT_TMA_MMA ? 0 : 1; }
+// The tcgen05 path has no L2 prefetch (its ring runs ahead the same way).
+int default_prefetch_distance(int path) { return path == PKD_VARIANT_TMA_MMA || path == PKD_VARIANT_TCGEN05 ? 0 : 1; }
 constexpr int kMinAutoPartition = 512;
 constexpr int kMaxAutoPartition = 2048;
 constexpr int kSplitWaves = 2;       // split when the (sequence, kv head) units cover fewer waves than this,
@@ -67,7 +69,7 @@ int sm_count() {
 int variant_path(int variant) { return variant & 0xff; }
 bool variant_ok(int variant) {
   const int path = variant_path(variant);
-  return variant >= 0 && path <= PKD_VARIANT_TMA_MMA &&
+  return variant >= 0 && path <= PKD_VARIANT_TCGEN05 &&
          (variant & ~0xff & ~PKD_FLAG_L2_EVICT_HINTS & ~PKD_FLAG_LONGEST_FIRST) == 0;
 }
 
@@ -171,7 +173,8 @@ bool auto_order(const Shape& s, int variant, int q_chunks, int partition) {
 // Whether a launch walks the sequences longest first: asked for by flag, on
 // the tensor-core path, for batches whose lengths fit the order kernel.
 bool want_order(int variant, int resolved_path, int num_seqs) {
-  return (variant & PKD_FLAG_LONGEST_FIRST) && resolved_path == PKD_VARIANT_TMA_MMA && num_seqs > 1 &&
+  return (variant & PKD_FLAG_LONGEST_FIRST) &&
+         (resolved_path == PKD_VARIANT_TMA_MMA || resolved_path == PKD_VARIANT_TCGEN05) && num_seqs > 1 &&
          num_seqs <= pkd::kOrderMaxSeqs;
 }
 
@@ -189,16 +192,30 @@ Workspace layout(void* base, int num_seqs, int num_q_heads, int head_dim, int np
 }
 
 // Query chunks per (sequence, kv head) of q_len query tokens: the
-// multi-token kernel serves 16 / G query tokens per CTA.
-int query_chunks(int q_len, int G) {
+// mma.sync kernel serves 16 / G query tokens per CTA (one 16-row tile), the
+// tcgen05 kernel kTcRowsPerCta / G.
+int query_chunks(int q_len, int G, int path = PKD_VARIANT_TMA_MMA) {
   if (q_len <= 1) return 1;
-  const int qc = 16 / G;
+  const int qc = (path == PKD_VARIANT_TCGEN05 ? pkd::kTcRowsPerCta : 16) / G;
   return (q_len + qc - 1) / qc;
+}
+
+// The tensor-core path the automatic variant runs for several query tokens
+// per sequence or E4M3 caches.  Where the rows of a (sequence, kv head) --
+// q_len x G -- need more than one 16-row mma.sync tile, that path reads the
+// partition's K and V once per tile and runs out of issue slots; the tcgen05
+// kernel serves up to 64 rows per CTA from one read, with S and O in tensor
+// memory (fp16 caches, head_dim 128).
+int auto_multi_path(const Shape& s, int q_len, int kv_fp8) {
+  const int G = s.num_q_heads / s.num_kv_heads;
+  if (!kv_fp8 && s.head_dim == 128 && (long long)q_len * G > 16) return PKD_VARIANT_TCGEN05;
+  return PKD_VARIANT_TMA_MMA;
 }
 
 // The launch plan of one decode call.
 struct CallPlan {
   int P;           // tokens per partition (the whole context, rounded up to 32, when unsplit)
+  int q_chunks;    // query chunks per (sequence, kv head)
   int np;          // partitions in the grid (1 when unsplit)
   bool split;      // the split-K merge runs
   long long grid;  // decode CTAs
@@ -210,14 +227,17 @@ struct CallPlan {
 // (the shape already checked).
 pkd_status plan_call(const Shape& s, int q_len, int variant, int partition_size, int kv_fp8, CallPlan* out) {
   const int G = s.num_q_heads / s.num_kv_heads;
-  const int q_chunks = query_chunks(q_len, G);
   const int flags = variant & ~0xff;
-  if (q_len > 1 || kv_fp8) {
-    // several query tokens per sequence, or E4M3 caches: the tensor-core path only
-    const int path = variant_path(variant);
+  const int path = variant_path(variant);
+  if (path == PKD_VARIANT_TCGEN05) {
+    if (kv_fp8 || s.head_dim != 128) return PKD_ERR_UNSUPPORTED;
+  } else if (q_len > 1 || kv_fp8) {
+    // several query tokens per sequence, or E4M3 caches: the tensor-core paths only
     if (path != PKD_VARIANT_AUTO && path != PKD_VARIANT_TMA_MMA) return PKD_ERR_UNSUPPORTED;
-    variant = PKD_VARIANT_TMA_MMA | flags;
+    variant = (path == PKD_VARIANT_AUTO ? auto_multi_path(s, q_len, kv_fp8) : PKD_VARIANT_TMA_MMA) | flags;
   }
+  const int q_chunks = query_chunks(q_len, G, variant_path(variant));
+  out->q_chunks = q_chunks;
   int P;
   int flags_eff = flags;
   if (partition_size == 0) {
@@ -251,6 +271,7 @@ pkd_status launch_decode(int variant, int D, int BS, int G, const pkd::DecodePar
     case PKD_VARIANT_L2_PREFETCH: e = pkd::launch_decode_l2_prefetch(D, BS, G, p, grid, stream); break;
     case PKD_VARIANT_TMA_STAGED: e = pkd::launch_decode_tma_staged(D, BS, G, p, grid, stream); break;
     case PKD_VARIANT_TMA_MMA: e = pkd::launch_decode_tma_mma(D, BS, G, p, grid, stream); break;
+    case PKD_VARIANT_TCGEN05: e = pkd::launch_decode_tcgen05(D, BS, p, grid, stream); break;
     default: return PKD_ERR_SHAPE;
   }
   return e == cudaSuccess ? PKD_OK : PKD_ERR_LAUNCH;
@@ -384,7 +405,6 @@ pkd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
   if (!variant_ok(variant)) return PKD_ERR_SHAPE;
   if (prefetch_distance < 0) return PKD_ERR_SHAPE;
   const int G = num_q_heads / num_kv_heads;
-  const int q_chunks = query_chunks(q_len, G);
   CallPlan plan;
   st = plan_call(s, q_len, variant, partition_size, kv_fp8, &plan);
   if (st != PKD_OK) return st;
@@ -410,7 +430,7 @@ pkd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
   p.max_partitions = np;
   p.mode = 0;
   p.q_len = q_len;
-  p.q_chunks = q_chunks;
+  p.q_chunks = plan.q_chunks;
   // E4M3 caches: K = code * k_scale enters the scores, V = code * v_scale the output
   p.scale_log2 = scale * (kv_fp8 ? k_scale : 1.f) * 1.4426950408889634f;
   p.v_scale = kv_fp8 ? v_scale : 1.f;
@@ -485,8 +505,20 @@ pkd_status paged_decode_attention_multi(const void* q, const void* k_cache, cons
                                         int* error_word, cudaStream_t stream) {
   return decode_impl(q, k_cache, v_cache, block_tables, context_lens, out, num_seqs, q_len, num_q_heads,
                      num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, max_context_len,
-                     scale, partition_size, PKD_VARIANT_TMA_MMA, 0, workspace, workspace_bytes,
+                     scale, partition_size, PKD_VARIANT_AUTO, 0, workspace, workspace_bytes,
                      error_word, stream);
+}
+
+pkd_status paged_decode_attention_multi_ex(const void* q, const void* k_cache, const void* v_cache,
+                                           const int32_t* block_tables, const int32_t* context_lens,
+                                           void* out, int num_seqs, int q_len, int num_q_heads,
+                                           int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                           int max_blocks_per_seq, int max_context_len, float scale,
+                                           int partition_size, int variant, void* workspace,
+                                           size_t workspace_bytes, int* error_word, cudaStream_t stream) {
+  return decode_impl(q, k_cache, v_cache, block_tables, context_lens, out, num_seqs, q_len, num_q_heads,
+                     num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, max_context_len,
+                     scale, partition_size, variant, 0, workspace, workspace_bytes, error_word, stream);
 }
 
 pkd_status paged_decode_attention_fp8(const void* q, const void* k_cache, const void* v_cache,
@@ -502,17 +534,27 @@ pkd_status paged_decode_attention_fp8(const void* q, const void* k_cache, const 
                      stream, 1, k_scale, v_scale);
 }
 
+int paged_decode_call_plan(int num_seqs, int q_len, int num_q_heads, int num_kv_heads, int head_dim,
+                           int block_size, int max_context_len, int kv_fp8, int partition_size, int variant,
+                           int* partition_out, int* longest_first, int* variant_out, long long* grid_out) {
+  Shape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, 1, 1 << 30, max_context_len};
+  if (check_shape(s) != PKD_OK || q_len < 1 || !variant_ok(variant)) return -2;
+  CallPlan plan;
+  if (plan_call(s, q_len, variant, partition_size, kv_fp8, &plan) != PKD_OK) return -2;
+  if (partition_out) *partition_out = plan.split ? plan.P : -1;
+  if (longest_first) *longest_first = plan.order ? 1 : 0;
+  if (variant_out) *variant_out = plan.variant;
+  if (grid_out) *grid_out = num_seqs == 0 ? 0 : plan.grid;
+  if (num_seqs == 0 || plan.grid == 0) return 0;
+  return 1 + (plan.split ? 1 : 0) + (plan.order ? 1 : 0);
+}
+
 int paged_decode_auto_plan(int num_seqs, int q_len, int num_q_heads, int num_kv_heads, int head_dim,
                            int block_size, int max_context_len, int kv_fp8, int* partition_size,
                            int* longest_first) {
-  Shape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, 1, 1 << 30, max_context_len};
-  if (check_shape(s) != PKD_OK || q_len < 1) return -2;
-  CallPlan plan;
-  if (plan_call(s, q_len, PKD_VARIANT_AUTO, 0, kv_fp8, &plan) != PKD_OK) return -2;
-  if (partition_size) *partition_size = plan.split ? plan.P : -1;
-  if (longest_first) *longest_first = plan.order ? 1 : 0;
-  if (num_seqs == 0 || plan.grid == 0) return 0;
-  return 1 + (plan.split ? 1 : 0) + (plan.order ? 1 : 0);
+  return paged_decode_call_plan(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size,
+                                max_context_len, kv_fp8, 0, PKD_VARIANT_AUTO, partition_size, longest_first,
+                                nullptr, nullptr);
 }
 
 size_t paged_decode_multi_workspace_size(int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
@@ -520,14 +562,21 @@ size_t paged_decode_multi_workspace_size(int num_seqs, int q_len, int num_q_head
                                          int partition_size) {
   Shape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, 1, 1 << 30, max_context_len};
   if (check_shape(s) != PKD_OK || q_len < 1) return 0;
-  const int qch = query_chunks(q_len, num_q_heads / num_kv_heads);
-  int P = partition_size == 0 ? auto_partition(s, PKD_VARIANT_TMA_MMA, qch) : partition_size;
-  size_t bytes = 0;
-  if (P > 0 && max_context_len > P)
-    bytes = layout(nullptr, num_seqs * q_len, num_q_heads, head_dim, (max_context_len + P - 1) / P).bytes;
-  if (partition_size == 0)  // the automatic split may order the batch
-    bytes += order_bytes(num_seqs, grid_partitions(max_context_len, P));
-  return bytes;
+  // with partition_size 0 the split depends on the path's query chunks: cover
+  // both tensor-core paths
+  size_t most = 0;
+  for (const int path : {PKD_VARIANT_TMA_MMA, PKD_VARIANT_TCGEN05}) {
+    if (path == PKD_VARIANT_TCGEN05 && head_dim != 128) continue;
+    const int qch = query_chunks(q_len, num_q_heads / num_kv_heads, path);
+    const int P = partition_size == 0 ? auto_partition(s, path, qch) : partition_size;
+    size_t bytes = 0;
+    if (P > 0 && max_context_len > P)
+      bytes = layout(nullptr, num_seqs * q_len, num_q_heads, head_dim, (max_context_len + P - 1) / P).bytes;
+    if (partition_size == 0)  // the automatic split may order the batch
+      bytes += order_bytes(num_seqs, grid_partitions(max_context_len, P));
+    most = std::max(most, bytes);
+  }
+  return most;
 }
 
 pkd_status paged_decode_attention_host(const void* q, const void* k_cache, const void* v_cache,
@@ -622,6 +671,7 @@ pkd_status paged_decode_partitions(const void* q, const void* k_cache, const voi
   if (!std::isfinite(scale)) return PKD_ERR_SHAPE;
   if (!variant_ok(variant) || prefetch_distance < 0)
     return PKD_ERR_SHAPE;
+  if (variant_path(variant) == PKD_VARIANT_TCGEN05 && head_dim != 128) return PKD_ERR_UNSUPPORTED;
   if (partition_size <= 0 || partition_size % 32 != 0 || partition_size % block_size != 0)
     return PKD_ERR_SHAPE;
   const int need = (max_context_len + partition_size - 1) / partition_size;

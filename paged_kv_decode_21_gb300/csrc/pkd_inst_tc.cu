@@ -1,0 +1,47 @@
+// Instantiations and launch of the tcgen05 decode kernel (pkd_decode_tc.cuh):
+// fp16 caches, head_dim 128, block sizes 16 and 32.
+#include "pkd_decode_tc.cuh"
+#include "pkd_mma_launch.cuh"
+#include "pkd_tc_launch.h"
+
+namespace pkd {
+static_assert(kTcRows == kTcRowsPerCta, "rows per CTA of the kernel and of its host entry");
+
+namespace {
+
+template <int BS>
+cudaError_t launch_tc_bs(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeParams& p, long long grid,
+                         cudaStream_t stream) {
+  using T = TcTraits<BS>;
+  auto* fn = paged_decode_tc_kernel<BS>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(T::THREADS);
+  cfg.dynamicSmemBytes = T::SMEM_BYTES;
+  cfg.stream = stream;
+  if (p.piece_order) {
+    // a programmatic dependent of the order kernel (griddepcontrol.wait in the kernel)
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  e = cudaLaunchKernelEx(&cfg, fn, mk, mv, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode_tcgen05(int D, int BS, const DecodeParams& p, long long grid, cudaStream_t stream) {
+  if (D != 128 || (BS != 16 && BS != 32)) return cudaErrorInvalidValue;
+  CUtensorMap mk, mv;
+  cudaError_t e = mma_host::make_maps(p, D, BS, 2, &mk, &mv);
+  if (e != cudaSuccess) return e;
+  return BS == 16 ? launch_tc_bs<16>(mk, mv, p, grid, stream) : launch_tc_bs<32>(mk, mv, p, grid, stream);
+}
+
+}  // namespace pkd

@@ -1,0 +1,113 @@
+// pkd_tc.cuh -- inline-PTX primitives of the fifth-generation tensor cores
+// (tcgen05) for sm_103a: tensor-memory allocation, the asynchronous MMA with
+// its completion on an mbarrier, tensor-memory loads and stores, and the
+// shared-memory and instruction descriptors the MMA reads its operands with.
+//
+// Operand layouts used here are the 128-byte-swizzled ones that a tiled
+// tensor copy with CU_TENSOR_MAP_SWIZZLE_128B writes: rows of 128 bytes, the
+// 16-byte chunk c of row r stored at chunk c ^ (r % 8), groups of 8 rows
+// 1024 bytes apart, every group 1024-byte aligned.
+//  * K-major (the contraction index runs along the 128-byte row): one MMA
+//    with K = 16 fp16 reads 32 bytes of each row; the next K step starts 32
+//    bytes further on (the swizzle is applied to the final address).
+//  * MN-major (the M or N index runs along the row, K down the rows): 64
+//    elements of M or N per 128-byte row, K steps of 16 rows = 2048 bytes;
+//    the next 64 elements of M or N sit `lbo` bytes further on.
+#pragma once
+#include <cstdint>
+#include "pkd_ptx.cuh"
+
+namespace pkd {
+
+// ---------------------------------------------------------------- tensor memory
+// Allocate `ncols` columns (a power of two, 32..512) of tensor memory for the
+// CTA; the address is written to shared memory at `dst`.  Whole warp.
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
+               "r"(ncols)
+               : "memory");
+}
+// Give up the right to allocate again, so other CTAs on the SM need not wait
+// for this one.  Whole warp.
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+// Free an allocation.  Whole warp (the allocating one).
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Order tcgen05 operations before / after a thread synchronisation (a
+// barrier or an mbarrier arrive / wait).
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// ---------------------------------------------------------------- MMA
+// D (tensor memory) = A * B (+ D when `accumulate`), fp16 inputs from shared
+// memory through descriptors, fp32 accumulation.  One thread issues it.
+__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive once on `bar` when every tcgen05 MMA this thread issued before has
+// completed.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// Shared-memory matrix descriptor: start address, leading- and stride-
+// dimension byte offsets (16-byte units, 14 bits each), the descriptor
+// version of this architecture (bit 46), base offset 0 (1024-byte aligned
+// swizzle groups) and the 128-byte swizzle (layout type 2 in bits 61-63).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo & 0x3FFFFu) >> 4) << 16) |
+         ((uint64_t)((sbo & 0x3FFFFu) >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor of a kind::f16 MMA: fp32 D (bits 4-5 = 1), fp16 A
+// and B (bits 7-9, 10-12 = 0), A K-major (bit 15 = 0), B K- or MN-major
+// (bit 16), N / 8 in bits 17-22, M / 16 in bits 24-28.
+constexpr uint32_t tc_idesc_f16(int M, int N, bool b_mn_major) {
+  return (1u << 4) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// ---------------------------------------------------------------- tensor memory <-> registers
+// Thread t of the warp reads 32 consecutive 32-bit columns of tensor-memory
+// lane (lane field of taddr) + t.  A warp reaches the 32 lanes of its
+// sub-partition (warp id % 4) only.  Whole warp; complete with tmem_ld_wait.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7]),
+        "=f"(v[8]), "=f"(v[9]), "=f"(v[10]), "=f"(v[11]), "=f"(v[12]), "=f"(v[13]), "=f"(v[14]), "=f"(v[15]),
+        "=f"(v[16]), "=f"(v[17]), "=f"(v[18]), "=f"(v[19]), "=f"(v[20]), "=f"(v[21]), "=f"(v[22]),
+        "=f"(v[23]), "=f"(v[24]), "=f"(v[25]), "=f"(v[26]), "=f"(v[27]), "=f"(v[28]), "=f"(v[29]),
+        "=f"(v[30]), "=f"(v[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// The store counterpart of tmem_ld32; complete with tmem_st_wait.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]), "f"(v[8]),
+      "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15]), "f"(v[16]),
+      "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]), "f"(v[24]),
+      "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+}  // namespace pkd

@@ -1,0 +1,16 @@
+// pkd_tc_launch.h -- host entry of the tcgen05 decode kernel (pkd_inst_tc.cu).
+#pragma once
+#include <cuda_runtime.h>
+#include "pkd_decode.cuh"
+
+namespace pkd {
+
+// Query rows (query tokens x group heads) one CTA of the tcgen05 kernel serves.
+constexpr int kTcRowsPerCta = 64;
+
+// Launch `grid` CTAs of the tcgen05 kernel; p.q_chunks must be
+// ceil(q_len / (kTcRowsPerCta / G)).  fp16 caches with head_dim 128 and block
+// size 16 or 32 only (cudaErrorInvalidValue otherwise).
+cudaError_t launch_decode_tcgen05(int D, int BS, const DecodeParams& p, long long grid, cudaStream_t stream);
+
+}  // namespace pkd

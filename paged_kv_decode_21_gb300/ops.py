@@ -21,7 +21,7 @@ PKD_OK = 0
 STATUS_NAMES = {0: "PKD_OK", 1: "PKD_ERR_NULL", 2: "PKD_ERR_SHAPE", 3: "PKD_ERR_UNSUPPORTED",
                 4: "PKD_ERR_ALIGN", 5: "PKD_ERR_WORKSPACE", 6: "PKD_ERR_LAUNCH",
                 7: "PKD_ERR_DEVICE", 8: "PKD_ERR_CUDA"}
-VARIANTS = {"auto": 0, "no_prefetch": 1, "l2_prefetch": 2, "tma_staged": 3, "tma_mma": 4}
+VARIANTS = {"auto": 0, "no_prefetch": 1, "l2_prefetch": 2, "tma_staged": 3, "tma_mma": 4, "tcgen05": 5}
 DEVERR_BAD_BLOCK = 1
 DEVERR_TIMEOUT = 2
 
@@ -68,6 +68,12 @@ def lib():
         L.paged_decode_attention_multi.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, I, P, S,
                                                    P, P]
         L.paged_decode_attention_multi.restype = I
+        L.paged_decode_attention_multi_ex.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, I, I, P, S,
+                                                      P, P]
+        L.paged_decode_attention_multi_ex.restype = I
+        L.paged_decode_call_plan.argtypes = [I] * 10 + [ctypes.POINTER(ctypes.c_int)] * 3 + [
+            ctypes.POINTER(ctypes.c_longlong)]
+        L.paged_decode_call_plan.restype = I
         L.paged_decode_attention_host.argtypes = [P] * 12 + [I] * 8 + [F, I, P, S, P, P]
         L.paged_decode_attention_host.restype = I
         L.paged_decode_auto_plan.argtypes = [I, I, I, I, I, I, I, I, ctypes.POINTER(ctypes.c_int),
@@ -214,6 +220,19 @@ def paged_decode_auto_plan(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim,
     return n, part.value, bool(order.value)
 
 
+def paged_decode_call_plan(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len,
+                           kv_fp8=False, partition_size=0, variant="auto"):
+    """The launch plan of a call: (launches, partition or -1, longest_first,
+    variant name it runs, decode CTAs)."""
+    part, order, var, grid = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0), ctypes.c_longlong(0)
+    n = lib().paged_decode_call_plan(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size,
+                                     max_context_len, int(bool(kv_fp8)), int(partition_size), _variant(variant),
+                                     ctypes.byref(part), ctypes.byref(order), ctypes.byref(var), ctypes.byref(grid))
+    if n < 0:
+        raise PagedDecodeError(2, "paged_decode_call_plan")
+    return n, part.value, bool(order.value), variant_name(var.value), grid.value
+
+
 def variant_name(v: int) -> str:
     """Name of a variant value, e.g. 'tma_staged+l2_hints'."""
     names = {n: k for k, n in VARIANTS.items()}
@@ -326,8 +345,9 @@ def paged_decode_multi_workspace_size(num_seqs, q_len, num_q_heads, num_kv_heads
 
 def paged_decode_attention_multi(q, k_cache, v_cache, block_tables, context_lens, scale, out=None,
                                  max_context_len=None, partition_size=0, workspace=None,
-                                 error_word=None, stream=None) -> torch.Tensor:
-    """q_len new tokens per sequence, q [B][q_len][Hq][D]; causal among them."""
+                                 error_word=None, stream=None, variant="auto") -> torch.Tensor:
+    """q_len new tokens per sequence, q [B][q_len][Hq][D]; causal among them.
+    variant: "auto", "tma_mma" or "tcgen05" (paged_decode_attention_multi_ex)."""
     _want(q, "q", torch.float16, 4)
     B, QL, Hq, D = q.shape
     _, _, Hkv, _, BS, NB, MB = _shape(q.view(B, QL * Hq, D), k_cache, v_cache, block_tables, context_lens)
@@ -339,11 +359,11 @@ def paged_decode_attention_multi(q, k_cache, v_cache, block_tables, context_lens
     if workspace is None:
         workspace = alloc_workspace(need, q.device)
     wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = lib().paged_decode_attention_multi(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
-                                            _ptr(context_lens), _ptr(out), B, QL, Hq, Hkv, D, BS, NB, MB,
-                                            maxlen, float(scale), int(partition_size), _ptr(workspace), wsb,
-                                            _ptr(error_word), _stream(stream))
-    _check(st, "paged_decode_attention_multi")
+    st = lib().paged_decode_attention_multi_ex(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                               _ptr(context_lens), _ptr(out), B, QL, Hq, Hkv, D, BS, NB, MB,
+                                               maxlen, float(scale), int(partition_size), _variant(variant),
+                                               _ptr(workspace), wsb, _ptr(error_word), _stream(stream))
+    _check(st, "paged_decode_attention_multi_ex")
     return out
 
 

@@ -80,7 +80,9 @@ def test_variant_flags(L):
     assert L.paged_decode_workspace_size(2, 8, 2, 128, 16, 100, 32, 0x200 | 4) == base + 256
     assert L.paged_decode_workspace_size(300, 8, 2, 128, 16, 100, -1, 0x200 | 4) == 1280
     assert call_ex(L, var=4, D=96) == 3                # the tensor-core path is a known variant
-    assert call_ex(L, var=5) == 2                      # past the last variant
+    assert call_ex(L, var=5, D=64) == 3                # tcgen05 path: head_dim 128 only
+    assert call_ex(L, var=0x200 | 5, D=96) == 3        # ... and a known variant with flags
+    assert call_ex(L, var=6) == 2                      # past the last variant
     assert L.paged_decode_workspace_size(2, 8, 2, 128, 16, 100, 32, 0x100 | 2) > 0
 
 
@@ -254,3 +256,52 @@ def test_host_entry_argument_checks(L):
     assert call(ptrs=(FAKE,) * 6 + (None,) + (FAKE,) * 5) == 1  # a device buffer missing
     assert call(ptrs=(MISALIGNED,) + (FAKE,) * 11) == 4
     assert call(D=96) == 3
+
+
+def test_call_plan_picks_the_tensor_core_path(L):
+    from paged_kv_decode_21_gb300 import ops
+    # q_len x G > 16 rows with fp16 caches and head_dim 128: the tcgen05 path
+    assert ops.paged_decode_call_plan(4, 8, 28, 4, 128, 16, 1000)[3] == "tcgen05"
+    assert ops.paged_decode_call_plan(4, 5, 32, 8, 128, 16, 1000)[3] == "tcgen05"
+    # one 16-row tile, head_dim 64, E4M3 caches or a single query: the mma.sync path
+    assert ops.paged_decode_call_plan(4, 2, 28, 4, 128, 16, 1000)[3] == "tma_mma"
+    assert ops.paged_decode_call_plan(4, 4, 32, 8, 128, 16, 1000)[3] == "tma_mma"
+    assert ops.paged_decode_call_plan(4, 8, 28, 4, 64, 16, 1000)[3] == "tma_mma"
+    assert ops.paged_decode_call_plan(4, 8, 28, 4, 128, 16, 1000, kv_fp8=True)[3] == "tma_mma"
+    assert ops.paged_decode_call_plan(4, 1, 28, 4, 128, 16, 1000)[3] == "tma_mma"
+    # grid: (sequence, kv head, chunk of 64 / G query tokens, partition)
+    n, part, ordered, var, grid = ops.paged_decode_call_plan(4, 10, 28, 4, 128, 16, 1000, partition_size=256,
+                                                             variant="tcgen05")
+    assert (n, part, var, grid) == (2, 256, "tcgen05", 4 * 4 * 2 * 4)
+    n, part, ordered, var, grid = ops.paged_decode_call_plan(4, 10, 28, 4, 128, 16, 1000, partition_size=-1,
+                                                             variant="tma_mma")
+    assert (n, part, grid) == (1, -1, 4 * 4 * 5)
+    # refused: tcgen05 with head_dim 64 or E4M3 caches, CUDA-core paths for several queries
+    for kw in ({"variant": "tcgen05", "kv_fp8": True}, {"variant": "tma_staged"}):
+        with pytest.raises(ops.PagedDecodeError):
+            ops.paged_decode_call_plan(4, 8, 28, 4, 128, 16, 1000, **kw)
+    with pytest.raises(ops.PagedDecodeError):
+        ops.paged_decode_call_plan(4, 1, 28, 4, 64, 16, 1000, variant="tcgen05")
+
+
+def test_multi_workspace_covers_both_tensor_core_paths(L):
+    from paged_kv_decode_21_gb300 import ops
+    # with partition 0 the split depends on the path; the size covers either
+    import random
+    rng = random.Random(5)
+    for _ in range(200):
+        G = rng.choice([1, 2, 4, 5, 7, 8])
+        Hkv = rng.choice([1, 2, 4, 8])
+        B = rng.choice([1, 2, 7, 32, 100, 300])
+        q_len = rng.choice([2, 3, 5, 8, 9, 17, 33])
+        maxlen = rng.choice([16, 100, 1000, 5000, 20000])
+        ws = L_size = ops.paged_decode_multi_workspace_size(B, q_len, G * Hkv, Hkv, 128, 16, maxlen, 0)
+        for variant in ("auto", "tma_mma", "tcgen05"):
+            n, part, ordered, var, grid = ops.paged_decode_call_plan(B, q_len, G * Hkv, Hkv, 128, 16, maxlen,
+                                                                     partition_size=0, variant=variant)
+            need = 0
+            if part > 0:
+                rows = B * q_len * G * Hkv * (-(-maxlen // part))
+                need = -(-rows * 128 * 4 // 256) * 256 + 2 * (-(-rows * 4 // 256) * 256)
+            assert ws >= need, (B, q_len, G, Hkv, maxlen, variant)
+        assert L_size == ws
