@@ -77,15 +77,19 @@ def kernel_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def kernel_name(cfg: workloads.DecodeConfig, variant: str, kv_fp8: bool = False, wide: bool = False) -> str:
+def kernel_name(cfg: workloads.DecodeConfig, variant: str, kv_fp8: bool = False, wide: bool = False,
+                q_len: int = 1) -> str:
     """The decode kernel a resolved variant launches for a shape (template arguments: head
     dim, block size, group, query tokens per CTA, bytes per K/V element, CTAs per SM with 0
-    for the default three)."""
+    for the default three; the tcgen05 kernel takes the block size only)."""
     path = variant.split("+")[0]
     shape = f"{cfg.head_dim},{cfg.block_size},{cfg.group}"
+    if path == "tcgen05":
+        return f"paged_decode_tc_kernel<{cfg.block_size}>"
     if path == "tma_mma":
         # single-query E4M3 grids of 3+ waves of four CTAs per SM run the four-per-SM build
-        return f"paged_decode_mma_kernel<{shape},1,{1 if kv_fp8 else 2},{4 if (kv_fp8 and wide) else 0}>"
+        qc = 1 if q_len <= 1 else 16 // cfg.group
+        return f"paged_decode_mma_kernel<{shape},{qc},{1 if kv_fp8 else 2},{4 if (kv_fp8 and wide) else 0}>"
     if path == "tma_staged" and cfg.group >= 6:
         return f"paged_decode_ws_kernel<{shape}>"
     return f"paged_decode_kernel<{shape},{variant}>"
@@ -207,22 +211,12 @@ def time_gpu(args, cfg, variant, dev, inp, steps, warmup, with_e2e=True, with_cl
     ws = ops.alloc_workspace(need, dev)
     q_len = getattr(args, "q_len", 1)
     kv_fp8 = getattr(args, "kv_fp8", False)
-    if P == 0 and (variant == "auto" or q_len > 1 or kv_fp8):
-        # the library's own plan for the automatic split: partition, order, launches
-        launches, eff_P, ordered = ops.paged_decode_auto_plan(
-            inp.num_seqs, q_len, inp.num_q_heads, inp.num_kv_heads, inp.head_dim, inp.block_size,
-            inp.max_context_len, kv_fp8)
-        split = eff_P > 0
-    else:
-        eff_P = P if P != 0 else ops.paged_decode_auto_partition_size(
-            inp.num_seqs, inp.num_q_heads, inp.num_kv_heads, inp.head_dim, inp.block_size,
-            inp.max_context_len, var)
-        split = eff_P > 0 and inp.max_context_len > eff_P
-        ordered = "longest_first" in variant and inp.num_seqs >= 2 and variant.startswith("tma_mma")
-        launches = 1 + int(split) + int(ordered)
-    # decode CTAs: (sequence, kv head, query chunk of 16 / G tokens, partition)
-    q_chunks = 1 if q_len <= 1 else -(-q_len // (16 // cfg.group))
-    grid = inp.num_seqs * inp.num_kv_heads * q_chunks * (-(-inp.max_context_len // eff_P) if split and eff_P > 0 else 1)
+    # the library's own plan: partition, order, data path, decode CTAs, launches
+    # (the E4M3 entry runs the mma.sync tensor-core path)
+    launches, eff_P, ordered, resolved, grid = ops.paged_decode_call_plan(
+        inp.num_seqs, q_len, inp.num_q_heads, inp.num_kv_heads, inp.head_dim, inp.block_size,
+        inp.max_context_len, kv_fp8, P, "tma_mma" if kv_fp8 else variant)
+    split = eff_P > 0
     out = torch.empty_like(inp.q)
     ew = torch.zeros(1, dtype=torch.int32, device=dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -270,7 +264,7 @@ def time_gpu(args, cfg, variant, dev, inp, steps, warmup, with_e2e=True, with_cl
             ops.paged_decode_attention_multi(qm, inp.k_cache, inp.v_cache, inp.block_tables,
                                              inp.context_lens, inp.scale, out=out,
                                              max_context_len=inp.max_context_len, partition_size=P,
-                                             workspace=ws, error_word=ew, stream=stream)
+                                             workspace=ws, error_word=ew, stream=stream, variant=variant)
 
     use_flush = algo < 4 * l2
 
@@ -308,6 +302,7 @@ def time_gpu(args, cfg, variant, dev, inp, steps, warmup, with_e2e=True, with_cl
         "algo_bytes": algo, "mean_ms": statistics.mean(times_ms), "median_ms": statistics.median(times_ms),
         "min_ms": min(times_ms), "wall_s": t_wall, "launches_per_call": launches, "grid": grid,
         "partition_size": eff_P if split else -1, "longest_first": ordered, "device_error": errbits,
+        "variant": resolved,
         "clocks": sampler.summary() if sampler else None,
         "l2": (f"an L2 flush (2x L2 read) before every timed call; inputs {algo / 1e6:.0f} MB" if use_flush
                else f"inputs larger than L2 ({algo / 1e9:.2f} GB against {l2 / 1e6:.0f} MB): calls back to "
@@ -662,14 +657,7 @@ def main():
     r = time_gpu(args, cfg, variant, dev, inp, args.steps, args.warmup, with_e2e=not args.no_e2e)
     mean_ms, value = aggregate_over_ranks(r["mean_ms"], r["algo_bytes"], ws, dev)
     achieved = r["algo_bytes"] / (r["mean_ms"] * 1e-3) / 1e9
-    resolved = variant
-    if args.q_len > 1 or args.kv_fp8:
-        resolved = "tma_mma" + ("+longest_first" if r["longest_first"] else "")
-    elif variant == "auto":
-        P_req = args.partition_size if args.partition_size is not None else (cfg.partition_size or 0)
-        resolved = ops.variant_name(ops.paged_decode_auto_variant(
-            cfg.num_seqs, cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim, cfg.block_size,
-            inp.max_context_len, P_req))
+    resolved = r["variant"]
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(mean_ms, 5), "higher_is_better": True,
@@ -688,7 +676,8 @@ def main():
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "traffic": ncu_traffic(cfg.name, resolved),
                      "kernel": kernel_name(cfg, resolved, args.kv_fp8,
-                                           wide=args.q_len == 1 and r["grid"] >= 3 * 4 * torch.cuda.get_device_properties(dev).multi_processor_count)},
+                                           wide=args.q_len == 1 and r["grid"] >= 3 * 4 * torch.cuda.get_device_properties(dev).multi_processor_count,
+                                           q_len=args.q_len)},
         "gpu_launches": r["launches_per_call"] * args.steps,
         "clocks": r["clocks"],
         "e2e": r.get("e2e"),

@@ -72,6 +72,9 @@ typedef enum {
                                    then read only the row's blocks; that sequence's output is
                                    undefined, and nothing outside the inputs is read) */
 #define PKD_DEVERR_TIMEOUT 2u   /* a bounded wait on a shared-memory barrier ran out */
+#define PKD_DEVERR_LAYOUT 4u    /* a CTA's dynamic shared memory did not start 1024-byte aligned
+                                   (the tcgen05 kernel relies on it for its swizzled operands and
+                                   then computes nothing for that CTA; not seen on sm_103a) */
 
 /* How K/V tiles reach the arithmetic.  All variants give the same result. */
 typedef enum {

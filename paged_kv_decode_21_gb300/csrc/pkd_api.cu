@@ -201,14 +201,19 @@ int query_chunks(int q_len, int G, int path = PKD_VARIANT_TMA_MMA) {
 }
 
 // The tensor-core path the automatic variant runs for several query tokens
-// per sequence or E4M3 caches.  Where the rows of a (sequence, kv head) --
-// q_len x G -- need more than one 16-row mma.sync tile, that path reads the
-// partition's K and V once per tile and runs out of issue slots; the tcgen05
-// kernel serves up to 64 rows per CTA from one read, with S and O in tensor
-// memory (fp16 caches, head_dim 128).
+// per sequence or E4M3 caches.  The mma.sync kernel serves one 16-row tile of
+// q_len x G rows per CTA and reads the partition's K and V once per tile; the
+// tcgen05 kernel serves up to 64 rows from one read, with S and O in tensor
+// memory (fp16 caches, head_dim 128), but its per-tile chain runs at about
+// three quarters of the copy bandwidth.  Measured on the full workloads, it
+// wins from kTcMinTiles tiles on (GQA 7:1, q_len 8, four tiles: 910 against
+// 1163 us; GQA 5:1, q_len 8, three: 935 against 1206 us) and loses at two
+// (GQA 7:1, q_len 4: 856 against 729 us; GQA 4:1, q_len 8: 233 against 226).
+constexpr int kTcMinTiles = 3;
 int auto_multi_path(const Shape& s, int q_len, int kv_fp8) {
   const int G = s.num_q_heads / s.num_kv_heads;
-  if (!kv_fp8 && s.head_dim == 128 && (long long)q_len * G > 16) return PKD_VARIANT_TCGEN05;
+  if (!kv_fp8 && s.head_dim == 128 && query_chunks(q_len, G, PKD_VARIANT_TMA_MMA) >= kTcMinTiles)
+    return PKD_VARIANT_TCGEN05;
   return PKD_VARIANT_TMA_MMA;
 }
 

@@ -13,23 +13,31 @@
 //
 // Roles (four warps):
 //   warp 2, lane 0   producer: 3-D tensor copies of the partition's K and V
-//                    into a ring of NS stages of TN tokens (the 128-byte
-//                    swizzled layout the MMA descriptors read), one mbarrier
-//                    per stage with the transaction count of its copies.
+//                    tiles of TN tokens (the 128-byte swizzled layout the MMA
+//                    descriptors read) into two rings, NSK stages for K and
+//                    NSV for V, one mbarrier per stage with the transaction
+//                    count of its copies.  A K stage is free again once S of
+//                    its tile is computed, a V stage only after P.V, so the
+//                    V ring is the deeper one; optionally, tiles beyond the
+//                    rings are prefetched into L2 (cp.async.bulk.prefetch.L2).
 //   warp 3, lane 0   MMA issuer: S = Q K^T (M = 128 rows, N = TN tokens,
 //                    K = 128 dims) into one of two S buffers in tensor memory,
 //                    then, once the softmax has written P, O += P V
 //                    (M = 128, N = 128 dims, K = TN tokens) into O in tensor
-//                    memory; completion is committed to mbarriers.  S of the
-//                    next tile is issued before waiting for P of this one, so
-//                    the tensor cores overlap the softmax.
+//                    memory; completion is committed to mbarriers.  It polls
+//                    both conditions and issues whichever is ready first: S of
+//                    the next tile as soon as its K landed (and its S buffer
+//                    is free), P.V as soon as P is written, so the tensor
+//                    cores overlap the softmax and neither stage is held
+//                    behind the other.
 //   warps 0-1        softmax, one thread per tile row (tensor-memory lane):
 //                    the row of S into registers, mask, online softmax in the
 //                    log2 domain with a lazy running maximum (the output is
 //                    rescaled in tensor memory only when the maximum grows by
 //                    more than kLazyTau), P rounded to fp16 into shared memory
-//                    (the MMA's A operand), and at the end O / l to the output
-//                    or the unnormalised partial for the split-K merge.
+//                    (the MMA's A operand; one buffer, written once P.V of the
+//                    previous tile completed), and at the end O / l to the
+//                    output or the unnormalised partial for the split-K merge.
 // The MMAs run M = 128 with the rows past kTcRows reading whatever follows
 // Q and P in shared memory: those accumulator rows are never read.
 //
@@ -53,6 +61,7 @@
 namespace pkd {
 
 constexpr int kTcRows = 64;  // query rows per CTA (query tokens x group heads)
+constexpr uint32_t kErrLayout = 4u;  // dynamic shared memory not 1024-byte aligned
 
 // Query tokens per CTA of the tcgen05 kernel for group size G.
 constexpr int tc_query_chunk(int G) { return kTcRows / G; }
@@ -64,24 +73,32 @@ struct TcTraits {
   static constexpr int ROWS = kTcRows;
   static constexpr int TN = 64;            // tokens per tile
   static constexpr int NBT = TN / BS;      // cache blocks per tile
-  static constexpr int NS = 2;             // ring stages
+  static constexpr int NSK = 2;            // K ring stages
+  static constexpr int NSV = 3;            // V ring stages
+  static constexpr int NPB = 2;            // P buffers
   static constexpr int ROWB = 128;         // bytes per swizzled row: 64 fp16
   static constexpr int QH = ROWS * ROWB;   // one 64-dim half of Q
   static constexpr int PB = ROWS * ROWB;   // one P buffer (TN = 64 tokens per row)
   static constexpr int KVH = TN * ROWB;    // one 64-dim half of a K or V tile
-  static constexpr int STAGE = 4 * KVH;    // K halves, then V halves
+  static constexpr int TILE = 2 * KVH;     // a K or V tile: two halves
   static constexpr int Q_OFF = 0;
   static constexpr int P_OFF = Q_OFF + 2 * QH;
-  static constexpr int RING_OFF = P_OFF + 2 * PB;
-  static constexpr int MAIN = RING_OFF + NS * STAGE;
-  static_assert(Q_OFF + QH + 128 * ROWB <= MAIN && P_OFF + PB + 128 * ROWB <= MAIN,
+  static constexpr int K_OFF = P_OFF + NPB * PB;
+  static constexpr int V_OFF = K_OFF + NSK * TILE;
+  static constexpr int MAIN = V_OFF + NSV * TILE;
+  static_assert(Q_OFF + QH + 128 * ROWB <= MAIN && P_OFF + (NPB - 1) * PB + 128 * ROWB <= MAIN,
                 "the M = 128 operand reads stay inside shared memory");
   static_assert(TN == 64, "a P row is one 128-byte swizzled row");
-  static constexpr int NBAR = 2 * NS + 7;  // full, empty, sfull[2], pfull[2], pfree[2], drain
-  static constexpr int TAIL = NBAR * 8 + 8 + NS * 4;
-  static constexpr int SMEM_BYTES = 1024 + MAIN + ((TAIL + 15) / 16) * 16;
+  // kfull, kempty [NSK]; vfull, vempty [NSV]; sfull[2]; pfull, pfree [NPB]; drain
+  static constexpr int NBAR = 2 * NSK + 2 * NSV + 2 + 2 * NPB + 1;
+  static constexpr int TAIL = NBAR * 8 + 8 + NSV * 4;
+  // No alignment slack: a kernel without static shared memory gets a dynamic
+  // window that starts 1024-byte aligned (checked at run time), and two CTAs
+  // of 112 KiB fill the SM's 228 KiB with the 1 KiB each reserves.
+  static constexpr int SMEM_BYTES = MAIN + ((TAIL + 15) / 16) * 16;
   static constexpr int THREADS = 128;
   static constexpr int MIN_BLOCKS = 2;
+  static_assert(MIN_BLOCKS * (SMEM_BYTES + 1024) <= 228 * 1024, "two CTAs per SM");
   static constexpr uint32_t TMEM_COLS = 256;  // O: columns 0-127; S buffer s: 128 + 64 s
   static constexpr uint32_t IDESC_S = tc_idesc_f16(128, TN, false);
   static constexpr uint32_t IDESC_O = tc_idesc_f16(128, D, true);
@@ -92,20 +109,24 @@ __global__ void __launch_bounds__(TcTraits<BS>::THREADS, TcTraits<BS>::MIN_BLOCK
     paged_decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                            const DecodeParams P) {
   using T = TcTraits<BS>;
-  constexpr int NS = T::NS, TN = T::TN, D = T::D;
-  extern __shared__ __align__(1024) unsigned char smem_raw[];
-  const uint32_t raw_u32 = smem_u32(smem_raw);
-  unsigned char* smem = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);
+  constexpr int NSK = T::NSK, NSV = T::NSV, NPB = T::NPB, TN = T::TN, D = T::D;
+  extern __shared__ __align__(1024) unsigned char smem[];
   const uint32_t sbase = smem_u32(smem);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + T::MAIN);  // [NS] a tile's copies landed
-  uint64_t* empty = full + NS;   // [NS] a tile's MMAs completed: its stage is free
-  uint64_t* sfull = empty + NS;  // [2] S of a tile is in tensor memory
-  uint64_t* pfull = sfull + 2;   // [2] P of a tile is in shared memory and its S was read
-  uint64_t* pfree = pfull + 2;   // [2] P.V of a tile completed
-  uint64_t* drain = pfree + 2;   // every MMA issued completed
+  if (sbase & 1023u) {  // the swizzled operands need 1024-byte aligned groups
+    if (threadIdx.x == 0) record_error(P.error_word, kErrLayout);
+    return;
+  }
+  uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + T::MAIN);  // [NSK] a K tile landed
+  uint64_t* kempty = kfull + NSK;  // [NSK] S of the tile computed: the K stage is free
+  uint64_t* vfull = kempty + NSK;  // [NSV] a V tile landed (with its bad-block mask)
+  uint64_t* vempty = vfull + NSV;  // [NSV] P.V of the tile completed: the V stage is free
+  uint64_t* sfull = vempty + NSV;  // [2] S of a tile is in tensor memory
+  uint64_t* pfull = sfull + 2;     // [NPB] P of a tile is in shared memory and its S was read
+  uint64_t* pfree = pfull + NPB;   // [NPB] P.V of a tile completed (its P buffer free, O stable)
+  uint64_t* drain = pfree + NPB;   // every MMA issued completed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile uint32_t* stage_bad = reinterpret_cast<volatile uint32_t*>(tmem_slot + 2);  // [NS]
+  volatile uint32_t* vbad = reinterpret_cast<volatile uint32_t*>(tmem_slot + 2);  // [NSV]
 
   // work item: query chunk fastest, then partition j, then (b, g)
   const int G = P.num_q_heads / P.num_kv_heads;
@@ -159,12 +180,17 @@ __global__ void __launch_bounds__(TcTraits<BS>::THREADS, TcTraits<BS>::MIN_BLOCK
   if (threadIdx.x == 0) {
     prefetch_tensormap(&tmap_k);
     prefetch_tensormap(&tmap_v);
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+    for (int s = 0; s < NSK; ++s) {
+      mbar_init(&kfull[s], 1);
+      mbar_init(&kempty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&sfull[s], 1);
+    for (int s = 0; s < NSV; ++s) {
+      mbar_init(&vfull[s], 1);
+      mbar_init(&vempty[s], 1);
+    }
+    mbar_init(&sfull[0], 1);
+    mbar_init(&sfull[1], 1);
+    for (int s = 0; s < NPB; ++s) {
       mbar_init(&pfull[s], 32 * nsw);
       mbar_init(&pfree[s], 1);
     }
@@ -196,15 +222,41 @@ __global__ void __launch_bounds__(TcTraits<BS>::THREADS, TcTraits<BS>::MIN_BLOCK
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const L2Hints l2h = make_l2_hints(P.l2_hints != 0);
-      int issued = 0;
-      for (int i = 0; i < ntiles; ++i) {
-        const int st = i % NS;
-        if (*abort_flag) break;
-        if (i >= NS && !mbar_wait_bounded(&empty[st], ((i / NS) - 1) & 1, P.timeout_ns)) {
-          record_error(P.error_word, kErrTimeout);
-          *abort_flag = 1;
-          break;
+      const size_t tile_bytes = (size_t)BS * D * sizeof(__half);  // one (block, head) tile
+      const size_t block_stride = (size_t)P.num_kv_heads * tile_bytes;
+      const char* kbase = reinterpret_cast<const char*>(P.k_cache) + (size_t)g * tile_bytes;
+      const char* vbase = reinterpret_cast<const char*>(P.v_cache) + (size_t)g * tile_bytes;
+      // tiles past the rings are prefetched into L2 prefetch_distance tiles ahead
+      int pf_next = NSV;
+      auto prefetch_upto = [&](int end) {
+        for (end = min(end, ntiles); pf_next < end; ++pf_next) {
+#pragma unroll
+          for (int kk = 0; kk < T::NBT; ++kk) {
+            const int k = pf_next * T::NBT + kk;
+            const int pb = k < nblk ? bt[k] : -1;
+            if (pb >= 0 && pb < P.num_blocks) {
+              prefetch_l2_bulk(kbase + (size_t)pb * block_stride, (uint32_t)tile_bytes, l2h);
+              prefetch_l2_bulk(vbase + (size_t)pb * block_stride, (uint32_t)tile_bytes, l2h);
+            }
+          }
         }
+      };
+      // the boxes of one tile of one cache into a stage
+      auto copy_tile = [&](uint32_t dst, const CUtensorMap* map, uint64_t* bar, const int (&pbs)[T::NBT]) {
+#pragma unroll
+        for (int kk = 0; kk < T::NBT; ++kk) {
+          if (pbs[kk] < 0) continue;
+#pragma unroll
+          for (int rg = 0; rg < BS / 16; ++rg) {
+            const uint32_t row = (kk * BS + 16 * rg) * T::ROWB;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) tma_load_3d(dst + h * T::KVH + row, map, bar, 64 * h, g * BS + 16 * rg, pbs[kk], l2h);
+          }
+        }
+      };
+      int kissued = 0, vissued = 0;
+      for (int i = 0; i < ntiles; ++i) {
+        if (*abort_flag) break;
         int pbs[T::NBT];
         uint32_t bad = 0, bytes = 0;
 #pragma unroll
@@ -217,30 +269,34 @@ __global__ void __launch_bounds__(TcTraits<BS>::THREADS, TcTraits<BS>::MIN_BLOCK
             pb = -1;
           }
           pbs[kk] = pb;
-          if (pb >= 0) bytes += 4 * BS * T::ROWB;  // K and V, two 64-dim halves each
+          if (pb >= 0) bytes += 2 * BS * T::ROWB;  // two 64-dim halves
         }
-        stage_bad[st] = bad;
-        const uint32_t stg = sbase + T::RING_OFF + st * T::STAGE;
-        mbar_arrive_expect_tx(&full[st], bytes);
-#pragma unroll
-        for (int kk = 0; kk < T::NBT; ++kk) {
-          if (pbs[kk] < 0) continue;
-#pragma unroll
-          for (int rg = 0; rg < BS / 16; ++rg) {
-            const int y = g * BS + 16 * rg;
-            const uint32_t row = (kk * BS + 16 * rg) * T::ROWB;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              tma_load_3d(stg + h * T::KVH + row, &tmap_k, &full[st], 64 * h, y, pbs[kk], l2h);
-              tma_load_3d(stg + (2 + h) * T::KVH + row, &tmap_v, &full[st], 64 * h, y, pbs[kk], l2h);
-            }
-          }
+        const int sk = i % NSK, sv = i % NSV;
+        if (i >= NSK && !mbar_wait_bounded(&kempty[sk], ((i / NSK) - 1) & 1, P.timeout_ns)) {
+          record_error(P.error_word, kErrTimeout);
+          *abort_flag = 1;
+          break;
         }
-        issued = i + 1;
+        mbar_arrive_expect_tx(&kfull[sk], bytes);
+        copy_tile(sbase + T::K_OFF + sk * T::TILE, &tmap_k, &kfull[sk], pbs);
+        kissued = i + 1;
+        if (i >= NSV && !mbar_wait_bounded(&vempty[sv], ((i / NSV) - 1) & 1, P.timeout_ns)) {
+          record_error(P.error_word, kErrTimeout);
+          *abort_flag = 1;
+          break;
+        }
+        vbad[sv] = bad;
+        mbar_arrive_expect_tx(&vfull[sv], bytes);
+        copy_tile(sbase + T::V_OFF + sv * T::TILE, &tmap_v, &vfull[sv], pbs);
+        vissued = i + 1;
+        prefetch_upto(i + NSV + P.prefetch_distance);
       }
-      if (*abort_flag)  // let the copies in flight land before the CTA exits
-        for (int k = issued > NS ? issued - NS : 0; k < issued; ++k)
-          mbar_wait_bounded(&full[k % NS], (k / NS) & 1, P.timeout_ns);
+      if (*abort_flag) {  // let the copies in flight land before the CTA exits
+        for (int k = kissued > NSK ? kissued - NSK : 0; k < kissued; ++k)
+          mbar_wait_bounded(&kfull[k % NSK], (k / NSK) & 1, P.timeout_ns);
+        for (int k = vissued > NSV ? vissued - NSV : 0; k < vissued; ++k)
+          mbar_wait_bounded(&vfull[k % NSV], (k / NSV) & 1, P.timeout_ns);
+      }
     }
   } else if (warp == 3) {
     // ------------------------------------------------------------ MMA issuer
@@ -248,10 +304,10 @@ __global__ void __launch_bounds__(TcTraits<BS>::THREADS, TcTraits<BS>::MIN_BLOCK
       const uint32_t qs = sbase + T::Q_OFF;
       bool any = false;
       auto issue_qk = [&](int i) -> bool {
-        const int st = i % NS;
-        if (!mbar_wait_bounded(&full[st], (i / NS) & 1, P.timeout_ns)) return false;
+        const int sk = i % NSK;
+        if (!mbar_wait_bounded(&kfull[sk], (i / NSK) & 1, P.timeout_ns)) return false;
         tc_fence_after();
-        const uint32_t ks = sbase + T::RING_OFF + st * T::STAGE;
+        const uint32_t ks = sbase + T::K_OFF + sk * T::TILE;
         const uint32_t d = tmem + 128 + 64 * (i & 1);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
@@ -260,26 +316,47 @@ __global__ void __launch_bounds__(TcTraits<BS>::THREADS, TcTraits<BS>::MIN_BLOCK
                      T::IDESC_S, k > 0 ? 1u : 0u);
         }
         tc_commit(&sfull[i & 1]);
+        tc_commit(&kempty[sk]);
         any = true;
         return true;
       };
-      bool ok = ntiles == 0 || issue_qk(0);
-      for (int i = 0; ok && i < ntiles; ++i) {
+      // Whichever is ready first: S of tile nq (its K landed, and its S buffer
+      // is free once P.V of tile nq - 2 was issued, i.e. nq <= npv + 1), or
+      // P.V of tile npv (its P written).  Neither waits behind the other.
+      int nq = 0, npv = 0;
+      bool ok = true;
+      uint64_t t_idle = 0;
+      while (npv < ntiles) {
         if (*abort_flag) {
           ok = false;
           break;
         }
-        if (i + 1 < ntiles && !(ok = issue_qk(i + 1))) break;
-        if (!(ok = mbar_wait_bounded(&pfull[i & 1], (i / 2) & 1, P.timeout_ns))) break;
-        tc_fence_after();
-        const uint32_t vs = sbase + T::RING_OFF + (i % NS) * T::STAGE + 2 * T::KVH;
-        const uint32_t ps = sbase + T::P_OFF + (i & 1) * T::PB;
+        if (nq < ntiles && nq <= npv + 1 && mbar_try_wait(&kfull[nq % NSK], (nq / NSK) & 1)) {
+          if (!(ok = issue_qk(nq))) break;
+          ++nq;
+          t_idle = 0;
+        } else if (npv < nq && mbar_try_wait(&pfull[npv % NPB], (npv / NPB) & 1)) {
+          tc_fence_after();
+          const uint32_t vs = sbase + T::V_OFF + (npv % NSV) * T::TILE;
+          const uint32_t ps = sbase + T::P_OFF + (npv % NPB) * T::PB;
 #pragma unroll
-        for (int k = 0; k < TN / 16; ++k)  // 16 tokens: 32 bytes of a P row, 16 rows of V
-          tc_mma_f16(tmem, sw128_desc(ps + k * 32, 16, 1024), sw128_desc(vs + k * 16 * T::ROWB, T::KVH, 1024),
-                     T::IDESC_O, (i > 0 || k > 0) ? 1u : 0u);
-        tc_commit(&pfree[i & 1]);
-        tc_commit(&empty[i % NS]);
+          for (int k = 0; k < TN / 16; ++k)  // 16 tokens: 32 bytes of a P row, 16 rows of V
+            tc_mma_f16(tmem, sw128_desc(ps + k * 32, 16, 1024), sw128_desc(vs + k * 16 * T::ROWB, T::KVH, 1024),
+                       T::IDESC_O, (npv > 0 || k > 0) ? 1u : 0u);
+          tc_commit(&pfree[npv % NPB]);
+          tc_commit(&vempty[npv % NSV]);
+          ++npv;
+          t_idle = 0;
+        } else {
+          // nothing ready: give up after timeout_ns without progress
+          const uint64_t now = globaltimer_ns();
+          if (t_idle == 0) {
+            t_idle = now;
+          } else if (now - t_idle > P.timeout_ns) {
+            ok = false;
+            break;
+          }
+        }
       }
       if (!ok) {
         record_error(P.error_word, kErrTimeout);
@@ -300,7 +377,7 @@ __global__ void __launch_bounds__(TcTraits<BS>::THREADS, TcTraits<BS>::MIN_BLOCK
     float m = -INFINITY, mt = -INFINITY, l = 0.f;  // running shift, exact maximum, sum of p
     bool ok = true;
     for (int i = 0; i < ntiles; ++i) {
-      const int st = i % NS, sb = i & 1;
+      const int sv = i % NSV, sb = i & 1;
       ok = __all_sync(0xffffffffu, !*abort_flag && mbar_wait_bounded(&sfull[sb], (i / 2) & 1, P.timeout_ns));
       if (!ok) break;
       tc_fence_after();
@@ -308,17 +385,18 @@ __global__ void __launch_bounds__(TcTraits<BS>::THREADS, TcTraits<BS>::MIN_BLOCK
       tmem_ld32(tl + 128 + 64 * sb, s[0]);
       tmem_ld32(tl + 128 + 64 * sb + 32, s[1]);
       tmem_ld_wait();
-      // S implies the tile's K landed; its V and bad-block mask come with the same phase
-      ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[st], (i / NS) & 1, P.timeout_ns));
+      // the tile's V and its bad-block mask
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(&vfull[sv], (i / NSV) & 1, P.timeout_ns));
       if (!ok) break;
-      const uint32_t bad = stage_bad[st];
+      const uint32_t bad = vbad[sv];
       const int tb = t0 + i * TN;
       const int nv = lim - tb;             // columns this row sees
       const int valid = min(TN, t1 - tb);  // columns holding the CTA's tokens
-      if (nv >= TN && bad == 0) {
-#pragma unroll
-        for (int e = 0; e < TN; ++e) s[e / 32][e % 32] *= P.scale_log2;
-      } else {
+      // Unmasked tile, scale >= 0: the maximum of the raw scores times the
+      // scale is the maximum of the scaled ones, and the scale goes into the
+      // exponent's FMA.  Otherwise scale, then mask (-inf), then the maximum.
+      const bool raw = nv >= TN && bad == 0 && P.scale_log2 >= 0.f;
+      if (!raw) {
 #pragma unroll
         for (int e = 0; e < TN; ++e)
           s[e / 32][e % 32] =
@@ -330,60 +408,67 @@ __global__ void __launch_bounds__(TcTraits<BS>::THREADS, TcTraits<BS>::MIN_BLOCK
         const float* v = &s[a / 4][(a % 4) * 8];
         mx[a] = fmaxf(fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])), fmaxf(fmaxf(v[4], v[5]), fmaxf(v[6], v[7])));
       }
-      const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      const float sc = raw ? P.scale_log2 : 1.f;  // the scale still to apply
+      if (raw) tmax *= sc;
       mt = fmaxf(mt, tmax);
-      if (__any_sync(0xffffffffu, tmax > m + kLazyTau)) {
+      const bool rescale = __any_sync(0xffffffffu, tmax > m + kLazyTau);
+      float alpha = 1.f;
+      if (rescale) {
         const float mn = fmaxf(m, tmax);
-        const float alpha = (mn == -INFINITY) ? 1.f : ex2_approx(m - mn);
+        alpha = (mn == -INFINITY) ? 1.f : ex2_approx(m - mn);
         l *= alpha;
         m = mn;
-        if (i > 0) {
-          // O holds the earlier tiles once the last P.V completed: rescale it in place
-          ok = __all_sync(0xffffffffu, mbar_wait_bounded(&pfree[(i - 1) & 1], ((i - 1) / 2) & 1, P.timeout_ns));
-          if (!ok) break;
-          tc_fence_after();
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            float o[32];
-            tmem_ld32(tl + 32 * c, o);
-            tmem_ld_wait();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] *= alpha;
-            tmem_st32(tl + 32 * c, o);
-          }
-          tmem_st_wait();
-        }
       }
       // a row that has seen no token yet keeps m = -inf: shift by 0 so that
       // its masked scores give p = 0 rather than NaN
       const float mu = m == -INFINITY ? 0.f : m;
-      // this P buffer was last read by the P.V of tile i - 2
-      if (i >= 2) {
-        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&pfree[sb], ((i - 2) / 2) & 1, P.timeout_ns));
+      // p = 2^(s * sc - mu), two lanes per packed FMA; the sum in four packed chains
+      const float2 sc2 = make_float2(sc, sc), nmu2 = make_float2(-mu, -mu);
+      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      uint32_t pk[TN / 2];  // p as fp16 pairs
+#pragma unroll
+      for (int e = 0; e < TN / 2; ++e) {
+        const float2 x = ffma2(make_float2(s[e / 16][(2 * e) % 32], s[e / 16][(2 * e + 1) % 32]), sc2, nmu2);
+        const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+        acc[e % 4] = __fadd2_rn(acc[e % 4], pp);
+        pk[e] = pack_half2(pp.x, pp.y);
+      }
+      const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
+      const float2 at = __fadd2_rn(a01, a23);
+      l += at.x + at.y;
+      // this P buffer was last read by P.V of tile i - NPB
+      if (i >= NPB) {
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&pfree[i % NPB], ((i - NPB) / NPB) & 1, P.timeout_ns));
         if (!ok) break;
       }
-      unsigned char* prow = smem + T::P_OFF + sb * T::PB + rr * T::ROWB;
-      float rs = 0.f;
+      // O holds the earlier tiles once P.V of the previous one completed: rescale it in place
+      if (i > 0 && rescale) {
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait_bounded(&pfree[(i - 1) % NPB], ((i - 1) / NPB) & 1, P.timeout_ns));
+        if (!ok) break;
+        tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < TN / 8; ++c) {
-        const float* v = &s[c / 4][(c % 4) * 8];
-        float p[8];
+        for (int c = 0; c < D / 32; ++c) {
+          float o[32];
+          tmem_ld32(tl + 32 * c, o);
+          tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 8; ++e) p[e] = ex2_approx(v[e] - mu);
-        rs += ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
-        uint4 w;
-        w.x = pack_half2(p[0], p[1]);
-        w.y = pack_half2(p[2], p[3]);
-        w.z = pack_half2(p[4], p[5]);
-        w.w = pack_half2(p[6], p[7]);
-        *reinterpret_cast<uint4*>(prow + ((c ^ (rr & 7)) << 4)) = w;
+          for (int e = 0; e < 32; ++e) o[e] *= alpha;
+          tmem_st32(tl + 32 * c, o);
+        }
+        tmem_st_wait();
       }
-      l += rs;
+      unsigned char* prow = smem + T::P_OFF + (i % NPB) * T::PB + rr * T::ROWB;
+#pragma unroll
+      for (int c = 0; c < TN / 8; ++c)
+        *reinterpret_cast<uint4*>(prow + ((c ^ (rr & 7)) << 4)) =
+            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
       if (valid < TN || bad) {
         // V rows that hold no token of the CTA, or a bad block's: p = 0 there,
         // and 0 * NaN would not be 0
-        unsigned char* vt = smem + T::RING_OFF + st * T::STAGE + 2 * T::KVH;
+        unsigned char* vt = smem + T::V_OFF + sv * T::TILE;
         for (int x = threadIdx.x; x < 2 * TN * 8; x += 32 * nsw) {
           const int h = x / (TN * 8), r = (x / 8) % TN, c = x % 8;
           if (r >= valid || ((bad >> (r / BS)) & 1u))
@@ -391,12 +476,12 @@ __global__ void __launch_bounds__(TcTraits<BS>::THREADS, TcTraits<BS>::MIN_BLOCK
         }
       }
       fence_proxy_async_smem();  // P (and zeroed V rows) visible to the tensor cores
-      tc_fence_before();         // our reads of S ordered before the arrive
-      mbar_arrive(&pfull[sb]);
+      tc_fence_before();         // our tensor-memory reads and writes ordered before the arrive
+      mbar_arrive(&pfull[i % NPB]);
     }
     if (ok && ntiles > 0)
-      ok = __all_sync(0xffffffffu,
-                      mbar_wait_bounded(&pfree[(ntiles - 1) & 1], ((ntiles - 1) / 2) & 1, P.timeout_ns));
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(&pfree[(ntiles - 1) % NPB], ((ntiles - 1) / NPB) & 1,
+                                                     P.timeout_ns));
     if (!ok) {
       if (lane == 0) record_error(P.error_word, kErrTimeout);
       *abort_flag = 1;

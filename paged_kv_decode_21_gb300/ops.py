@@ -24,6 +24,7 @@ STATUS_NAMES = {0: "PKD_OK", 1: "PKD_ERR_NULL", 2: "PKD_ERR_SHAPE", 3: "PKD_ERR_
 VARIANTS = {"auto": 0, "no_prefetch": 1, "l2_prefetch": 2, "tma_staged": 3, "tma_mma": 4, "tcgen05": 5}
 DEVERR_BAD_BLOCK = 1
 DEVERR_TIMEOUT = 2
+DEVERR_LAYOUT = 4
 
 _lock = threading.Lock()
 _lib = None
