@@ -204,12 +204,12 @@ int query_chunks(int q_len, int G, int path = PKD_VARIANT_TMA_MMA) {
 // per sequence or E4M3 caches.  The mma.sync kernel serves one 16-row tile of
 // q_len x G rows per CTA and reads the partition's K and V once per tile; the
 // tcgen05 kernel serves up to 64 rows from one read, with S and O in tensor
-// memory (fp16 caches, head_dim 128), but its per-tile chain runs at about
-// three quarters of the copy bandwidth.  Measured on the full workloads, it
-// wins from kTcMinTiles tiles on (GQA 7:1, q_len 8, four tiles: 910 against
-// 1163 us; GQA 5:1, q_len 8, three: 935 against 1206 us) and loses at two
-// (GQA 7:1, q_len 4: 856 against 729 us; GQA 4:1, q_len 8: 233 against 226).
-constexpr int kTcMinTiles = 3;
+// memory (fp16 caches, head_dim 128).  Measured on the full workloads it wins
+// or ties from kTcMinTiles tiles on (GQA 7:1: q_len 8, four tiles, 786 against
+// 1163 us; q_len 4, two tiles, 730 against 729 us; GQA 4:1, q_len 8, two
+// tiles, 204 against 226 us) and loses at one (GQA 4:1, q_len 4: 203 against
+// 183 us).
+constexpr int kTcMinTiles = 2;
 int auto_multi_path(const Shape& s, int q_len, int kv_fp8) {
   const int G = s.num_q_heads / s.num_kv_heads;
   if (!kv_fp8 && s.head_dim == 128 && query_chunks(q_len, G, PKD_VARIANT_TMA_MMA) >= kTcMinTiles)

@@ -11,15 +11,19 @@
 // multi-token query (speculative verification) reads the cache once per
 // chunk of kTcRows / G tokens rather than once per 16 / G.
 //
-// Roles (four warps):
-//   warp 2, lane 0   producer: 3-D tensor copies of the partition's K and V
-//                    tiles of TN tokens (the 128-byte swizzled layout the MMA
-//                    descriptors read) into two rings, NSK stages for K and
-//                    NSV for V, one mbarrier per stage with the transaction
-//                    count of its copies.  A K stage is free again once S of
-//                    its tile is computed, a V stage only after P.V, so the
-//                    V ring is the deeper one; optionally, tiles beyond the
-//                    rings are prefetched into L2 (cp.async.bulk.prefetch.L2).
+// Roles (five warps):
+//   warps 2 and 4,   producers: 3-D tensor copies of the partition's K (warp 2)
+//   lane 0           and V (warp 4) tiles of TN tokens (the 128-byte swizzled
+//                    layout the MMA descriptors read) into two rings, NSK
+//                    stages for K and NSV for V, one mbarrier per stage with
+//                    the transaction count of its copies.  A K stage is free
+//                    again once S of its tile is computed, a V stage only
+//                    after P.V, so the V ring is the deeper one.  One thread
+//                    per ring: a tile's eight copies take about a thousand
+//                    cycles to issue from one thread, which bounded the tile
+//                    rate when one thread fed both rings.  Optionally, tiles
+//                    beyond the K ring are prefetched into L2
+//                    (cp.async.bulk.prefetch.L2).
 //   warp 3, lane 0   MMA issuer: S = Q K^T (M = 128 rows, N = TN tokens,
 //                    K = 128 dims) into one of two S buffers in tensor memory,
 //                    then, once the softmax has written P, O += P V
@@ -96,7 +100,7 @@ struct TcTraits {
   // window that starts 1024-byte aligned (checked at run time), and two CTAs
   // of 112 KiB fill the SM's 228 KiB with the 1 KiB each reserves.
   static constexpr int SMEM_BYTES = MAIN + ((TAIL + 15) / 16) * 16;
-  static constexpr int THREADS = 128;
+  static constexpr int THREADS = 160;
   static constexpr int MIN_BLOCKS = 2;
   static_assert(MIN_BLOCKS * (SMEM_BYTES + 1024) <= 228 * 1024, "two CTAs per SM");
   static constexpr uint32_t TMEM_COLS = 256;  // O: columns 0-127; S buffer s: 128 + 64 s
@@ -178,7 +182,7 @@ __global__ void __launch_bounds__(TcTraits<BS>::THREADS, TcTraits<BS>::MIN_BLOCK
   const int lane = threadIdx.x % 32;
   const int nsw = rows > 32 ? 2 : 1;  // softmax warps
 
-  // ---- producer state (used by warp 2, lane 0)
+  // ---- producer state (warp 2, lane 0: K; warp 4, lane 0: V)
   const L2Hints l2h = make_l2_hints(P.l2_hints != 0);
   const size_t tile_bytes = (size_t)BS * D * sizeof(__half);  // one (block, head) tile
   const size_t block_stride = (size_t)P.num_kv_heads * tile_bytes;
@@ -236,34 +240,24 @@ __global__ void __launch_bounds__(TcTraits<BS>::THREADS, TcTraits<BS>::MIN_BLOCK
     for (int kk = 0; kk < T::NBT; ++kk) bytes += pbs[kk] >= 0 ? 2 * BS * T::ROWB : 0;  // two 64-dim halves
     return bytes;
   };
-  // One producer step: the next K copy if its stage is free, then the next V
-  // copy (never ahead of K) if its stage is free.  Returns whether a copy was
-  // issued.
-  auto produce_step = [&]() -> bool {
-    bool progress = false;
-    const bool kfree = kissued < NSK || mbar_test(&kempty[kissued % NSK], ((kissued / NSK) - 1) & 1);
-    if (kissued < ntiles && kfree) {
-      int pbs[T::NBT];
-      tile_blocks(kissued, pbs, true);
-      const int sk = kissued % NSK;
-      mbar_arrive_expect_tx(&kfull[sk], tile_bytes_of(pbs));
-      copy_tile(sbase + T::K_OFF + sk * T::TILE, &tmap_k, &kfull[sk], pbs);
-      ++kissued;
-      prefetch_upto(kissued + P.prefetch_distance);
-      progress = true;
-    }
-    const bool vfree = vissued < NSV || mbar_test(&vempty[vissued % NSV], ((vissued / NSV) - 1) & 1);
-    if (vissued < kissued && vfree) {
-      int pbs[T::NBT];
-      const uint32_t bad = tile_blocks(vissued, pbs, false);
-      const int sv = vissued % NSV;
-      vbad[sv] = bad;
-      mbar_arrive_expect_tx(&vfull[sv], tile_bytes_of(pbs));
-      copy_tile(sbase + T::V_OFF + sv * T::TILE, &tmap_v, &vfull[sv], pbs);
-      ++vissued;
-      progress = true;
-    }
-    return progress;
+  // Issue the copies of tile kissued (K) / vissued (V) into its stage.
+  auto issue_k = [&]() {
+    int pbs[T::NBT];
+    tile_blocks(kissued, pbs, true);
+    const int sk = kissued % NSK;
+    mbar_arrive_expect_tx(&kfull[sk], tile_bytes_of(pbs));
+    copy_tile(sbase + T::K_OFF + sk * T::TILE, &tmap_k, &kfull[sk], pbs);
+    ++kissued;
+    prefetch_upto(kissued + P.prefetch_distance);
+  };
+  auto issue_v = [&]() {
+    int pbs[T::NBT];
+    const uint32_t bad = tile_blocks(vissued, pbs, false);
+    const int sv = vissued % NSV;
+    vbad[sv] = bad;
+    mbar_arrive_expect_tx(&vfull[sv], tile_bytes_of(pbs));
+    copy_tile(sbase + T::V_OFF + sv * T::TILE, &tmap_v, &vfull[sv], pbs);
+    ++vissued;
   };
 
   // Barriers are set up before the CTA-wide barrier; the producer starts after
@@ -311,33 +305,31 @@ __global__ void __launch_bounds__(TcTraits<BS>::THREADS, TcTraits<BS>::MIN_BLOCK
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 2) {
-    // ------------------------------------------------------------ producer
+  if (warp == 2 || warp == 4) {
+    // ------------------------------------------------------------ producers
     if (lane == 0) {
-      // The K and V rings advance independently, each as soon as its next
-      // stage is free (polled, so neither waits behind the other).
-      // (an idle pass reads the global timer, which also spaces the polls)
-      uint64_t t_idle = 0;
-      while (vissued < ntiles || kissued < ntiles) {
+      const bool is_k = warp == 2;
+      const int ns = is_k ? NSK : NSV;
+      uint64_t* empty_bar = is_k ? kempty : vempty;
+      while ((is_k ? kissued : vissued) < ntiles) {
         if (*abort_flag) break;
-        if (produce_step()) {
-          t_idle = 0;
-        } else {  // nothing free: give up after timeout_ns without progress
-          const uint64_t now = globaltimer_ns();
-          if (t_idle == 0) {
-            t_idle = now;
-          } else if (now - t_idle > P.timeout_ns) {
-            record_error(P.error_word, kErrTimeout);
-            *abort_flag = 1;
-            break;
-          }
+        const int i = is_k ? kissued : vissued;
+        if (i >= ns && !mbar_wait_bounded(&empty_bar[i % ns], ((i / ns) - 1) & 1, P.timeout_ns)) {
+          record_error(P.error_word, kErrTimeout);
+          *abort_flag = 1;
+          break;
+        }
+        if (is_k) {
+          issue_k();
+        } else {
+          issue_v();
         }
       }
       if (*abort_flag) {  // let the copies in flight land before the CTA exits
-        for (int k = kissued > NSK ? kissued - NSK : 0; k < kissued; ++k)
-          mbar_wait_bounded(&kfull[k % NSK], (k / NSK) & 1, P.timeout_ns);
-        for (int k = vissued > NSV ? vissued - NSV : 0; k < vissued; ++k)
-          mbar_wait_bounded(&vfull[k % NSV], (k / NSV) & 1, P.timeout_ns);
+        const int issued = is_k ? kissued : vissued;
+        uint64_t* full_bar = is_k ? kfull : vfull;
+        for (int k = issued > ns ? issued - ns : 0; k < issued; ++k)
+          mbar_wait_bounded(&full_bar[k % ns], (k / ns) & 1, P.timeout_ns);
       }
     }
   } else if (warp == 3) {

@@ -260,15 +260,15 @@ def test_host_entry_argument_checks(L):
 
 def test_call_plan_picks_the_tensor_core_path(L):
     from paged_kv_decode_21_gb300 import ops
-    # three or more 16-row mma.sync tiles of q_len x G rows, fp16 caches, head_dim 128: tcgen05
+    # two or more 16-row mma.sync tiles of q_len x G rows, fp16 caches, head_dim 128: tcgen05
     assert ops.paged_decode_call_plan(4, 8, 28, 4, 128, 16, 1000)[3] == "tcgen05"   # 4 tiles
-    assert ops.paged_decode_call_plan(4, 8, 40, 8, 128, 16, 1000)[3] == "tcgen05"   # 3 tiles
-    assert ops.paged_decode_call_plan(4, 9, 32, 8, 128, 16, 1000)[3] == "tcgen05"   # 3 tiles
-    # one or two tiles, head_dim 64, E4M3 caches or a single query: the mma.sync path
+    assert ops.paged_decode_call_plan(4, 4, 28, 4, 128, 16, 1000)[3] == "tcgen05"   # 2 tiles
+    assert ops.paged_decode_call_plan(4, 8, 32, 8, 128, 16, 1000)[3] == "tcgen05"   # 2 tiles
+    assert ops.paged_decode_call_plan(4, 17, 4, 4, 128, 16, 1000)[3] == "tcgen05"   # G=1: 2 tiles
+    # one tile, head_dim 64, E4M3 caches or a single query: the mma.sync path
     assert ops.paged_decode_call_plan(4, 2, 28, 4, 128, 16, 1000)[3] == "tma_mma"
-    assert ops.paged_decode_call_plan(4, 4, 28, 4, 128, 16, 1000)[3] == "tma_mma"   # 2 tiles
-    assert ops.paged_decode_call_plan(4, 8, 32, 8, 128, 16, 1000)[3] == "tma_mma"   # 2 tiles
     assert ops.paged_decode_call_plan(4, 4, 32, 8, 128, 16, 1000)[3] == "tma_mma"
+    assert ops.paged_decode_call_plan(4, 16, 4, 4, 128, 16, 1000)[3] == "tma_mma"
     assert ops.paged_decode_call_plan(4, 8, 28, 4, 64, 16, 1000)[3] == "tma_mma"
     assert ops.paged_decode_call_plan(4, 8, 28, 4, 128, 16, 1000, kv_fp8=True)[3] == "tma_mma"
     assert ops.paged_decode_call_plan(4, 1, 28, 4, 128, 16, 1000)[3] == "tma_mma"
