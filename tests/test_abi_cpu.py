@@ -231,7 +231,7 @@ def test_workspace_sizes_cover_every_plan(L):
         maxlen = rng.randint(1, 20000)
         MB = -(-maxlen // BS) + rng.randint(0, 3)
         P = rng.choice([0, 0, -1, 32 * BS // 16 * rng.randint(1, 64)])
-        var = rng.choice([0, 4, 4 | 0x200, 3, 0x100 | 4])
+        var = rng.choice([0, 4, 4 | 0x200, 3, 0x100 | 4] + ([5, 5 | 0x200] if D == 128 else []))
         need = L.paged_decode_workspace_size(B, G * Hkv, Hkv, D, BS, maxlen, P, var)
         st = L.paged_decode_attention_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, B, G * Hkv, Hkv, D, BS, 64, MB, maxlen,
                                          ctypes.c_float(0.1), P, var, 0, ws_ptr if need else None, need, None, None)
@@ -241,10 +241,33 @@ def test_workspace_sizes_cover_every_plan(L):
         stm = L.paged_decode_attention_multi(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, B, q_len, G * Hkv, Hkv, D, BS, 64, MB,
                                              maxlen, ctypes.c_float(0.1), P, ws_ptr if needm else None, needm, None, None)
         assert stm in (6, 8), (B, q_len, G, Hkv, D, BS, maxlen, P, needm, stm)
+        # the multi-token entry with each tensor-core path forced (tcgen05: head_dim 128 only)
+        for mvar in (4, 5, 5 | 0x200):
+            stx = L.paged_decode_attention_multi_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, B, q_len, G * Hkv, Hkv, D, BS,
+                                                    64, MB, maxlen, ctypes.c_float(0.1), P, mvar,
+                                                    ws_ptr if needm else None, needm, None, None)
+            if (mvar & 0xff) == 5 and D != 128:
+                assert stx == 3, (D, mvar, stx)
+            else:
+                assert stx in (6, 8), (B, q_len, G, Hkv, D, BS, maxlen, P, mvar, needm, stx)
         stf = L.paged_decode_attention_fp8(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, B, q_len, G * Hkv, Hkv, D, BS, 64, MB,
                                            maxlen, ctypes.c_float(0.1), ctypes.c_float(0.5), ctypes.c_float(0.5), P,
                                            ws_ptr if needm else None, needm, None, None)
         assert stf in (6, 8), (B, q_len, G, Hkv, D, BS, maxlen, P, needm, stf)
+
+
+def test_multi_ex_argument_checks(L):
+    # (q, k, v, bt, cl, out, B, q_len, Hq, Hkv, D, BS, NB, MB, maxlen, scale, P, variant, ws, wsb, err, stream)
+    def call(*, QL=3, D=128, var=5, P=-1):
+        return L.paged_decode_attention_multi_ex(*(FAKE,) * 6, 2, QL, 8, 2, D, 16, 64, 8, 100, ctypes.c_float(0.1),
+                                                 P, var, None, 0, None, None)
+    assert call(var=5, D=64) == 3            # tcgen05: head_dim 128 only
+    assert call(var=1) == 3 and call(var=3) == 3   # CUDA-core paths: single query only
+    assert call(var=6) == 2                  # not a variant
+    assert call(var=5, P=64) == 5            # split without a workspace
+    assert call(var=5, QL=0) == 2
+    assert call(var=5) in (6, 8)             # passes every host check (no GPU here)
+    assert call(var=4) in (6, 8) and call(var=0) in (6, 8)
 
 
 def test_host_entry_argument_checks(L):
