@@ -212,10 +212,10 @@ def time_gpu(args, cfg, variant, dev, inp, steps, warmup, with_e2e=True, with_cl
     q_len = getattr(args, "q_len", 1)
     kv_fp8 = getattr(args, "kv_fp8", False)
     # the library's own plan: partition, order, data path, decode CTAs, launches
-    # (the E4M3 entry runs the mma.sync tensor-core path)
+    # (the E4M3 entry takes no variant: it runs the automatic choice)
     launches, eff_P, ordered, resolved, grid = ops.paged_decode_call_plan(
         inp.num_seqs, q_len, inp.num_q_heads, inp.num_kv_heads, inp.head_dim, inp.block_size,
-        inp.max_context_len, kv_fp8, P, "tma_mma" if kv_fp8 else variant)
+        inp.max_context_len, kv_fp8, P, "auto" if kv_fp8 else variant)
     split = eff_P > 0
     out = torch.empty_like(inp.q)
     ew = torch.zeros(1, dtype=torch.int32, device=dev)

@@ -209,10 +209,16 @@ int query_chunks(int q_len, int G, int path = PKD_VARIANT_TMA_MMA) {
 // 1163 us; q_len 4, two tiles, 730 against 729 us; GQA 4:1, q_len 8, two
 // tiles, 204 against 226 us) and loses at one (GQA 4:1, q_len 4: 203 against
 // 183 us).
+// E4M3 caches are widened to fp16 in shared memory by the producer warps on
+// the tcgen05 path, on the critical path of every tile; there it only wins
+// from kTcMinTilesFp8 tiles on (GQA 7:1, q_len 8, four tiles: 1027 against
+// 1171 us) and loses at two (GQA 7:1, q_len 4: 970 against 629 us; GQA 4:1,
+// q_len 8: 269 against 215 us).
 constexpr int kTcMinTiles = 2;
+constexpr int kTcMinTilesFp8 = 4;
 int auto_multi_path(const Shape& s, int q_len, int kv_fp8) {
   const int G = s.num_q_heads / s.num_kv_heads;
-  if (!kv_fp8 && s.head_dim == 128 && query_chunks(q_len, G, PKD_VARIANT_TMA_MMA) >= kTcMinTiles)
+  if (s.head_dim == 128 && query_chunks(q_len, G, PKD_VARIANT_TMA_MMA) >= (kv_fp8 ? kTcMinTilesFp8 : kTcMinTiles))
     return PKD_VARIANT_TCGEN05;
   return PKD_VARIANT_TMA_MMA;
 }
@@ -235,7 +241,7 @@ pkd_status plan_call(const Shape& s, int q_len, int variant, int partition_size,
   const int flags = variant & ~0xff;
   const int path = variant_path(variant);
   if (path == PKD_VARIANT_TCGEN05) {
-    if (kv_fp8 || s.head_dim != 128) return PKD_ERR_UNSUPPORTED;
+    if (s.head_dim != 128) return PKD_ERR_UNSUPPORTED;
   } else if (q_len > 1 || kv_fp8) {
     // several query tokens per sequence, or E4M3 caches: the tensor-core paths only
     if (path != PKD_VARIANT_AUTO && path != PKD_VARIANT_TMA_MMA) return PKD_ERR_UNSUPPORTED;
@@ -463,7 +469,12 @@ pkd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
     if (cudaGetLastError() != cudaSuccess) return PKD_ERR_LAUNCH;
     p.piece_order = order;
   }
-  if (kv_fp8) {
+  if (kv_fp8 && variant_path(variant) == PKD_VARIANT_TCGEN05) {
+    if (grid > 0x7fffffffLL) return PKD_ERR_SHAPE;
+    const cudaError_t e =
+        grid <= 0 ? cudaSuccess : pkd::launch_decode_tcgen05(head_dim, block_size, p, grid, stream, /*kvb=*/1);
+    st = e == cudaSuccess ? PKD_OK : PKD_ERR_LAUNCH;
+  } else if (kv_fp8) {
     if (grid > 0x7fffffffLL) return PKD_ERR_SHAPE;
     // single-query grids of kWideFp8Waves waves or more of four CTAs per SM
     // run the four-per-SM build
@@ -535,7 +546,7 @@ pkd_status paged_decode_attention_fp8(const void* q, const void* k_cache, const 
                                       int* error_word, cudaStream_t stream) {
   return decode_impl(q, k_cache, v_cache, block_tables, context_lens, out, num_seqs, q_len, num_q_heads,
                      num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, max_context_len,
-                     scale, partition_size, PKD_VARIANT_TMA_MMA, 0, workspace, workspace_bytes, error_word,
+                     scale, partition_size, PKD_VARIANT_AUTO, 0, workspace, workspace_bytes, error_word,
                      stream, 1, k_scale, v_scale);
 }
 

@@ -70,9 +70,13 @@ constexpr uint32_t kErrLayout = 4u;  // dynamic shared memory not 1024-byte alig
 // Query tokens per CTA of the tcgen05 kernel for group size G.
 constexpr int tc_query_chunk(int G) { return kTcRows / G; }
 
-template <int BS>
+// KVB: bytes per K/V element in the caches (2: fp16; 1: E4M3 bytes, widened
+// to fp16 in shared memory by the producer warps before the MMAs read them).
+template <int BS, int KVB = 2>
 struct TcTraits {
   static_assert(BS == 16 || BS == 32, "block_size");
+  static_assert(KVB == 1 || KVB == 2, "fp16 or E4M3 caches");
+  static constexpr bool F8 = KVB == 1;
   static constexpr int D = 128;
   static constexpr int ROWS = kTcRows;
   static constexpr int TN = 64;            // tokens per tile
@@ -93,8 +97,9 @@ struct TcTraits {
   static_assert(Q_OFF + QH + 128 * ROWB <= MAIN && P_OFF + (NPB - 1) * PB + 128 * ROWB <= MAIN,
                 "the M = 128 operand reads stay inside shared memory");
   static_assert(TN == 64, "a P row is one 128-byte swizzled row");
-  // kfull, kempty [NSK]; vfull, vempty [NSV]; sfull[2]; pfull, pfree [NPB]; drain
-  static constexpr int NBAR = 2 * NSK + 2 * NSV + 2 + 2 * NPB + 1;
+  // kfull, kempty [NSK]; vfull, vempty [NSV]; sfull[2]; pfull, pfree [NPB]; drain;
+  // E4M3: kland [NSK], vland [NSV] (the bytes landed, before widening)
+  static constexpr int NBAR = 2 * NSK + 2 * NSV + 2 + 2 * NPB + 1 + (F8 ? NSK + NSV : 0);
   static constexpr int TAIL = NBAR * 8 + 8 + NSV * 4;
   // No alignment slack: a kernel without static shared memory gets a dynamic
   // window that starts 1024-byte aligned (checked at run time), and two CTAs
@@ -108,11 +113,12 @@ struct TcTraits {
   static constexpr uint32_t IDESC_O = tc_idesc_f16(128, D, true);
 };
 
-template <int BS>
-__global__ void __launch_bounds__(TcTraits<BS>::THREADS, TcTraits<BS>::MIN_BLOCKS)
+template <int BS, int KVB>
+__global__ void __launch_bounds__(TcTraits<BS, KVB>::THREADS, TcTraits<BS, KVB>::MIN_BLOCKS)
     paged_decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                            const DecodeParams P) {
-  using T = TcTraits<BS>;
+  using T = TcTraits<BS, KVB>;
+  constexpr bool F8 = T::F8;
   constexpr int NSK = T::NSK, NSV = T::NSV, NPB = T::NPB, TN = T::TN, D = T::D;
   extern __shared__ __align__(1024) unsigned char smem_tc[];
   unsigned char* smem = smem_tc;
@@ -129,7 +135,9 @@ __global__ void __launch_bounds__(TcTraits<BS>::THREADS, TcTraits<BS>::MIN_BLOCK
   uint64_t* pfull = sfull + 2;     // [NPB] P of a tile is in shared memory and its S was read
   uint64_t* pfree = pfull + NPB;   // [NPB] P.V of a tile completed (its P buffer free, O stable)
   uint64_t* drain = pfree + NPB;   // every MMA issued completed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* kland = drain + 1;     // E4M3: [NSK] a K tile's bytes landed
+  uint64_t* vland = kland + NSK;   // E4M3: [NSV] a V tile's bytes landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1 + (F8 ? NSK + NSV : 0));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile uint32_t* vbad = reinterpret_cast<volatile uint32_t*>(tmem_slot + 2);  // [NSV]
 
@@ -184,7 +192,7 @@ __global__ void __launch_bounds__(TcTraits<BS>::THREADS, TcTraits<BS>::MIN_BLOCK
 
   // ---- producer state (warp 2, lane 0: K; warp 4, lane 0: V)
   const L2Hints l2h = make_l2_hints(P.l2_hints != 0);
-  const size_t tile_bytes = (size_t)BS * D * sizeof(__half);  // one (block, head) tile
+  const size_t tile_bytes = (size_t)BS * D * KVB;  // one (block, head) tile
   const size_t block_stride = (size_t)P.num_kv_heads * tile_bytes;
   const char* kbase = reinterpret_cast<const char*>(P.k_cache) + (size_t)g * tile_bytes;
   const char* vbase = reinterpret_cast<const char*>(P.v_cache) + (size_t)g * tile_bytes;
@@ -213,8 +221,13 @@ __global__ void __launch_bounds__(TcTraits<BS>::THREADS, TcTraits<BS>::MIN_BLOCK
 #pragma unroll
       for (int rg = 0; rg < BS / 16; ++rg) {
         const uint32_t row = (kk * BS + 16 * rg) * T::ROWB;
+        if constexpr (F8) {
+          // E4M3 rows of 128 bytes land in the stage's first 8 KiB, 128-byte swizzled
+          tma_load_3d(dst + row, map, bar, 0, g * BS + 16 * rg, pbs[kk], l2h);
+        } else {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) tma_load_3d(dst + h * T::KVH + row, map, bar, 64 * h, g * BS + 16 * rg, pbs[kk], l2h);
+          for (int h = 0; h < 2; ++h) tma_load_3d(dst + h * T::KVH + row, map, bar, 64 * h, g * BS + 16 * rg, pbs[kk], l2h);
+        }
       }
     }
   };
@@ -237,7 +250,7 @@ __global__ void __launch_bounds__(TcTraits<BS>::THREADS, TcTraits<BS>::MIN_BLOCK
   auto tile_bytes_of = [&](const int (&pbs)[T::NBT]) {
     uint32_t bytes = 0;
 #pragma unroll
-    for (int kk = 0; kk < T::NBT; ++kk) bytes += pbs[kk] >= 0 ? 2 * BS * T::ROWB : 0;  // two 64-dim halves
+    for (int kk = 0; kk < T::NBT; ++kk) bytes += pbs[kk] >= 0 ? BS * D * KVB : 0;  // the block's rows
     return bytes;
   };
   // Issue the copies of tile kissued (K) / vissued (V) into its stage.
@@ -267,13 +280,16 @@ __global__ void __launch_bounds__(TcTraits<BS>::THREADS, TcTraits<BS>::MIN_BLOCK
   if (threadIdx.x == 0) {
     prefetch_tensormap(&tmap_k);
     prefetch_tensormap(&tmap_v);
+    // E4M3: the full barriers count the 32 lanes of the widening warp
     for (int s = 0; s < NSK; ++s) {
-      mbar_init(&kfull[s], 1);
+      mbar_init(&kfull[s], F8 ? 32 : 1);
       mbar_init(&kempty[s], 1);
+      if (F8) mbar_init(&kland[s], 1);
     }
     for (int s = 0; s < NSV; ++s) {
-      mbar_init(&vfull[s], 1);
+      mbar_init(&vfull[s], F8 ? 32 : 1);
       mbar_init(&vempty[s], 1);
+      if (F8) mbar_init(&vland[s], 1);
     }
     mbar_init(&sfull[0], 1);
     mbar_init(&sfull[1], 1);
@@ -305,8 +321,91 @@ __global__ void __launch_bounds__(TcTraits<BS>::THREADS, TcTraits<BS>::MIN_BLOCK
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 2 || warp == 4) {
-    // ------------------------------------------------------------ producers
+  if ((warp == 2 || warp == 4) && F8) {
+    // ------------------------------------------------------------ producers, E4M3
+    // Lane 0 issues the copies of the bytes; once a tile's bytes landed the
+    // whole warp widens them in place to the fp16 layout the MMAs read (every
+    // lane reads its 16 chunks of the 8 KiB before any lane writes the 16 KiB),
+    // then arrives on the tile's full barrier.  Lane 0 decides, the warp follows.
+    const bool is_k = warp == 2;
+    const int ns = is_k ? NSK : NSV;
+    uint64_t* empty_bar = is_k ? kempty : vempty;
+    uint64_t* land_bar = is_k ? kland : vland;
+    uint64_t* full_bar = is_k ? kfull : vfull;
+    const uint32_t ring = is_k ? T::K_OFF : T::V_OFF;
+    int issued = 0, conv = 0;
+    uint64_t t_idle = 0;
+    bool failed = false;
+    while (conv < ntiles) {
+      if (*abort_flag) break;
+      bool progress = false;
+      int can = lane == 0 && issued < ntiles &&
+                (issued < ns || mbar_test(&empty_bar[issued % ns], ((issued / ns) - 1) & 1));
+      if (__shfl_sync(0xffffffffu, can, 0)) {
+        if (lane == 0) {
+          int pbs[T::NBT];
+          const uint32_t bad = tile_blocks(issued, pbs, is_k);
+          const int st = issued % ns;
+          if (!is_k) vbad[st] = bad;
+          mbar_arrive_expect_tx(&land_bar[st], tile_bytes_of(pbs));
+          copy_tile(sbase + ring + st * T::TILE, is_k ? &tmap_k : &tmap_v, &land_bar[st], pbs);
+        }
+        ++issued;
+        progress = true;
+      }
+      can = lane == 0 && conv < issued && mbar_test(&land_bar[conv % ns], (conv / ns) & 1);
+      if (__shfl_sync(0xffffffffu, can, 0)) {
+        const int st = conv % ns;
+        mbar_wait_bounded(&land_bar[st], (conv / ns) & 1, P.timeout_ns);  // every lane acquires the bytes
+        unsigned char* stg = smem + ring + st * T::TILE;
+        uint4 in[16];  // chunk q = lane + 32 k: row q / 8, stored chunk q % 8
+#pragma unroll
+        for (int k = 0; k < 16; ++k) in[k] = *reinterpret_cast<const uint4*>(stg + 16 * (lane + 32 * k));
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const int q = lane + 32 * k, r = q >> 3;
+          const int j = (q & 7) ^ (r & 7);  // dims 16 j .. 16 j + 15 of row r
+          uint4 lo, hi;                     // fp16 dims 16 j .. +7 and 16 j + 8 .. +15
+          e4m3x4_to_f16x2x2(in[k].x, lo.x, lo.y);
+          e4m3x4_to_f16x2x2(in[k].y, lo.z, lo.w);
+          e4m3x4_to_f16x2x2(in[k].z, hi.x, hi.y);
+          e4m3x4_to_f16x2x2(in[k].w, hi.z, hi.w);
+          const int c0 = 2 * j;  // fp16 chunk (of 16 over both 64-dim halves)
+          *reinterpret_cast<uint4*>(stg + (c0 >> 3) * T::KVH + r * T::ROWB + (((c0 & 7) ^ (r & 7)) << 4)) = lo;
+          const int c1 = c0 + 1;
+          *reinterpret_cast<uint4*>(stg + (c1 >> 3) * T::KVH + r * T::ROWB + (((c1 & 7) ^ (r & 7)) << 4)) = hi;
+        }
+        fence_proxy_async_smem();  // visible to the tensor cores
+        mbar_arrive(&full_bar[st]);
+        ++conv;
+        progress = true;
+      }
+      if (progress) {
+        t_idle = 0;
+      } else {  // nothing to do: give up after timeout_ns without progress
+        int give_up = 0;
+        if (lane == 0) {
+          const uint64_t now = globaltimer_ns();
+          if (t_idle == 0) t_idle = now;
+          else give_up = now - t_idle > P.timeout_ns;
+        }
+        if (__shfl_sync(0xffffffffu, give_up, 0)) {
+          failed = true;
+          break;
+        }
+      }
+    }
+    if (lane == 0) {
+      if (failed) {
+        record_error(P.error_word, kErrTimeout);
+        *abort_flag = 1;
+      }
+      if (*abort_flag)  // let the copies in flight land before the CTA exits
+        for (int t = conv; t < issued; ++t) mbar_wait_bounded(&land_bar[t % ns], (t / ns) & 1, P.timeout_ns);
+    }
+  } else if (warp == 2 || warp == 4) {
+    // ------------------------------------------------------------ producers, fp16
     if (lane == 0) {
       const bool is_k = warp == 2;
       const int ns = is_k ? NSK : NSV;
@@ -525,9 +624,11 @@ __global__ void __launch_bounds__(TcTraits<BS>::THREADS, TcTraits<BS>::MIN_BLOCK
       tc_fence_after();
       const size_t orow = live ? out_row(rr) : 0;
       const size_t pidx = orow * P.max_partitions + j;
-      const float inv = l > 0.f ? 1.f / l : 0.f;  // l = 0: the query saw no token
+      // l = 0: the query saw no token.  V = code * v_scale for E4M3 caches (1 for fp16)
+      const float inv = l > 0.f ? P.v_scale / l : 0.f;
       // partials are relative to the exact maximum mt; O and l to the shift m
       const float f = m == -INFINITY ? 0.f : ex2_approx(m - mt);
+      const float fo = f * P.v_scale;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         float o[32];
@@ -554,7 +655,7 @@ __global__ void __launch_bounds__(TcTraits<BS>::THREADS, TcTraits<BS>::MIN_BLOCK
 #pragma unroll
           for (int q = 0; q < 8; ++q)
             *reinterpret_cast<float4*>(dst + 4 * q) =
-                make_float4(o[4 * q] * f, o[4 * q + 1] * f, o[4 * q + 2] * f, o[4 * q + 3] * f);
+                make_float4(o[4 * q] * fo, o[4 * q + 1] * fo, o[4 * q + 2] * fo, o[4 * q + 3] * fo);
         }
       }
       if (live && !final_out) {

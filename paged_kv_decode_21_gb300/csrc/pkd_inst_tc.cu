@@ -1,5 +1,5 @@
 // Instantiations and launch of the tcgen05 decode kernel (pkd_decode_tc.cuh):
-// fp16 caches, head_dim 128, block sizes 16 and 32.
+// fp16 or E4M3 caches, head_dim 128, block sizes 16 and 32.
 #include "pkd_decode_tc.cuh"
 #include "pkd_mma_launch.cuh"
 #include "pkd_tc_launch.h"
@@ -9,11 +9,11 @@ static_assert(kTcRows == kTcRowsPerCta, "rows per CTA of the kernel and of its h
 
 namespace {
 
-template <int BS>
+template <int BS, int KVB>
 cudaError_t launch_tc_bs(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeParams& p, long long grid,
                          cudaStream_t stream) {
-  using T = TcTraits<BS>;
-  auto* fn = paged_decode_tc_kernel<BS>;
+  using T = TcTraits<BS, KVB>;
+  auto* fn = paged_decode_tc_kernel<BS, KVB>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
@@ -36,12 +36,15 @@ cudaError_t launch_tc_bs(const CUtensorMap& mk, const CUtensorMap& mv, const Dec
 
 }  // namespace
 
-cudaError_t launch_decode_tcgen05(int D, int BS, const DecodeParams& p, long long grid, cudaStream_t stream) {
-  if (D != 128 || (BS != 16 && BS != 32)) return cudaErrorInvalidValue;
+cudaError_t launch_decode_tcgen05(int D, int BS, const DecodeParams& p, long long grid, cudaStream_t stream,
+                                  int kvb) {
+  if (D != 128 || (BS != 16 && BS != 32) || (kvb != 1 && kvb != 2)) return cudaErrorInvalidValue;
   CUtensorMap mk, mv;
-  cudaError_t e = mma_host::make_maps(p, D, BS, 2, &mk, &mv);
+  cudaError_t e = mma_host::make_maps(p, D, BS, kvb, &mk, &mv);
   if (e != cudaSuccess) return e;
-  return BS == 16 ? launch_tc_bs<16>(mk, mv, p, grid, stream) : launch_tc_bs<32>(mk, mv, p, grid, stream);
+  if (kvb == 1)
+    return BS == 16 ? launch_tc_bs<16, 1>(mk, mv, p, grid, stream) : launch_tc_bs<32, 1>(mk, mv, p, grid, stream);
+  return BS == 16 ? launch_tc_bs<16, 2>(mk, mv, p, grid, stream) : launch_tc_bs<32, 2>(mk, mv, p, grid, stream);
 }
 
 }  // namespace pkd

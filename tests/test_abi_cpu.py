@@ -288,12 +288,17 @@ def test_call_plan_picks_the_tensor_core_path(L):
     assert ops.paged_decode_call_plan(4, 4, 28, 4, 128, 16, 1000)[3] == "tcgen05"   # 2 tiles
     assert ops.paged_decode_call_plan(4, 8, 32, 8, 128, 16, 1000)[3] == "tcgen05"   # 2 tiles
     assert ops.paged_decode_call_plan(4, 17, 4, 4, 128, 16, 1000)[3] == "tcgen05"   # G=1: 2 tiles
-    # one tile, head_dim 64, E4M3 caches or a single query: the mma.sync path
+    # E4M3 caches: from four tiles on
+    assert ops.paged_decode_call_plan(4, 8, 28, 4, 128, 16, 1000, kv_fp8=True)[3] == "tcgen05"   # 4 tiles
+    assert ops.paged_decode_call_plan(4, 4, 28, 4, 128, 16, 1000, kv_fp8=True)[3] == "tma_mma"   # 2 tiles
+    assert ops.paged_decode_call_plan(4, 8, 32, 8, 128, 16, 1000, kv_fp8=True)[3] == "tma_mma"   # 2 tiles
+    # one tile, head_dim 64 or a single query: the mma.sync path
     assert ops.paged_decode_call_plan(4, 2, 28, 4, 128, 16, 1000)[3] == "tma_mma"
     assert ops.paged_decode_call_plan(4, 4, 32, 8, 128, 16, 1000)[3] == "tma_mma"
     assert ops.paged_decode_call_plan(4, 16, 4, 4, 128, 16, 1000)[3] == "tma_mma"
     assert ops.paged_decode_call_plan(4, 8, 28, 4, 64, 16, 1000)[3] == "tma_mma"
-    assert ops.paged_decode_call_plan(4, 8, 28, 4, 128, 16, 1000, kv_fp8=True)[3] == "tma_mma"
+    assert ops.paged_decode_call_plan(4, 2, 28, 4, 128, 16, 1000, kv_fp8=True)[3] == "tma_mma"
+    assert ops.paged_decode_call_plan(4, 1, 28, 4, 128, 16, 1000, kv_fp8=True)[3] == "tma_mma"
     assert ops.paged_decode_call_plan(4, 1, 28, 4, 128, 16, 1000)[3] == "tma_mma"
     # grid: (sequence, kv head, chunk of 64 / G query tokens, partition)
     n, part, ordered, var, grid = ops.paged_decode_call_plan(4, 10, 28, 4, 128, 16, 1000, partition_size=256,
@@ -302,10 +307,9 @@ def test_call_plan_picks_the_tensor_core_path(L):
     n, part, ordered, var, grid = ops.paged_decode_call_plan(4, 10, 28, 4, 128, 16, 1000, partition_size=-1,
                                                              variant="tma_mma")
     assert (n, part, grid) == (1, -1, 4 * 4 * 5)
-    # refused: tcgen05 with head_dim 64 or E4M3 caches, CUDA-core paths for several queries
-    for kw in ({"variant": "tcgen05", "kv_fp8": True}, {"variant": "tma_staged"}):
-        with pytest.raises(ops.PagedDecodeError):
-            ops.paged_decode_call_plan(4, 8, 28, 4, 128, 16, 1000, **kw)
+    # refused: tcgen05 with head_dim 64, CUDA-core paths for several queries
+    with pytest.raises(ops.PagedDecodeError):
+        ops.paged_decode_call_plan(4, 8, 28, 4, 128, 16, 1000, variant="tma_staged")
     with pytest.raises(ops.PagedDecodeError):
         ops.paged_decode_call_plan(4, 1, 28, 4, 64, 16, 1000, variant="tcgen05")
 

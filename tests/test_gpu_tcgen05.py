@@ -324,3 +324,82 @@ def test_multi_query_full_size_sampled(name, q_len):
     rows = sample_rows(cfg.num_seqs * q_len, cfg.num_q_heads, 96, seed=q_len + len(name))
     got = out.view(-1, cfg.head_dim)[torch.from_numpy(rows).long().cuda()]
     assert_close(got, oracle_multi(inp, q, rows=rows), f"{name} q_len={q_len}")
+
+
+# --------------------------------------------------------------------------- E4M3 caches
+K_SCALE, V_SCALE = 0.05, 0.11
+
+
+def make_fp8(lens, q_len, Hq, Hkv, BS, seed):
+    inp, q = make_multi(lens, q_len, Hq, Hkv, BS, seed)
+    g = torch.Generator(device="cuda").manual_seed(seed + 3)
+    k8 = workloads.rand_e4m3(inp.k_cache.shape, g, "cuda")
+    v8 = workloads.rand_e4m3(inp.v_cache.shape, g, "cuda")
+    return inp, q, k8, v8
+
+
+def run_fp8(inp, q, k8, v8, partition, **kw):
+    return ops.paged_decode_attention_fp8(q, k8, v8, inp.block_tables, inp.context_lens, inp.scale, K_SCALE,
+                                          V_SCALE, max_context_len=inp.max_context_len, partition_size=partition,
+                                          **kw)
+
+
+def oracle_fp8(inp, q, k8, v8, rows=None):
+    return oracle.attention_fp8(q.cpu(), k8.cpu(), v8.cpu(), inp.block_tables.cpu(), inp.context_lens.cpu(),
+                                inp.scale, K_SCALE, V_SCALE, rows=rows)
+
+
+FP8_MULTI = [
+    # (BS, Hq, Hkv, lens, q_len): four or more 16-row tiles, so the automatic path is tcgen05
+    (16, 28, 4, [0, 5, 257, 700], 8),      # G=7: 56 rows
+    (16, 28, 4, [130, 64], 10),            # G=7: chunks of 9 + 1
+    (32, 16, 2, [2, 100, 65], 8),          # G=8: 64 rows, L < q_len, BS=32
+    (16, 32, 8, [300, 33], 17),            # G=4: chunks of 16 + 1
+    (16, 4, 4, [40, 300], 65),             # G=1: chunks of 64 + 1
+]
+
+
+@pytest.mark.parametrize("shape", FP8_MULTI, ids=lambda s: f"BS{s[0]}G{s[1] // s[2]}Q{s[4]}")
+@pytest.mark.parametrize("partition", [-1, 64, 0])
+def test_fp8_multi_query_on_tcgen05_matches_oracle(shape, partition):
+    BS, Hq, Hkv, lens, q_len = shape
+    assert ops.paged_decode_call_plan(len(lens), q_len, Hq, Hkv, 128, BS, max(lens), kv_fp8=True)[3] == TC
+    inp, q, k8, v8 = make_fp8(lens, q_len, Hq, Hkv, BS, seed=BS + Hq + q_len + 1)
+    ew = errword()
+    out = run_fp8(inp, q, k8, v8, partition, error_word=ew)
+    assert ops.pkd_read_device_error(ew) == 0
+    assert_close(out, oracle_fp8(inp, q, k8, v8), f"E4M3 {shape} P={partition}")
+
+
+def test_fp8_multi_query_nan_codes_in_unused_slots():
+    lens = [21, 9, 70]
+    inp, q, k8, v8 = make_fp8(lens, 8, 28, 4, 16, seed=17)
+    used = torch.zeros(inp.num_blocks, 16, dtype=torch.bool)
+    for b, L in enumerate(lens):
+        for t in range(L):
+            used[int(inp.block_tables[b, t // 16]), t % 16] = True
+    a = run_fp8(inp, q, k8, v8, -1)
+    mask = (~used).cuda()
+    k8.permute(0, 2, 1, 3)[mask] = 0x7F  # the NaN code
+    v8.permute(0, 2, 1, 3)[mask] = 0xFF
+    b = run_fp8(inp, q, k8, v8, -1)
+    assert torch.isfinite(b).all()
+    assert torch.equal(a, b)
+
+
+def test_fp8_multi_query_full_size_sampled():
+    # Qwen2.5-7B shape over E4M3 caches verifying 8 draft tokens, at the automatic split
+    cfg = workloads.CONFIGS["qwen25_7b_gqa7"]
+    inp = workloads.make_inputs(cfg, device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(81)
+    k8 = workloads.rand_e4m3(inp.k_cache.shape, g, "cuda")
+    v8 = workloads.rand_e4m3(inp.v_cache.shape, g, "cuda")
+    del inp.k_cache, inp.v_cache
+    q = workloads.randn_f16((cfg.num_seqs, 8, cfg.num_q_heads, cfg.head_dim), g, "cuda")
+    ew = errword()
+    out = ops.paged_decode_attention_fp8(q, k8, v8, inp.block_tables, inp.context_lens, inp.scale, K_SCALE, V_SCALE,
+                                         max_context_len=inp.max_context_len, error_word=ew)
+    assert ops.pkd_read_device_error(ew) == 0
+    rows = sample_rows(cfg.num_seqs * 8, cfg.num_q_heads, 64, seed=81)
+    got = out.view(-1, cfg.head_dim)[torch.from_numpy(rows).long().cuda()]
+    assert_close(got, oracle_fp8(inp, q, k8, v8, rows=rows), "qwen25_7b_gqa7 E4M3 q_len=8")
