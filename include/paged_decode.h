@@ -86,12 +86,14 @@ typedef enum {
                                   prefetch beyond it with prefetch_distance >= 1); Q.K^T and P.V
                                   on the tensor cores (mma, fp16 operands, fp32 accumulation; p
                                   rounded to fp16 for P.V) */
-  PKD_VARIANT_TCGEN05 = 5      /* the same copies into a two-stage ring of 64-token tiles; Q.K^T
+  PKD_VARIANT_TCGEN05 = 5      /* the same copies into K and V rings of 64-token tiles; Q.K^T
                                   and P.V as tcgen05 MMAs with S and O in tensor memory, one
                                   softmax thread per query row; up to 64 query rows (query
-                                  tokens x group heads) share one read of the K/V tiles (fp16
-                                  caches, head_dim 128 only: PKD_ERR_UNSUPPORTED otherwise; no
-                                  L2 prefetch) */
+                                  tokens x group heads) share one read of the K/V tiles
+                                  (head_dim 128 only: PKD_ERR_UNSUPPORTED otherwise).  fp16
+                                  caches by this variant; E4M3 caches when the automatic
+                                  choice of paged_decode_attention_fp8 picks it (the bytes are
+                                  widened to fp16 in shared memory) */
 } pkd_variant;
 
 /*

@@ -212,10 +212,11 @@ int query_chunks(int q_len, int G, int path = PKD_VARIANT_TMA_MMA) {
 // E4M3 caches are widened to fp16 in shared memory by the producer warps on
 // the tcgen05 path, on the critical path of every tile; there it only wins
 // from kTcMinTilesFp8 tiles on (GQA 7:1, q_len 8, four tiles: 1027 against
-// 1171 us) and loses at two (GQA 7:1, q_len 4: 970 against 629 us; GQA 4:1,
+// 1171 us; GQA 5:1 at 512-token partitions, q_len 8, three tiles: 980 against
+// 1190 us) and loses at two (GQA 7:1, q_len 4: 970 against 629 us; GQA 4:1,
 // q_len 8: 269 against 215 us).
 constexpr int kTcMinTiles = 2;
-constexpr int kTcMinTilesFp8 = 4;
+constexpr int kTcMinTilesFp8 = 3;
 int auto_multi_path(const Shape& s, int q_len, int kv_fp8) {
   const int G = s.num_q_heads / s.num_kv_heads;
   if (s.head_dim == 128 && query_chunks(q_len, G, PKD_VARIANT_TMA_MMA) >= (kv_fp8 ? kTcMinTilesFp8 : kTcMinTiles))

@@ -350,12 +350,13 @@ def oracle_fp8(inp, q, k8, v8, rows=None):
 
 
 FP8_MULTI = [
-    # (BS, Hq, Hkv, lens, q_len): four or more 16-row tiles, so the automatic path is tcgen05
+    # (BS, Hq, Hkv, lens, q_len): three or more 16-row tiles, so the automatic path is tcgen05
     (16, 28, 4, [0, 5, 257, 700], 8),      # G=7: 56 rows
     (16, 28, 4, [130, 64], 10),            # G=7: chunks of 9 + 1
     (32, 16, 2, [2, 100, 65], 8),          # G=8: 64 rows, L < q_len, BS=32
     (16, 32, 8, [300, 33], 17),            # G=4: chunks of 16 + 1
     (16, 4, 4, [40, 300], 65),             # G=1: chunks of 64 + 1
+    (16, 40, 8, [200, 64, 1], 9),          # G=5: 45 rows (three mma.sync tiles)
 ]
 
 
