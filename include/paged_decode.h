@@ -89,11 +89,11 @@ typedef enum {
   PKD_VARIANT_TCGEN05 = 5      /* the same copies into K and V rings of 64-token tiles; Q.K^T
                                   and P.V as tcgen05 MMAs with S and O in tensor memory, one
                                   softmax thread per query row; up to 64 query rows (query
-                                  tokens x group heads) share one read of the K/V tiles
-                                  (head_dim 128 only: PKD_ERR_UNSUPPORTED otherwise).  fp16
-                                  caches by this variant; E4M3 caches when the automatic
-                                  choice of paged_decode_attention_fp8 picks it (the bytes are
-                                  widened to fp16 in shared memory) */
+                                  tokens x group heads) share one read of the K/V tiles.
+                                  fp16 caches at head_dim 64 or 128 by this variant; E4M3
+                                  caches at head_dim 128 when the automatic choice of
+                                  paged_decode_attention_fp8 picks it (the bytes are widened
+                                  to fp16 in shared memory); PKD_ERR_UNSUPPORTED otherwise */
 } pkd_variant;
 
 /*
@@ -318,10 +318,10 @@ pkd_status paged_decode_validate_tables(const int32_t* block_tables, const int32
  *   other arguments as for paged_decode_attention_ex; context_lens[b] counts
  *   the new tokens.  Runs a tensor-core path (PKD_VARIANT_AUTO of
  *   paged_decode_attention_multi_ex): where the rows of a (sequence, kv
- *   head), q_len x G, fit one 16-row tile or the caches are not fp16 with
- *   head_dim 128, PKD_VARIANT_TMA_MMA, whose CTAs serve 16 / G query tokens
- *   each; otherwise PKD_VARIANT_TCGEN05, whose CTAs serve 64 / G, so every
- *   K/V tile is read once per group of 64 / G query tokens.
+ *   head), q_len x G, fit one 16-row tile, PKD_VARIANT_TMA_MMA, whose CTAs
+ *   serve 16 / G query tokens each; otherwise PKD_VARIANT_TCGEN05, whose CTAs
+ *   serve 64 / G, so every K/V tile is read once per group of 64 / G query
+ *   tokens.
  *   workspace      required when the context is split
  *                  (paged_decode_multi_workspace_size bytes, 256-byte aligned);
  *                  with partition_size 0 it also keeps the longest-first

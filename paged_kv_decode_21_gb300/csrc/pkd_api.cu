@@ -216,10 +216,12 @@ int query_chunks(int q_len, int G, int path = PKD_VARIANT_TMA_MMA) {
 // 1190 us) and loses at two (GQA 7:1, q_len 4: 970 against 629 us; GQA 4:1,
 // q_len 8: 269 against 215 us).
 constexpr int kTcMinTiles = 2;
+// head_dim 128, or 64 with fp16 caches (E4M3 rows are widened at 128 only)
+bool tc_supports(const Shape& s, int kv_fp8) { return s.head_dim == 128 || (s.head_dim == 64 && !kv_fp8); }
 constexpr int kTcMinTilesFp8 = 3;
 int auto_multi_path(const Shape& s, int q_len, int kv_fp8) {
   const int G = s.num_q_heads / s.num_kv_heads;
-  if (s.head_dim == 128 && query_chunks(q_len, G, PKD_VARIANT_TMA_MMA) >= (kv_fp8 ? kTcMinTilesFp8 : kTcMinTiles))
+  if (tc_supports(s, kv_fp8) && query_chunks(q_len, G, PKD_VARIANT_TMA_MMA) >= (kv_fp8 ? kTcMinTilesFp8 : kTcMinTiles))
     return PKD_VARIANT_TCGEN05;
   return PKD_VARIANT_TMA_MMA;
 }
@@ -242,7 +244,7 @@ pkd_status plan_call(const Shape& s, int q_len, int variant, int partition_size,
   const int flags = variant & ~0xff;
   const int path = variant_path(variant);
   if (path == PKD_VARIANT_TCGEN05) {
-    if (s.head_dim != 128) return PKD_ERR_UNSUPPORTED;
+    if (!tc_supports(s, kv_fp8)) return PKD_ERR_UNSUPPORTED;
   } else if (q_len > 1 || kv_fp8) {
     // several query tokens per sequence, or E4M3 caches: the tensor-core paths only
     if (path != PKD_VARIANT_AUTO && path != PKD_VARIANT_TMA_MMA) return PKD_ERR_UNSUPPORTED;
@@ -583,7 +585,7 @@ size_t paged_decode_multi_workspace_size(int num_seqs, int q_len, int num_q_head
   // both tensor-core paths
   size_t most = 0;
   for (const int path : {PKD_VARIANT_TMA_MMA, PKD_VARIANT_TCGEN05}) {
-    if (path == PKD_VARIANT_TCGEN05 && head_dim != 128) continue;
+    if (path == PKD_VARIANT_TCGEN05 && head_dim != 128 && head_dim != 64) continue;
     const int qch = query_chunks(q_len, num_q_heads / num_kv_heads, path);
     const int P = partition_size == 0 ? auto_partition(s, path, qch) : partition_size;
     size_t bytes = 0;
@@ -688,7 +690,7 @@ pkd_status paged_decode_partitions(const void* q, const void* k_cache, const voi
   if (!std::isfinite(scale)) return PKD_ERR_SHAPE;
   if (!variant_ok(variant) || prefetch_distance < 0)
     return PKD_ERR_SHAPE;
-  if (variant_path(variant) == PKD_VARIANT_TCGEN05 && head_dim != 128) return PKD_ERR_UNSUPPORTED;
+  if (variant_path(variant) == PKD_VARIANT_TCGEN05 && head_dim != 128 && head_dim != 64) return PKD_ERR_UNSUPPORTED;
   if (partition_size <= 0 || partition_size % 32 != 0 || partition_size % block_size != 0)
     return PKD_ERR_SHAPE;
   const int need = (max_context_len + partition_size - 1) / partition_size;

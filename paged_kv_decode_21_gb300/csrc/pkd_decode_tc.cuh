@@ -72,12 +72,16 @@ constexpr int tc_query_chunk(int G) { return kTcRows / G; }
 
 // KVB: bytes per K/V element in the caches (2: fp16; 1: E4M3 bytes, widened
 // to fp16 in shared memory by the producer warps before the MMAs read them).
-template <int BS, int KVB = 2>
+// HD: head_dim, 128 (two 64-dim halves per row) or 64 (one; fp16 only).
+template <int BS, int KVB = 2, int HD = 128>
 struct TcTraits {
   static_assert(BS == 16 || BS == 32, "block_size");
   static_assert(KVB == 1 || KVB == 2, "fp16 or E4M3 caches");
+  static_assert(HD == 64 || HD == 128, "head_dim");
+  static_assert(KVB == 2 || HD == 128, "E4M3 rows are widened at head_dim 128 only");
   static constexpr bool F8 = KVB == 1;
-  static constexpr int D = 128;
+  static constexpr int D = HD;
+  static constexpr int NH = D / 64;        // 64-dim halves of a row
   static constexpr int ROWS = kTcRows;
   static constexpr int TN = 64;            // tokens per tile
   static constexpr int NBT = TN / BS;      // cache blocks per tile
@@ -88,13 +92,13 @@ struct TcTraits {
   static constexpr int QH = ROWS * ROWB;   // one 64-dim half of Q
   static constexpr int PB = ROWS * ROWB;   // one P buffer (TN = 64 tokens per row)
   static constexpr int KVH = TN * ROWB;    // one 64-dim half of a K or V tile
-  static constexpr int TILE = 2 * KVH;     // a K or V tile: two halves
+  static constexpr int TILE = NH * KVH;    // a K or V tile: its halves
   static constexpr int Q_OFF = 0;
-  static constexpr int P_OFF = Q_OFF + 2 * QH;
+  static constexpr int P_OFF = Q_OFF + NH * QH;
   static constexpr int K_OFF = P_OFF + NPB * PB;
   static constexpr int V_OFF = K_OFF + NSK * TILE;
   static constexpr int MAIN = V_OFF + NSV * TILE;
-  static_assert(Q_OFF + QH + 128 * ROWB <= MAIN && P_OFF + (NPB - 1) * PB + 128 * ROWB <= MAIN,
+  static_assert(Q_OFF + (NH - 1) * QH + 128 * ROWB <= MAIN && P_OFF + (NPB - 1) * PB + 128 * ROWB <= MAIN,
                 "the M = 128 operand reads stay inside shared memory");
   static_assert(TN == 64, "a P row is one 128-byte swizzled row");
   // kfull, kempty [NSK]; vfull, vempty [NSV]; sfull[2]; pfull, pfree [NPB]; drain;
@@ -113,11 +117,11 @@ struct TcTraits {
   static constexpr uint32_t IDESC_O = tc_idesc_f16(128, D, true);
 };
 
-template <int BS, int KVB>
-__global__ void __launch_bounds__(TcTraits<BS, KVB>::THREADS, TcTraits<BS, KVB>::MIN_BLOCKS)
+template <int BS, int KVB, int HD>
+__global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, KVB, HD>::MIN_BLOCKS)
     paged_decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                            const DecodeParams P) {
-  using T = TcTraits<BS, KVB>;
+  using T = TcTraits<BS, KVB, HD>;
   constexpr bool F8 = T::F8;
   constexpr int NSK = T::NSK, NSV = T::NSV, NPB = T::NPB, TN = T::TN, D = T::D;
   extern __shared__ __align__(1024) unsigned char smem_tc[];
@@ -226,7 +230,8 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB>::THREADS, TcTraits<BS, KVB>:
           tma_load_3d(dst + row, map, bar, 0, g * BS + 16 * rg, pbs[kk], l2h);
         } else {
 #pragma unroll
-          for (int h = 0; h < 2; ++h) tma_load_3d(dst + h * T::KVH + row, map, bar, 64 * h, g * BS + 16 * rg, pbs[kk], l2h);
+          for (int h = 0; h < T::NH; ++h)
+            tma_load_3d(dst + h * T::KVH + row, map, bar, 64 * h, g * BS + 16 * rg, pbs[kk], l2h);
         }
       }
     }
@@ -604,7 +609,7 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB>::THREADS, TcTraits<BS, KVB>:
         // V rows that hold no token of the CTA, or a bad block's: p = 0 there,
         // and 0 * NaN would not be 0
         unsigned char* vt = smem + T::V_OFF + sv * T::TILE;
-        for (int x = threadIdx.x; x < 2 * TN * 8; x += 32 * nsw) {
+        for (int x = threadIdx.x; x < T::NH * TN * 8; x += 32 * nsw) {
           const int h = x / (TN * 8), r = (x / 8) % TN, c = x % 8;
           if (r >= valid || ((bad >> (r / BS)) & 1u))
             *reinterpret_cast<uint4*>(vt + h * T::KVH + r * T::ROWB + c * 16) = make_uint4(0u, 0u, 0u, 0u);

@@ -1,5 +1,6 @@
 // Instantiations and launch of the tcgen05 decode kernel (pkd_decode_tc.cuh):
-// fp16 or E4M3 caches, head_dim 128, block sizes 16 and 32.
+// fp16 caches at head_dim 64 or 128, E4M3 caches at head_dim 128, block sizes
+// 16 and 32.
 #include "pkd_decode_tc.cuh"
 #include "pkd_mma_launch.cuh"
 #include "pkd_tc_launch.h"
@@ -9,11 +10,11 @@ static_assert(kTcRows == kTcRowsPerCta, "rows per CTA of the kernel and of its h
 
 namespace {
 
-template <int BS, int KVB>
+template <int BS, int KVB, int HD>
 cudaError_t launch_tc_bs(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeParams& p, long long grid,
                          cudaStream_t stream) {
-  using T = TcTraits<BS, KVB>;
-  auto* fn = paged_decode_tc_kernel<BS, KVB>;
+  using T = TcTraits<BS, KVB, HD>;
+  auto* fn = paged_decode_tc_kernel<BS, KVB, HD>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
@@ -38,13 +39,16 @@ cudaError_t launch_tc_bs(const CUtensorMap& mk, const CUtensorMap& mv, const Dec
 
 cudaError_t launch_decode_tcgen05(int D, int BS, const DecodeParams& p, long long grid, cudaStream_t stream,
                                   int kvb) {
-  if (D != 128 || (BS != 16 && BS != 32) || (kvb != 1 && kvb != 2)) return cudaErrorInvalidValue;
+  if ((D != 128 && !(D == 64 && kvb == 2)) || (BS != 16 && BS != 32) || (kvb != 1 && kvb != 2))
+    return cudaErrorInvalidValue;
   CUtensorMap mk, mv;
   cudaError_t e = mma_host::make_maps(p, D, BS, kvb, &mk, &mv);
   if (e != cudaSuccess) return e;
   if (kvb == 1)
-    return BS == 16 ? launch_tc_bs<16, 1>(mk, mv, p, grid, stream) : launch_tc_bs<32, 1>(mk, mv, p, grid, stream);
-  return BS == 16 ? launch_tc_bs<16, 2>(mk, mv, p, grid, stream) : launch_tc_bs<32, 2>(mk, mv, p, grid, stream);
+    return BS == 16 ? launch_tc_bs<16, 1, 128>(mk, mv, p, grid, stream) : launch_tc_bs<32, 1, 128>(mk, mv, p, grid, stream);
+  if (D == 64)
+    return BS == 16 ? launch_tc_bs<16, 2, 64>(mk, mv, p, grid, stream) : launch_tc_bs<32, 2, 64>(mk, mv, p, grid, stream);
+  return BS == 16 ? launch_tc_bs<16, 2, 128>(mk, mv, p, grid, stream) : launch_tc_bs<32, 2, 128>(mk, mv, p, grid, stream);
 }
 
 }  // namespace pkd

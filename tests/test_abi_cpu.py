@@ -80,7 +80,7 @@ def test_variant_flags(L):
     assert L.paged_decode_workspace_size(2, 8, 2, 128, 16, 100, 32, 0x200 | 4) == base + 256
     assert L.paged_decode_workspace_size(300, 8, 2, 128, 16, 100, -1, 0x200 | 4) == 1280
     assert call_ex(L, var=4, D=96) == 3                # the tensor-core path is a known variant
-    assert call_ex(L, var=5, D=64) == 3                # tcgen05 path: head_dim 128 only
+    assert call_ex(L, var=5, D=96) == 3                # tcgen05 path: head_dim 64 or 128
     assert call_ex(L, var=0x200 | 5, D=96) == 3        # ... and a known variant with flags
     assert call_ex(L, var=6) == 2                      # past the last variant
     assert L.paged_decode_workspace_size(2, 8, 2, 128, 16, 100, 32, 0x100 | 2) > 0
@@ -231,7 +231,7 @@ def test_workspace_sizes_cover_every_plan(L):
         maxlen = rng.randint(1, 20000)
         MB = -(-maxlen // BS) + rng.randint(0, 3)
         P = rng.choice([0, 0, -1, 32 * BS // 16 * rng.randint(1, 64)])
-        var = rng.choice([0, 4, 4 | 0x200, 3, 0x100 | 4] + ([5, 5 | 0x200] if D == 128 else []))
+        var = rng.choice([0, 4, 4 | 0x200, 3, 0x100 | 4, 5, 5 | 0x200])
         need = L.paged_decode_workspace_size(B, G * Hkv, Hkv, D, BS, maxlen, P, var)
         st = L.paged_decode_attention_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, B, G * Hkv, Hkv, D, BS, 64, MB, maxlen,
                                          ctypes.c_float(0.1), P, var, 0, ws_ptr if need else None, need, None, None)
@@ -246,10 +246,7 @@ def test_workspace_sizes_cover_every_plan(L):
             stx = L.paged_decode_attention_multi_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, B, q_len, G * Hkv, Hkv, D, BS,
                                                     64, MB, maxlen, ctypes.c_float(0.1), P, mvar,
                                                     ws_ptr if needm else None, needm, None, None)
-            if (mvar & 0xff) == 5 and D != 128:
-                assert stx == 3, (D, mvar, stx)
-            else:
-                assert stx in (6, 8), (B, q_len, G, Hkv, D, BS, maxlen, P, mvar, needm, stx)
+            assert stx in (6, 8), (B, q_len, G, Hkv, D, BS, maxlen, P, mvar, needm, stx)
         stf = L.paged_decode_attention_fp8(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, B, q_len, G * Hkv, Hkv, D, BS, 64, MB,
                                            maxlen, ctypes.c_float(0.1), ctypes.c_float(0.5), ctypes.c_float(0.5), P,
                                            ws_ptr if needm else None, needm, None, None)
@@ -261,7 +258,7 @@ def test_multi_ex_argument_checks(L):
     def call(*, QL=3, D=128, var=5, P=-1):
         return L.paged_decode_attention_multi_ex(*(FAKE,) * 6, 2, QL, 8, 2, D, 16, 64, 8, 100, ctypes.c_float(0.1),
                                                  P, var, None, 0, None, None)
-    assert call(var=5, D=64) == 3            # tcgen05: head_dim 128 only
+    assert call(var=5, D=96) == 3            # tcgen05: head_dim 64 or 128
     assert call(var=1) == 3 and call(var=3) == 3   # CUDA-core paths: single query only
     assert call(var=6) == 2                  # not a variant
     assert call(var=5, P=64) == 5            # split without a workspace
@@ -297,7 +294,8 @@ def test_call_plan_picks_the_tensor_core_path(L):
     assert ops.paged_decode_call_plan(4, 2, 28, 4, 128, 16, 1000)[3] == "tma_mma"
     assert ops.paged_decode_call_plan(4, 4, 32, 8, 128, 16, 1000)[3] == "tma_mma"
     assert ops.paged_decode_call_plan(4, 16, 4, 4, 128, 16, 1000)[3] == "tma_mma"
-    assert ops.paged_decode_call_plan(4, 8, 28, 4, 64, 16, 1000)[3] == "tma_mma"
+    assert ops.paged_decode_call_plan(4, 8, 28, 4, 64, 16, 1000)[3] == "tcgen05"                # head_dim 64
+    assert ops.paged_decode_call_plan(4, 8, 28, 4, 64, 16, 1000, kv_fp8=True)[3] == "tma_mma"   # E4M3 at 64
     assert ops.paged_decode_call_plan(4, 2, 28, 4, 128, 16, 1000, kv_fp8=True)[3] == "tma_mma"
     assert ops.paged_decode_call_plan(4, 1, 28, 4, 128, 16, 1000, kv_fp8=True)[3] == "tma_mma"
     assert ops.paged_decode_call_plan(4, 1, 28, 4, 128, 16, 1000)[3] == "tma_mma"
@@ -311,8 +309,8 @@ def test_call_plan_picks_the_tensor_core_path(L):
     # refused: tcgen05 with head_dim 64, CUDA-core paths for several queries
     with pytest.raises(ops.PagedDecodeError):
         ops.paged_decode_call_plan(4, 8, 28, 4, 128, 16, 1000, variant="tma_staged")
-    with pytest.raises(ops.PagedDecodeError):
-        ops.paged_decode_call_plan(4, 1, 28, 4, 64, 16, 1000, variant="tcgen05")
+    with pytest.raises(ops.PagedDecodeError):  # E4M3 at head_dim 64
+        ops.paged_decode_call_plan(4, 8, 28, 4, 64, 16, 1000, kv_fp8=True, variant="tcgen05")
 
 
 def test_multi_workspace_covers_both_tensor_core_paths(L):

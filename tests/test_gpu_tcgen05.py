@@ -89,10 +89,37 @@ def test_single_query_matches_oracle(shape, partition):
     assert_close(out, oracle_out(inp), f"{shape} P={partition}")
 
 
-def test_head_dim_64_and_fp8_are_refused():
-    inp = workloads.make_custom(2, 4, 4, 64, 16, [20, 40], seed=1, device="cuda")
-    with pytest.raises(ops.PagedDecodeError):
-        run_ex(inp, TC, -1)
+HD64 = [
+    # (BS, Hq, Hkv, lens): head_dim 64 (one 64-dim half per row)
+    (16, 4, 4, [1, 37, 64, 65, 100]),
+    (32, 14, 2, [1, 63, 64, 65, 190]),
+    (16, 5, 1, [40, 128, 0]),
+]
+
+
+@pytest.mark.parametrize("shape", HD64, ids=lambda s: f"D64BS{s[0]}G{s[1] // s[2]}")
+@pytest.mark.parametrize("partition", [-1, 64])
+def test_head_dim_64_single_query_matches_oracle(shape, partition):
+    BS, Hq, Hkv, lens = shape
+    inp = workloads.make_custom(len(lens), Hq, Hkv, 64, BS, lens, seed=BS + Hq + 64, device="cuda",
+                                max_blocks_per_seq=-(-max(lens) // BS) + 2)
+    ew = errword()
+    out = run_ex(inp, TC, partition, error_word=ew)
+    assert ops.pkd_read_device_error(ew) == 0
+    assert_close(out, oracle_out(inp), f"D64 {shape} P={partition}")
+
+
+@pytest.mark.parametrize("shape", [(32, 14, 2, [1, 63, 64, 65, 190], 3), (16, 4, 4, [37, 100], 17),
+                                   (16, 28, 4, [130, 5], 8)],
+                         ids=lambda s: f"D64BS{s[0]}G{s[1] // s[2]}Q{s[4]}")
+@pytest.mark.parametrize("partition", [-1, 64, 0])
+def test_head_dim_64_multi_query_matches_oracle(shape, partition):
+    BS, Hq, Hkv, lens, q_len = shape
+    inp, q = make_multi(lens, q_len, Hq, Hkv, BS, seed=BS + Hq + q_len + 64, D=64)
+    ew = errword()
+    out = run_multi(inp, q, partition, error_word=ew)
+    assert ops.pkd_read_device_error(ew) == 0
+    assert_close(out, oracle_multi(inp, q), f"D64 {shape} P={partition}")
 
 
 def test_single_token_is_exactly_v0():
