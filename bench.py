@@ -85,7 +85,7 @@ def kernel_name(cfg: workloads.DecodeConfig, variant: str, kv_fp8: bool = False,
     path = variant.split("+")[0]
     shape = f"{cfg.head_dim},{cfg.block_size},{cfg.group}"
     if path == "tcgen05":
-        return f"paged_decode_tc_kernel<{cfg.block_size}>"
+        return f"paged_decode_tc_kernel<{cfg.block_size},{1 if kv_fp8 else 2},{cfg.head_dim}>"
     if path == "tma_mma":
         # single-query E4M3 grids of 3+ waves of four CTAs per SM run the four-per-SM build
         qc = 1 if q_len <= 1 else 16 // cfg.group
