@@ -25,6 +25,16 @@ constexpr unsigned long long kWaitBudgetNs = 100ull * 1000ull * 1000ull;  // 100
 int default_prefetch_distance(int path) { return path == PKD_VARIANT_TMA_MMA || path == PKD_VARIANT_TCGEN05 ? 0 : 1; }
 constexpr int kMinAutoPartition = 512;
 constexpr int kMaxAutoPartition = 2048;
+// The tcgen05 kernel pays a longer fill per CTA (its two-stage K ring meets the
+// first copies' full HBM latency), so it is split less: only below kSplitWaves
+// waves whatever the context length, into partitions of up to
+// kMaxAutoPartitionTc tokens.  Measured on its multi-token workloads: GQA 7:1
+// at 8192 tokens, q_len 8, unsplit 708 against 788 us at 2048-token
+// partitions (q_len 4: 703 against 735); GQA 5:1 at 16K-32K tokens, q_len 8,
+// 4096-token partitions 545 against 564 at 2048 and 607 unsplit.  Through the
+// automatic path (longest first when unsplit): GQA 7:1, q_len 8, 717 against
+// 788 us; q_len 4, 709 against 735.
+constexpr int kMaxAutoPartitionTc = 8192;
 constexpr int kSplitWaves = 2;       // split when the (sequence, kv head) units cover fewer waves than this,
 constexpr int kTargetWaves = 6;      // into enough partitions for this many waves;
 constexpr int kLongContext = 8192;   // contexts this long split below kTargetWaves waves
@@ -129,13 +139,15 @@ int auto_partition(const Shape& s, int variant = PKD_VARIANT_AUTO, int q_chunks 
   const long long units = (long long)s.num_seqs * s.num_kv_heads * q_chunks;
   if (units <= 0 || s.max_context_len <= kMinAutoPartition) return -1;
   const long long wave = wave_ctas(variant, s.num_q_heads / s.num_kv_heads);
-  const long long split_below = (s.max_context_len >= kLongContext ? kTargetWaves : kSplitWaves) * wave;
+  const bool tc = variant_path(variant) == PKD_VARIANT_TCGEN05;
+  const long long split_below = (!tc && s.max_context_len >= kLongContext ? kTargetWaves : kSplitWaves) * wave;
   if (units >= split_below) return -1;
   const long long want = kTargetWaves * wave;
   const long long np = (want + units - 1) / units;
   const long long per = (s.max_context_len + np - 1) / np;
+  const long long pmax = tc ? kMaxAutoPartitionTc : kMaxAutoPartition;
   long long p = kMinAutoPartition;
-  while (p * 2 <= per && p * 2 <= kMaxAutoPartition) p *= 2;
+  while (p * 2 <= per && p * 2 <= pmax) p *= 2;
   if (p >= s.max_context_len) return -1;
   return (int)p;
 }
@@ -204,11 +216,10 @@ int query_chunks(int q_len, int G, int path = PKD_VARIANT_TMA_MMA) {
 // per sequence or E4M3 caches.  The mma.sync kernel serves one 16-row tile of
 // q_len x G rows per CTA and reads the partition's K and V once per tile; the
 // tcgen05 kernel serves up to 64 rows from one read, with S and O in tensor
-// memory (fp16 caches, head_dim 128).  Measured on the full workloads it wins
-// or ties from kTcMinTiles tiles on (GQA 7:1: q_len 8, four tiles, 786 against
-// 1163 us; q_len 4, two tiles, 730 against 729 us; GQA 4:1, q_len 8, two
-// tiles, 204 against 226 us) and loses at one (GQA 4:1, q_len 4: 203 against
-// 183 us).
+// memory.  Measured on the full workloads it wins from kTcMinTiles tiles on
+// (GQA 7:1: q_len 8, four tiles, 717 against 1163 us; q_len 4, two tiles, 709
+// against 721 us; GQA 4:1, q_len 8, two tiles, 207 against 227 us) and loses
+// at one (GQA 4:1, q_len 4: 203 against 183 us).
 // E4M3 caches are widened to fp16 in shared memory by the producer warps on
 // the tcgen05 path, on the critical path of every tile; there it only wins
 // from kTcMinTilesFp8 tiles on (GQA 7:1, q_len 8, four tiles: 1027 against
