@@ -334,3 +334,27 @@ def test_multi_workspace_covers_both_tensor_core_paths(L):
                 need = -(-rows * 128 * 4 // 256) * 256 + 2 * (-(-rows * 4 // 256) * 256)
             assert ws >= need, (B, q_len, G, Hkv, maxlen, variant)
         assert L_size == ws
+
+
+def test_tcgen05_split_policy(L):
+    # the tcgen05 path splits only below two waves of units (two CTAs per SM), into
+    # partitions of up to 8192 tokens; the mma.sync path also splits long contexts
+    # below six waves, into partitions of at most 2048 tokens
+    from paged_kv_decode_21_gb300 import ops
+    sms = 148  # no device here: the library's default SM count
+    # GQA 7:1, 256 x 8192 tokens, q_len 8: 1024 units, three waves and more
+    n, part, ordered, var, grid = ops.paged_decode_call_plan(256, 8, 28, 4, 128, 16, 8192)
+    assert var.startswith("tcgen05") and part == -1 and grid == 1024
+    n, part, ordered, var, grid = ops.paged_decode_call_plan(256, 8, 28, 4, 128, 16, 8192, variant="tma_mma")
+    assert part == -1 and grid == 256 * 4 * 4  # four 16-row chunks: many waves, unsplit too
+    n, part, ordered, var, grid = ops.paged_decode_call_plan(256, 1, 28, 4, 128, 16, 8192)
+    assert var == "tma_mma" and part == 2048  # single query: 1024 units, long context, split
+    # GQA 5:1, 32 x 32768 tokens, q_len 8: 256 units, below two waves: split
+    n, part, ordered, var, grid = ops.paged_decode_call_plan(32, 8, 40, 8, 128, 16, 32768)
+    want = 6 * 2 * sms
+    np_ = -(-want // 256)
+    per = -(-32768 // np_)
+    p = 512
+    while p * 2 <= per and p * 2 <= 8192:
+        p *= 2
+    assert var == "tcgen05" and part == p and part > 2048
