@@ -23,11 +23,14 @@
 //                    cycles to issue from one thread, which bounded the tile
 //                    rate when one thread fed both rings.  Optionally, tiles
 //                    beyond the K ring are prefetched into L2
-//                    (cp.async.bulk.prefetch.L2).
+//                    (cp.async.bulk.prefetch.L2).  E4M3 caches: the bytes land
+//                    in a stage's first 8 KiB behind a landing barrier, and
+//                    the whole producer warp widens them to the fp16 layout in
+//                    place before arriving on the stage's full barrier.
 //   warp 3, lane 0   MMA issuer: S = Q K^T (M = 128 rows, N = TN tokens,
-//                    K = 128 dims) into one of two S buffers in tensor memory,
+//                    K = head_dim) into one of two S buffers in tensor memory,
 //                    then, once the softmax has written P, O += P V
-//                    (M = 128, N = 128 dims, K = TN tokens) into O in tensor
+//                    (M = 128, N = head_dim, K = TN tokens) into O in tensor
 //                    memory; completion is committed to mbarriers.  It polls
 //                    both conditions and issues whichever is ready first: S of
 //                    the next tile as soon as its K landed (and its S buffer
@@ -39,9 +42,10 @@
 //                    log2 domain with a lazy running maximum (the output is
 //                    rescaled in tensor memory only when the maximum grows by
 //                    more than kLazyTau), P rounded to fp16 into shared memory
-//                    (the MMA's A operand; one buffer, written once P.V of the
-//                    previous tile completed), and at the end O / l to the
-//                    output or the unnormalised partial for the split-K merge.
+//                    (the MMA's A operand; two buffers, each rewritten once
+//                    P.V of the tile two back completed), and at the end O / l
+//                    to the output or the unnormalised partial for the split-K
+//                    merge.
 // The MMAs run M = 128 with the rows past kTcRows reading whatever follows
 // Q and P in shared memory: those accumulator rows are never read.
 //
