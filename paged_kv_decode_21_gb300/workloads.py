@@ -164,18 +164,51 @@ def randn_f16(shape, generator: torch.Generator, device) -> torch.Tensor:
     return out
 
 
-def rand_e4m3(shape, generator: torch.Generator, device, exp_lo: int = 4, exp_hi: int = 10) -> torch.Tensor:
-    """Random E4M3 bit patterns (uint8): random sign and mantissa, biased
-    exponent uniform in [exp_lo, exp_hi] (magnitudes 2^(exp_lo-7) .. 2^(exp_hi-6)),
-    never a NaN code.  A bit-pattern generator: no rounding or scaling."""
+# Per-cache scales (k_scale, v_scale) that go with each code set of rand_e4m3:
+# they keep the scores of N(0,1) queries at a few units and |V| at most 1.75
+# (448 / 256), so an fp16 output stays well inside the parity tolerance's
+# range.  For the code sets, 448 = 0x7e and the subnormals are m * 2^-9.
+E4M3_SCALES = {
+    "full": (1.0 / 64, 1.0 / 256),
+    "narrow": (0.05, 0.11),
+    "max": (1.0 / 448, 1.0 / 256),
+    "subnormal": (64.0, 64.0),
+}
+
+
+def rand_e4m3(shape, generator: torch.Generator, device, codes: str = "full") -> torch.Tensor:
+    """Random E4M3 bit patterns (uint8), never a NaN code (0x7f, 0xff).  A
+    bit-pattern generator: no rounding or scaling.
+
+    codes:
+      "full"       uniform over the 254 finite codes: +-0, the subnormals
+                   (exponent field 0), every normal exponent 1..15, and the
+                   largest magnitude 448 (0x7e, 0xfe)
+      "narrow"     random sign and mantissa, biased exponent uniform in
+                   [4, 10] (magnitudes 2^-3 .. 2^4)
+      "max"        only +-448
+      "subnormal"  only the exponent field 0: +-0 and the seven subnormal
+                   magnitudes m * 2^-9
+    """
     n = 1
     for x in shape:
         n *= int(x)
     bits = torch.randint(0, 1 << 16, (n,), generator=generator, device=device, dtype=torch.int32)
     sign = (bits & 1) << 7
-    mant = (bits >> 1) & 7
-    expo = exp_lo + ((bits >> 4) % (exp_hi - exp_lo + 1))
-    return (sign | (expo << 3) | mant).to(torch.uint8).view(*shape)
+    if codes == "full":
+        r = (bits >> 1) % 254                  # 0..253 -> codes 0x00..0x7e, 0x80..0xfe
+        code = torch.where(r < 127, r, r + 1)
+    elif codes == "narrow":
+        mant = (bits >> 1) & 7
+        expo = 4 + ((bits >> 4) % 7)
+        code = sign | (expo << 3) | mant
+    elif codes == "max":
+        code = sign | 0x7E
+    elif codes == "subnormal":
+        code = sign | ((bits >> 1) & 7)
+    else:
+        raise ValueError(f"unknown E4M3 code set {codes!r}")
+    return code.to(torch.uint8).view(*shape)
 
 
 def make_inputs(cfg: DecodeConfig, device="cpu", context_lens: Optional[torch.Tensor] = None,

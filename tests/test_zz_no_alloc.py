@@ -4,9 +4,10 @@ paged_decode_attention_static_scratch keeps its partials in a fixed device
 array owned by the library (for callers such as plugins or code under a
 foreign allocator that may not call cudaMalloc nor pass a workspace).  Here it
 is called through the C ABI twice in a row, on two different shapes, and each
-result is checked against the ordinary entry point, paged_decode_attention_ex
-with a caller workspace, within the parity tolerance of the GPU suite.  A
-shape whose partials would not fit in the array is refused before launch.
+result is checked against the fp64 CPU oracle and against the ordinary entry
+point, paged_decode_attention_ex with a caller workspace, within the parity
+tolerance of the GPU suite.  A shape whose partials would not fit in the array
+is refused before launch.
 
 This file is collected last on purpose; it also passes alone in a fresh
 process.
@@ -15,7 +16,7 @@ import numpy as np
 import pytest
 import torch
 
-from helpers import MAX_ABS_TOL, MEAN_ABS_TOL
+from helpers import MAX_ABS_TOL, MEAN_ABS_TOL, assert_close, oracle_out
 from paged_kv_decode_21_gb300 import ops, workloads
 
 pytestmark = pytest.mark.gpu
@@ -55,10 +56,12 @@ def test_static_scratch_matches_workspace_path_twice(variant):
     # first call: GQA 7:1 with long, ragged and empty sequences, split at 256
     a = workloads.make_custom(4, 28, 4, 128, 16, [700, 33, 0, 1500], seed=41, device="cuda")
     got_a, ref_a = _both(a, 256, variant)
+    assert_close(got_a, oracle_out(a), "first call against the oracle")
     _close(got_a, ref_a, "first call")
     # second call in a row: a smaller, different shape reusing the same array
     b = workloads.make_custom(3, 8, 8, 64, 32, [100, 37, 300], seed=43, device="cuda")
     got_b, ref_b = _both(b, 64, variant)
+    assert_close(got_b, oracle_out(b), "second call against the oracle")
     _close(got_b, ref_b, "second call")
     # and the first shape again, after the array holds the second call's partials
     got_a2, _ = _both(a, 256, variant)
@@ -68,6 +71,7 @@ def test_static_scratch_matches_workspace_path_twice(variant):
 def test_static_scratch_automatic_partition():
     c = workloads.make_custom(2, 40, 8, 128, 16, [5000, 9000], seed=47, device="cuda")
     got, ref = _both(c, 0, "auto")
+    assert_close(got, oracle_out(c), "automatic partition against the oracle")
     _close(got, ref, "automatic partition")
 
 
