@@ -31,9 +31,12 @@
  * device.  K and V rows that are used must hold finite values.
  *
  * Ownership and threading: every buffer belongs to the caller.  The library
- * allocates no memory, keeps no state between calls, and may be called from
- * several host threads at once.  Work is enqueued on `stream` and the calls
- * return without waiting for it.
+ * allocates no memory and may be called from several host threads at once.
+ * The only state it keeps between calls is read-only: each device's SM
+ * count, L2 size and memory bandwidth, queried on the first call that needs
+ * them (the prefetch-distance model), and the device address of the
+ * static-scratch array.  Work is enqueued on `stream` and the calls return
+ * without waiting for it.
  *
  * Errors: arguments are checked on the host before any launch; a failed
  * check returns a status and launches nothing.  PKD_ERR_LAUNCH reports a
@@ -199,10 +202,13 @@ pkd_status paged_decode_attention_host(const void* q, const void* k_cache, const
  *                   workspace has room for the order.
  *   variant         pkd_variant, optionally ORed with PKD_FLAG_* bits
  *   prefetch_distance  how many of a warp's iterations ahead the L2 prefetch
- *                   runs; 0 = the data path's default: 1 for the CUDA-core
- *                   paths, none for PKD_VARIANT_TMA_MMA (its ring of tensor
- *                   copies already runs ahead; an L2 prefetch beyond it
- *                   measured slower); ignored by PKD_VARIANT_NO_PREFETCH
+ *                   runs: -1 = no L2 prefetch; 0 = the default of the L2
+ *                   capacity model (paged_decode_prefetch_model: the
+ *                   smallest distance whose bytes in flight cover the HBM
+ *                   latency, 0 when the ring of copies alone covers it,
+ *                   capped so the prefetched blocks stay within an eighth of
+ *                   L2); >= 1 = that distance.  Ignored by
+ *                   PKD_VARIANT_NO_PREFETCH and PKD_VARIANT_TCGEN05.
  *   workspace, workspace_bytes  device scratch of at least
  *                   paged_decode_workspace_size(...) bytes, 256-byte aligned
  *                   (may be NULL when no sequence is split; the automatic
@@ -358,14 +364,65 @@ pkd_status paged_decode_attention_multi_ex(const void* q, const void* k_cache, c
  * partition, or -1 when unsplit), *longest_first (1 when the batch is walked
  * longest first, given a workspace of the size the *_workspace_size
  * functions return), *variant_out (the data path with the PKD_FLAG_* bits
- * that apply) and *grid_out (decode CTAs); any pointer may be NULL.
+ * that apply), *grid_out (decode CTAs) and *prefetch_distance_out (the L2
+ * prefetch distance the call runs with prefetch_distance 0; 0 = none); any
+ * pointer may be NULL.
  * Returns the kernel launches (decode grid, split-K merge, order kernel; 0
  * for an empty batch), or -2 for a shape, partition or variant the call
  * would refuse.
  */
 int paged_decode_call_plan(int num_seqs, int q_len, int num_q_heads, int num_kv_heads, int head_dim,
                            int block_size, int max_context_len, int kv_fp8, int partition_size, int variant,
-                           int* partition_out, int* longest_first, int* variant_out, long long* grid_out);
+                           int* partition_out, int* longest_first, int* variant_out, long long* grid_out,
+                           int* prefetch_distance_out);
+
+/*
+ * pkd_l2_prefetch_model -- the rule that sizes the default L2 prefetch
+ * distance, as plain host arithmetic (no GPU is needed).  Source: section
+ * 4.2 of the review "Accelerating LLM Inference Throughput via Asynchronous
+ * KV Cache Prefetching": a (block, head) tile is M_block = b * d_h * T_block
+ * bytes, and the prefetched tiles of one iteration of every warp occupy
+ * M_total = M_block * (N_thread / 32) * H * B of L2, which must fit in it.
+ * For resident_ctas CTAs in flight on sm_count SMs, each with
+ * streams_per_cta warps (block streams) that prefetch tiles_per_step tiles of
+ * m_block bytes per unit of distance d:
+ *   footprint(d) = resident_ctas * d * streams_per_cta * tiles_per_step * m_block
+ *     (M_total, with H * B the CTAs in flight and d tiles per warp)
+ *   inflight(d)  = resident_ctas / active_sms * (ahead_bytes_per_cta + footprint(d) / resident_ctas)
+ *   need         = hbm_bytes_per_s / active_sms * latency_s   (Little's law)
+ * with active_sms = min(sm_count, resident_ctas).  Returns the smallest d in
+ * [0, max_distance] with inflight(d) >= need, then lowered until
+ * footprint(d) <= l2_fraction * l2_bytes (0 when no d >= 1 fits), and writes
+ * footprint(d), inflight(d) and need (bytes; pointers may be NULL).  Returns
+ * -2 for a negative size or fraction, or sm_count, streams_per_cta, m_block or
+ * tiles_per_step <= 0.
+ */
+int pkd_l2_prefetch_model(long long resident_ctas, int sm_count, int streams_per_cta, long long m_block,
+                          int tiles_per_step, long long ahead_bytes_per_cta, long long l2_bytes,
+                          double l2_fraction, double hbm_bytes_per_s, double latency_s, int max_distance,
+                          long long* footprint_bytes, long long* inflight_bytes_per_sm,
+                          long long* need_bytes_per_sm);
+
+/*
+ * paged_decode_prefetch_model -- the default L2 prefetch distance
+ * (prefetch_distance 0) of a decode call, for a GPU described by sm_count,
+ * l2_bytes and hbm_bytes_per_s (its nominal bandwidth) instead of the
+ * current device: pkd_l2_prefetch_model over the call's resident CTAs, with
+ * the data path's warps per CTA, two tiles (K and V) of block_size x
+ * head_dim elements per unit of distance, the bytes its ring or loads keep
+ * in flight, an eighth of L2 and a loaded HBM latency of 1.5 us, and no
+ * more blocks ahead than a warp's share of the partition holds.  The call's
+ * partition and data path are planned as by paged_decode_call_plan (the
+ * automatic split on the current device, or the fallback SM count without
+ * one).  Writes the model's footprint, in-flight and need bytes (pointers
+ * may be NULL).  Returns the distance (0 for paths that never prefetch to
+ * L2), or -2 for an invalid shape, variant or description.
+ */
+int paged_decode_prefetch_model(int num_seqs, int q_len, int num_q_heads, int num_kv_heads, int head_dim,
+                                int block_size, int max_context_len, int kv_fp8, int partition_size, int variant,
+                                int sm_count, long long l2_bytes, double hbm_bytes_per_s,
+                                long long* footprint_bytes, long long* inflight_bytes_per_sm,
+                                long long* need_bytes_per_sm);
 
 /*
  * paged_decode_auto_plan -- what a call with partition_size 0 runs on the
@@ -500,6 +557,10 @@ pkd_status pkd_read_device_error(int* error_word, unsigned* host_bits, int clear
  *     with PKD_ERR_WORKSPACE before anything is launched.
  *   - The first call on a device looks up the array's device address (with
  *     that device current); make that first call before any stream capture.
+ *     The address is kept for the life of the process, so this entry must
+ *     not be used on a device after cudaDeviceReset (or any other teardown
+ *     of its primary context) in the same process: the kept address would
+ *     no longer name the array.
  *   - Every call shares the one array, and each call leaves its partials in
  *     it; nothing in it needs to start at zero.  Calls that overlap on the
  *     GPU (other streams, other host threads) race on the array: serialise

@@ -1,28 +1,22 @@
 // pkd_api.cu -- the C ABI of libpaged_decode.so (declared in paged_decode.h):
 // argument checks, the split-K policy, workspace layout and launches.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
+#include <mutex>
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
 
 #include "../../include/paged_decode.h"
 #include "pkd_aux.cuh"
+#include "pkd_decode_mma.cuh"
 #include "pkd_launch.cuh"
 #include "pkd_tc_launch.h"
 
 namespace {
 
 constexpr unsigned long long kWaitBudgetNs = 100ull * 1000ull * 1000ull;  // 100 ms per bounded wait
-// The default L2 prefetch distance of a data path (prefetch_distance 0).  The
-// CUDA-core paths prefetch the block a warp takes next: distance 1 measured
-// best or tied on every workload.  The tensor-core path does not prefetch to
-// L2 by default: its ring of tensor copies already runs a warp's next
-// sub-tiles ahead into shared memory, and a prefetch beyond the ring measured
-// 0-1.4% slower with fp16 caches (distance 1; 2-4 lose 1-18% more) and 3-4%
-// slower with E4M3.
-// The tcgen05 path has no L2 prefetch (its ring runs ahead the same way).
-int default_prefetch_distance(int path) { return path == PKD_VARIANT_TMA_MMA || path == PKD_VARIANT_TCGEN05 ? 0 : 1; }
 constexpr int kMinAutoPartition = 512;
 constexpr int kMaxAutoPartition = 2048;
 // The tcgen05 kernel pays a longer fill per CTA (its two-stage K ring meets the
@@ -47,6 +41,15 @@ constexpr int kOrderMinContext = 1024;  // when their contexts reach this many t
 constexpr int kWideFp8Waves = 3;
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int sm_count();
+// Whether an E4M3 launch runs the four-per-SM build (single-query grids of
+// kWideFp8Waves waves or more of four CTAs per SM).
+bool wide_fp8_grid(int kv_fp8, int q_len, long long grid) {
+  int sms = sm_count();
+  if (sms <= 0) sms = 148;
+  return kv_fp8 && q_len == 1 && grid >= (long long)kWideFp8Waves * 4 * sms;
+}
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -73,6 +76,179 @@ int sm_count() {
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
   return n;
+}
+
+// ------------------------------------------------------------ L2 prefetch distance
+// The default distance (prefetch_distance 0) comes from two bounds.
+//  * Capacity, after section 4.2 of the review "Accelerating LLM Inference
+//    Throughput via Asynchronous KV Cache Prefetching": a (block, head) tile
+//    is M_block = b * d_h * T_block bytes, and one prefetched tile per warp of
+//    every CTA in flight occupies M_total = M_block * (N_thread / 32) * H * B
+//    of L2 (all H * B CTAs resident there).  Prefetched tiles past the L2
+//    size evict one another before use.  Here only resident CTAs prefetch,
+//    and each unit of distance is one more block of K and of V per warp, so
+//    footprint(d) = resident CTAs * d * warps * 2 * M_block.  On GB300 the
+//    prefetched tiles share L2 with the stream's own lines: distances whose
+//    footprint passed about an eighth of L2 measured 1-3% slower, a third
+//    5-12% (MHA: the staged path at distances 2 and 4, the tensor-core path
+//    at 1-3), so the cap is kL2PrefetchFraction of L2.
+//  * Need (Little's law): HBM holds its bandwidth only while each SM keeps
+//    about (its share of the bandwidth) x (loaded latency) bytes requested
+//    ahead of use.  A CUDA-core warp has one 16-row group of K and V in
+//    flight; a staged warp keeps its ring's other slots in flight.  The
+//    distance is the smallest that reaches the need, and 0 when the ring
+//    alone reaches it.  kLoadedLatencyS is 1.5 us: at 64 KiB per SM the
+//    CUDA-core path measured 0.7-10% faster with distance 1 than with none
+//    (more at higher group sizes, whose longer iterations hold fewer bytes
+//    in flight), while the tensor-core path's 96 KiB per SM gained nothing
+//    from any distance.
+constexpr double kL2PrefetchFraction = 0.125;
+constexpr double kLoadedLatencyS = 1.5e-6;
+constexpr int kMaxPrefetchDistance = 8;
+
+// How a data path streams K/V: resident CTAs per SM, block streams (warps)
+// per CTA, and bytes each CTA keeps requested ahead of use with no L2
+// prefetch.  The values restate the kernels' traits (checked below).
+struct PathStream {
+  int ctas_per_sm;
+  int streams;
+  long long ahead_bytes;
+  bool prefetches;  // the path issues L2 prefetches at all
+};
+
+constexpr int clamp_slots(long long s) { return s > 8 ? 8 : (s < 2 ? 2 : (int)s); }
+// slots of a staged ring of ring_kib KiB over `streams` streams of slot_bytes each
+constexpr int ring_slots(int ring_kib, int streams, long long slot_bytes) {
+  return clamp_slots((ring_kib * 1024LL) / (streams * slot_bytes));
+}
+static_assert(ring_slots(64, 4, 2 * 16 * 128 * 2) == pkd::MmaTraits<128, 16, 7, 1, 2>::SW, "mma ring (fp16)");
+static_assert(ring_slots(64, 4, 2 * 16 * 128 * 1) == pkd::MmaTraits<128, 16, 7, 1, 1>::SW, "mma ring (E4M3)");
+static_assert(ring_slots(48, 4, 2 * 16 * 128 * 1) == pkd::MmaTraits<128, 16, 1, 1, 1, 4>::SW, "mma ring (4/SM)");
+static_assert(ring_slots(96, 4, 2 * 16 * 128 * 2) == pkd::DecodeTraits<128, 16, 1, pkd::kTmaStaged>::SW, "staged");
+static_assert(ring_slots(64, 4, 2 * 16 * 128 * 2) == pkd::DecodeTraits<128, 16, 4, pkd::kTmaStaged>::SW, "staged 3/SM");
+static_assert(pkd::DecodeTraits<128, 16, 4, pkd::kTmaStaged>::MIN_BLOCKS == 3 &&
+              pkd::DecodeTraits<128, 16, 1, pkd::kTmaStaged>::MIN_BLOCKS == 2 &&
+              pkd::DecodeTraits<128, 16, 4, pkd::kL2Prefetch>::MIN_BLOCKS == 2 &&
+              pkd::WsTraits<128, 16, 7>::MIN_BLOCKS == 2 && pkd::WsTraits<128, 16, 7>::NS == 3 &&
+              pkd::WsTraits<128, 16, 7>::SW == 4 && pkd::WsTraits<64, 16, 7>::SW == 8,
+              "residency and streams of the CUDA-core kernels");
+
+PathStream path_stream(int path, int D, int G, int kvb, bool wide_fp8) {
+  const long long slot = 2LL * 16 * D * kvb;  // one 16-row group of K and of V
+  switch (path) {
+    case PKD_VARIANT_NO_PREFETCH:
+    case PKD_VARIANT_L2_PREFETCH:
+      return {2, 4, 4 * slot, path == PKD_VARIANT_L2_PREFETCH};
+    case PKD_VARIANT_TMA_STAGED:
+      if (G >= pkd::kWsMinGroup) return {2, 3, 3LL * ((D == 128 ? 4 : 8) - 1) * slot, true};
+      if (G >= 2 && G <= 5) return {3, 4, 4LL * (ring_slots(64, 4, slot) - 1) * slot, true};
+      return {2, 4, 4LL * (ring_slots(96, 4, slot) - 1) * slot, true};
+    case PKD_VARIANT_TMA_MMA: {
+      const int cps = wide_fp8 ? 4 : 3;
+      return {cps, 4, 4LL * (ring_slots(cps >= 4 ? 48 : 64, 4, slot) - 1) * slot, true};
+    }
+    default:  // the tcgen05 path streams whole 64-token tiles and never prefetches to L2
+      return {2, 2, 0, false};
+  }
+}
+
+struct DeviceNumbers {
+  int sms;
+  long long l2_bytes;
+  double hbm_bytes_per_s;
+};
+
+// The current device's SM count, L2 size and nominal HBM bandwidth (2 x
+// memory clock x bus width); GB300-like values where a query fails (no GPU).
+// Queried once per device and kept: the memory-clock query costs hundreds of
+// microseconds, far more than a decode launch, and none of these change.
+DeviceNumbers query_device_numbers(int dev) {
+  DeviceNumbers n{148, 126LL << 20, 8.0e12};
+  int v = 0;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) n.sms = v;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) == cudaSuccess && v > 0) n.l2_bytes = v;
+  int clk_khz = 0, bus_bits = 0;
+  if (cudaDeviceGetAttribute(&clk_khz, cudaDevAttrMemoryClockRate, dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&bus_bits, cudaDevAttrGlobalMemoryBusWidth, dev) == cudaSuccess && clk_khz > 0 &&
+      bus_bits > 0)
+    n.hbm_bytes_per_s = 2.0 * clk_khz * 1e3 * (bus_bits / 8.0);
+  return n;
+}
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mu;
+std::atomic<int> g_dev_ready[kMaxDevices];
+DeviceNumbers g_dev_numbers[kMaxDevices];
+
+DeviceNumbers device_numbers() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();  // no device: leave no sticky error behind
+    return DeviceNumbers{148, 126LL << 20, 8.0e12};
+  }
+  if (dev < 0 || dev >= kMaxDevices) return query_device_numbers(dev);
+  if (!g_dev_ready[dev].load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    if (!g_dev_ready[dev].load(std::memory_order_relaxed)) {
+      g_dev_numbers[dev] = query_device_numbers(dev);
+      g_dev_ready[dev].store(1, std::memory_order_release);
+    }
+  }
+  return g_dev_numbers[dev];
+}
+
+}  // namespace
+
+extern "C" int pkd_l2_prefetch_model(long long resident_ctas, int sm_count, int streams_per_cta,
+                                     long long m_block, int tiles_per_step, long long ahead_bytes_per_cta,
+                                     long long l2_bytes, double l2_fraction, double hbm_bytes_per_s,
+                                     double latency_s, int max_distance, long long* footprint_bytes,
+                                     long long* inflight_bytes_per_sm, long long* need_bytes_per_sm) {
+  if (resident_ctas < 0 || sm_count <= 0 || streams_per_cta <= 0 || m_block <= 0 || tiles_per_step <= 0 ||
+      ahead_bytes_per_cta < 0 || l2_bytes < 0 || !(l2_fraction >= 0.0) || !(hbm_bytes_per_s >= 0.0) ||
+      !(latency_s >= 0.0) || max_distance < 0)
+    return -2;
+  const long long step = (long long)streams_per_cta * tiles_per_step * m_block;  // per CTA per unit of distance
+  const long long active = std::max(1LL, std::min<long long>(sm_count, resident_ctas));
+  const double ctas_per_sm = (double)resident_ctas / (double)active;
+  const double need = hbm_bytes_per_s / (double)active * latency_s;
+  int d = 0;
+  while (d < max_distance && ctas_per_sm * (double)(ahead_bytes_per_cta + d * step) < need) ++d;
+  const double cap = l2_fraction * (double)l2_bytes;
+  while (d > 0 && (double)resident_ctas * d * step > cap) --d;
+  if (footprint_bytes) *footprint_bytes = resident_ctas * d * step;
+  if (inflight_bytes_per_sm) *inflight_bytes_per_sm = (long long)(ctas_per_sm * (double)(ahead_bytes_per_cta + d * step));
+  if (need_bytes_per_sm) *need_bytes_per_sm = (long long)need;
+  return d;
+}
+
+namespace {
+
+// The distance a launch of `grid` CTAs of this data path runs with by
+// default: the model above on the device's numbers, and no more blocks
+// ahead than a stream of the CTA has after its first (blocks_per_cta over
+// the CTA's streams).
+int model_prefetch_distance(int path, int D, int BS, int G, int kvb, bool wide_fp8, long long grid,
+                            long long blocks_per_cta, const DeviceNumbers& dn) {
+  const PathStream ps = path_stream(path, D, G, kvb, wide_fp8);
+  if (!ps.prefetches || grid <= 0) return 0;
+  const long long resident = std::min<long long>(grid, (long long)ps.ctas_per_sm * dn.sms);
+  int d = pkd_l2_prefetch_model(resident, dn.sms, ps.streams, (long long)BS * D * kvb, 2, ps.ahead_bytes,
+                                dn.l2_bytes, kL2PrefetchFraction, dn.hbm_bytes_per_s, kLoadedLatencyS,
+                                kMaxPrefetchDistance, nullptr, nullptr, nullptr);
+  const long long per_stream = (blocks_per_cta + ps.streams - 1) / ps.streams;
+  return (int)std::max(0LL, std::min<long long>(d, per_stream - 1));
+}
+
+// The L2 prefetch distance a launch runs: none for -1, the model's default
+// for 0, otherwise as requested.  tokens_per_cta is the partition (or the
+// whole context, unsplit).
+int effective_prefetch(int requested, int path, int D, int BS, int G, int kvb, bool wide_fp8, long long grid,
+                       int tokens_per_cta) {
+  if (requested < 0) return 0;
+  if (requested > 0) return requested;
+  return model_prefetch_distance(path, D, BS, G, kvb, wide_fp8, grid, (tokens_per_cta + BS - 1) / BS,
+                                 device_numbers());
 }
 
 // `variant` carries the data path in its low byte and PKD_FLAG_* bits above.
@@ -352,7 +528,7 @@ pkd_status check_inputs(const void* q, const void* k_cache, const void* v_cache,
 
 extern "C" {
 
-int pkd_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+int pkd_version(void) { return 1 * 10000 + 1 * 100 + 0; }
 
 const char* pkd_status_string(int status) {
   switch (status) {
@@ -428,7 +604,7 @@ pkd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
   if (!aligned(out, 16) || (error_word && !aligned(error_word, 4))) return PKD_ERR_ALIGN;
   if (!std::isfinite(scale)) return PKD_ERR_SHAPE;
   if (!variant_ok(variant)) return PKD_ERR_SHAPE;
-  if (prefetch_distance < 0) return PKD_ERR_SHAPE;
+  if (prefetch_distance < -1) return PKD_ERR_SHAPE;
   const int G = num_q_heads / num_kv_heads;
   CallPlan plan;
   st = plan_call(s, q_len, variant, partition_size, kv_fp8, &plan);
@@ -459,7 +635,8 @@ pkd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
   // E4M3 caches: K = code * k_scale enters the scores, V = code * v_scale the output
   p.scale_log2 = scale * (kv_fp8 ? k_scale : 1.f) * 1.4426950408889634f;
   p.v_scale = kv_fp8 ? v_scale : 1.f;
-  p.prefetch_distance = prefetch_distance == 0 ? default_prefetch_distance(variant_path(variant)) : prefetch_distance;
+  p.prefetch_distance = effective_prefetch(prefetch_distance, variant_path(variant), head_dim, block_size, G,
+                                          kv_fp8 ? 1 : 2, wide_fp8_grid(kv_fp8, q_len, grid), grid, P);
   p.l2_hints = (variant & PKD_FLAG_L2_EVICT_HINTS) ? 1 : 0;
   p.timeout_ns = kWaitBudgetNs;
   size_t used = 0;
@@ -492,9 +669,7 @@ pkd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
     if (grid > 0x7fffffffLL) return PKD_ERR_SHAPE;
     // single-query grids of kWideFp8Waves waves or more of four CTAs per SM
     // run the four-per-SM build
-    int sms = sm_count();
-    if (sms <= 0) sms = 148;
-    const bool w4 = q_len == 1 && grid >= (long long)kWideFp8Waves * 4 * sms;
+    const bool w4 = wide_fp8_grid(kv_fp8, q_len, grid);
     const cudaError_t e = grid <= 0 ? cudaSuccess
                           : w4      ? pkd::launch_decode_tma_mma_fp8_w4(head_dim, block_size, G, p, grid, stream)
                                     : pkd::launch_decode_tma_mma_fp8(head_dim, block_size, G, p, grid, stream);
@@ -566,7 +741,8 @@ pkd_status paged_decode_attention_fp8(const void* q, const void* k_cache, const 
 
 int paged_decode_call_plan(int num_seqs, int q_len, int num_q_heads, int num_kv_heads, int head_dim,
                            int block_size, int max_context_len, int kv_fp8, int partition_size, int variant,
-                           int* partition_out, int* longest_first, int* variant_out, long long* grid_out) {
+                           int* partition_out, int* longest_first, int* variant_out, long long* grid_out,
+                           int* prefetch_distance_out) {
   Shape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, 1, 1 << 30, max_context_len};
   if (check_shape(s) != PKD_OK || q_len < 1 || !variant_ok(variant)) return -2;
   CallPlan plan;
@@ -575,8 +751,39 @@ int paged_decode_call_plan(int num_seqs, int q_len, int num_q_heads, int num_kv_
   if (longest_first) *longest_first = plan.order ? 1 : 0;
   if (variant_out) *variant_out = plan.variant;
   if (grid_out) *grid_out = num_seqs == 0 ? 0 : plan.grid;
+  if (prefetch_distance_out)
+    *prefetch_distance_out =
+        num_seqs == 0 ? 0
+                      : effective_prefetch(0, variant_path(plan.variant), head_dim, block_size,
+                                           num_q_heads / num_kv_heads, kv_fp8 ? 1 : 2,
+                                           wide_fp8_grid(kv_fp8, q_len, plan.grid), plan.grid, plan.P);
   if (num_seqs == 0 || plan.grid == 0) return 0;
   return 1 + (plan.split ? 1 : 0) + (plan.order ? 1 : 0);
+}
+
+int paged_decode_prefetch_model(int num_seqs, int q_len, int num_q_heads, int num_kv_heads, int head_dim,
+                                int block_size, int max_context_len, int kv_fp8, int partition_size, int variant,
+                                int sm_count_, long long l2_bytes, double hbm_bytes_per_s,
+                                long long* footprint_bytes, long long* inflight_bytes_per_sm,
+                                long long* need_bytes_per_sm) {
+  Shape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, 1, 1 << 30, max_context_len};
+  if (check_shape(s) != PKD_OK || q_len < 1 || !variant_ok(variant) || sm_count_ <= 0 || l2_bytes <= 0 ||
+      !(hbm_bytes_per_s > 0.0))
+    return -2;
+  CallPlan plan;
+  if (plan_call(s, q_len, variant, partition_size, kv_fp8, &plan) != PKD_OK) return -2;
+  const int path = variant_path(plan.variant);
+  const int G = num_q_heads / num_kv_heads, kvb = kv_fp8 ? 1 : 2;
+  const bool wide = kv_fp8 && q_len == 1 && plan.grid >= (long long)kWideFp8Waves * 4 * sm_count_;
+  const PathStream ps = path_stream(path, head_dim, G, kvb, wide);
+  const long long grid = num_seqs == 0 ? 0 : plan.grid;
+  const long long resident = std::min<long long>(grid, (long long)ps.ctas_per_sm * sm_count_);
+  int d = pkd_l2_prefetch_model(resident, sm_count_, ps.streams, (long long)block_size * head_dim * kvb, 2,
+                                ps.ahead_bytes, l2_bytes, kL2PrefetchFraction, hbm_bytes_per_s, kLoadedLatencyS,
+                                ps.prefetches ? kMaxPrefetchDistance : 0, footprint_bytes, inflight_bytes_per_sm,
+                                need_bytes_per_sm);
+  const long long per_stream = ((plan.P + block_size - 1) / block_size + ps.streams - 1) / ps.streams;
+  return (int)std::max(0LL, std::min<long long>(d, per_stream - 1));
 }
 
 int paged_decode_auto_plan(int num_seqs, int q_len, int num_q_heads, int num_kv_heads, int head_dim,
@@ -584,7 +791,7 @@ int paged_decode_auto_plan(int num_seqs, int q_len, int num_q_heads, int num_kv_
                            int* longest_first) {
   return paged_decode_call_plan(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size,
                                 max_context_len, kv_fp8, 0, PKD_VARIANT_AUTO, partition_size, longest_first,
-                                nullptr, nullptr);
+                                nullptr, nullptr, nullptr);
 }
 
 size_t paged_decode_multi_workspace_size(int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
@@ -699,7 +906,7 @@ pkd_status paged_decode_partitions(const void* q, const void* k_cache, const voi
       (error_word && !aligned(error_word, 4)))
     return PKD_ERR_ALIGN;
   if (!std::isfinite(scale)) return PKD_ERR_SHAPE;
-  if (!variant_ok(variant) || prefetch_distance < 0)
+  if (!variant_ok(variant) || prefetch_distance < -1)
     return PKD_ERR_SHAPE;
   if (variant_path(variant) == PKD_VARIANT_TCGEN05 && head_dim != 128 && head_dim != 64) return PKD_ERR_UNSUPPORTED;
   if (partition_size <= 0 || partition_size % 32 != 0 || partition_size % block_size != 0)
@@ -732,7 +939,8 @@ pkd_status paged_decode_partitions(const void* q, const void* k_cache, const voi
   const int G = num_q_heads / num_kv_heads;
   const long long grid = (long long)num_seqs * num_kv_heads * max_num_partitions;
   variant = pick_auto(variant, G, grid, partition_size);
-  p.prefetch_distance = prefetch_distance == 0 ? default_prefetch_distance(variant_path(variant)) : prefetch_distance;
+  p.prefetch_distance = effective_prefetch(prefetch_distance, variant_path(variant), head_dim, block_size, G, 2,
+                                           false, grid, partition_size);
   p.l2_hints = (variant & PKD_FLAG_L2_EVICT_HINTS) ? 1 : 0;
   p.timeout_ns = kWaitBudgetNs;
   return launch_decode(variant_path(variant), head_dim, block_size, G, p, grid, stream);

@@ -73,8 +73,15 @@ def lib():
                                                       P, P]
         L.paged_decode_attention_multi_ex.restype = I
         L.paged_decode_call_plan.argtypes = [I] * 10 + [ctypes.POINTER(ctypes.c_int)] * 3 + [
-            ctypes.POINTER(ctypes.c_longlong)]
+            ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(ctypes.c_int)]
         L.paged_decode_call_plan.restype = I
+        LLP = ctypes.POINTER(ctypes.c_longlong)
+        D_ = ctypes.c_double
+        L.pkd_l2_prefetch_model.argtypes = [ctypes.c_longlong, I, I, ctypes.c_longlong, I, ctypes.c_longlong,
+                                            ctypes.c_longlong, D_, D_, D_, I, LLP, LLP, LLP]
+        L.pkd_l2_prefetch_model.restype = I
+        L.paged_decode_prefetch_model.argtypes = [I] * 11 + [ctypes.c_longlong, D_, LLP, LLP, LLP]
+        L.paged_decode_prefetch_model.restype = I
         L.paged_decode_attention_host.argtypes = [P] * 12 + [I] * 8 + [F, I, P, S, P, P]
         L.paged_decode_attention_host.restype = I
         L.paged_decode_auto_plan.argtypes = [I, I, I, I, I, I, I, I, ctypes.POINTER(ctypes.c_int),
@@ -224,14 +231,44 @@ def paged_decode_auto_plan(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim,
 def paged_decode_call_plan(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len,
                            kv_fp8=False, partition_size=0, variant="auto"):
     """The launch plan of a call: (launches, partition or -1, longest_first,
-    variant name it runs, decode CTAs)."""
+    variant name it runs, decode CTAs, default L2 prefetch distance)."""
     part, order, var, grid = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0), ctypes.c_longlong(0)
+    pd = ctypes.c_int(0)
     n = lib().paged_decode_call_plan(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size,
                                      max_context_len, int(bool(kv_fp8)), int(partition_size), _variant(variant),
-                                     ctypes.byref(part), ctypes.byref(order), ctypes.byref(var), ctypes.byref(grid))
+                                     ctypes.byref(part), ctypes.byref(order), ctypes.byref(var), ctypes.byref(grid),
+                                     ctypes.byref(pd))
     if n < 0:
         raise PagedDecodeError(2, "paged_decode_call_plan")
-    return n, part.value, bool(order.value), variant_name(var.value), grid.value
+    return n, part.value, bool(order.value), variant_name(var.value), grid.value, pd.value
+
+
+def pkd_l2_prefetch_model(resident_ctas, sm_count, streams_per_cta, m_block, tiles_per_step, ahead_bytes_per_cta,
+                          l2_bytes, l2_fraction, hbm_bytes_per_s, latency_s, max_distance):
+    """The prefetch-distance rule: (distance, footprint bytes, in-flight bytes per SM, need bytes per SM)."""
+    fp, inf, need = ctypes.c_longlong(0), ctypes.c_longlong(0), ctypes.c_longlong(0)
+    d = lib().pkd_l2_prefetch_model(int(resident_ctas), int(sm_count), int(streams_per_cta), int(m_block),
+                                    int(tiles_per_step), int(ahead_bytes_per_cta), int(l2_bytes), float(l2_fraction),
+                                    float(hbm_bytes_per_s), float(latency_s), int(max_distance), ctypes.byref(fp),
+                                    ctypes.byref(inf), ctypes.byref(need))
+    if d < 0:
+        raise PagedDecodeError(2, "pkd_l2_prefetch_model")
+    return d, fp.value, inf.value, need.value
+
+
+def paged_decode_prefetch_model(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len,
+                                sm_count, l2_bytes, hbm_bytes_per_s, kv_fp8=False, partition_size=0,
+                                variant="auto"):
+    """Default L2 prefetch distance of a call on a described GPU:
+    (distance, footprint bytes, in-flight bytes per SM, need bytes per SM)."""
+    fp, inf, need = ctypes.c_longlong(0), ctypes.c_longlong(0), ctypes.c_longlong(0)
+    d = lib().paged_decode_prefetch_model(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size,
+                                          max_context_len, int(bool(kv_fp8)), int(partition_size),
+                                          _variant(variant), int(sm_count), int(l2_bytes), float(hbm_bytes_per_s),
+                                          ctypes.byref(fp), ctypes.byref(inf), ctypes.byref(need))
+    if d < 0:
+        raise PagedDecodeError(2, "paged_decode_prefetch_model")
+    return d, fp.value, inf.value, need.value
 
 
 def variant_name(v: int) -> str:

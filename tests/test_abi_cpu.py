@@ -300,10 +300,10 @@ def test_call_plan_picks_the_tensor_core_path(L):
     assert ops.paged_decode_call_plan(4, 1, 28, 4, 128, 16, 1000, kv_fp8=True)[3] == "tma_mma"
     assert ops.paged_decode_call_plan(4, 1, 28, 4, 128, 16, 1000)[3] == "tma_mma"
     # grid: (sequence, kv head, chunk of 64 / G query tokens, partition)
-    n, part, ordered, var, grid = ops.paged_decode_call_plan(4, 10, 28, 4, 128, 16, 1000, partition_size=256,
+    n, part, ordered, var, grid, _ = ops.paged_decode_call_plan(4, 10, 28, 4, 128, 16, 1000, partition_size=256,
                                                              variant="tcgen05")
     assert (n, part, var, grid) == (2, 256, "tcgen05", 4 * 4 * 2 * 4)
-    n, part, ordered, var, grid = ops.paged_decode_call_plan(4, 10, 28, 4, 128, 16, 1000, partition_size=-1,
+    n, part, ordered, var, grid, _ = ops.paged_decode_call_plan(4, 10, 28, 4, 128, 16, 1000, partition_size=-1,
                                                              variant="tma_mma")
     assert (n, part, grid) == (1, -1, 4 * 4 * 5)
     # refused: tcgen05 with head_dim 64, CUDA-core paths for several queries
@@ -326,7 +326,7 @@ def test_multi_workspace_covers_both_tensor_core_paths(L):
         maxlen = rng.choice([16, 100, 1000, 5000, 20000])
         ws = L_size = ops.paged_decode_multi_workspace_size(B, q_len, G * Hkv, Hkv, 128, 16, maxlen, 0)
         for variant in ("auto", "tma_mma", "tcgen05"):
-            n, part, ordered, var, grid = ops.paged_decode_call_plan(B, q_len, G * Hkv, Hkv, 128, 16, maxlen,
+            n, part, ordered, var, grid, _ = ops.paged_decode_call_plan(B, q_len, G * Hkv, Hkv, 128, 16, maxlen,
                                                                      partition_size=0, variant=variant)
             need = 0
             if part > 0:
@@ -343,14 +343,14 @@ def test_tcgen05_split_policy(L):
     from paged_kv_decode_21_gb300 import ops
     sms = 148  # no device here: the library's default SM count
     # GQA 7:1, 256 x 8192 tokens, q_len 8: 1024 units, three waves and more
-    n, part, ordered, var, grid = ops.paged_decode_call_plan(256, 8, 28, 4, 128, 16, 8192)
+    n, part, ordered, var, grid, _ = ops.paged_decode_call_plan(256, 8, 28, 4, 128, 16, 8192)
     assert var.startswith("tcgen05") and part == -1 and grid == 1024
-    n, part, ordered, var, grid = ops.paged_decode_call_plan(256, 8, 28, 4, 128, 16, 8192, variant="tma_mma")
+    n, part, ordered, var, grid, _ = ops.paged_decode_call_plan(256, 8, 28, 4, 128, 16, 8192, variant="tma_mma")
     assert part == -1 and grid == 256 * 4 * 4  # four 16-row chunks: many waves, unsplit too
-    n, part, ordered, var, grid = ops.paged_decode_call_plan(256, 1, 28, 4, 128, 16, 8192)
+    n, part, ordered, var, grid, _ = ops.paged_decode_call_plan(256, 1, 28, 4, 128, 16, 8192)
     assert var == "tma_mma" and part == 2048  # single query: 1024 units, long context, split
     # GQA 5:1, 32 x 32768 tokens, q_len 8: 256 units, below two waves: split
-    n, part, ordered, var, grid = ops.paged_decode_call_plan(32, 8, 40, 8, 128, 16, 32768)
+    n, part, ordered, var, grid, _ = ops.paged_decode_call_plan(32, 8, 40, 8, 128, 16, 32768)
     want = 6 * 2 * sms
     np_ = -(-want // 256)
     per = -(-32768 // np_)
