@@ -42,7 +42,14 @@ from paged_kv_decode_21_gb300 import traffic, workloads  # noqa: E402
 
 METRIC = "paged decode-attention achieved HBM GB/s (% of GB300 peak); μs per call"
 DEFAULT_CONFIG = "llama2_7b_mha"
+# the other large workloads the default run also times and checks, each as an extra key of the line
+EXTRA_CONFIGS = ["llama3_8b_gqa4", "qwen25_7b_gqa7", "qwen25_14b_gqa5_splitk"]
 FALLBACK_HBM_GBS = 6800.0
+# GB300's nominal HBM3e bandwidth (datasheet figure), for a fraction of the nameplate peak
+NOMINAL_HBM_GBS = 7900.0
+# parity contract of the fp16 output against the fp64 oracle, over every output element
+PARITY_MAX_ABS = 4e-3
+PARITY_MEAN_ABS = 5e-4
 KERNEL_SOURCES = ["paged_kv_decode_21_gb300/csrc/pkd_decode.cuh", "paged_kv_decode_21_gb300/csrc/pkd_decode_ws.cuh",
                   "paged_kv_decode_21_gb300/csrc/pkd_decode_mma.cuh", "paged_kv_decode_21_gb300/csrc/pkd_ptx.cuh",
                   "paged_kv_decode_21_gb300/csrc/pkd_launch.cuh", "paged_kv_decode_21_gb300/csrc/pkd_inst_tma_mma.cu"]
@@ -95,6 +102,29 @@ def kernel_name(cfg: workloads.DecodeConfig, variant: str, kv_fp8: bool = False,
     return f"paged_decode_kernel<{shape},{variant}>"
 
 
+def dtype_label(resolved: str, kv_fp8: bool) -> str:
+    """The arithmetic a resolved data path does: fp32 scores, softmax and
+    accumulation; on the tensor-core paths the weights p are rounded to fp16
+    before P.V (the normaliser sums the fp32 p)."""
+    tc = resolved.split("+")[0] in ("tma_mma", "tcgen05")
+    base = ("e4m3 K/V (widened exactly to f16), f16 q/out" if kv_fp8 else "f16 q/K/V/out") + ", f32 arithmetic"
+    return base + ("; p rounded to f16 for P.V" if tc else "")
+
+
+def parity(out: torch.Tensor, ref) -> dict:
+    """Element-by-element comparison of a GPU output with the oracle's, over every row."""
+    import numpy as np
+    got = out.detach().cpu().to(torch.float64).numpy().reshape(ref.shape)
+    err = np.abs(got - ref)
+    finite = bool(np.isfinite(got).all())
+    mx = float(err.max(initial=0.0)) if finite else float("inf")
+    mean = float(err.mean()) if finite and err.size else 0.0
+    return {"max_abs": mx, "mean_abs": mean, "max_abs_ref": float(np.abs(ref).max(initial=0.0)),
+            "rows": "all", "n_rows": int(err.size // ref.shape[-1]),
+            "tol": {"max_abs": PARITY_MAX_ABS, "mean_abs": PARITY_MEAN_ABS},
+            "ok": bool(finite and mx <= PARITY_MAX_ABS and mean <= PARITY_MEAN_ABS)}
+
+
 def ncu_traffic(workload: str, variant: str):
     """dram bytes per launch from the committed ncu capture, if it matches this kernel."""
     try:
@@ -113,7 +143,7 @@ class ClockSampler:
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-              "clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_power_cap,clocks.mem,temperature.memory")
 
     def __init__(self, device_index: int):
         self.samples = []
@@ -151,7 +181,7 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
+        sm, mx, reasons, mem, mtemp = [], [], set(), [], []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for s in self.samples:
             try:
@@ -162,10 +192,20 @@ class ClockSampler:
             for n, v in zip(names, s[3:7]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
+            for dst, v in ((mem, s[7:8]), (mtemp, s[8:9])):
+                try:
+                    dst.append(float(v[0]))
+                except Exception:
+                    pass
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+               "samples": len(sm)}
+        if mem:
+            out["mem_mhz"] = statistics.median(mem)
+        if mtemp:
+            out["mem_temp_c_max"] = max(mtemp)
+        return out
 
 
 def dist_env():
@@ -213,7 +253,7 @@ def time_gpu(args, cfg, variant, dev, inp, steps, warmup, with_e2e=True, with_cl
     kv_fp8 = getattr(args, "kv_fp8", False)
     # the library's own plan: partition, order, data path, decode CTAs, launches
     # (the E4M3 entry takes no variant: it runs the automatic choice)
-    launches, eff_P, ordered, resolved, grid = ops.paged_decode_call_plan(
+    launches, eff_P, ordered, resolved, grid, pdist = ops.paged_decode_call_plan(
         inp.num_seqs, q_len, inp.num_q_heads, inp.num_kv_heads, inp.head_dim, inp.block_size,
         inp.max_context_len, kv_fp8, P, "auto" if kv_fp8 else variant)
     split = eff_P > 0
@@ -229,11 +269,18 @@ def time_gpu(args, cfg, variant, dev, inp, steps, warmup, with_e2e=True, with_cl
                                       variant=variant, prefetch_distance=args.prefetch_distance,
                                       workspace=ws, error_word=ew, stream=stream)
 
+    def oracle_ref(threads):
+        import oracle
+        return oracle.attention(inp.q.cpu(), inp.k_cache.cpu(), inp.v_cache.cpu(), inp.block_tables.cpu(),
+                                inp.context_lens.cpu(), inp.scale, threads=threads)
+
     if kv_fp8:
         # E4M3 caches (one byte per element): the K/V stream halves
         g = torch.Generator(device=dev).manual_seed(cfg.seed + 9)
-        k8 = workloads.rand_e4m3(inp.k_cache.shape, g, dev)
-        v8 = workloads.rand_e4m3(inp.v_cache.shape, g, dev)
+        codes = getattr(args, "e4m3_codes", "full")
+        k8 = workloads.rand_e4m3(inp.k_cache.shape, g, dev, codes=codes)
+        v8 = workloads.rand_e4m3(inp.v_cache.shape, g, dev, codes=codes)
+        ks, vs = workloads.E4M3_SCALES[codes]
         kv16 = 2 * sum(lens) * inp.num_kv_heads * inp.head_dim * 2
         algo -= kv16 // 2
         qm = inp.q
@@ -247,8 +294,13 @@ def time_gpu(args, cfg, variant, dev, inp, steps, warmup, with_e2e=True, with_cl
 
         def call():  # noqa: F811
             ops.paged_decode_attention_fp8(qm, k8, v8, inp.block_tables, inp.context_lens, inp.scale,
-                                           0.05, 0.11, out=out, max_context_len=inp.max_context_len,
+                                           ks, vs, out=out, max_context_len=inp.max_context_len,
                                            partition_size=P, workspace=ws, error_word=ew, stream=stream)
+
+        def oracle_ref(threads):  # noqa: F811
+            import oracle
+            return oracle.attention_fp8(qm.cpu(), k8.cpu(), v8.cpu(), inp.block_tables.cpu(),
+                                        inp.context_lens.cpu(), inp.scale, ks, vs, threads=threads)
     elif q_len > 1:
         # q_len new tokens per sequence (causal among them): the K/V stream is
         # the same, q and out grow by q_len
@@ -265,6 +317,11 @@ def time_gpu(args, cfg, variant, dev, inp, steps, warmup, with_e2e=True, with_cl
                                              inp.context_lens, inp.scale, out=out,
                                              max_context_len=inp.max_context_len, partition_size=P,
                                              workspace=ws, error_word=ew, stream=stream, variant=variant)
+
+        def oracle_ref(threads):  # noqa: F811
+            import oracle
+            return oracle.attention_multi(qm.cpu(), inp.k_cache.cpu(), inp.v_cache.cpu(), inp.block_tables.cpu(),
+                                          inp.context_lens.cpu(), inp.scale, threads=threads)
 
     use_flush = algo < 4 * l2
 
@@ -302,14 +359,16 @@ def time_gpu(args, cfg, variant, dev, inp, steps, warmup, with_e2e=True, with_cl
         "algo_bytes": algo, "mean_ms": statistics.mean(times_ms), "median_ms": statistics.median(times_ms),
         "min_ms": min(times_ms), "wall_s": t_wall, "launches_per_call": launches, "grid": grid,
         "partition_size": eff_P if split else -1, "longest_first": ordered, "device_error": errbits,
-        "variant": resolved,
+        # the L2 prefetch distance the call ran: -1 asks for none, 0 for the model's default
+        "prefetch_distance": 0 if args.prefetch_distance < 0 else (args.prefetch_distance or pdist),
+        "variant": resolved, "out": out, "oracle_ref": oracle_ref,
         "clocks": sampler.summary() if sampler else None,
         "l2": (f"an L2 flush (2x L2 read) before every timed call; inputs {algo / 1e6:.0f} MB" if use_flush
                else f"inputs larger than L2 ({algo / 1e9:.2f} GB against {l2 / 1e6:.0f} MB): calls back to "
                     "back, no flush"),
     }
     if with_e2e:
-        e2e_steps = max(3, min(20, steps // 10))
+        e2e_steps = max(10, min(20, steps // 10))
         if variant == "auto" and q_len == 1 and not kv_fp8 and P == 0:
             res["e2e"] = time_e2e_host_api(inp, stream, dev, algo, e2e_steps)
         else:
@@ -410,7 +469,25 @@ def time_e2e_host_api(inp, stream, dev, algo, steps):
 
     st = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     en = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    call()
+    # the host link itself, right before the timed steps: a pinned 512 MiB copy to the device,
+    # best of three (what any host-buffer call on this machine can reach)
+    probe_h = torch.empty(512 << 20, dtype=torch.uint8).pin_memory()
+    probe_d = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    link = []
+    for _ in range(3):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        probe_d.copy_(probe_h, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        link.append(probe_h.numel() / (a.elapsed_time(b) * 1e-3) / 1e9)
+    del probe_h, probe_d
+    # warm-up calls (their times are recorded below); the timed steps follow them
+    warm = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(3)]
+    for a, b in warm:
+        a.record(stream)
+        call()
+        b.record(stream)
     torch.cuda.synchronize(dev)
     for i in range(steps):
         st[i].record(stream)
@@ -420,7 +497,28 @@ def time_e2e_host_api(inp, stream, dev, algo, steps):
     ms = statistics.mean(s.elapsed_time(e) for s, e in zip(st, en))
     return {"value": round(algo / (ms * 1e-3) / 1e9, 2), "unit": "GB/s", "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "warmup_ms": [round(a.elapsed_time(b), 3) for a, b in warm],
+            "h2d_link_gbs": round(max(link), 1),
+            "host_numa_node": host_numa_node(dev),
             "api": "paged_decode_attention_host (used blocks only)"}
+
+
+def host_numa_node(dev):
+    """The host NUMA node the driver reports closest to the GPU
+    (cudaDevAttrHostNumaId), or None where it cannot be read."""
+    try:
+        import ctypes
+        import glob
+        libs = sorted(glob.glob("/usr/local/cuda/lib64/libcudart.so*"))
+        if not libs:
+            return None
+        rt = ctypes.CDLL(libs[0])
+        v = ctypes.c_int(-1)
+        if rt.cudaDeviceGetAttribute(ctypes.byref(v), 134, int(dev.index or 0)) != 0:  # cudaDevAttrHostNumaId
+            return None
+        return v.value
+    except Exception:
+        return None
 
 
 def time_e2e(call, inp, out, stream, dev, algo, steps):
@@ -456,15 +554,15 @@ def cpu_oracle_rate(inp, target_s=10.0, max_passes=50):
     cpu = inp.to("cpu")
     lens = cpu.context_lens.tolist()
     algo = traffic.algorithmic_bytes(lens, cpu.num_q_heads, cpu.num_kv_heads, cpu.head_dim)
-    passes, t = 0, 0.0
+    passes, t, ref = 0, 0.0, None
     while passes < max_passes and (t < target_s or passes == 0):
         t0 = time.perf_counter()
-        oracle.attention(cpu.q, cpu.k_cache, cpu.v_cache, cpu.block_tables, cpu.context_lens, cpu.scale,
-                         threads=cores)
+        ref = oracle.attention(cpu.q, cpu.k_cache, cpu.v_cache, cpu.block_tables, cpu.context_lens, cpu.scale,
+                               threads=cores)
         t += time.perf_counter() - t0
         passes += 1
     sample = f"{passes} full pass(es) over the workload ({algo / 1e9:.3f} GB each), {t:.1f} s"
-    return algo * passes / t / 1e9, cores, sample, t / passes
+    return algo * passes / t / 1e9, cores, sample, t / passes, ref
 
 
 def cpu_oracle_rate_1thread(inp, nseq=4):
@@ -492,6 +590,31 @@ def make_workload(name, dev, batch=None):
     return cfg, workloads.make_inputs(cfg, device=dev)
 
 
+def time_extra_config(args, name, dev, peak):
+    """One more large workload timed like the headline one (its configured
+    partition, L2 rule and clock sampling; no e2e leg), with every output row
+    compared with the oracle."""
+    import copy
+    cfg, inp = make_workload(name, dev)
+    a = copy.copy(args)
+    a.partition_size = None
+    r = time_gpu(a, cfg, args.variant, dev, inp, min(args.steps, 200), args.warmup, with_e2e=False)
+    gbs = r["algo_bytes"] / (r["mean_ms"] * 1e-3) / 1e9
+    par = parity(r["out"], r["oracle_ref"](os.cpu_count() or 1))
+    res = {"workload": describe(cfg), "variant": r["variant"], "partition_size": r["partition_size"],
+           "longest_first": r["longest_first"],
+           "us_per_call": round(r["mean_ms"] * 1e3, 2), "us_per_call_median": round(r["median_ms"] * 1e3, 2),
+           "us_per_call_min": round(r["min_ms"] * 1e3, 2), "steps": min(args.steps, 200),
+           "algorithmic_bytes_per_call": r["algo_bytes"], "GB_s": round(gbs, 1),
+           "frac": round(gbs / peak, 4), "frac_of_nominal": round(gbs / NOMINAL_HBM_GBS, 4),
+           "kernel": kernel_name(cfg, r["variant"], False, wide=False),
+           "gpu_launches_per_call": r["launches_per_call"], "l2": r["l2"], "clocks": r["clocks"],
+           "device_error_bits": r["device_error"], "parity": par}
+    del inp, r
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
@@ -506,18 +629,25 @@ def run_reference(args):
     for _ in range(args.warmup):
         oracle.attention(cpu.q, cpu.k_cache, cpu.v_cache, cpu.block_tables, cpu.context_lens, cpu.scale,
                          threads=cores)
-    t0 = time.perf_counter()
+    times = []
     for _ in range(args.steps):
+        t0 = time.perf_counter()
         oracle.attention(cpu.q, cpu.k_cache, cpu.v_cache, cpu.block_tables, cpu.context_lens, cpu.scale,
                          threads=cores)
-    dt = (time.perf_counter() - t0) / args.steps
+        times.append(time.perf_counter() - t0)
+    dt = statistics.mean(times)
     value = algo / dt / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s",
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": describe(cfg), "impl": "CPU fp64 oracle (plain C, pthreads)"},
+        # the same keys as the GPU arm's config: the same workload, run by the oracle
+        "config": {"workload": describe(cfg), "variant": "oracle", "partition_size": -1,
+                   "us_per_call": round(dt * 1e6, 2), "us_per_call_median": round(statistics.median(times) * 1e6, 2),
+                   "us_per_call_min": round(min(times) * 1e6, 2), "algorithmic_bytes_per_call": algo,
+                   "l2": "CPU fp64 oracle (plain C, pthreads): host memory, no GPU L2",
+                   "parallelism": f"host threads x{cores} (no collective)"},
         "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": f"each step is one full pass over the workload ({algo / 1e9:.3f} GB)"},
         "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -537,12 +667,14 @@ def main():
                     help="auto|no_prefetch|l2_prefetch|tma_staged|tma_mma, optionally +l2_hints "
                          "(L2 eviction priorities)")
     ap.add_argument("--partition-size", type=int, default=None)
-    ap.add_argument("--prefetch-distance", type=int, default=0)
+    ap.add_argument("--prefetch-distance", type=int, default=0,
+                    help="L2 prefetch distance: -1 none, 0 the library's model (default), >= 1 that distance")
     ap.add_argument("--sweep", action="store_true", help="every workload x variant, one line each")
     ap.add_argument("--sweep-configs", default=",".join(workloads.CONFIG_ORDER[1:]))
     ap.add_argument("--sweep-variants", default="no_prefetch,l2_prefetch,tma_staged")
     ap.add_argument("--sweep-partitions", default="", help="comma list of partition sizes (default: the config's)")
-    ap.add_argument("--sweep-pd", default="", help="comma list of prefetch distances (default: the library's)")
+    ap.add_argument("--sweep-pd", default="",
+                    help="comma list of prefetch distances (-1 none, 0 the library's model; default: the model)")
     ap.add_argument("--fig4", action="store_true",
                     help="batch x context grid on the MHA shape: each data path's speed over NO_PREFETCH")
     ap.add_argument("--fig4-config", default=DEFAULT_CONFIG,
@@ -556,6 +688,12 @@ def main():
                     help="time paged_kv_append alone and in front of the decode call, on --config")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-parity", action="store_true",
+                    help="skip the all-row comparison of the timed call's output with the oracle")
+    ap.add_argument("--no-extra-configs", action="store_true",
+                    help="time only --config (the default run also times and checks the other large workloads)")
+    ap.add_argument("--e4m3-codes", default="full", choices=sorted(workloads.E4M3_SCALES),
+                    help="code set of the E4M3 caches of --kv-fp8 (and its per-cache scales)")
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch (profiling runs)")
     ap.add_argument("--kv-fp8", action="store_true",
                     help="E4M3 K/V caches (one byte per element, per-cache scales)")
@@ -645,7 +783,8 @@ def main():
                                       "us_min": round(r["min_ms"] * 1e3, 2), "GB_s": round(gbs, 1),
                                       "frac_of_peak": round(gbs / peak, 4),
                                       "partition_size": r["partition_size"],
-                                      "prefetch_distance": pdist or "default",
+                                      "prefetch_distance": r["prefetch_distance"],
+                                      "prefetch_requested": pdist if pdist else "model",
                                       "launches_per_call": r["launches_per_call"],
                                       "device_error": r["device_error"]}), flush=True)
             del inp
@@ -661,12 +800,13 @@ def main():
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(mean_ms, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": ("e4m3 KV, f16 q/out, f32 arithmetic" if args.kv_fp8 else "f16 in, f32 arithmetic"),
+        "scaling": "weak", "vs_baseline": None, "dtype": dtype_label(resolved, args.kv_fp8),
         "data": "synthetic",
         "config": {"workload": describe(cfg) + (f", q_len={args.q_len} (causal)" if args.q_len > 1 else "")
                    + (", KV in E4M3 (1 byte/element)" if args.kv_fp8 else ""),
                    "variant": resolved,
                    "partition_size": r["partition_size"],
+                   "prefetch_distance": r["prefetch_distance"],
                    "us_per_call": round(mean_ms * 1e3, 2), "us_per_call_median": round(r["median_ms"] * 1e3, 2),
                    "us_per_call_min": round(r["min_ms"] * 1e3, 2),
                    "algorithmic_bytes_per_call": r["algo_bytes"],
@@ -674,6 +814,7 @@ def main():
                    "parallelism": f"replicas x{ws} (no collective)"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                     "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4), "nominal_peak": NOMINAL_HBM_GBS,
                      "traffic": ncu_traffic(cfg.name, resolved),
                      "kernel": kernel_name(cfg, resolved, args.kv_fp8,
                                            wide=args.q_len == 1 and r["grid"] >= 3 * 4 * torch.cuda.get_device_properties(dev).multi_processor_count,
@@ -683,17 +824,38 @@ def main():
         "e2e": r.get("e2e"),
         "device_error_bits": r["device_error"],
     }
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        v, cores, sample, _ = cpu_oracle_rate(inp)
+    cpu_ref = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline and args.q_len == 1 and not args.kv_fp8:
+        v, cores, sample, _, cpu_ref = cpu_oracle_rate(inp)
         v1, sample1 = cpu_oracle_rate_1thread(inp)
         line["cpu_baseline"] = {"value": round(v, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
                                 "value_1_thread": round(v1, 3), "sample_1_thread": sample1,
                                 "sample": sample}
+    ok = True
+    if not args.no_parity:
+        # every output element of the last timed call against the oracle (each rank checks its own)
+        ref = cpu_ref if cpu_ref is not None else r["oracle_ref"](os.cpu_count() or 1)
+        line["parity"] = parity(r["out"], ref)
+        ok = line["parity"]["ok"]
+        del ref, cpu_ref
+    del r, inp
+    torch.cuda.empty_cache()
+    if (rank == 0 and ws == 1 and args.config == DEFAULT_CONFIG and args.batch is None and args.q_len == 1
+            and not args.kv_fp8 and not args.no_extra_configs):
+        line["other_configs"] = {}
+        for name in EXTRA_CONFIGS:
+            extra = time_extra_config(args, name, dev, peak)
+            line["other_configs"][name] = extra
+            ok = ok and extra["parity"]["ok"] and extra["device_error_bits"] == 0
+    ok = ok and line["device_error_bits"] == 0
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
+    if not ok:
+        sys.stderr.write("bench: parity or device-error check failed (see the line's parity keys)\n")
+        return 1
     return 0
 
 

@@ -507,7 +507,11 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, K
       }
       if (any) {  // every MMA completes before tensor memory is freed
         tc_commit(drain);
-        mbar_wait_bounded(drain, 0, P.timeout_ns);
+        if (!mbar_wait_bounded(drain, 0, P.timeout_ns)) {
+          // the output of this CTA cannot be trusted: report it like any other wait that ran out
+          record_error(P.error_word, kErrTimeout);
+          *abort_flag = 1;
+        }
       }
     }
   } else if (warp < nsw) {

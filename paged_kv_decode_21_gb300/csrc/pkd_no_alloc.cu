@@ -31,6 +31,9 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Device address of the scratch on the current device, looked up on the
 // first call per device (with that device current).  nullptr on failure.
+// The address is kept until the process exits: after a cudaDeviceReset the
+// reloaded module's array may sit elsewhere, so the entry point is not for
+// use across a reset (the header says so).
 void* scratch_for_current_device(cudaError_t* err) {
   int dev = -1;
   *err = cudaGetDevice(&dev);
