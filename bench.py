@@ -252,10 +252,9 @@ def time_gpu(args, cfg, variant, dev, inp, steps, warmup, with_e2e=True, with_cl
     q_len = getattr(args, "q_len", 1)
     kv_fp8 = getattr(args, "kv_fp8", False)
     # the library's own plan: partition, order, data path, decode CTAs, launches
-    # (the E4M3 entry takes no variant: it runs the automatic choice)
     launches, eff_P, ordered, resolved, grid, pdist = ops.paged_decode_call_plan(
         inp.num_seqs, q_len, inp.num_q_heads, inp.num_kv_heads, inp.head_dim, inp.block_size,
-        inp.max_context_len, kv_fp8, P, "auto" if kv_fp8 else variant)
+        inp.max_context_len, kv_fp8, P, variant)
     split = eff_P > 0
     out = torch.empty_like(inp.q)
     ew = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -295,7 +294,8 @@ def time_gpu(args, cfg, variant, dev, inp, steps, warmup, with_e2e=True, with_cl
         def call():  # noqa: F811
             ops.paged_decode_attention_fp8(qm, k8, v8, inp.block_tables, inp.context_lens, inp.scale,
                                            ks, vs, out=out, max_context_len=inp.max_context_len,
-                                           partition_size=P, workspace=ws, error_word=ew, stream=stream)
+                                           partition_size=P, workspace=ws, error_word=ew, stream=stream,
+                                           variant=None if variant == "auto" else variant)
 
         def oracle_ref(threads):  # noqa: F811
             import oracle

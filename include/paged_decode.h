@@ -475,6 +475,22 @@ pkd_status paged_decode_attention_fp8(const void* q, const void* k_cache, const 
                                       int* error_word, cudaStream_t stream);
 
 /*
+ * paged_decode_attention_fp8_ex -- paged_decode_attention_fp8 with the data
+ * path chosen by the caller: variant PKD_VARIANT_AUTO (the choice
+ * paged_decode_attention_fp8 makes), PKD_VARIANT_TMA_MMA or
+ * PKD_VARIANT_TCGEN05 (head_dim 128), optionally ORed with PKD_FLAG_* bits;
+ * PKD_ERR_UNSUPPORTED for the CUDA-core paths.  Both tensor-core paths give
+ * the same result up to fp32 rounding order.
+ */
+pkd_status paged_decode_attention_fp8_ex(const void* q, const void* k_cache, const void* v_cache,
+                                         const int32_t* block_tables, const int32_t* context_lens, void* out,
+                                         int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
+                                         int head_dim, int block_size, int num_blocks, int max_blocks_per_seq,
+                                         int max_context_len, float scale, float k_scale, float v_scale,
+                                         int partition_size, int variant, void* workspace, size_t workspace_bytes,
+                                         int* error_word, cudaStream_t stream);
+
+/*
  * paged_kv_append_fp8 -- paged_kv_append into E4M3 caches: every element x
  * of the new fp16 rows is stored as e4m3(fp32(x) / scale), the division in
  * IEEE fp32 and the conversion round-to-nearest-even, saturating at +-448

@@ -739,6 +739,19 @@ pkd_status paged_decode_attention_fp8(const void* q, const void* k_cache, const 
                      stream, 1, k_scale, v_scale);
 }
 
+pkd_status paged_decode_attention_fp8_ex(const void* q, const void* k_cache, const void* v_cache,
+                                         const int32_t* block_tables, const int32_t* context_lens, void* out,
+                                         int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
+                                         int head_dim, int block_size, int num_blocks, int max_blocks_per_seq,
+                                         int max_context_len, float scale, float k_scale, float v_scale,
+                                         int partition_size, int variant, void* workspace, size_t workspace_bytes,
+                                         int* error_word, cudaStream_t stream) {
+  return decode_impl(q, k_cache, v_cache, block_tables, context_lens, out, num_seqs, q_len, num_q_heads,
+                     num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, max_context_len,
+                     scale, partition_size, variant, 0, workspace, workspace_bytes, error_word, stream, 1, k_scale,
+                     v_scale);
+}
+
 int paged_decode_call_plan(int num_seqs, int q_len, int num_q_heads, int num_kv_heads, int head_dim,
                            int block_size, int max_context_len, int kv_fp8, int partition_size, int variant,
                            int* partition_out, int* longest_first, int* variant_out, long long* grid_out,

@@ -92,6 +92,9 @@ def lib():
         L.paged_decode_attention_fp8.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, F, F, I, P, S,
                                                  P, P]
         L.paged_decode_attention_fp8.restype = I
+        L.paged_decode_attention_fp8_ex.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, F, F, I, I, P,
+                                                    S, P, P]
+        L.paged_decode_attention_fp8_ex.restype = I
         L.paged_kv_append_fp8.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, F, F, P, P]
         L.paged_kv_append_fp8.restype = I
         L.paged_kv_append.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, P]
@@ -414,9 +417,11 @@ def _want_fp8_cache(t: torch.Tensor, name: str):
 
 def paged_decode_attention_fp8(q, k_cache, v_cache, block_tables, context_lens, scale, k_scale, v_scale,
                                out=None, max_context_len=None, partition_size=0, workspace=None,
-                               error_word=None, stream=None) -> torch.Tensor:
+                               error_word=None, stream=None, variant=None) -> torch.Tensor:
     """Decode over E4M3 caches (value = code * k_scale / v_scale); q is
-    [B][Hq][D] (single query) or [B][q_len][Hq][D] (causal multi-token)."""
+    [B][Hq][D] (single query) or [B][q_len][Hq][D] (causal multi-token).
+    With ``variant`` (auto, tma_mma, tcgen05) this calls
+    paged_decode_attention_fp8_ex."""
     single = q.dim() == 3
     qm = q.unsqueeze(1) if single else q
     _want(qm, "q", torch.float16, 4)
@@ -438,11 +443,18 @@ def paged_decode_attention_fp8(q, k_cache, v_cache, block_tables, context_lens, 
     if workspace is None:
         workspace = alloc_workspace(need, q.device)
     wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = lib().paged_decode_attention_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
-                                          _ptr(context_lens), _ptr(out), B, QL, Hq, Hkv, D, BS, NB,
-                                          block_tables.shape[1], maxlen, float(scale), float(k_scale),
-                                          float(v_scale), int(partition_size), _ptr(workspace), wsb,
-                                          _ptr(error_word), _stream(stream))
+    if variant is None:
+        st = lib().paged_decode_attention_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                              _ptr(context_lens), _ptr(out), B, QL, Hq, Hkv, D, BS, NB,
+                                              block_tables.shape[1], maxlen, float(scale), float(k_scale),
+                                              float(v_scale), int(partition_size), _ptr(workspace), wsb,
+                                              _ptr(error_word), _stream(stream))
+    else:
+        st = lib().paged_decode_attention_fp8_ex(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                                 _ptr(context_lens), _ptr(out), B, QL, Hq, Hkv, D, BS, NB,
+                                                 block_tables.shape[1], maxlen, float(scale), float(k_scale),
+                                                 float(v_scale), int(partition_size), _variant(variant),
+                                                 _ptr(workspace), wsb, _ptr(error_word), _stream(stream))
     _check(st, "paged_decode_attention_fp8")
     return out
 

@@ -146,7 +146,7 @@ def test_fp8_append_then_decode():
     check(out, inp, q, k8, v8, "fp8 append + decode", context_lens=grown)
 
 
-def test_fp8_full_size_gqa_sampled():
+def test_fp8_full_size_gqa_all_rows():
     # Qwen2.5-7B attention shape (256 sequences x 8192 tokens, 28 q / 4 kv heads) in E4M3
     cfg = workloads.CONFIGS["qwen25_7b_gqa7"]
     inp = workloads.make_inputs(cfg, device="cuda")
@@ -158,9 +158,7 @@ def test_fp8_full_size_gqa_sampled():
     ew = torch.zeros(1, dtype=torch.int32, device="cuda")
     out = run(inp, inp.q, k8, v8, 0, error_word=ew)
     assert ops.pkd_read_device_error(ew) == 0
-    rows = sample_rows(cfg.num_seqs, cfg.num_q_heads, 64, seed=5)
-    got = out.view(-1, cfg.head_dim)[torch.from_numpy(rows).long().cuda()]
-    check(got, inp, inp.q, k8, v8, "qwen25_7b_gqa7 fp8", rows=rows)
+    check(out, inp, inp.q, k8, v8, "qwen25_7b_gqa7 fp8")
 
 
 @pytest.mark.parametrize("shape", [

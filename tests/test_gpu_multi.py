@@ -126,7 +126,7 @@ def test_multi_query_nan_poison_in_unused_slots():
     assert torch.equal(a, b)
 
 
-def test_multi_query_full_size_gqa_sampled():
+def test_multi_query_full_size_gqa_all_rows():
     # Llama3-8B shape (128 sequences, 32 q / 8 kv heads, contexts U[512, 4096])
     # verifying 4 draft tokens per sequence, at the automatic split
     cfg = workloads.CONFIGS["llama3_8b_gqa4"]
@@ -136,10 +136,7 @@ def test_multi_query_full_size_gqa_sampled():
     ew = torch.zeros(1, dtype=torch.int32, device="cuda")
     out = run_multi(inp, q, 0, error_word=ew)
     assert ops.pkd_read_device_error(ew) == 0
-    rows = sample_rows(cfg.num_seqs * 4, cfg.num_q_heads, 96, seed=11)
-    ref = oracle_multi(inp, q, rows=rows)
-    got = out.view(-1, cfg.head_dim)[torch.from_numpy(rows).long().cuda()]
-    assert_close(got, ref, "llama3_8b_gqa4 q_len=4")
+    assert_close(out, oracle_multi(inp, q), "llama3_8b_gqa4 q_len=4")
 
 
 def test_multi_query_automatic_order_is_bitwise_neutral():

@@ -340,7 +340,7 @@ def test_multi_query_longest_first_is_bitwise_neutral():
 
 @pytest.mark.parametrize("name,q_len,min_partition", [("qwen25_7b_gqa7", 8, None), ("llama3_8b_gqa4", 8, None),
                                                      ("qwen25_14b_gqa5_splitk", 8, 2049)])
-def test_multi_query_full_size_sampled(name, q_len, min_partition):
+def test_multi_query_full_size_all_rows(name, q_len, min_partition):
     # the full workloads verifying q_len draft tokens per sequence, at the automatic split; the
     # GQA 5:1 long-context batch has too few (sequence, kv head) units for two waves, so the
     # tcgen05 plan splits it into partitions longer than the mma.sync path's 2048 tokens
@@ -359,9 +359,7 @@ def test_multi_query_full_size_sampled(name, q_len, min_partition):
     ew = errword()
     out = run_multi(inp, q, 0, variant="auto", error_word=ew)
     assert ops.pkd_read_device_error(ew) == 0
-    rows = sample_rows(cfg.num_seqs * q_len, cfg.num_q_heads, 192, seed=q_len + len(name))
-    got = out.view(-1, cfg.head_dim)[torch.from_numpy(rows).long().cuda()]
-    assert_close(got, oracle_multi(inp, q, rows=rows), f"{name} q_len={q_len}")
+    assert_close(out, oracle_multi(inp, q), f"{name} q_len={q_len}")
 
 
 @pytest.mark.parametrize("q_len", [1, 8])
@@ -446,7 +444,7 @@ def test_fp8_multi_query_nan_codes_in_unused_slots():
     assert torch.equal(a, b)
 
 
-def test_fp8_multi_query_full_size_sampled():
+def test_fp8_multi_query_full_size_all_rows():
     # Qwen2.5-7B shape over E4M3 caches verifying 8 draft tokens, at the automatic split
     cfg = workloads.CONFIGS["qwen25_7b_gqa7"]
     inp = workloads.make_inputs(cfg, device="cuda")
@@ -459,6 +457,29 @@ def test_fp8_multi_query_full_size_sampled():
     out = ops.paged_decode_attention_fp8(q, k8, v8, inp.block_tables, inp.context_lens, inp.scale, K_SCALE, V_SCALE,
                                          max_context_len=inp.max_context_len, error_word=ew)
     assert ops.pkd_read_device_error(ew) == 0
-    rows = sample_rows(cfg.num_seqs * 8, cfg.num_q_heads, 64, seed=81)
-    got = out.view(-1, cfg.head_dim)[torch.from_numpy(rows).long().cuda()]
-    check_fp8(got, inp, q, k8, v8, "qwen25_7b_gqa7 E4M3 q_len=8", rows=rows)
+    check_fp8(out, inp, q, k8, v8, "qwen25_7b_gqa7 E4M3 q_len=8")
+
+
+@pytest.mark.parametrize("q_len", [4, 8])
+@pytest.mark.parametrize("variant", ["tma_mma", "tcgen05"])
+def test_fp8_ex_runs_the_requested_path(q_len, variant):
+    # paged_decode_attention_fp8_ex: either tensor-core path on request, whichever the
+    # automatic choice would take (GQA 7:1: q_len 4 is two 16-row tiles, mma.sync by default;
+    # q_len 8 is four, tcgen05 by default)
+    lens = [300, 33, 130, 1]
+    inp, q, k8, v8 = make_fp8(lens, q_len, 28, 4, 16, seed=101 + q_len)
+    plan = ops.paged_decode_call_plan(len(lens), q_len, 28, 4, 128, 16, max(lens), kv_fp8=True, variant=variant)
+    assert plan[3].split("+")[0] == variant
+    ew = errword()
+    out = ops.paged_decode_attention_fp8(q, k8, v8, inp.block_tables, inp.context_lens, inp.scale, K_SCALE, V_SCALE,
+                                         max_context_len=inp.max_context_len, variant=variant, error_word=ew)
+    assert ops.pkd_read_device_error(ew) == 0
+    check_fp8(out, inp, q, k8, v8, f"E4M3 {variant} q_len={q_len}")
+
+
+def test_fp8_ex_refuses_cuda_core_paths():
+    inp, q, k8, v8 = make_fp8([64, 20], 4, 28, 4, 16, seed=7)
+    with pytest.raises(ops.PagedDecodeError) as e:
+        ops.paged_decode_attention_fp8(q, k8, v8, inp.block_tables, inp.context_lens, inp.scale, K_SCALE, V_SCALE,
+                                       max_context_len=inp.max_context_len, variant="tma_staged")
+    assert e.value.status == 3  # PKD_ERR_UNSUPPORTED
