@@ -385,3 +385,34 @@ def test_length_past_the_table_row_is_reported_and_contained(variant, partition)
                                         error_word=ew)
     assert ops.pkd_read_device_error(ew) & ops.DEVERR_BAD_BLOCK
     assert_close(out[[0, 2]], ref[[0, 2]], "sequences with valid lengths")
+
+
+# --------------------------------------------------------------------------- prefetch distance
+def test_call_plan_reports_the_model_distance_for_this_device():
+    # the plan's default distance is the capacity model on this GPU's own numbers
+    props = torch.cuda.get_device_properties(0)
+    for name in FULL:
+        cfg = workloads.CONFIGS[name]
+        for variant in ("l2_prefetch", "tma_staged", "tma_mma"):
+            plan = ops.paged_decode_call_plan(cfg.num_seqs, 1, cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim,
+                                              cfg.block_size, cfg.max_context_len,
+                                              partition_size=cfg.partition_size or 0, variant=variant)
+            # the device's nominal bandwidth is not exposed to Python: a distance that the model gives
+            # for a range of bandwidths around GB300's must contain the one the library picked
+            ds = {ops.paged_decode_prefetch_model(cfg.num_seqs, 1, cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim,
+                                                  cfg.block_size, cfg.max_context_len, props.multi_processor_count,
+                                                  props.L2_cache_size, bw, partition_size=cfg.partition_size or 0,
+                                                  variant=variant)[0]
+                  for bw in (7.0e12, 8.18e12, 9.0e12)}
+            assert plan[5] in ds, (name, variant, plan, ds)
+
+
+@pytest.mark.parametrize("variant", ["l2_prefetch", "tma_staged", "tma_mma"])
+def test_prefetch_distances_change_no_bit(variant):
+    # none (-1), the model's default (0) and explicit distances give the same result bitwise
+    lens = [700, 33, 1500, 0, 129]
+    inp = workloads.make_custom(len(lens), 28, 4, 128, 16, lens, seed=61, device="cuda")
+    ref = run_ex(inp, variant, -1, prefetch_distance=-1)
+    for pd in (0, 1, 3):
+        assert torch.equal(run_ex(inp, variant, -1, prefetch_distance=pd), ref), pd
+    assert_close(ref, oracle_out(inp), f"{variant} without L2 prefetch")
