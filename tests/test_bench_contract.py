@@ -48,3 +48,31 @@ def test_l2_flush_reads_its_buffer():
     f = bench.L2Flush(torch.device("cpu"), 1 << 16)
     f()
     assert int(f.sink) == f.buf.numel()
+
+
+def test_parity_check_catches_wrong_rows():
+    # the bench's all-row comparison: passes within the tolerance, fails on one bad element,
+    # on a mean drift, and on a non-finite output
+    import numpy as np
+    import torch
+    import bench
+    ref = np.random.default_rng(0).standard_normal((4, 8, 16)) * 0.1
+    good = torch.from_numpy(ref).half()
+    p = bench.parity(good, ref)
+    assert p["ok"] and p["rows"] == "all" and p["n_rows"] == 32 and p["max_abs"] <= 1e-3
+    bad = good.clone()
+    bad[2, 5, 7] += 0.01
+    assert not bench.parity(bad, ref)["ok"]
+    drift = (good.double() + 6e-4).half()
+    assert not bench.parity(drift, ref)["ok"]
+    nan = good.clone()
+    nan[0, 0, 0] = float("nan")
+    assert not bench.parity(nan, ref)["ok"]
+
+
+def test_dtype_label_states_the_p_rounding():
+    import bench
+    assert "p rounded to f16" in bench.dtype_label("tma_mma", False)
+    assert "p rounded to f16" in bench.dtype_label("tcgen05+longest_first", True)
+    assert "e4m3" in bench.dtype_label("tma_mma", True)
+    assert "p rounded" not in bench.dtype_label("l2_prefetch", False)
