@@ -29,25 +29,27 @@
 //                    place before arriving on the stage's full barrier.
 //   warp 3, lane 0   MMA issuer: S = Q K^T (M = 128 rows, N = TN tokens,
 //                    K = head_dim) into one of two S buffers in tensor memory,
-//                    then, once the softmax has written P, O += P V
-//                    (M = 128, N = head_dim, K = TN tokens) into O in tensor
-//                    memory; completion is committed to mbarriers.  It polls
-//                    both conditions and issues whichever is ready first: S of
-//                    the next tile as soon as its K landed (and its S buffer
-//                    is free), P.V as soon as P is written, so the tensor
-//                    cores overlap the softmax and neither stage is held
-//                    behind the other.
+//                    then, once the softmax has written P over those S
+//                    columns, O += P V (M = 128, N = head_dim, K = TN tokens;
+//                    A read from tensor memory) into O in tensor memory;
+//                    completion is committed to mbarriers.  It polls both
+//                    conditions and issues whichever is ready first: S of the
+//                    next tile as soon as its K landed and its S buffer is
+//                    free (P.V of the tile two back completed), P.V as soon as
+//                    P is written, so the tensor cores overlap the softmax and
+//                    neither stage is held behind the other.
 //   warps 0-1        softmax, one thread per tile row (tensor-memory lane):
 //                    the row of S into registers, mask, online softmax in the
 //                    log2 domain with a lazy running maximum (the output is
 //                    rescaled in tensor memory only when the maximum grows by
-//                    more than kLazyTau), P rounded to fp16 into shared memory
-//                    (the MMA's A operand; two buffers, each rewritten once
-//                    P.V of the tile two back completed), and at the end O / l
-//                    to the output or the unnormalised partial for the split-K
-//                    merge.
+//                    more than kLazyTau), P rounded to fp16 and stored as
+//                    fp16 pairs over the tile's S columns (the A operand of
+//                    P.V, so no shared memory holds P and the K ring gets a
+//                    third stage), and at the end O / l to the output or the
+//                    unnormalised partial for the split-K merge.
 // The MMAs run M = 128 with the rows past kTcRows reading whatever follows
-// Q and P in shared memory: those accumulator rows are never read.
+// Q in shared memory: those accumulator rows, and the P rows made from them,
+// are never read, and each output row depends on its own A row only.
 //
 // The causal rule of multi-token queries is the one of the mma.sync path:
 // query jq sits at position L - q_len + jq and sees the tokens before and at
@@ -89,22 +91,19 @@ struct TcTraits {
   static constexpr int ROWS = kTcRows;
   static constexpr int TN = 64;            // tokens per tile
   static constexpr int NBT = TN / BS;      // cache blocks per tile
-  static constexpr int NSK = 2;            // K ring stages
-  static constexpr int NSV = 3;            // V ring stages
-  static constexpr int NPB = 2;            // P buffers
+  static constexpr int NSK = HD == 128 ? 3 : 4;  // K ring stages
+  static constexpr int NSV = HD == 128 ? 3 : 5;  // V ring stages
+  static constexpr int NPB = 2;            // S buffers in tensor memory, each then holding its tile's P
   static constexpr int ROWB = 128;         // bytes per swizzled row: 64 fp16
   static constexpr int QH = ROWS * ROWB;   // one 64-dim half of Q
-  static constexpr int PB = ROWS * ROWB;   // one P buffer (TN = 64 tokens per row)
   static constexpr int KVH = TN * ROWB;    // one 64-dim half of a K or V tile
   static constexpr int TILE = NH * KVH;    // a K or V tile: its halves
   static constexpr int Q_OFF = 0;
-  static constexpr int P_OFF = Q_OFF + NH * QH;
-  static constexpr int K_OFF = P_OFF + NPB * PB;
+  static constexpr int K_OFF = Q_OFF + NH * QH;
   static constexpr int V_OFF = K_OFF + NSK * TILE;
   static constexpr int MAIN = V_OFF + NSV * TILE;
-  static_assert(Q_OFF + (NH - 1) * QH + 128 * ROWB <= MAIN && P_OFF + (NPB - 1) * PB + 128 * ROWB <= MAIN,
-                "the M = 128 operand reads stay inside shared memory");
-  static_assert(TN == 64, "a P row is one 128-byte swizzled row");
+  static_assert(Q_OFF + (NH - 1) * QH + 128 * ROWB <= MAIN, "the M = 128 operand reads stay inside shared memory");
+  static_assert(TN % 16 == 0 && TN / 2 == 32, "P of a row: 32 columns of fp16 pairs, K = 16 tokens per 8");
   // kfull, kempty [NSK]; vfull, vempty [NSV]; sfull[2]; pfull, pfree [NPB]; drain;
   // E4M3: kland [NSK], vland [NSV] (the bytes landed, before widening)
   static constexpr int NBAR = 2 * NSK + 2 * NSV + 2 + 2 * NPB + 1 + (F8 ? NSK + NSV : 0);
@@ -116,7 +115,9 @@ struct TcTraits {
   static constexpr int THREADS = 160;
   static constexpr int MIN_BLOCKS = 2;
   static_assert(MIN_BLOCKS * (SMEM_BYTES + 1024) <= 228 * 1024, "two CTAs per SM");
-  static constexpr uint32_t TMEM_COLS = 256;  // O: columns 0-127; S buffer s: 128 + 64 s
+  // and never three: a third CTA's tensor-memory allocation would wait for one of them to finish
+  static_assert(3 * (SMEM_BYTES + 1024) > 228 * 1024, "at most two CTAs per SM");
+  static constexpr uint32_t TMEM_COLS = 256;  // O: columns 0-127; S (then P) buffer s: 128 + 64 s
   static constexpr uint32_t IDESC_S = tc_idesc_f16(128, TN, false);
   static constexpr uint32_t IDESC_O = tc_idesc_f16(128, D, true);
 };
@@ -140,8 +141,8 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, K
   uint64_t* vfull = kempty + NSK;  // [NSV] a V tile landed (with its bad-block mask)
   uint64_t* vempty = vfull + NSV;  // [NSV] P.V of the tile completed: the V stage is free
   uint64_t* sfull = vempty + NSV;  // [2] S of a tile is in tensor memory
-  uint64_t* pfull = sfull + 2;     // [NPB] P of a tile is in shared memory and its S was read
-  uint64_t* pfree = pfull + NPB;   // [NPB] P.V of a tile completed (its P buffer free, O stable)
+  uint64_t* pfull = sfull + 2;     // [NPB] P of a tile is in tensor memory over its S columns
+  uint64_t* pfree = pfull + NPB;   // [NPB] P.V of a tile completed (its S/P columns free, O stable)
   uint64_t* drain = pfree + NPB;   // every MMA issued completed
   uint64_t* kland = drain + 1;     // E4M3: [NSK] a K tile's bytes landed
   uint64_t* vland = kland + NSK;   // E4M3: [NSV] a V tile's bytes landed
@@ -344,6 +345,7 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, K
     const uint32_t ring = is_k ? T::K_OFF : T::V_OFF;
     int issued = 0, conv = 0;
     uint64_t t_idle = 0;
+    uint32_t idle_polls = 0;
     bool failed = false;
     while (conv < ntiles) {
       if (*abort_flag) break;
@@ -392,7 +394,7 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, K
       }
       if (progress) {
         t_idle = 0;
-      } else {  // nothing to do: give up after timeout_ns without progress
+      } else if ((++idle_polls & 15u) == 0u) {  // nothing to do: give up after timeout_ns without progress
         int give_up = 0;
         if (lane == 0) {
           const uint64_t now = globaltimer_ns();
@@ -462,36 +464,40 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, K
         any = true;
         return true;
       };
-      // Whichever is ready first: S of tile nq (its K landed, and its S buffer
-      // is free once P.V of tile nq - 2 was issued, i.e. nq <= npv + 1), or
-      // P.V of tile npv (its P written).  Neither waits behind the other.
+      // Whichever is ready first: S of tile nq (its K landed, and its S
+      // columns are free once P.V of tile nq - 2, which read its P from
+      // them, completed), or P.V of tile npv (its P written).  Neither waits
+      // behind the other.
       int nq = 0, npv = 0;
       bool ok = true;
       uint64_t t_idle = 0;
+      uint32_t idle_polls = 0;
       while (npv < ntiles) {
         if (*abort_flag) {
           ok = false;
           break;
         }
-        if (nq < ntiles && nq <= npv + 1 && mbar_test(&kfull[nq % NSK], (nq / NSK) & 1)) {
+        if (nq < ntiles && nq <= npv + 1 && (nq < NPB || mbar_test(&pfree[nq % NPB], ((nq - NPB) / NPB) & 1)) &&
+            mbar_test(&kfull[nq % NSK], (nq / NSK) & 1)) {
           if (!(ok = issue_qk(nq))) break;
           ++nq;
           t_idle = 0;
         } else if (npv < nq && mbar_test(&pfull[npv % NPB], (npv / NPB) & 1)) {
           tc_fence_after();
           const uint32_t vs = sbase + T::V_OFF + (npv % NSV) * T::TILE;
-          const uint32_t ps = sbase + T::P_OFF + (npv % NPB) * T::PB;
+          const uint32_t pa = tmem + 128 + 64 * (npv % NPB);  // P: 8 columns per 16 tokens
 #pragma unroll
-          for (int k = 0; k < TN / 16; ++k)  // 16 tokens: 32 bytes of a P row, 16 rows of V
-            tc_mma_f16(tmem, sw128_desc(ps + k * 32, 16, 1024), sw128_desc(vs + k * 16 * T::ROWB, T::KVH, 1024),
-                       T::IDESC_O, (npv > 0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < TN / 16; ++k)  // 16 tokens: 8 columns of P, 16 rows of V
+            tc_mma_f16_ts(tmem, pa + 8 * k, sw128_desc(vs + k * 16 * T::ROWB, T::KVH, 1024), T::IDESC_O,
+                          (npv > 0 || k > 0) ? 1u : 0u);
           tc_commit(&pfree[npv % NPB]);
           tc_commit(&vempty[npv % NSV]);
           ++npv;
           t_idle = 0;
-        } else {
+        } else if ((++idle_polls & 15u) == 0u) {
           // nothing ready: give up after timeout_ns without progress (the
-          // timer read also spaces the polls)
+          // timer is read on every 16th idle poll only: its read is slow,
+          // and it would delay noticing the barrier that completes next)
           const uint64_t now = globaltimer_ns();
           if (t_idle == 0) {
             t_idle = now;
@@ -575,7 +581,7 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, K
       // p = 2^(s * sc - mu), two lanes per packed FMA; the sum in four packed chains
       const float2 sc2 = make_float2(sc, sc), nmu2 = make_float2(-mu, -mu);
       float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      uint32_t pk[TN / 2];  // p as fp16 pairs
+      uint32_t pk[TN / 2];  // p as fp16 pairs: tokens 2e (lower half) and 2e + 1
 #pragma unroll
       for (int e = 0; e < TN / 2; ++e) {
         const float2 x = ffma2(make_float2(s[e / 16][(2 * e) % 32], s[e / 16][(2 * e + 1) % 32]), sc2, nmu2);
@@ -586,11 +592,6 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, K
       const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
       const float2 at = __fadd2_rn(a01, a23);
       l += at.x + at.y;
-      // this P buffer was last read by P.V of tile i - NPB
-      if (i >= NPB) {
-        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&pfree[i % NPB], ((i - NPB) / NPB) & 1, P.timeout_ns));
-        if (!ok) break;
-      }
       // O holds the earlier tiles once P.V of the previous one completed: rescale it in place
       if (i > 0 && rescale) {
         ok = __all_sync(0xffffffffu,
@@ -606,13 +607,10 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, K
           for (int e = 0; e < 32; ++e) o[e] *= alpha;
           tmem_st32(tl + 32 * c, o);
         }
-        tmem_st_wait();
       }
-      unsigned char* prow = smem + T::P_OFF + (i % NPB) * T::PB + rr * T::ROWB;
-#pragma unroll
-      for (int c = 0; c < TN / 8; ++c)
-        *reinterpret_cast<uint4*>(prow + ((c ^ (rr & 7)) << 4)) =
-            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      // P over this tile's S columns (read into registers above): the A operand of its P.V
+      tmem_st32u(tl + 128 + 64 * sb, pk);
+      tmem_st_wait();
       if (valid < TN || bad) {
         // V rows that hold no token of the CTA, or a bad block's: p = 0 there,
         // and 0 * NaN would not be 0
@@ -622,9 +620,9 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, K
           if (r >= valid || ((bad >> (r / BS)) & 1u))
             *reinterpret_cast<uint4*>(vt + h * T::KVH + r * T::ROWB + c * 16) = make_uint4(0u, 0u, 0u, 0u);
         }
+        fence_proxy_async_smem();  // the zeroed V rows visible to the tensor cores
       }
-      fence_proxy_async_smem();  // P (and zeroed V rows) visible to the tensor cores
-      tc_fence_before();         // our tensor-memory reads and writes ordered before the arrive
+      tc_fence_before();  // our tensor-memory reads and writes ordered before the arrive
       mbar_arrive(&pfull[i % NPB]);
     }
     if (ok && ntiles > 0)
