@@ -11,23 +11,35 @@
 // multi-token query (speculative verification) reads the cache once per
 // chunk of kTcRows / G tokens rather than once per 16 / G.
 //
-// Roles (five warps):
-//   warps 2 and 4,   producers: 3-D tensor copies of the partition's K (warp 2)
-//   lane 0           and V (warp 4) tiles of TN tokens (the 128-byte swizzled
+// Roles (five warps over fp16 caches, six over E4M3):
+//   fp16: warps 2    producers: 3-D tensor copies of the partition's K (warp 2)
+//   and 4, lane 0    and V (warp 4) tiles of TN tokens (the 128-byte swizzled
 //                    layout the MMA descriptors read) into two rings, NSK
 //                    stages for K and NSV for V, one mbarrier per stage with
 //                    the transaction count of its copies.  A K stage is free
 //                    again once S of its tile is computed, a V stage only
-//                    after P.V, so the V ring is the deeper one.  One thread
-//                    per ring: a tile's eight copies take about a thousand
-//                    cycles to issue from one thread, which bounded the tile
-//                    rate when one thread fed both rings.  Optionally, tiles
-//                    beyond the K ring are prefetched into L2
-//                    (cp.async.bulk.prefetch.L2).  E4M3 caches: the bytes land
-//                    in a stage's first 8 KiB behind a landing barrier, and
-//                    the whole producer warp widens them to the fp16 layout in
-//                    place before arriving on the stage's full barrier.
-//   warp 3, lane 0   MMA issuer: S = Q K^T (M = 128 rows, N = TN tokens,
+//                    after P.V.  One thread per ring: a tile's eight copies
+//                    take about a thousand cycles to issue from one thread,
+//                    which bounded the tile rate when one thread fed both
+//                    rings.  The block ids of a tile are read one issue ahead.
+//                    Optionally, tiles beyond the K ring are prefetched into
+//                    L2 (cp.async.bulk.prefetch.L2).
+//   E4M3: warp 5,    copy issuer: the copies of both rings (four per tile and
+//   lane 0           cache at block size 16), each as soon as its stage is
+//                    free; the bytes land in a stage's first 8 KiB behind a
+//                    landing barrier.  The block ids of a K tile are kept for
+//                    its V copy.
+//   E4M3: warps 2    wideners of the K (warp 2) and V (warp 3) rings: once a
+//   and 3            tile's bytes landed, the whole warp widens them in place
+//                    to the fp16 layout the MMAs read and arrives on the
+//                    stage's full barrier.  A warp that both issued and
+//                    widened was busy for about 70% of a tile period, and its
+//                    conversions delayed the next copies.  Warps 2 and 3 sit
+//                    on sub-partitions of their own (warp w runs on
+//                    sub-partition w % 4), where the softmax warps are not.
+//   warp 3 (fp16)    MMA issuer:
+//   or 4 (E4M3),
+//   lane 0 S = Q K^T (M = 128 rows, N = TN tokens,
 //                    K = head_dim) into one of two S buffers in tensor memory,
 //                    then, once the softmax has written P over those S
 //                    columns, O += P V (M = 128, N = head_dim, K = TN tokens;
@@ -107,12 +119,20 @@ struct TcTraits {
   // kfull, kempty [NSK]; vfull, vempty [NSV]; sfull[2]; pfull, pfree [NPB]; drain;
   // E4M3: kland [NSK], vland [NSV] (the bytes landed, before widening)
   static constexpr int NBAR = 2 * NSK + 2 * NSV + 2 + 2 * NPB + 1 + (F8 ? NSK + NSV : 0);
-  static constexpr int TAIL = NBAR * 8 + 8 + NSV * 4;
+  // roles: warps 0-1 softmax; fp16: warp 2 K producer, 3 MMA issuer, 4 V producer;
+  // E4M3: warp 2 K widener, 3 V widener, 4 MMA issuer, 5 copy issuer
+  static constexpr int W_K = 2;
+  static constexpr int W_V = F8 ? 3 : 4;
+  static constexpr int W_MMA = F8 ? 4 : 3;
+  static constexpr int W_COPY = 5;
+  static constexpr int NIDS = 8;  // E4M3: block ids (and bad mask) of the last NIDS K tiles, for their V copies
+  // barriers; tensor-memory address, abort flag; vbad [NSV]; E4M3: ids [NIDS][NBT + 1]
+  static constexpr int TAIL = NBAR * 8 + 8 + NSV * 4 + (F8 ? NIDS * (NBT + 1) * 4 : 0);
   // No alignment slack: a kernel without static shared memory gets a dynamic
   // window that starts 1024-byte aligned (checked at run time), and two CTAs
   // of 112 KiB fill the SM's 228 KiB with the 1 KiB each reserves.
   static constexpr int SMEM_BYTES = MAIN + ((TAIL + 15) / 16) * 16;
-  static constexpr int THREADS = 160;
+  static constexpr int THREADS = F8 ? 192 : 160;
   static constexpr int MIN_BLOCKS = 2;
   static_assert(MIN_BLOCKS * (SMEM_BYTES + 1024) <= 228 * 1024, "two CTAs per SM");
   // and never three: a third CTA's tensor-memory allocation would wait for one of them to finish
@@ -149,6 +169,7 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, K
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1 + (F8 ? NSK + NSV : 0));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile uint32_t* vbad = reinterpret_cast<volatile uint32_t*>(tmem_slot + 2);  // [NSV]
+  int32_t* tile_ids = reinterpret_cast<int32_t*>(tmem_slot + 2 + NSV);            // E4M3: [NIDS][NBT + 1]
 
   // work item: query chunk fastest, then partition j, then (b, g)
   const int G = P.num_q_heads / P.num_kv_heads;
@@ -199,7 +220,7 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, K
   const int lane = threadIdx.x % 32;
   const int nsw = rows > 32 ? 2 : 1;  // softmax warps
 
-  // ---- producer state (warp 2, lane 0: K; warp 4, lane 0: V)
+  // ---- producer state (fp16: warp 2, lane 0: K; warp 4, lane 0: V; E4M3: warp 5, lane 0: both)
   const L2Hints l2h = make_l2_hints(P.l2_hints != 0);
   const size_t tile_bytes = (size_t)BS * D * KVB;  // one (block, head) tile
   const size_t block_stride = (size_t)P.num_kv_heads * tile_bytes;
@@ -241,13 +262,23 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, K
       }
     }
   };
-  // block ids of tile i; bad ones (reported once, with the K copy) are skipped
-  auto tile_blocks = [&](int i, int (&pbs)[T::NBT], bool report) -> uint32_t {
+  // Block ids of tile i as stored (-1 past the partition), read one issue
+  // ahead of their use so that no copy waits for a block-table read.
+  auto load_ids = [&](int i, int (&raw)[T::NBT]) {
+#pragma unroll
+    for (int kk = 0; kk < T::NBT; ++kk) {
+      const int k = i * T::NBT + kk;
+      raw[kk] = (i < ntiles && k < nblk) ? bt[k] : -1;
+    }
+  };
+  // The ids of tile i to copy: bad ones (reported once, with the K copy) and
+  // those past the partition are skipped (-1); returns the bad-block mask.
+  auto check_ids = [&](int i, const int (&raw)[T::NBT], int (&pbs)[T::NBT], bool report) -> uint32_t {
     uint32_t bad = 0;
 #pragma unroll
     for (int kk = 0; kk < T::NBT; ++kk) {
       const int k = i * T::NBT + kk;
-      int pb = k < nblk ? bt[k] : -1;
+      int pb = k < nblk ? raw[kk] : -1;
       if (k < nblk && (pb < 0 || pb >= P.num_blocks)) {
         bad |= 1u << kk;
         if (report) record_error(P.error_word, kErrBadBlock);
@@ -263,24 +294,28 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, K
     for (int kk = 0; kk < T::NBT; ++kk) bytes += pbs[kk] >= 0 ? BS * D * KVB : 0;  // the block's rows
     return bytes;
   };
-  // Issue the copies of tile kissued (K) / vissued (V) into its stage.
+  // fp16: issue the copies of tile kissued (K) / vissued (V) into its stage;
+  // kraw / vraw hold that tile's block ids.
+  int kraw[T::NBT], vraw[T::NBT];
   auto issue_k = [&]() {
     int pbs[T::NBT];
-    tile_blocks(kissued, pbs, true);
+    check_ids(kissued, kraw, pbs, true);
     const int sk = kissued % NSK;
     mbar_arrive_expect_tx(&kfull[sk], tile_bytes_of(pbs));
     copy_tile(sbase + T::K_OFF + sk * T::TILE, &tmap_k, &kfull[sk], pbs);
     ++kissued;
+    load_ids(kissued, kraw);
     prefetch_upto(kissued + P.prefetch_distance);
   };
   auto issue_v = [&]() {
     int pbs[T::NBT];
-    const uint32_t bad = tile_blocks(vissued, pbs, false);
+    const uint32_t bad = check_ids(vissued, vraw, pbs, false);
     const int sv = vissued % NSV;
     vbad[sv] = bad;
     mbar_arrive_expect_tx(&vfull[sv], tile_bytes_of(pbs));
     copy_tile(sbase + T::V_OFF + sv * T::TILE, &tmap_v, &vfull[sv], pbs);
     ++vissued;
+    load_ids(vissued, vraw);
   };
 
   // Barriers are set up before the CTA-wide barrier; the producer starts after
@@ -311,7 +346,7 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, K
     *abort_flag = 0;
     fence_mbarrier_init();
   }
-  if (warp == 3) {
+  if (warp == T::W_MMA) {
     tmem_alloc(tmem_slot, T::TMEM_COLS);
     tmem_relinquish();
   }
@@ -331,94 +366,122 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, K
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if ((warp == 2 || warp == 4) && F8) {
-    // ------------------------------------------------------------ producers, E4M3
-    // Lane 0 issues the copies of the bytes; once a tile's bytes landed the
-    // whole warp widens them in place to the fp16 layout the MMAs read (every
-    // lane reads its 16 chunks of the 8 KiB before any lane writes the 16 KiB),
-    // then arrives on the tile's full barrier.  Lane 0 decides, the warp follows.
-    const bool is_k = warp == 2;
-    const int ns = is_k ? NSK : NSV;
-    uint64_t* empty_bar = is_k ? kempty : vempty;
-    uint64_t* land_bar = is_k ? kland : vland;
-    uint64_t* full_bar = is_k ? kfull : vfull;
-    const uint32_t ring = is_k ? T::K_OFF : T::V_OFF;
-    int issued = 0, conv = 0;
-    uint64_t t_idle = 0;
-    uint32_t idle_polls = 0;
-    bool failed = false;
-    while (conv < ntiles) {
-      if (*abort_flag) break;
-      bool progress = false;
-      int can = lane == 0 && issued < ntiles &&
-                (issued < ns || mbar_test(&empty_bar[issued % ns], ((issued / ns) - 1) & 1));
-      if (__shfl_sync(0xffffffffu, can, 0)) {
-        if (lane == 0) {
-          int pbs[T::NBT];
-          const uint32_t bad = tile_blocks(issued, pbs, is_k);
-          const int st = issued % ns;
-          if (!is_k) vbad[st] = bad;
-          mbar_arrive_expect_tx(&land_bar[st], tile_bytes_of(pbs));
-          copy_tile(sbase + ring + st * T::TILE, is_k ? &tmap_k : &tmap_v, &land_bar[st], pbs);
-        }
-        ++issued;
-        progress = true;
-      }
-      can = lane == 0 && conv < issued && mbar_test(&land_bar[conv % ns], (conv / ns) & 1);
-      if (__shfl_sync(0xffffffffu, can, 0)) {
-        const int st = conv % ns;
-        mbar_wait_bounded(&land_bar[st], (conv / ns) & 1, P.timeout_ns);  // every lane acquires the bytes
-        unsigned char* stg = smem + ring + st * T::TILE;
-        uint4 in[16];  // chunk q = lane + 32 k: row q / 8, stored chunk q % 8
-#pragma unroll
-        for (int k = 0; k < 16; ++k) in[k] = *reinterpret_cast<const uint4*>(stg + 16 * (lane + 32 * k));
-        __syncwarp();
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const int q = lane + 32 * k, r = q >> 3;
-          const int j = (q & 7) ^ (r & 7);  // dims 16 j .. 16 j + 15 of row r
-          uint4 lo, hi;                     // fp16 dims 16 j .. +7 and 16 j + 8 .. +15
-          e4m3x4_to_f16x2x2(in[k].x, lo.x, lo.y);
-          e4m3x4_to_f16x2x2(in[k].y, lo.z, lo.w);
-          e4m3x4_to_f16x2x2(in[k].z, hi.x, hi.y);
-          e4m3x4_to_f16x2x2(in[k].w, hi.z, hi.w);
-          const int c0 = 2 * j;  // fp16 chunk (of 16 over both 64-dim halves)
-          *reinterpret_cast<uint4*>(stg + (c0 >> 3) * T::KVH + r * T::ROWB + (((c0 & 7) ^ (r & 7)) << 4)) = lo;
-          const int c1 = c0 + 1;
-          *reinterpret_cast<uint4*>(stg + (c1 >> 3) * T::KVH + r * T::ROWB + (((c1 & 7) ^ (r & 7)) << 4)) = hi;
-        }
-        fence_proxy_async_smem();  // visible to the tensor cores
-        mbar_arrive(&full_bar[st]);
-        ++conv;
-        progress = true;
-      }
-      if (progress) {
-        t_idle = 0;
-      } else if ((++idle_polls & 15u) == 0u) {  // nothing to do: give up after timeout_ns without progress
-        int give_up = 0;
-        if (lane == 0) {
-          const uint64_t now = globaltimer_ns();
-          if (t_idle == 0) t_idle = now;
-          else give_up = now - t_idle > P.timeout_ns;
-        }
-        if (__shfl_sync(0xffffffffu, give_up, 0)) {
-          failed = true;
-          break;
-        }
-      }
-    }
+  if (F8 && warp == T::W_COPY) {
+    // ------------------------------------------------------------ copy issuer, E4M3
+    // K copies of tile kissued once its stage is free (S of the tile NSK back
+    // computed), V copies of tile vissued once its stage is free (P.V of the
+    // tile NSV back completed), whichever is possible first.
     if (lane == 0) {
+      int raw[T::NBT];
+      load_ids(0, raw);
+      uint64_t t_idle = 0;
+      uint32_t idle_polls = 0;
+      bool failed = false;
+      while (vissued < ntiles) {
+        if (*abort_flag) break;
+        bool progress = false;
+        if (kissued < ntiles && kissued - vissued < T::NIDS &&
+            (kissued < NSK || mbar_test(&kempty[kissued % NSK], ((kissued / NSK) - 1) & 1))) {
+          int pbs[T::NBT];
+          const uint32_t bad = check_ids(kissued, raw, pbs, true);
+          int32_t* ids = tile_ids + (kissued % T::NIDS) * (T::NBT + 1);
+#pragma unroll
+          for (int kk = 0; kk < T::NBT; ++kk) ids[kk] = pbs[kk];
+          ids[T::NBT] = (int32_t)bad;
+          const int sk = kissued % NSK;
+          mbar_arrive_expect_tx(&kland[sk], tile_bytes_of(pbs));
+          copy_tile(sbase + T::K_OFF + sk * T::TILE, &tmap_k, &kland[sk], pbs);
+          ++kissued;
+          load_ids(kissued, raw);
+          prefetch_upto(kissued + P.prefetch_distance);
+          progress = true;
+        }
+        if (vissued < kissued && (vissued < NSV || mbar_test(&vempty[vissued % NSV], ((vissued / NSV) - 1) & 1))) {
+          const int32_t* ids = tile_ids + (vissued % T::NIDS) * (T::NBT + 1);
+          int pbs[T::NBT];
+#pragma unroll
+          for (int kk = 0; kk < T::NBT; ++kk) pbs[kk] = ids[kk];
+          const int sv = vissued % NSV;
+          vbad[sv] = (uint32_t)ids[T::NBT];
+          mbar_arrive_expect_tx(&vland[sv], tile_bytes_of(pbs));
+          copy_tile(sbase + T::V_OFF + sv * T::TILE, &tmap_v, &vland[sv], pbs);
+          ++vissued;
+          progress = true;
+        }
+        if (progress) {
+          t_idle = 0;
+        } else if ((++idle_polls & 15u) == 0u) {  // nothing to do: give up after timeout_ns without progress
+          const uint64_t now = globaltimer_ns();
+          if (t_idle == 0) {
+            t_idle = now;
+          } else if (now - t_idle > P.timeout_ns) {
+            failed = true;
+            break;
+          }
+        }
+      }
       if (failed) {
         record_error(P.error_word, kErrTimeout);
         *abort_flag = 1;
       }
-      if (*abort_flag)  // let the copies in flight land before the CTA exits
-        for (int t = conv; t < issued; ++t) mbar_wait_bounded(&land_bar[t % ns], (t / ns) & 1, P.timeout_ns);
+      if (*abort_flag) {  // let the copies in flight land before the CTA exits
+        for (int t = kissued > NSK ? kissued - NSK : 0; t < kissued; ++t)
+          mbar_wait_bounded(&kland[t % NSK], (t / NSK) & 1, P.timeout_ns);
+        for (int t = vissued > NSV ? vissued - NSV : 0; t < vissued; ++t)
+          mbar_wait_bounded(&vland[t % NSV], (t / NSV) & 1, P.timeout_ns);
+      }
     }
-  } else if (warp == 2 || warp == 4) {
+  } else if (F8 && (warp == T::W_K || warp == T::W_V)) {
+    // ------------------------------------------------------------ wideners, E4M3
+    // Once a tile's bytes landed, the whole warp widens them in place to the
+    // fp16 layout the MMAs read (every lane reads its 16 chunks of the 8 KiB
+    // before any lane writes the 16 KiB), then arrives on the tile's full barrier.
+    const bool is_k = warp == T::W_K;
+    const int ns = is_k ? NSK : NSV;
+    uint64_t* land_bar = is_k ? kland : vland;
+    uint64_t* full_bar = is_k ? kfull : vfull;
+    const uint32_t ring = is_k ? T::K_OFF : T::V_OFF;
+    for (int t = 0; t < ntiles; ++t) {
+      const int st = t % ns;
+      const bool got = !*abort_flag && mbar_wait_bounded(&land_bar[st], (t / ns) & 1, P.timeout_ns);
+      if (!__all_sync(0xffffffffu, got)) {
+        if (lane == 0) {
+          if (!*abort_flag) record_error(P.error_word, kErrTimeout);
+          *abort_flag = 1;
+        }
+        break;
+      }
+      unsigned char* stg = smem + ring + st * T::TILE;
+      uint4 in[16];  // chunk q = lane + 32 k: row q / 8, stored chunk q % 8
+#pragma unroll
+      for (int k = 0; k < 16; ++k) in[k] = *reinterpret_cast<const uint4*>(stg + 16 * (lane + 32 * k));
+      __syncwarp();
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const int q = lane + 32 * k, r = q >> 3;
+        const int j = (q & 7) ^ (r & 7);  // dims 16 j .. 16 j + 15 of row r
+        uint4 lo, hi;                     // fp16 dims 16 j .. +7 and 16 j + 8 .. +15
+        e4m3x4_to_f16x2x2(in[k].x, lo.x, lo.y);
+        e4m3x4_to_f16x2x2(in[k].y, lo.z, lo.w);
+        e4m3x4_to_f16x2x2(in[k].z, hi.x, hi.y);
+        e4m3x4_to_f16x2x2(in[k].w, hi.z, hi.w);
+        const int c0 = 2 * j;  // fp16 chunk (of 16 over both 64-dim halves)
+        *reinterpret_cast<uint4*>(stg + (c0 >> 3) * T::KVH + r * T::ROWB + (((c0 & 7) ^ (r & 7)) << 4)) = lo;
+        const int c1 = c0 + 1;
+        *reinterpret_cast<uint4*>(stg + (c1 >> 3) * T::KVH + r * T::ROWB + (((c1 & 7) ^ (r & 7)) << 4)) = hi;
+      }
+      fence_proxy_async_smem();  // visible to the tensor cores
+      mbar_arrive(&full_bar[st]);
+    }
+  } else if (!F8 && (warp == T::W_K || warp == T::W_V)) {
     // ------------------------------------------------------------ producers, fp16
     if (lane == 0) {
-      const bool is_k = warp == 2;
+      const bool is_k = warp == T::W_K;
+      if (is_k) {
+        load_ids(0, kraw);
+      } else {
+        load_ids(0, vraw);
+      }
       const int ns = is_k ? NSK : NSV;
       uint64_t* empty_bar = is_k ? kempty : vempty;
       while ((is_k ? kissued : vissued) < ntiles) {
@@ -442,7 +505,7 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, K
           mbar_wait_bounded(&full_bar[k % ns], (k / ns) & 1, P.timeout_ns);
       }
     }
-  } else if (warp == 3) {
+  } else if (warp == T::W_MMA) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t qs = sbase + T::Q_OFF;
@@ -679,7 +742,7 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, K
   // tensor memory is freed once every warp is done with it
   tc_fence_before();
   __syncthreads();
-  if (warp == 3) {
+  if (warp == T::W_MMA) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, T::TMEM_COLS);
