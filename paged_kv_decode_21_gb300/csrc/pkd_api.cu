@@ -393,22 +393,20 @@ int query_chunks(int q_len, int G, int path = PKD_VARIANT_TMA_MMA) {
 // q_len x G rows per CTA and reads the partition's K and V once per tile; the
 // tcgen05 kernel serves up to 64 rows from one read, with S and O in tensor
 // memory.  Measured on the full workloads it wins from kTcMinTiles tiles on
-// (GQA 7:1: q_len 8, four tiles, 717 against 1163 us; q_len 4, two tiles, 709
-// against 721 us; GQA 4:1, q_len 8, two tiles, 207 against 227 us) and loses
-// at one (GQA 4:1, q_len 4: 203 against 183 us).
-// E4M3 caches are widened to fp16 in shared memory by the producer warps on
-// the tcgen05 path, on the critical path of every tile; there it only wins
-// from kTcMinTilesFp8 tiles on (GQA 7:1, q_len 8, four tiles: 1027 against
-// 1171 us; GQA 5:1 at 512-token partitions, q_len 8, three tiles: 980 against
-// 1190 us) and loses at two (GQA 7:1, q_len 4: 970 against 629 us; GQA 4:1,
-// q_len 8: 269 against 215 us).
+// and loses at one, over fp16 caches (GQA 7:1: q_len 8, four tiles, 686
+// against 1164 us; q_len 4, two tiles, 682 against 719 us; GQA 4:1, q_len 8,
+// two tiles, 200 against 226 us; q_len 4, one tile, 200 against 182 us) and
+// over E4M3 caches, whose tiles the tcgen05 kernel widens to fp16 in shared
+// memory (GQA 7:1, q_len 8: 661 against 1175 us; GQA 4:1, q_len 8, two tiles:
+// 191 against 217 us; the other two-tile shapes within 2%: GQA 7:1, q_len 4,
+// 639 against 629 us; GQA 5:1 at 512-token partitions, q_len 4, 763 against
+// 749 us).
 constexpr int kTcMinTiles = 2;
 // head_dim 128, or 64 with fp16 caches (E4M3 rows are widened at 128 only)
 bool tc_supports(const Shape& s, int kv_fp8) { return s.head_dim == 128 || (s.head_dim == 64 && !kv_fp8); }
-constexpr int kTcMinTilesFp8 = 3;
 int auto_multi_path(const Shape& s, int q_len, int kv_fp8) {
   const int G = s.num_q_heads / s.num_kv_heads;
-  if (tc_supports(s, kv_fp8) && query_chunks(q_len, G, PKD_VARIANT_TMA_MMA) >= (kv_fp8 ? kTcMinTilesFp8 : kTcMinTiles))
+  if (tc_supports(s, kv_fp8) && query_chunks(q_len, G, PKD_VARIANT_TMA_MMA) >= kTcMinTiles)
     return PKD_VARIANT_TCGEN05;
   return PKD_VARIANT_TMA_MMA;
 }

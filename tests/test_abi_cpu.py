@@ -285,11 +285,11 @@ def test_call_plan_picks_the_tensor_core_path(L):
     assert ops.paged_decode_call_plan(4, 4, 28, 4, 128, 16, 1000)[3] == "tcgen05"   # 2 tiles
     assert ops.paged_decode_call_plan(4, 8, 32, 8, 128, 16, 1000)[3] == "tcgen05"   # 2 tiles
     assert ops.paged_decode_call_plan(4, 17, 4, 4, 128, 16, 1000)[3] == "tcgen05"   # G=1: 2 tiles
-    # E4M3 caches: from three tiles on
+    # E4M3 caches: the same rule
     assert ops.paged_decode_call_plan(4, 8, 28, 4, 128, 16, 1000, kv_fp8=True)[3] == "tcgen05"   # 4 tiles
     assert ops.paged_decode_call_plan(4, 8, 40, 8, 128, 16, 1000, kv_fp8=True)[3] == "tcgen05"   # 3 tiles
-    assert ops.paged_decode_call_plan(4, 4, 28, 4, 128, 16, 1000, kv_fp8=True)[3] == "tma_mma"   # 2 tiles
-    assert ops.paged_decode_call_plan(4, 8, 32, 8, 128, 16, 1000, kv_fp8=True)[3] == "tma_mma"   # 2 tiles
+    assert ops.paged_decode_call_plan(4, 4, 28, 4, 128, 16, 1000, kv_fp8=True)[3] == "tcgen05"   # 2 tiles
+    assert ops.paged_decode_call_plan(4, 8, 32, 8, 128, 16, 1000, kv_fp8=True)[3] == "tcgen05"   # 2 tiles
     # one tile, head_dim 64 or a single query: the mma.sync path
     assert ops.paged_decode_call_plan(4, 2, 28, 4, 128, 16, 1000)[3] == "tma_mma"
     assert ops.paged_decode_call_plan(4, 4, 32, 8, 128, 16, 1000)[3] == "tma_mma"

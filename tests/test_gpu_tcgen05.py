@@ -464,8 +464,8 @@ def test_fp8_multi_query_full_size_all_rows():
 @pytest.mark.parametrize("variant", ["tma_mma", "tcgen05"])
 def test_fp8_ex_runs_the_requested_path(q_len, variant):
     # paged_decode_attention_fp8_ex: either tensor-core path on request, whichever the
-    # automatic choice would take (GQA 7:1: q_len 4 is two 16-row tiles, mma.sync by default;
-    # q_len 8 is four, tcgen05 by default)
+    # automatic choice would take (GQA 7:1: q_len 4 is two 16-row mma.sync tiles, q_len 8
+    # four; both run tcgen05 by default)
     lens = [300, 33, 130, 1]
     inp, q, k8, v8 = make_fp8(lens, q_len, 28, 4, 16, seed=101 + q_len)
     plan = ops.paged_decode_call_plan(len(lens), q_len, 28, 4, 128, 16, max(lens), kv_fp8=True, variant=variant)
