@@ -94,9 +94,10 @@ typedef enum {
                                   softmax thread per query row; up to 64 query rows (query
                                   tokens x group heads) share one read of the K/V tiles.
                                   fp16 caches at head_dim 64 or 128 by this variant; E4M3
-                                  caches at head_dim 128 when the automatic choice of
-                                  paged_decode_attention_fp8 picks it (the bytes are widened
-                                  to fp16 in shared memory); PKD_ERR_UNSUPPORTED otherwise */
+                                  caches at head_dim 128 through paged_decode_attention_fp8
+                                  (its automatic choice) or _fp8_ex (on request), the bytes
+                                  widened to fp16 in shared memory; PKD_ERR_UNSUPPORTED
+                                  otherwise */
 } pkd_variant;
 
 /*
@@ -465,6 +466,9 @@ size_t paged_decode_multi_workspace_size(int num_seqs, int q_len, int num_q_head
  * The scores use the exact fp16 value of every code (all E4M3 values are
  * fp16 values); the K scale multiplies the softmax scale, and the V scale the
  * result.  Codes that are NaN (0x7f, 0xff) must not appear in used rows.
+ * Data path, as for paged_decode_attention_multi: PKD_VARIANT_TMA_MMA where
+ * the q_len x G rows of a (sequence, kv head) fit one 16-row tile or
+ * head_dim is 64, else PKD_VARIANT_TCGEN05.
  */
 pkd_status paged_decode_attention_fp8(const void* q, const void* k_cache, const void* v_cache,
                                       const int32_t* block_tables, const int32_t* context_lens, void* out,
