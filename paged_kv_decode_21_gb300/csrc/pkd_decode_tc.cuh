@@ -318,6 +318,14 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, K
     load_ids(vissued, vraw);
   };
 
+  // fp16: the first tile's block ids are read before the CTA-wide barrier, so
+  // that the first copies do not wait for the block table (2% on 512-token
+  // partitions; the E4M3 copy issuer measured 3-6% slower with it).
+  if (!F8 && lane == 0) {
+    if (warp == T::W_K) load_ids(0, kraw);
+    if (warp == T::W_V) load_ids(0, vraw);
+  }
+
   // Barriers are set up before the CTA-wide barrier; the producer starts after
   // it.  (Issuing the first copies from the producer lane before that barrier,
   // to overlap the Q load, measured 13-16% slower on the same GPU: MHA 412
@@ -477,11 +485,6 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, K
     // ------------------------------------------------------------ producers, fp16
     if (lane == 0) {
       const bool is_k = warp == T::W_K;
-      if (is_k) {
-        load_ids(0, kraw);
-      } else {
-        load_ids(0, vraw);
-      }
       const int ns = is_k ? NSK : NSV;
       uint64_t* empty_bar = is_k ? kempty : vempty;
       while ((is_k ? kissued : vissued) < ntiles) {
