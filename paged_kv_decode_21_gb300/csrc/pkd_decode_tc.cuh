@@ -34,14 +34,10 @@
 //                    to the fp16 layout the MMAs read and arrives on the
 //                    stage's full barrier.  A warp that both issued and
 //                    widened was busy for about 70% of a tile period, and its
-//                    conversions delayed the next copies.  Warps 2 and 3 sit
-//                    on sub-partitions of their own (warp w runs on
-//                    sub-partition w % 4), where the softmax warps are not.
-//   warp 3 (fp16)    MMA issuer:
-//   or 4 (E4M3),
-//   lane 0 S = Q K^T (M = 128 rows, N = TN tokens,
-//                    K = head_dim) into one of two S buffers in tensor memory,
-//                    then, once the softmax has written P over those S
+//                    conversions delayed the next copies.
+//   warp 3 (fp16)    MMA issuer: S = Q K^T (M = 128 rows, N = TN tokens,
+//   or 4 (E4M3),     K = head_dim) into one of two S buffers in tensor memory,
+//   lane 0           then, once the softmax has written P over those S
 //                    columns, O += P V (M = 128, N = head_dim, K = TN tokens;
 //                    A read from tensor memory) into O in tensor memory;
 //                    completion is committed to mbarriers.  It polls both
@@ -89,7 +85,7 @@ constexpr uint32_t kErrLayout = 4u;  // dynamic shared memory not 1024-byte alig
 constexpr int tc_query_chunk(int G) { return kTcRows / G; }
 
 // KVB: bytes per K/V element in the caches (2: fp16; 1: E4M3 bytes, widened
-// to fp16 in shared memory by the producer warps before the MMAs read them).
+// to fp16 in shared memory by the widening warps before the MMAs read them).
 // HD: head_dim, 128 (two 64-dim halves per row) or 64 (one; fp16 only).
 template <int BS, int KVB = 2, int HD = 128>
 struct TcTraits {
