@@ -215,6 +215,26 @@ def test_auto_partition_policy(L):
         assert 0 < p1 and p1 % 32 == 0
 
 
+def test_small_grid_split_fills_one_wave():
+    # Single-query calls on the mma.sync tensor-core path whose (sequence, kv head) units cover
+    # less than one resident wave take the shortest power-of-two partition (128..2048 tokens)
+    # whose grid still fits one wave (three CTAs per SM; 148 SMs without a GPU).
+    from paged_kv_decode_21_gb300 import ops
+    slots = 148 * 3
+    for B, Hq, Hkv, L, want in [(1, 32, 32, 2048, 256), (4, 32, 32, 2048, 1024), (1, 32, 8, 2048, 128),
+                                (16, 32, 8, 2048, 1024), (16, 28, 4, 8192, 2048), (4, 28, 4, 8192, 512),
+                                (1, 28, 4, 8192, 128)]:
+        n, P, _, var, grid, _ = ops.paged_decode_call_plan(B, 1, Hq, Hkv, 128, 16, L)
+        assert var == "tma_mma" and P == want, (B, Hq, Hkv, L, P)
+        assert grid == B * Hkv * -(-L // P) <= slots
+        assert P == 128 or B * Hkv * -(-L // (P // 2)) > slots
+    # more units than a wave: the waves-based split (512 at least), unchanged
+    assert ops.paged_decode_call_plan(16, 1, 32, 32, 128, 16, 2048)[1] == 512
+    assert ops.paged_decode_call_plan(16, 1, 32, 32, 128, 16, 8192)[1] == 2048
+    # the CUDA-core paths keep the waves-based split
+    assert ops.paged_decode_call_plan(1, 1, 32, 32, 128, 16, 2048, variant="tma_staged")[1] == 512
+
+
 def test_workspace_sizes_cover_every_plan(L):
     # For random shapes, partitions and flags, a workspace of exactly the reported size is
     # never refused (PKD_ERR_WORKSPACE = 5); without a GPU the call then fails at launch
