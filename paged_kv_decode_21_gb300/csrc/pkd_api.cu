@@ -19,7 +19,8 @@ namespace {
 constexpr unsigned long long kWaitBudgetNs = 100ull * 1000ull * 1000ull;  // 100 ms per bounded wait
 constexpr int kMinAutoPartition = 512;
 constexpr int kMaxAutoPartition = 2048;
-constexpr int kMinSmallGridPartition = 128;  // the shortest partition of the one-wave rule (auto_partition)
+constexpr int kMinSmallGridPartition = 128;    // the shortest partition of the one-wave rule (auto_partition)
+constexpr int kMinSmallGridPartitionTc = 256;  // the same on the tcgen05 path (64-token tiles)
 // The tcgen05 kernel pays a longer fill per CTA (its two-stage K ring meets the
 // first copies' full HBM latency), so it is split less: only below kSplitWaves
 // waves whatever the context length, into partitions of up to
@@ -322,22 +323,31 @@ int auto_partition(const Shape& s, int variant = PKD_VARIANT_AUTO, int q_chunks 
   const long long want = kTargetWaves * wave;
   const long long np = (want + units - 1) / units;
   const long long per = (s.max_context_len + np - 1) / np;
-  // Small grids on the mma.sync tensor-core path: the target above would
-  // want partitions shorter than kMinAutoPartition, and a grid just past one
-  // resident wave runs a second, nearly empty one.  Measured on single-query
-  // batches of 1-16 (MHA, GQA 4:1 and GQA 7:1 shapes at 2048 and 8192
-  // tokens, every power-of-two partition from 128 to 2048), the fastest
-  // split was the one with the most CTAs that still fit one resident wave in
-  // 15 of 18 shapes (7-32% faster than the 512-token minimum, e.g. GQA 7:1,
-  // batch 16, 8192 tokens: 50.1 us at 2048 against 57.4 at 512), and within
-  // 6% of it in the others.
-  if (!tc && q_chunks == 1 && resolve_variant(variant) == PKD_VARIANT_TMA_MMA) {
+  // Small grids on the tensor-core paths: the target above would want
+  // partitions shorter than kMinAutoPartition, and a grid just past one
+  // resident wave runs a second, nearly empty one.  The partition is the
+  // shortest power of two whose grid still fits one resident wave (three
+  // CTAs per SM on the mma.sync path, two on the tcgen05 path).  Measured on
+  // batches of 1-16 at 2048 and 8192 tokens, every power-of-two partition:
+  //  * mma.sync, single query (MHA, GQA 4:1, GQA 7:1): the fastest split in
+  //    15 of 18 shapes and within 6% in the others (the 512-token minimum
+  //    was up to 1.34x slower: GQA 4:1, batch 1, 2048 tokens, 12.5 against
+  //    16.4 us);
+  //  * tcgen05, 8 query tokens (GQA 4:1, GQA 7:1; fp16 and E4M3): the
+  //    fastest in 23 of 24 and within 2.5% in the last (the automatic split
+  //    before was up to 1.39x slower: GQA 7:1, batch 16, 8192 tokens, E4M3,
+  //    57.6 against 80.2 us).
+  // Ragged batches gain less: the plan sees only the longest context.
+  if (tc || (q_chunks == 1 && resolve_variant(variant) == PKD_VARIANT_TMA_MMA)) {
     int sms = sm_count();
     if (sms <= 0) sms = 148;
+    const int G = s.num_q_heads / s.num_kv_heads;
     const long long slots =
-        (long long)sms * path_stream(PKD_VARIANT_TMA_MMA, s.head_dim, s.num_q_heads / s.num_kv_heads, 2, false)
-                             .ctas_per_sm;
-    for (long long q = kMinSmallGridPartition; q <= kMaxAutoPartition && q < s.max_context_len; q *= 2)
+        (long long)sms * (tc ? path_stream(PKD_VARIANT_TCGEN05, s.head_dim, G, 2, false).ctas_per_sm
+                             : path_stream(PKD_VARIANT_TMA_MMA, s.head_dim, G, 2, false).ctas_per_sm);
+    const long long qmax = tc ? kMaxAutoPartitionTc : kMaxAutoPartition;
+    for (long long q = tc ? kMinSmallGridPartitionTc : kMinSmallGridPartition; q <= qmax && q < s.max_context_len;
+         q *= 2)
       if (units * ((s.max_context_len + q - 1) / q) <= slots) return (int)q;
   }
   const long long pmax = tc ? kMaxAutoPartitionTc : kMaxAutoPartition;

@@ -216,9 +216,9 @@ def test_auto_partition_policy(L):
 
 
 def test_small_grid_split_fills_one_wave():
-    # Single-query calls on the mma.sync tensor-core path whose (sequence, kv head) units cover
-    # less than one resident wave take the shortest power-of-two partition (128..2048 tokens)
-    # whose grid still fits one wave (three CTAs per SM; 148 SMs without a GPU).
+    # Calls on a tensor-core path whose (sequence, kv head) units cover less than one resident
+    # wave take the shortest power-of-two partition whose grid still fits one wave: single query
+    # on mma.sync, 128..2048 tokens, three CTAs per SM (148 SMs without a GPU).
     from paged_kv_decode_21_gb300 import ops
     slots = 148 * 3
     for B, Hq, Hkv, L, want in [(1, 32, 32, 2048, 256), (4, 32, 32, 2048, 1024), (1, 32, 8, 2048, 128),
@@ -228,6 +228,14 @@ def test_small_grid_split_fills_one_wave():
         assert var == "tma_mma" and P == want, (B, Hq, Hkv, L, P)
         assert grid == B * Hkv * -(-L // P) <= slots
         assert P == 128 or B * Hkv * -(-L // (P // 2)) > slots
+    # the tcgen05 path (multi-token queries): two CTAs per SM, partitions of 256..8192 tokens
+    for B, Hq, Hkv, L, want in [(1, 32, 8, 2048, 256), (16, 32, 8, 2048, 1024), (16, 32, 8, 8192, 4096),
+                                (16, 28, 4, 8192, 2048), (4, 28, 4, 8192, 512)]:
+        for fp8 in (False, True):
+            n, P, _, var, grid, _ = ops.paged_decode_call_plan(B, 8, Hq, Hkv, 128, 16, L, kv_fp8=fp8)
+            assert var.startswith("tcgen05") and P == want, (B, Hq, Hkv, L, fp8, P)
+            assert grid == B * Hkv * -(-L // P) <= 148 * 2
+            assert P == 256 or B * Hkv * -(-L // (P // 2)) > 148 * 2
     # more units than a wave: the waves-based split (512 at least), unchanged
     assert ops.paged_decode_call_plan(16, 1, 32, 32, 128, 16, 2048)[1] == 512
     assert ops.paged_decode_call_plan(16, 1, 32, 32, 128, 16, 8192)[1] == 2048
