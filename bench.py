@@ -684,6 +684,13 @@ def main():
     ap.add_argument("--fig4-contexts", default="512,1024,2048,4096,8192")
     ap.add_argument("--fig4-ragged", action="store_true",
                     help="per-sequence contexts drawn from U[context/8, context] (seeded) instead of all equal")
+    ap.add_argument("--split-sweep", action="store_true",
+                    help="small grids: the automatic split against every partition of --split-partitions, "
+                         "over --split-batches x --split-contexts of --config's heads (--q-len, --kv-fp8, "
+                         "--variant and --fig4-ragged apply); one line per batch x context")
+    ap.add_argument("--split-batches", default="1,4,16")
+    ap.add_argument("--split-contexts", default="2048,8192")
+    ap.add_argument("--split-partitions", default="128,256,512,1024,2048,4096")
     ap.add_argument("--append", action="store_true",
                     help="time paged_kv_append alone and in front of the decode call, on --config")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -757,6 +764,39 @@ def main():
                                      "speedup_vs_no_prefetch": round(base_us / us, 3)}
                 print(json.dumps(line), flush=True)
                 del inp
+                torch.cuda.empty_cache()
+        return 0
+
+    if args.split_sweep:
+        import dataclasses
+        base = workloads.CONFIGS[args.config]
+        parts = [int(x) for x in args.split_partitions.split(",") if x.strip()]
+        for L in [int(x) for x in args.split_contexts.split(",")]:
+            for B in [int(x) for x in args.split_batches.split(",")]:
+                if args.fig4_ragged:
+                    cfg = dataclasses.replace(base, name=f"{base.name}_b{B}_L{L}r", num_seqs=B, context_lens=None,
+                                              len_range=(max(1, L // 8), L), num_blocks=None, partition_size=0)
+                else:
+                    cfg = dataclasses.replace(base, name=f"{base.name}_b{B}_L{L}", num_seqs=B,
+                                              context_lens=(L,) * B, len_range=None, num_blocks=None,
+                                              partition_size=0)
+                inp = workloads.make_inputs(cfg, device=dev)
+                res = {}
+                # the automatic split last, so that it is not the first call timed on fresh inputs
+                for P in [-1] + [p for p in parts if p < inp.max_context_len] + [0]:
+                    args.partition_size = P
+                    r = time_gpu(args, cfg, args.variant, dev, inp, min(args.steps, 50), args.warmup,
+                                 with_e2e=False, with_clocks=False)
+                    res[P] = r
+                us = {str(P): round(r["median_ms"] * 1e3, 2) for P, r in res.items()}
+                best = min(us, key=us.get)
+                print(json.dumps({"shape": f"{cfg.num_q_heads}q/{cfg.num_kv_heads}kv", "batch": B, "context": L,
+                                  "ragged": bool(args.fig4_ragged), "q_len": args.q_len, "kv_fp8": bool(args.kv_fp8),
+                                  "automatic": {"partition_size": res[0]["partition_size"],
+                                                "variant": res[0]["variant"], "grid": res[0]["grid"]},
+                                  "us_median": us, "best": best, "automatic_over_best": round(us["0"] / us[best], 3)}),
+                      flush=True)
+                del inp, res
                 torch.cuda.empty_cache()
         return 0
 
