@@ -1,0 +1,86 @@
+"""GPU parity at the partitions the small-grid split picks.
+
+A call whose (sequence, kv head) units cover less than one resident wave takes the
+shortest power-of-two partition whose grid still fits that wave: down to 128 tokens on
+the mma.sync path, up to 4096 and more on the tcgen05 path.  Each case checks the plan
+picks that partition, runs the automatic call, and compares every output row with the
+fp64 oracle (E4M3 also against the element bound of the tensor-core arithmetic).
+"""
+import pytest
+import torch
+
+import oracle
+from helpers import assert_close, assert_close_weighted, e4m3_magnitudes, oracle_out
+from paged_kv_decode_21_gb300 import ops, workloads
+
+pytestmark = pytest.mark.gpu
+
+KS, VS = workloads.E4M3_SCALES["full"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_decode_21_gb300 import build
+    build.build()
+    ops.lib()
+
+
+def slots(path_ctas_per_sm):
+    return torch.cuda.get_device_properties(0).multi_processor_count * path_ctas_per_sm
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("B,Hq,Hkv,L", [(1, 32, 8, 2048), (1, 28, 4, 8192), (4, 32, 32, 2048), (3, 32, 8, 3000)])
+def test_single_query_small_grid(B, Hq, Hkv, L, fp8):
+    lens = [L] + [max(1, L - 997 * i) for i in range(1, B)]  # the longest first, the rest shorter
+    inp = workloads.make_custom(B, Hq, Hkv, 128, 16, lens, seed=B + Hkv, device="cuda")
+    n, P, _, var, grid, _ = ops.paged_decode_call_plan(B, 1, Hq, Hkv, 128, 16, L, kv_fp8=fp8)
+    assert var == "tma_mma" and 128 <= P <= 2048 and grid <= slots(3)
+    assert P == 128 or B * Hkv * -(-L // (P // 2)) > slots(3)
+    ew = torch.zeros(1, dtype=torch.int32, device="cuda")
+    if fp8:
+        g = torch.Generator(device="cuda").manual_seed(11)
+        k8 = workloads.rand_e4m3(inp.k_cache.shape, g, "cuda")
+        v8 = workloads.rand_e4m3(inp.v_cache.shape, g, "cuda")
+        out = ops.paged_decode_attention_fp8(inp.q, k8, v8, inp.block_tables, inp.context_lens, inp.scale, KS, VS,
+                                             max_context_len=L, error_word=ew)
+        host = (inp.block_tables.cpu(), inp.context_lens.cpu())
+        ref = oracle.attention_fp8(inp.q.cpu(), k8.cpu(), v8.cpu(), *host, inp.scale, KS, VS)
+        absref = oracle.attention_fp8(inp.q.cpu(), k8.cpu(), e4m3_magnitudes(v8).cpu(), *host, inp.scale, KS, VS)
+        assert_close_weighted(out, ref, absref, 448.0 * VS, L, f"E4M3 P={P}")
+    else:
+        out = ops.paged_decode_attention_ex(inp.q, inp.k_cache, inp.v_cache, inp.block_tables, inp.context_lens,
+                                            inp.scale, max_context_len=L, error_word=ew)
+        assert_close(out, oracle_out(inp), f"fp16 P={P}")
+    assert ops.pkd_read_device_error(ew) == 0
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("B,Hq,Hkv,L", [(16, 32, 8, 8192), (1, 28, 4, 2048), (3, 28, 4, 5000)])
+def test_multi_token_small_grid_on_tcgen05(B, Hq, Hkv, L, fp8):
+    q_len = 8
+    lens = [L] + [max(q_len, L - 1999 * i) for i in range(1, B)]
+    inp = workloads.make_custom(B, Hq, Hkv, 128, 16, lens, seed=B + 3, device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(13)
+    q = workloads.randn_f16((B, q_len, Hq, 128), g, "cuda")
+    n, P, _, var, grid, _ = ops.paged_decode_call_plan(B, q_len, Hq, Hkv, 128, 16, L, kv_fp8=fp8)
+    assert var.startswith("tcgen05") and 256 <= P <= 8192 and grid <= slots(2)
+    assert P == 256 or B * Hkv * -(-L // (P // 2)) > slots(2)
+    ew = torch.zeros(1, dtype=torch.int32, device="cuda")
+    host = (inp.block_tables.cpu(), inp.context_lens.cpu())
+    if fp8:
+        k8 = workloads.rand_e4m3(inp.k_cache.shape, g, "cuda")
+        v8 = workloads.rand_e4m3(inp.v_cache.shape, g, "cuda")
+        out = ops.paged_decode_attention_fp8(q, k8, v8, inp.block_tables, inp.context_lens, inp.scale, KS, VS,
+                                             max_context_len=L, error_word=ew)
+        ref = oracle.attention_fp8(q.cpu(), k8.cpu(), v8.cpu(), *host, inp.scale, KS, VS)
+        absref = oracle.attention_fp8(q.cpu(), k8.cpu(), e4m3_magnitudes(v8).cpu(), *host, inp.scale, KS, VS)
+        assert_close_weighted(out, ref, absref, 448.0 * VS, L, f"E4M3 q_len=8 P={P}")
+    else:
+        out = ops.paged_decode_attention_multi(q, inp.k_cache, inp.v_cache, inp.block_tables, inp.context_lens,
+                                               inp.scale, max_context_len=L, error_word=ew)
+        ref = oracle.attention_multi(q.cpu(), inp.k_cache.cpu(), inp.v_cache.cpu(), *host, inp.scale)
+        assert_close(out, ref, f"fp16 q_len=8 P={P}")
+    assert ops.pkd_read_device_error(ew) == 0
