@@ -198,9 +198,15 @@ pkd_status paged_decode_attention_host(const void* q, const void* k_cache, const
  *                   and merged by the split-K reduce; shorter ones are
  *                   written directly.  The automatic choice splits only
  *                   grids of fewer than two waves of (sequence, kv head)
- *                   units, and walks unsplit grids of one to six waves
- *                   longest first (PKD_FLAG_LONGEST_FIRST) when the
- *                   workspace has room for the order.
+ *                   units (on the mma.sync path also contexts of 8192
+ *                   tokens or more below six waves), into power-of-two
+ *                   partitions: for units below one resident wave the
+ *                   shortest one (from 128 tokens, 256 on the tcgen05
+ *                   path) whose grid still fits that wave, else from 512
+ *                   tokens up, sized for six waves.  It walks unsplit
+ *                   grids of one to six waves longest first
+ *                   (PKD_FLAG_LONGEST_FIRST) when the workspace has room
+ *                   for the order.
  *   variant         pkd_variant, optionally ORed with PKD_FLAG_* bits
  *   prefetch_distance  how many of a warp's iterations ahead the L2 prefetch
  *                   runs: -1 = no L2 prefetch; 0 = the default of the L2
