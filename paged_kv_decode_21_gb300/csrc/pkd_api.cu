@@ -21,6 +21,8 @@ constexpr int kMinAutoPartition = 512;
 constexpr int kMaxAutoPartition = 2048;
 constexpr int kMinSmallGridPartition = 128;    // the shortest partition of the one-wave rule (auto_partition)
 constexpr int kMinSmallGridPartitionTc = 256;  // the same on the tcgen05 path (64-token tiles)
+constexpr int kTcRunTokens = 2048;  // tcgen05: tokens a CTA streams when it takes a run of short partitions
+constexpr int kTcRunWaves = 4;      // ... while the grid keeps at least this many waves
 // The tcgen05 kernel pays a longer fill per CTA (its two-stage K ring meets the
 // first copies' full HBM latency), so it is split less: only below kSplitWaves
 // waves whatever the context length, into partitions of up to
@@ -445,6 +447,7 @@ struct CallPlan {
   int P;           // tokens per partition (the whole context, rounded up to 32, when unsplit)
   int q_chunks;    // query chunks per (sequence, kv head)
   int np;          // partitions in the grid (1 when unsplit)
+  int runs;        // tcgen05: consecutive partitions per CTA (grid = units x ceil(np / runs))
   bool split;      // the split-K merge runs
   long long grid;  // decode CTAs
   int variant;     // the data path it runs, with the PKD_FLAG_* bits that apply
@@ -486,6 +489,22 @@ pkd_status plan_call(const Shape& s, int q_len, int variant, int partition_size,
   const int v = pick_auto(variant, G, out->grid, P);
   out->order = out->grid > 0 && want_order(flags_eff, variant_path(v), s.num_seqs);
   out->variant = (v & ~PKD_FLAG_LONGEST_FIRST) | (out->order ? PKD_FLAG_LONGEST_FIRST : 0);
+  // Runs of partitions on the tcgen05 path: a CTA streams R consecutive
+  // partitions of its (sequence, kv head) and writes each one's partial, so
+  // short partitions do not each pay the CTA's fill.  R covers up to
+  // kTcRunTokens tokens and keeps at least kTcRunWaves waves of CTAs.
+  out->runs = 1;
+  if (variant_path(v) == PKD_VARIANT_TCGEN05 && s.head_dim == 128 && out->split && !out->order && P % 64 == 0 &&
+      P < kTcRunTokens) {
+    int sms = sm_count();
+    if (sms <= 0) sms = 148;
+    const long long units = (long long)s.num_seqs * s.num_kv_heads * q_chunks;
+    const long long floor_ctas = (long long)kTcRunWaves * sms * path_stream(PKD_VARIANT_TCGEN05, s.head_dim, G, 2, false).ctas_per_sm;
+    int r = kTcRunTokens / P;
+    while (r > 1 && units * ((out->np + r - 1) / r) < floor_ctas) r /= 2;
+    out->runs = r;
+    out->grid = units * ((out->np + r - 1) / r);
+  }
   return PKD_OK;
 }
 
@@ -659,6 +678,7 @@ pkd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
   p.mode = 0;
   p.q_len = q_len;
   p.q_chunks = plan.q_chunks;
+  p.parts_per_cta = plan.runs;
   // E4M3 caches: K = code * k_scale enters the scores, V = code * v_scale the output
   p.scale_log2 = scale * (kv_fp8 ? k_scale : 1.f) * 1.4426950408889634f;
   p.v_scale = kv_fp8 ? v_scale : 1.f;

@@ -71,6 +71,7 @@ struct DecodeParams {
   int l2_hints;         // 1: evict_first on consuming loads/copies, evict_last on prefetches
   unsigned long long timeout_ns;
   const int32_t* piece_order;  // nullable: grid piece p -> b * NP + j (longest first); tensor-core path only
+  int parts_per_cta;           // tcgen05 path: consecutive partitions per CTA (0 or 1: one; needs no piece order)
 };
 
 template <int D, int BS, int G, int VARIANT>

@@ -138,7 +138,9 @@ struct TcTraits {
   static constexpr uint32_t IDESC_O = tc_idesc_f16(128, D, true);
 };
 
-template <int BS, int KVB, int HD>
+// RUNS: the build for runs of consecutive partitions per CTA (P.parts_per_cta
+// > 1); the other build has one partition per CTA fixed at compile time.
+template <int BS, int KVB, int HD, bool RUNS = false>
 __global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, KVB, HD>::MIN_BLOCKS)
     paged_decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                            const DecodeParams P) {
@@ -167,9 +169,11 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, K
   volatile uint32_t* vbad = reinterpret_cast<volatile uint32_t*>(tmem_slot + 2);  // [NSV]
   int32_t* tile_ids = reinterpret_cast<int32_t*>(tmem_slot + 2 + NSV);            // E4M3: [NIDS][NBT + 1]
 
-  // work item: query chunk fastest, then partition j, then (b, g)
+  // work item: query chunk fastest, then partition j (a run of R consecutive
+  // partitions from j), then (b, g)
   const int G = P.num_q_heads / P.num_kv_heads;
   const int np_grid = P.max_partitions;
+  const int R = (RUNS && P.parts_per_cta > 1 && !P.piece_order) ? P.parts_per_cta : 1;
   const int qc = blockIdx.x % P.q_chunks;
   const int rest = blockIdx.x / P.q_chunks;
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -181,8 +185,9 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, K
     b = piece / np_grid;
     j = piece % np_grid;
   } else {
-    j = rest % np_grid;
-    const int bg = rest / np_grid;
+    const int nruns = (np_grid + R - 1) / R;
+    j = (rest % nruns) * R;
+    const int bg = rest / nruns;
     g = bg % P.num_kv_heads;
     b = bg / P.num_kv_heads;
   }
@@ -205,10 +210,15 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, K
     return;
   }
   if (j >= np_b) return;
+  // the CTA's partitions [j, j_end); with R > 1 the partition size is a
+  // multiple of TN, so every tile lies in one partition, tpp tiles each
+  const int j_end = min(j + R, np_b);
+  constexpr int kOneRun = 1 << 30;  // tiles per partition when a CTA has one
+  const int tpp = RUNS ? (R > 1 ? PS / TN : kOneRun) : kOneRun;
 
   const int t0 = j * PS;
   // the chunk's last query sees tokens < L - QL + jq0 + nq; nothing past that is read
-  const int t1 = min(min(t0 + PS, L), L - QL + jq0 + nq);
+  const int t1 = min(min(j_end * PS, L), L - QL + jq0 + nq);
   const int ntiles = t1 > t0 ? (t1 - t0 + TN - 1) / TN : 0;
   const int nblk = t1 > t0 ? (t1 - t0 + BS - 1) / BS : 0;
   const int32_t* bt = P.block_tables + (size_t)b * P.max_blocks_per_seq + t0 / BS;
@@ -551,7 +561,7 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, K
 #pragma unroll
           for (int k = 0; k < TN / 16; ++k)  // 16 tokens: 8 columns of P, 16 rows of V
             tc_mma_f16_ts(tmem, pa + 8 * k, sw128_desc(vs + k * 16 * T::ROWB, T::KVH, 1024), T::IDESC_O,
-                          (npv > 0 || k > 0) ? 1u : 0u);
+                          ((RUNS ? npv % tpp : npv) != 0 || k > 0) ? 1u : 0u);  // a partition's first tile starts O
           tc_commit(&pfree[npv % NPB]);
           tc_commit(&vempty[npv % NSV]);
           ++npv;
@@ -591,9 +601,67 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, K
     const int lim = min(t1, L - QL + jq0 + (live ? rr : rows - 1) / G + 1);
     const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
     float m = -INFINITY, mt = -INFINITY, l = 0.f;  // running shift, exact maximum, sum of p
+    // The result of partition pj: O / l to the output (a sequence of one
+    // partition) or the unnormalised partial for the split-K merge; O is read
+    // from tensor memory when have_o (whole warp), else zero.
+    auto emit = [&](int pj, bool have_o) {
+      const size_t orow = live ? out_row(rr) : 0;
+      const size_t pidx = orow * P.max_partitions + pj;
+      // l = 0: the query saw no token.  V = code * v_scale for E4M3 caches (1 for fp16)
+      const float inv = l > 0.f ? P.v_scale / l : 0.f;
+      // partials are relative to the exact maximum mt; O and l to the shift m
+      const float f = m == -INFINITY ? 0.f : ex2_approx(m - mt);
+      const float fo = f * P.v_scale;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        float o[32];
+        if (have_o) {
+          tmem_ld32(tl + 32 * c, o);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = 0.f;
+        }
+        if (!live) continue;
+        if (final_out) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 w;
+            w.x = pack_half2(o[8 * q] * inv, o[8 * q + 1] * inv);
+            w.y = pack_half2(o[8 * q + 2] * inv, o[8 * q + 3] * inv);
+            w.z = pack_half2(o[8 * q + 4] * inv, o[8 * q + 5] * inv);
+            w.w = pack_half2(o[8 * q + 6] * inv, o[8 * q + 7] * inv);
+            *reinterpret_cast<uint4*>(P.out + orow * D + 32 * c + 8 * q) = w;
+          }
+        } else {
+          float* dst = P.tmp_out + pidx * D + 32 * c;
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4*>(dst + 4 * q) =
+                make_float4(o[4 * q] * fo, o[4 * q + 1] * fo, o[4 * q + 2] * fo, o[4 * q + 3] * fo);
+        }
+      }
+      if (live && !final_out) {
+        P.max_logits[pidx] = mt * 0.69314718055994530942f;  // log2 units -> natural; -inf if empty
+        P.exp_sums[pidx] = l * f;
+      }
+    };
     bool ok = true;
     for (int i = 0; i < ntiles; ++i) {
       const int sv = i % NSV, sb = i & 1;
+      const bool part_start = RUNS && i > 0 && i % tpp == 0;
+      if (part_start) {
+        // the previous partition is complete once P.V of its last tile is:
+        // its partial out of O, then a fresh state (that tile's P.V starts O anew)
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait_bounded(&pfree[(i - 1) % NPB], ((i - 1) / NPB) & 1, P.timeout_ns));
+        if (!ok) break;
+        tc_fence_after();
+        emit(j + i / tpp - 1, true);
+        m = -INFINITY;
+        mt = -INFINITY;
+        l = 0.f;
+      }
       ok = __all_sync(0xffffffffu, !*abort_flag && mbar_wait_bounded(&sfull[sb], (i / 2) & 1, P.timeout_ns));
       if (!ok) break;
       tc_fence_after();
@@ -655,7 +723,7 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, K
       const float2 at = __fadd2_rn(a01, a23);
       l += at.x + at.y;
       // O holds the earlier tiles once P.V of the previous one completed: rescale it in place
-      if (i > 0 && rescale) {
+      if (i > 0 && rescale && !part_start) {
         ok = __all_sync(0xffffffffu,
                         mbar_wait_bounded(&pfree[(i - 1) % NPB], ((i - 1) / NPB) & 1, P.timeout_ns));
         if (!ok) break;
@@ -695,45 +763,17 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, K
       *abort_flag = 1;
     } else {
       tc_fence_after();
-      const size_t orow = live ? out_row(rr) : 0;
-      const size_t pidx = orow * P.max_partitions + j;
-      // l = 0: the query saw no token.  V = code * v_scale for E4M3 caches (1 for fp16)
-      const float inv = l > 0.f ? P.v_scale / l : 0.f;
-      // partials are relative to the exact maximum mt; O and l to the shift m
-      const float f = m == -INFINITY ? 0.f : ex2_approx(m - mt);
-      const float fo = f * P.v_scale;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        float o[32];
-        if (ntiles > 0) {
-          tmem_ld32(tl + 32 * c, o);
-          tmem_ld_wait();
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = 0.f;
-        }
-        if (!live) continue;
-        if (final_out) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 w;
-            w.x = pack_half2(o[8 * q] * inv, o[8 * q + 1] * inv);
-            w.y = pack_half2(o[8 * q + 2] * inv, o[8 * q + 3] * inv);
-            w.z = pack_half2(o[8 * q + 4] * inv, o[8 * q + 5] * inv);
-            w.w = pack_half2(o[8 * q + 6] * inv, o[8 * q + 7] * inv);
-            *reinterpret_cast<uint4*>(P.out + orow * D + 32 * c + 8 * q) = w;
-          }
-        } else {
-          float* dst = P.tmp_out + pidx * D + 32 * c;
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            *reinterpret_cast<float4*>(dst + 4 * q) =
-                make_float4(o[4 * q] * fo, o[4 * q + 1] * fo, o[4 * q + 2] * fo, o[4 * q + 3] * fo);
-        }
-      }
-      if (live && !final_out) {
-        P.max_logits[pidx] = mt * 0.69314718055994530942f;  // log2 units -> natural; -inf if empty
-        P.exp_sums[pidx] = l * f;
+      if constexpr (RUNS) {
+        // the partition of the last tile, then the CTA's partitions past it
+        // (none of the chunk's queries sees their tokens): empty partials
+        const int jl = ntiles > 0 ? j + (ntiles - 1) / tpp : j - 1;
+        if (ntiles > 0) emit(jl, true);
+        m = -INFINITY;
+        mt = -INFINITY;
+        l = 0.f;
+        for (int pj = max(jl + 1, j); pj < j_end; ++pj) emit(pj, false);
+      } else {
+        emit(j, ntiles > 0);
       }
     }
   }

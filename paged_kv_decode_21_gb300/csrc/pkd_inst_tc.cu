@@ -14,7 +14,9 @@ template <int BS, int KVB, int HD>
 cudaError_t launch_tc_bs(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeParams& p, long long grid,
                          cudaStream_t stream) {
   using T = TcTraits<BS, KVB, HD>;
-  auto* fn = paged_decode_tc_kernel<BS, KVB, HD>;
+  // runs of partitions per CTA: head_dim 128 only (the plan asks for them there)
+  auto* fn = (HD == 128 && p.parts_per_cta > 1) ? paged_decode_tc_kernel<BS, KVB, HD, HD == 128>
+                                                 : paged_decode_tc_kernel<BS, KVB, HD, false>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];

@@ -84,3 +84,38 @@ def test_multi_token_small_grid_on_tcgen05(B, Hq, Hkv, L, fp8):
         ref = oracle.attention_multi(q.cpu(), inp.k_cache.cpu(), inp.v_cache.cpu(), *host, inp.scale)
         assert_close(out, ref, f"fp16 q_len=8 P={P}")
     assert ops.pkd_read_device_error(ew) == 0
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_tcgen05_partition_runs(fp8):
+    # Many units at a short explicit partition: the tcgen05 plan gives each CTA a run of
+    # consecutive partitions (fewer CTAs than partitions), each partial written on its own.
+    # Ragged lengths put runs across the end of a sequence, a last run shorter than the others,
+    # and sequences shorter than a partition or than the query tokens.
+    B, Hq, Hkv, q_len, P = 16, 40, 8, 8, 512
+    rng = torch.Generator().manual_seed(31)
+    lens = torch.randint(1, 16385, (B,), generator=rng).tolist()
+    lens[:5] = [16384, 0, 5, 511, 1537]
+    L = max(lens)
+    inp = workloads.make_custom(B, Hq, Hkv, 128, 16, lens, seed=33, device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(34)
+    q = workloads.randn_f16((B, q_len, Hq, 128), g, "cuda")
+    n, part, _, var, grid, _ = ops.paged_decode_call_plan(B, q_len, Hq, Hkv, 128, 16, L, kv_fp8=fp8, partition_size=P)
+    units, npart = B * Hkv, -(-L // P)
+    assert var == "tcgen05" and part == P and grid < units * npart  # runs of partitions
+    ew = torch.zeros(1, dtype=torch.int32, device="cuda")
+    host = (inp.block_tables.cpu(), inp.context_lens.cpu())
+    if fp8:
+        k8 = workloads.rand_e4m3(inp.k_cache.shape, g, "cuda")
+        v8 = workloads.rand_e4m3(inp.v_cache.shape, g, "cuda")
+        out = ops.paged_decode_attention_fp8(q, k8, v8, inp.block_tables, inp.context_lens, inp.scale, KS, VS,
+                                             max_context_len=L, partition_size=P, error_word=ew)
+        ref = oracle.attention_fp8(q.cpu(), k8.cpu(), v8.cpu(), *host, inp.scale, KS, VS)
+        absref = oracle.attention_fp8(q.cpu(), k8.cpu(), e4m3_magnitudes(v8).cpu(), *host, inp.scale, KS, VS)
+        assert_close_weighted(out, ref, absref, 448.0 * VS, L, "E4M3 runs")
+    else:
+        out = ops.paged_decode_attention_multi(q, inp.k_cache, inp.v_cache, inp.block_tables, inp.context_lens,
+                                               inp.scale, max_context_len=L, partition_size=P, error_word=ew)
+        ref = oracle.attention_multi(q.cpu(), inp.k_cache.cpu(), inp.v_cache.cpu(), *host, inp.scale)
+        assert_close(out, ref, "fp16 runs")
+    assert ops.pkd_read_device_error(ew) == 0
