@@ -197,12 +197,12 @@ pkd_status paged_decode_attention_host(const void* q, const void* k_cache, const
  *                   computed by one CTA per (sequence, kv head, partition)
  *                   and merged by the split-K reduce; shorter ones are
  *                   written directly.  On the tcgen05 path at head_dim 128,
- *                   partitions shorter than 2048 tokens (multiples of 64)
- *                   of a grid walked in plain order are taken in runs: one
- *                   CTA streams up to 2048 tokens of consecutive partitions
- *                   of its (sequence, kv head) and writes each one's
- *                   partial, while the grid keeps four waves of CTAs; the
- *                   result is the same.  The automatic choice splits only
+ *                   partitions of up to 1024 tokens (multiples of 64) of a
+ *                   grid walked in plain order are taken in runs: one CTA
+ *                   streams up to 4096 tokens of consecutive partitions of
+ *                   its (sequence, kv head) and writes each one's partial,
+ *                   while the grid keeps four waves of CTAs; the result is
+ *                   the same.  The automatic choice splits only
  *                   grids of fewer than two waves of (sequence, kv head)
  *                   units (on the mma.sync path also contexts of 8192
  *                   tokens or more below six waves), into power-of-two

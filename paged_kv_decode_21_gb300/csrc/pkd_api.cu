@@ -21,8 +21,9 @@ constexpr int kMinAutoPartition = 512;
 constexpr int kMaxAutoPartition = 2048;
 constexpr int kMinSmallGridPartition = 128;    // the shortest partition of the one-wave rule (auto_partition)
 constexpr int kMinSmallGridPartitionTc = 256;  // the same on the tcgen05 path (64-token tiles)
-constexpr int kTcRunTokens = 2048;  // tcgen05: tokens a CTA streams when it takes a run of short partitions
-constexpr int kTcRunWaves = 4;      // ... while the grid keeps at least this many waves
+constexpr int kTcRunMaxPartition = 1024;  // tcgen05: partitions up to this long are taken in runs,
+constexpr int kTcRunTokens = 4096;        // ... a CTA streaming up to this many tokens of them
+constexpr int kTcRunWaves = 4;            // ... while the grid keeps at least this many waves
 // The tcgen05 kernel pays a longer fill per CTA (its two-stage K ring meets the
 // first copies' full HBM latency), so it is split less: only below kSplitWaves
 // waves whatever the context length, into partitions of up to
@@ -493,9 +494,10 @@ pkd_status plan_call(const Shape& s, int q_len, int variant, int partition_size,
   // partitions of its (sequence, kv head) and writes each one's partial, so
   // short partitions do not each pay the CTA's fill.  R covers up to
   // kTcRunTokens tokens and keeps at least kTcRunWaves waves of CTAs.
+  // (Runs of two 2048-token partitions measured slower than one.)
   out->runs = 1;
   if (variant_path(v) == PKD_VARIANT_TCGEN05 && s.head_dim == 128 && out->split && !out->order && P % 64 == 0 &&
-      P < kTcRunTokens) {
+      P <= kTcRunMaxPartition) {
     int sms = sm_count();
     if (sms <= 0) sms = 148;
     const long long units = (long long)s.num_seqs * s.num_kv_heads * q_chunks;

@@ -604,13 +604,13 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, K
     // The result of partition pj: O / l to the output (a sequence of one
     // partition) or the unnormalised partial for the split-K merge; O is read
     // from tensor memory when have_o (whole warp), else zero.
-    auto emit = [&](int pj, bool have_o) {
+    auto emit = [&](int pj, bool have_o, float em, float emt, float el) {
       const size_t orow = live ? out_row(rr) : 0;
       const size_t pidx = orow * P.max_partitions + pj;
-      // l = 0: the query saw no token.  V = code * v_scale for E4M3 caches (1 for fp16)
-      const float inv = l > 0.f ? P.v_scale / l : 0.f;
-      // partials are relative to the exact maximum mt; O and l to the shift m
-      const float f = m == -INFINITY ? 0.f : ex2_approx(m - mt);
+      // el = 0: the query saw no token.  V = code * v_scale for E4M3 caches (1 for fp16)
+      const float inv = el > 0.f ? P.v_scale / el : 0.f;
+      // partials are relative to the exact maximum emt; O and el to the shift em
+      const float f = em == -INFINITY ? 0.f : ex2_approx(em - emt);
       const float fo = f * P.v_scale;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
@@ -642,22 +642,21 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, K
         }
       }
       if (live && !final_out) {
-        P.max_logits[pidx] = mt * 0.69314718055994530942f;  // log2 units -> natural; -inf if empty
-        P.exp_sums[pidx] = l * f;
+        P.max_logits[pidx] = emt * 0.69314718055994530942f;  // log2 units -> natural; -inf if empty
+        P.exp_sums[pidx] = el * f;
       }
     };
     bool ok = true;
     for (int i = 0; i < ntiles; ++i) {
       const int sv = i % NSV, sb = i & 1;
+      // A new partition starts from a fresh state; the previous one's result
+      // leaves O below, once this tile's P is written and before it is released
       const bool part_start = RUNS && i > 0 && i % tpp == 0;
+      float pm = 0.f, pmt = 0.f, pl = 0.f;
       if (part_start) {
-        // the previous partition is complete once P.V of its last tile is:
-        // its partial out of O, then a fresh state (that tile's P.V starts O anew)
-        ok = __all_sync(0xffffffffu,
-                        mbar_wait_bounded(&pfree[(i - 1) % NPB], ((i - 1) / NPB) & 1, P.timeout_ns));
-        if (!ok) break;
-        tc_fence_after();
-        emit(j + i / tpp - 1, true);
+        pm = m;
+        pmt = mt;
+        pl = l;
         m = -INFINITY;
         mt = -INFINITY;
         l = 0.f;
@@ -752,6 +751,15 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, K
         }
         fence_proxy_async_smem();  // the zeroed V rows visible to the tensor cores
       }
+      if (part_start) {
+        // the previous partition is complete once P.V of its last tile is; this
+        // tile's P.V (released below) starts O anew
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait_bounded(&pfree[(i - 1) % NPB], ((i - 1) / NPB) & 1, P.timeout_ns));
+        if (!ok) break;
+        tc_fence_after();
+        emit(j + i / tpp - 1, true, pm, pmt, pl);
+      }
       tc_fence_before();  // our tensor-memory reads and writes ordered before the arrive
       mbar_arrive(&pfull[i % NPB]);
     }
@@ -767,13 +775,10 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, K
         // the partition of the last tile, then the CTA's partitions past it
         // (none of the chunk's queries sees their tokens): empty partials
         const int jl = ntiles > 0 ? j + (ntiles - 1) / tpp : j - 1;
-        if (ntiles > 0) emit(jl, true);
-        m = -INFINITY;
-        mt = -INFINITY;
-        l = 0.f;
-        for (int pj = max(jl + 1, j); pj < j_end; ++pj) emit(pj, false);
+        if (ntiles > 0) emit(jl, true, m, mt, l);
+        for (int pj = max(jl + 1, j); pj < j_end; ++pj) emit(pj, false, -INFINITY, -INFINITY, 0.f);
       } else {
-        emit(j, ntiles > 0);
+        emit(j, ntiles > 0, m, mt, l);
       }
     }
   }

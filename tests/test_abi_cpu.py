@@ -244,14 +244,16 @@ def test_small_grid_split_fills_one_wave():
 
 
 def test_tcgen05_partition_runs_plan():
-    # Short explicit partitions on the tcgen05 path at head_dim 128: a CTA takes a run of up
-    # to 2048 tokens of consecutive partitions while the grid keeps four waves of CTAs (two
-    # per SM, 148 SMs without a GPU); every other path and shape keeps one partition per CTA.
+    # Explicit partitions of up to 1024 tokens on the tcgen05 path at head_dim 128: a CTA takes
+    # a run of up to 4096 tokens of consecutive partitions while the grid keeps four waves of
+    # CTAs (two per SM, 148 SMs without a GPU); every other path and shape keeps one partition
+    # per CTA.
     from paged_kv_decode_21_gb300 import ops
     floor = 4 * 148 * 2
-    for B, Hq, Hkv, L, P, want_runs in [(32, 40, 8, 32768, 512, 4), (16, 40, 8, 16384, 512, 2),
-                                        (64, 40, 8, 16384, 256, 8), (32, 40, 8, 32768, 1024, 2),
-                                        (4, 40, 8, 8192, 512, 1), (32, 40, 8, 32768, 2048, 1)]:
+    for B, Hq, Hkv, L, P, want_runs in [(32, 40, 8, 32768, 512, 8), (16, 40, 8, 16384, 512, 2),
+                                        (64, 40, 8, 16384, 256, 16), (32, 40, 8, 32768, 1024, 4),
+                                        (4, 40, 8, 8192, 512, 1), (32, 40, 8, 32768, 2048, 1),
+                                        (64, 40, 8, 32768, 2048, 1)]:
         for fp8 in (False, True):
             n, part, order, var, grid, _ = ops.paged_decode_call_plan(B, 8, Hq, Hkv, 128, 16, L, kv_fp8=fp8,
                                                                       partition_size=P)
@@ -259,7 +261,7 @@ def test_tcgen05_partition_runs_plan():
             assert var == "tcgen05" and part == P and not order, (B, L, P, fp8)
             assert grid == units * -(-npart // want_runs), (B, L, P, fp8, grid)
             assert want_runs == 1 or grid >= floor
-            assert want_runs * 2 > 2048 // P or units * -(-npart // (want_runs * 2)) < floor
+            assert P > 1024 or want_runs * 2 > 4096 // P or units * -(-npart // (want_runs * 2)) < floor
     # single query (mma.sync) and head_dim 64 keep one partition per CTA
     assert ops.paged_decode_call_plan(32, 1, 40, 8, 128, 16, 32768, partition_size=512)[4] == 32 * 8 * 64
     assert ops.paged_decode_call_plan(32, 8, 40, 8, 64, 16, 32768, partition_size=512,
