@@ -612,7 +612,9 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, K
       // partials are relative to the exact maximum emt; O and el to the shift em
       const float f = em == -INFINITY ? 0.f : ex2_approx(em - emt);
       const float fo = f * P.v_scale;
-#pragma unroll
+      // once per partition: kept rolled, as is the rescale below, because the
+      // kernel's size costs instruction-cache misses in the hot loops
+#pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         float o[32];
         if (have_o) {
@@ -644,6 +646,30 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, K
       if (live && !final_out) {
         P.max_logits[pidx] = emt * 0.69314718055994530942f;  // log2 units -> natural; -inf if empty
         P.exp_sums[pidx] = el * f;
+      }
+    };
+    // Inside a run: the partial of a finished partition (the sequence is split,
+    // so never the final output), in a loop kept rolled to keep the kernel's
+    // code small
+    auto emit_partial = [&](int pj, float em, float emt, float el) {
+      const size_t pidx = (live ? out_row(rr) : 0) * P.max_partitions + pj;
+      const float fo = (em == -INFINITY ? 0.f : ex2_approx(em - emt)) * P.v_scale;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        float o[32];
+        tmem_ld32(tl + 32 * c, o);
+        tmem_ld_wait();
+        if (live) {
+          float* dst = P.tmp_out + pidx * D + 32 * c;
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4*>(dst + 4 * q) =
+                make_float4(o[4 * q] * fo, o[4 * q + 1] * fo, o[4 * q + 2] * fo, o[4 * q + 3] * fo);
+        }
+      }
+      if (live) {
+        P.max_logits[pidx] = emt * 0.69314718055994530942f;
+        P.exp_sums[pidx] = el * (fo / P.v_scale);
       }
     };
     bool ok = true;
@@ -727,7 +753,7 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, K
                         mbar_wait_bounded(&pfree[(i - 1) % NPB], ((i - 1) / NPB) & 1, P.timeout_ns));
         if (!ok) break;
         tc_fence_after();
-#pragma unroll
+#pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           float o[32];
           tmem_ld32(tl + 32 * c, o);
@@ -758,7 +784,7 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, K
                         mbar_wait_bounded(&pfree[(i - 1) % NPB], ((i - 1) / NPB) & 1, P.timeout_ns));
         if (!ok) break;
         tc_fence_after();
-        emit(j + i / tpp - 1, true, pm, pmt, pl);
+        emit_partial(j + i / tpp - 1, pm, pmt, pl);
       }
       tc_fence_before();  // our tensor-memory reads and writes ordered before the arrive
       mbar_arrive(&pfull[i % NPB]);
@@ -775,8 +801,10 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, K
         // the partition of the last tile, then the CTA's partitions past it
         // (none of the chunk's queries sees their tokens): empty partials
         const int jl = ntiles > 0 ? j + (ntiles - 1) / tpp : j - 1;
-        if (ntiles > 0) emit(jl, true, m, mt, l);
-        for (int pj = max(jl + 1, j); pj < j_end; ++pj) emit(pj, false, -INFINITY, -INFINITY, 0.f);
+        for (int pj = max(jl, j); pj < j_end; ++pj) {
+          const bool last = pj == jl;  // else no query of the chunk sees its tokens
+          emit(pj, last, last ? m : -INFINITY, last ? mt : -INFINITY, last ? l : 0.f);
+        }
       } else {
         emit(j, ntiles > 0, m, mt, l);
       }
