@@ -530,11 +530,10 @@ pkd_status launch_reduce(const float* tmp_out, const float* max_logits, const fl
                          const int32_t* context_lens, void* out, int num_seqs, int num_q_heads,
                          int head_dim, int partition_size, int max_num_partitions, int min_merge,
                          cudaStream_t stream) {
-  const long long grid = (long long)num_seqs * num_q_heads;
-  if (grid <= 0) return PKD_OK;
-  if (grid > 0x7fffffffLL) return PKD_ERR_SHAPE;
-  const size_t smem = (size_t)max_num_partitions * sizeof(float);
-  if (smem > 48 * 1024) return PKD_ERR_SHAPE;
+  const long long rows = (long long)num_seqs * num_q_heads;
+  if (rows <= 0) return PKD_OK;
+  if (rows > 0x7fffffffLL) return PKD_ERR_SHAPE;
+  const long long grid = (rows + pkd::kReduceRowsPerCta - 1) / pkd::kReduceRowsPerCta;
   __half* o = static_cast<__half*>(out);
   // Programmatic dependent launch: the merge may become resident while the
   // decode grid's last CTAs still run; its griddepcontrol.wait holds it until
@@ -544,19 +543,17 @@ pkd_status launch_reduce(const float* tmp_out, const float* max_logits, const fl
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
-  cfg.dynamicSmemBytes = smem;
+  cfg.blockDim = dim3(32 * pkd::kReduceRowsPerCta);
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e;
   if (head_dim == 128) {
-    cfg.blockDim = dim3(128);
     e = cudaLaunchKernelEx(&cfg, pkd::paged_decode_reduce_kernel<128>, tmp_out, max_logits, exp_sums,
-                           context_lens, o, num_q_heads, partition_size, max_num_partitions, min_merge);
+                           context_lens, o, (int)rows, num_q_heads, partition_size, max_num_partitions, min_merge);
   } else if (head_dim == 64) {
-    cfg.blockDim = dim3(64);
     e = cudaLaunchKernelEx(&cfg, pkd::paged_decode_reduce_kernel<64>, tmp_out, max_logits, exp_sums,
-                           context_lens, o, num_q_heads, partition_size, max_num_partitions, min_merge);
+                           context_lens, o, (int)rows, num_q_heads, partition_size, max_num_partitions, min_merge);
   } else {
     return PKD_ERR_UNSUPPORTED;
   }

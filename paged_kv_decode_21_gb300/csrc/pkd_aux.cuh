@@ -8,17 +8,27 @@
 namespace pkd {
 
 // ---------------------------------------------------------------------------
-// Split-K merge: one CTA of D threads per (b, h).
+// Split-K merge: one warp per (b, h) row, four CTA rows; lane l owns dims
+// [V l, V l + V), V = D / 32.  Lane l computes the weights of partitions
+// j = l (mod 32), a shuffle hands each weight to the whole warp, and every
+// lane keeps 16 partitions' vectors in flight (a row's reads are a chain of
+// DRAM round trips otherwise).  Per dim the sum runs over j in order, as the
+// definition reads.
+constexpr int kReduceRowsPerCta = 4;
 template <int D>
-__global__ void __launch_bounds__(D) paged_decode_reduce_kernel(
+__global__ void __launch_bounds__(32 * kReduceRowsPerCta) paged_decode_reduce_kernel(
     const float* __restrict__ tmp_out, const float* __restrict__ max_logits,
     const float* __restrict__ exp_sums, const int32_t* __restrict__ context_lens, __half* out,
-    int num_q_heads, int partition_size, int max_partitions, int min_partitions_to_merge) {
-  extern __shared__ float wsm[];  // [max_partitions] weights, then [1] 1/Z
+    int num_rows, int num_q_heads, int partition_size, int max_partitions, int min_partitions_to_merge) {
+  static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+  constexpr int V = D / 32;
+  constexpr int U = 16;  // partitions in flight per lane
   // launched as a programmatic dependent of the decode grid: wait until that
   // grid has completed and its partials are visible (a no-op otherwise)
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int row = blockIdx.x;     // b * Hq + h
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kReduceRowsPerCta + (threadIdx.x >> 5);  // b * Hq + h
+  if (row >= num_rows) return;
   const int b = row / num_q_heads;
   const int L = context_lens[b];
   // partitions the first kernel wrote (none past its grid)
@@ -26,38 +36,62 @@ __global__ void __launch_bounds__(D) paged_decode_reduce_kernel(
   // min_partitions_to_merge > 0: those sequences were written by the
   // partition kernel itself; 0 merges every sequence (empty ones get zeros)
   if (min_partitions_to_merge > 0 && np <= min_partitions_to_merge) return;
-  const int d = threadIdx.x;
-  if (np <= 0) {
-    out[(size_t)row * D + d] = __float2half_rn(0.f);
-    return;
-  }
-  const float* ml = max_logits + (size_t)row * max_partitions;
-  const float* es = exp_sums + (size_t)row * max_partitions;
-  // global max over partitions (warp 0)
-  __shared__ float s_max, s_invz;
-  if (threadIdx.x < 32) {
-    float M = -INFINITY;
-    for (int jj = threadIdx.x; jj < np; jj += 32) M = fmaxf(M, ml[jj]);
+  __half* o_row = out + (size_t)row * D + V * lane;
+  float acc[V];
+#pragma unroll
+  for (int v = 0; v < V; ++v) acc[v] = 0.f;
+  float Z = 0.f;
+  if (np > 0) {
+    const float* ml = max_logits + (size_t)row * max_partitions;
+    const float* es = exp_sums + (size_t)row * max_partitions;
+    float M = -INFINITY;  // the maximum over partitions
+    for (int j = lane; j < np; j += 32) M = fmaxf(M, ml[j]);
 #pragma unroll
     for (int msk = 16; msk > 0; msk >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, msk));
-    float Z = 0.f;
-    for (int jj = threadIdx.x; jj < np; jj += 32) {
-      const float w = ml[jj] == -INFINITY ? 0.f : __expf(ml[jj] - M);
-      wsm[jj] = w;
-      Z = fmaf(w, es[jj], Z);
+    const float* to = tmp_out + (size_t)row * max_partitions * D + V * lane;
+    for (int j0 = 0; j0 < np; j0 += 32) {
+      float w = 0.f;  // the weight of partition j0 + lane
+      if (j0 + lane < np) {
+        const float m = ml[j0 + lane];
+        w = m == -INFINITY ? 0.f : __expf(m - M);
+        Z = fmaf(w, es[j0 + lane], Z);
+      }
+      const int nj = min(32, np - j0);
+      int k = 0;
+      for (; k + U <= nj; k += U) {
+        float x[U][V];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const float* src = to + (size_t)(j0 + k + u) * D;
+          if constexpr (V == 4) {
+            const float4 t = *reinterpret_cast<const float4*>(src);
+            x[u][0] = t.x; x[u][1] = t.y; x[u][2] = t.z; x[u][3] = t.w;
+          } else {
+            const float2 t = *reinterpret_cast<const float2*>(src);
+            x[u][0] = t.x; x[u][1] = t.y;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const float wu = __shfl_sync(0xffffffffu, w, k + u);
+#pragma unroll
+          for (int v = 0; v < V; ++v) acc[v] = fmaf(wu, x[u][v], acc[v]);
+        }
+      }
+      for (; k < nj; ++k) {
+        const float wu = __shfl_sync(0xffffffffu, w, k);
+        const float* src = to + (size_t)(j0 + k) * D;
+#pragma unroll
+        for (int v = 0; v < V; ++v) acc[v] = fmaf(wu, src[v], acc[v]);
+      }
     }
 #pragma unroll
     for (int msk = 16; msk > 0; msk >>= 1) Z += __shfl_xor_sync(0xffffffffu, Z, msk);
-    if (threadIdx.x == 0) {
-      s_max = M;
-      s_invz = Z > 0.f ? 1.f / Z : 0.f;  // Z = 0: a query that saw no token (multi-token queries)
-    }
   }
-  __syncthreads();
-  const float* to = tmp_out + (size_t)row * max_partitions * D + d;
-  float o = 0.f;
-  for (int jj = 0; jj < np; ++jj) o = fmaf(wsm[jj], to[(size_t)jj * D], o);
-  out[(size_t)row * D + d] = __float2half_rn(o * s_invz);
+  const float invz = Z > 0.f ? 1.f / Z : 0.f;  // Z = 0: no token (empty sequence, or a query that saw none)
+#pragma unroll
+  for (int v = 0; v < V; v += 2)
+    *reinterpret_cast<__half2*>(o_row + v) = __floats2half2_rn(acc[v] * invz, acc[v + 1] * invz);
 }
 
 // ---------------------------------------------------------------------------
