@@ -24,8 +24,8 @@ constexpr int kMinSmallGridPartitionTc = 256;  // the same on the tcgen05 path (
 constexpr int kTcRunMaxPartition = 1024;  // tcgen05: partitions up to this long are taken in runs,
 constexpr int kTcRunTokens = 4096;        // ... a CTA streaming up to this many tokens of them
 constexpr int kTcRunWaves = 4;            // ... while the grid keeps at least this many waves
-// The tcgen05 kernel pays a longer fill per CTA (its two-stage K ring meets the
-// first copies' full HBM latency), so it is split less: only below kSplitWaves
+// The tcgen05 kernel pays a longer fill per CTA (barriers, tensor memory, and
+// the first copies' full HBM latency), so it is split less: only below kSplitWaves
 // waves whatever the context length, into partitions of up to
 // kMaxAutoPartitionTc tokens.  Measured on its multi-token workloads: GQA 7:1
 // at 8192 tokens, q_len 8, unsplit 708 against 788 us at 2048-token
@@ -355,7 +355,11 @@ int auto_partition(const Shape& s, int variant = PKD_VARIANT_AUTO, int q_chunks 
   }
   const long long pmax = tc ? kMaxAutoPartitionTc : kMaxAutoPartition;
   long long p = kMinAutoPartition;
-  while (p * 2 <= per && p * 2 <= pmax) p *= 2;
+  // mma.sync: the largest power of two within per; tcgen05: the smallest
+  // power of two that covers per (its longer CTAs pay back their fill: GQA 5:1
+  // with 8 query tokens at 16K-32K tokens, per = 4088, took 4096-token
+  // partitions at 523 us fp16 and 535 us E4M3 against 540 and 572 at 2048)
+  while (p * 2 <= pmax && (tc ? p < per : p * 2 <= per)) p *= 2;
   if (p >= s.max_context_len) return -1;
   return (int)p;
 }

@@ -393,7 +393,7 @@ def test_multi_workspace_covers_both_tensor_core_paths(L):
 
 def test_tcgen05_split_policy(L):
     # the tcgen05 path splits only below two waves of units (two CTAs per SM), into
-    # partitions of up to 8192 tokens; the mma.sync path also splits long contexts
+    # partitions of up to 8192 tokens (per rounded up to a power of two); the mma.sync path also splits long contexts
     # below six waves, into partitions of at most 2048 tokens
     from paged_kv_decode_21_gb300 import ops
     sms = 148  # no device here: the library's default SM count
@@ -409,7 +409,10 @@ def test_tcgen05_split_policy(L):
     want = 6 * 2 * sms
     np_ = -(-want // 256)
     per = -(-32768 // np_)
-    p = 512
-    while p * 2 <= per and p * 2 <= 8192:
+    p = 512  # the smallest power of two covering per (at most 8192)
+    while p < per and p * 2 <= 8192:
         p *= 2
     assert var == "tcgen05" and part == p and part > 2048
+    # a longest context just below 32768 takes the same partition (per just below a power of
+    # two rounds up to it, not down to half of it)
+    assert ops.paged_decode_call_plan(32, 8, 40, 8, 128, 16, 32700)[1] == p
