@@ -86,16 +86,18 @@ def test_multi_token_small_grid_on_tcgen05(B, Hq, Hkv, L, fp8):
     assert ops.pkd_read_device_error(ew) == 0
 
 
-@pytest.mark.parametrize("fp8", [False, True])
-def test_tcgen05_partition_runs(fp8):
+@pytest.mark.parametrize("B,Hq,q_len,P,fp8", [(16, 40, 8, 512, False), (16, 40, 8, 512, True),
+                                              (16, 40, 4, 256, False), (16, 40, 8, 256, True),
+                                              (64, 28, 8, 1024, False), (32, 40, 4, 1024, True)])
+def test_tcgen05_partition_runs(B, Hq, q_len, P, fp8):
     # Many units at a short explicit partition: the tcgen05 plan gives each CTA a run of
     # consecutive partitions (fewer CTAs than partitions), each partial written on its own.
     # Ragged lengths put runs across the end of a sequence, a last run shorter than the others,
     # and sequences shorter than a partition or than the query tokens.
-    B, Hq, Hkv, q_len, P = 16, 40, 8, 8, 512
-    rng = torch.Generator().manual_seed(31)
+    Hkv = 8 if Hq == 40 else 4
+    rng = torch.Generator().manual_seed(31 + P + q_len)
     lens = torch.randint(1, 16385, (B,), generator=rng).tolist()
-    lens[:5] = [16384, 0, 5, 511, 1537]
+    lens[:6] = [16384, 0, 5, P - 1, 3 * P + 1, 16384 - P]
     L = max(lens)
     inp = workloads.make_custom(B, Hq, Hkv, 128, 16, lens, seed=33, device="cuda")
     g = torch.Generator(device="cuda").manual_seed(34)
