@@ -39,6 +39,8 @@ constexpr int kTargetWaves = 6;      // into enough partitions for this many wav
 constexpr int kLongContext = 8192;   // contexts this long split below kTargetWaves waves
 constexpr int kOrderMaxWaves = 6;    // unsplit grids below this many waves walk longest first,
 constexpr int kOrderMinContext = 1024;  // when their contexts reach this many tokens
+constexpr int kTailMinContext = 1024;   // tcgen05: the order splits the tail of contexts this long
+constexpr size_t kTailInfoBytes = 256;  // the order's tail record (two int32), after the order
 // Single-query E4M3 grids of at least this many waves of four CTAs per SM run
 // the four-per-SM build: 2-7% faster there (MHA, GQA 7:1 and 5:1, ragged
 // GQA 4:1 at batch 256), while a ragged GQA 4:1 batch of 1024 CTAs, bounded by
@@ -447,6 +449,41 @@ int auto_multi_path(const Shape& s, int q_len, int kv_fp8) {
   return PKD_VARIANT_TMA_MMA;
 }
 
+// Sequences the longest-first order may split in two on the tcgen05 path (0:
+// none); the grid has room for all of them.  An unsplit grid whose last round
+// of resident CTAs is at most half full runs that round as long as a full
+// one: a tcgen05 CTA is bounded by its own chain of hand-offs, so the round's
+// few CTAs go no faster.  Splitting the shortest sequences that fill it in two
+// gives the round twice the CTAs of half the length; the order kernel splits
+// those of them at least half as long as the batch's longest (a ragged batch
+// walked longest first already ends on short CTAs).  Measured on GQA 7:1 with
+// 8 query tokens, 8192-token contexts: 3 full rounds (batch 228) 567 us fp16
+// and 516 us E4M3, with a fourth round of 112 CTAs (batch 256) 676 and 668 us,
+// and with its 28 sequences split 672 and 601 us.
+int tail_split_seqs(const Shape& s, int q_chunks, int path, bool split, bool order) {
+  if (path != PKD_VARIANT_TCGEN05 || split || !order || s.max_context_len < kTailMinContext) return 0;
+  int sms = sm_count();
+  if (sms <= 0) sms = 148;
+  const int G = s.num_q_heads / s.num_kv_heads;
+  const long long slots = (long long)sms * path_stream(PKD_VARIANT_TCGEN05, s.head_dim, G, 2, false).ctas_per_sm;
+  const long long per_seq = (long long)s.num_kv_heads * q_chunks;
+  const long long units = (long long)s.num_seqs * per_seq;
+  if (units <= slots) return 0;
+  const long long last = units - (units - 1) / slots * slots;  // CTAs of the last round
+  if (2 * last > slots) return 0;
+  return (int)std::min<long long>(s.num_seqs, (last + per_seq - 1) / per_seq);
+}
+
+// Workspace of an automatic call whose plan splits the tail (0 when it does
+// not): partials for two partitions per row, the order and its tail record.
+size_t tail_split_bytes(const Shape& s, int q_len, int q_chunks, int path, int P) {
+  const bool split = P > 0 && s.max_context_len > P;
+  const int tail = tail_split_seqs(s, q_chunks, path, split, auto_order(s, path, q_chunks, P));
+  if (tail <= 0) return 0;
+  return layout(nullptr, s.num_seqs * q_len, s.num_q_heads, s.head_dim, 2).bytes + order_bytes(s.num_seqs + tail) +
+         kTailInfoBytes;
+}
+
 // The launch plan of one decode call.
 struct CallPlan {
   int P;           // tokens per partition (the whole context, rounded up to 32, when unsplit)
@@ -457,6 +494,7 @@ struct CallPlan {
   long long grid;  // decode CTAs
   int variant;     // the data path it runs, with the PKD_FLAG_* bits that apply
   bool order;      // the batch is walked longest first (when the workspace has room)
+  int tail;        // tcgen05, ordered: the shortest sequences the order splits in two (0: none)
 };
 
 // The partition, grid, data path and order a call with these arguments runs
@@ -511,6 +549,8 @@ pkd_status plan_call(const Shape& s, int q_len, int variant, int partition_size,
     out->runs = r;
     out->grid = units * ((out->np + r - 1) / r);
   }
+  out->tail = tail_split_seqs(s, q_chunks, variant_path(v), out->split, out->order);
+  if (out->tail > 0) out->grid = ((long long)s.num_seqs + out->tail) * s.num_kv_heads * q_chunks;
   return PKD_OK;
 }
 
@@ -533,7 +573,8 @@ pkd_status launch_decode(int variant, int D, int BS, int G, const pkd::DecodePar
 pkd_status launch_reduce(const float* tmp_out, const float* max_logits, const float* exp_sums,
                          const int32_t* context_lens, void* out, int num_seqs, int num_q_heads,
                          int head_dim, int partition_size, int max_num_partitions, int min_merge,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, const int32_t* tail_order = nullptr,
+                         const int32_t* tail_info = nullptr) {
   const long long rows = (long long)num_seqs * num_q_heads;
   if (rows <= 0) return PKD_OK;
   if (rows > 0x7fffffffLL) return PKD_ERR_SHAPE;
@@ -554,10 +595,12 @@ pkd_status launch_reduce(const float* tmp_out, const float* max_logits, const fl
   cudaError_t e;
   if (head_dim == 128) {
     e = cudaLaunchKernelEx(&cfg, pkd::paged_decode_reduce_kernel<128>, tmp_out, max_logits, exp_sums,
-                           context_lens, o, (int)rows, num_q_heads, partition_size, max_num_partitions, min_merge);
+                           context_lens, o, (int)rows, num_q_heads, partition_size, max_num_partitions, min_merge,
+                           tail_order, tail_info);
   } else if (head_dim == 64) {
     e = cudaLaunchKernelEx(&cfg, pkd::paged_decode_reduce_kernel<64>, tmp_out, max_logits, exp_sums,
-                           context_lens, o, (int)rows, num_q_heads, partition_size, max_num_partitions, min_merge);
+                           context_lens, o, (int)rows, num_q_heads, partition_size, max_num_partitions, min_merge,
+                           tail_order, tail_info);
   } else {
     return PKD_ERR_UNSUPPORTED;
   }
@@ -623,6 +666,8 @@ size_t paged_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_hea
     bytes = layout(nullptr, num_seqs, num_q_heads, head_dim, (max_context_len + P - 1) / P).bytes;
   if ((variant & PKD_FLAG_LONGEST_FIRST) || partition_size == 0)
     bytes += order_bytes(num_seqs, grid_partitions(max_context_len, P));
+  if (partition_size == 0 && variant_path(variant) == PKD_VARIANT_TCGEN05)
+    bytes = std::max(bytes, tail_split_bytes(s, 1, 1, PKD_VARIANT_TCGEN05, P));
   return bytes;
 }
 
@@ -660,8 +705,17 @@ pkd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
   if (st != PKD_OK) return st;
   const int P = plan.P, np = plan.np;
   const bool split = plan.split;
-  const long long grid = plan.grid;
+  long long grid = plan.grid;
   variant = plan.variant;
+  // The tail split keeps its partials (two per row), the order and the
+  // order's tail record in the workspace; without room the grid runs unsplit.
+  int tail = plan.tail;
+  if (tail > 0 && (!workspace || !aligned(workspace, 256) ||
+                   workspace_bytes < layout(nullptr, num_seqs * q_len, num_q_heads, head_dim, 2).bytes +
+                                         order_bytes(num_seqs + tail) + kTailInfoBytes)) {
+    tail = 0;
+    grid = (long long)num_seqs * num_kv_heads * plan.q_chunks;
+  }
 
   pkd::DecodeParams p{};
   p.q = static_cast<const __half*>(q);
@@ -690,11 +744,11 @@ pkd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
   p.l2_hints = (variant & PKD_FLAG_L2_EVICT_HINTS) ? 1 : 0;
   p.timeout_ns = kWaitBudgetNs;
   size_t used = 0;
-  if (split) {
+  if (split || tail > 0) {
     // partial rows are (sequence, query token, head)
     if (!workspace) return PKD_ERR_WORKSPACE;
     if (!aligned(workspace, 256)) return PKD_ERR_ALIGN;
-    Workspace w = layout(workspace, num_seqs * q_len, num_q_heads, head_dim, np);
+    Workspace w = layout(workspace, num_seqs * q_len, num_q_heads, head_dim, tail > 0 ? 2 : np);
     if (workspace_bytes < w.bytes) return PKD_ERR_WORKSPACE;
     p.tmp_out = w.tmp_out;
     p.max_logits = w.max_logits;
@@ -702,13 +756,20 @@ pkd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
     used = w.bytes;
   }
   // the order sits after the partials; it only reschedules, so a workspace
-  // without room for it runs the plain grid order instead
-  if (grid > 0 && plan.order && workspace &&
-      aligned(workspace, 256) && workspace_bytes >= used + order_bytes(num_seqs, np)) {
-    int32_t* order = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(workspace) + used);
-    pkd::piece_order_kernel<<<(num_seqs + 127) / 128, 128, 0, stream>>>(context_lens, num_seqs, P, np, order);
+  // without room for it runs the plain grid order instead (a tail split's
+  // record follows the order)
+  int32_t* tail_info = nullptr;
+  if (tail > 0) p.max_partitions = 2;
+  if (grid > 0 && plan.order && workspace && aligned(workspace, 256) &&
+      workspace_bytes >= used + (tail > 0 ? order_bytes(num_seqs + tail) + kTailInfoBytes : order_bytes(num_seqs, np))) {
+    unsigned char* at = static_cast<unsigned char*>(workspace) + used;
+    int32_t* order = reinterpret_cast<int32_t*>(at);
+    if (tail > 0) tail_info = reinterpret_cast<int32_t*>(at + order_bytes(num_seqs + tail));
+    pkd::piece_order_kernel<<<(num_seqs + 127) / 128, 128, 0, stream>>>(context_lens, num_seqs, P, np, order, tail,
+                                                                        tail_info);
     if (cudaGetLastError() != cudaSuccess) return PKD_ERR_LAUNCH;
     p.piece_order = order;
+    p.tail_split = tail > 0 ? 1 : 0;
   }
   if (kv_fp8 && variant_path(variant) == PKD_VARIANT_TCGEN05) {
     if (grid > 0x7fffffffLL) return PKD_ERR_SHAPE;
@@ -727,8 +788,12 @@ pkd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
   } else {
     st = launch_decode(variant_path(variant), head_dim, block_size, G, p, grid, stream);
   }
-  if (st != PKD_OK || !split) return st;
-  // the merge sees q_len * Hq rows per sequence
+  if (st != PKD_OK || (!split && tail == 0)) return st;
+  // the merge sees q_len * Hq rows per sequence; after a tail split, those of
+  // the (at most tail) sequences the order split
+  if (tail > 0)
+    return launch_reduce(p.tmp_out, p.max_logits, p.exp_sums, context_lens, out, tail, q_len * num_q_heads,
+                         head_dim, P, 2, /*min_merge=*/1, stream, p.piece_order, tail_info);
   return launch_reduce(p.tmp_out, p.max_logits, p.exp_sums, context_lens, out, num_seqs, q_len * num_q_heads,
                        head_dim, P, np, /*min_merge=*/1, stream);
 }
@@ -821,7 +886,7 @@ int paged_decode_call_plan(int num_seqs, int q_len, int num_q_heads, int num_kv_
                                            num_q_heads / num_kv_heads, kv_fp8 ? 1 : 2,
                                            wide_fp8_grid(kv_fp8, q_len, plan.grid), plan.grid, plan.P);
   if (num_seqs == 0 || plan.grid == 0) return 0;
-  return 1 + (plan.split ? 1 : 0) + (plan.order ? 1 : 0);
+  return 1 + (plan.split || plan.tail > 0 ? 1 : 0) + (plan.order ? 1 : 0);
 }
 
 int paged_decode_prefetch_model(int num_seqs, int q_len, int num_q_heads, int num_kv_heads, int head_dim,
@@ -875,6 +940,8 @@ size_t paged_decode_multi_workspace_size(int num_seqs, int q_len, int num_q_head
     if (partition_size == 0)  // the automatic split may order the batch
       bytes += order_bytes(num_seqs, grid_partitions(max_context_len, P));
     most = std::max(most, bytes);
+    if (partition_size == 0)  // ... and split its tail
+      most = std::max(most, tail_split_bytes(s, q_len, qch, path, P));
   }
   return most;
 }

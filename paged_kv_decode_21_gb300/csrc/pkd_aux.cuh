@@ -19,7 +19,8 @@ template <int D>
 __global__ void __launch_bounds__(32 * kReduceRowsPerCta) paged_decode_reduce_kernel(
     const float* __restrict__ tmp_out, const float* __restrict__ max_logits,
     const float* __restrict__ exp_sums, const int32_t* __restrict__ context_lens, __half* out,
-    int num_rows, int num_q_heads, int partition_size, int max_partitions, int min_partitions_to_merge) {
+    int num_rows, int num_q_heads, int partition_size, int max_partitions, int min_partitions_to_merge,
+    const int32_t* __restrict__ tail_order, const int32_t* __restrict__ tail_info) {
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
   constexpr int V = D / 32;
   constexpr int U = 16;  // partitions in flight per lane
@@ -27,12 +28,21 @@ __global__ void __launch_bounds__(32 * kReduceRowsPerCta) paged_decode_reduce_ke
   // grid has completed and its partials are visible (a no-op otherwise)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
-  const int row = blockIdx.x * kReduceRowsPerCta + (threadIdx.x >> 5);  // b * Hq + h
+  int row = blockIdx.x * kReduceRowsPerCta + (threadIdx.x >> 5);  // b * Hq + h
   if (row >= num_rows) return;
+  if (tail_order) {
+    // a grid whose order split its tail (piece_order_kernel): rows of the
+    // split sequences only, sequence t of them at order position
+    // tail_info[0] + 2 t, its partitions tail_half_partition(L) long
+    const int t = row / num_q_heads;
+    if (t >= tail_info[1]) return;
+    row = (tail_order[tail_info[0] + 2 * t] >> 2) * num_q_heads + row % num_q_heads;
+  }
   const int b = row / num_q_heads;
   const int L = context_lens[b];
+  const int PS = tail_order ? tail_half_partition(L) : partition_size;
   // partitions the first kernel wrote (none past its grid)
-  const int np = min((L + partition_size - 1) / partition_size, max_partitions);
+  const int np = min((L + PS - 1) / PS, max_partitions);
   // min_partitions_to_merge > 0: those sequences were written by the
   // partition kernel itself; 0 merges every sequence (empty ones get zeros)
   if (min_partitions_to_merge > 0 && np <= min_partitions_to_merge) return;
@@ -237,30 +247,51 @@ __global__ void __launch_bounds__(256) gather_used_blocks_kernel(
 // decreasing length.  Each CTA holds every sequence's piece count and last
 // piece in shared memory and places the pieces of 128 sequences.  The decode
 // grid reading the order is launched as its programmatic dependent.
+//
+// tail_seqs = K > 0 (unsplit grids, NP = 1): of the K shortest sequences
+// with tokens (the grid's last round), those at least half as long as the
+// batch's longest are split in two, each half its own piece, so that the
+// round holds twice as many pieces of half the length (shorter ones already
+// make a short round).  The split ones are the longest of the K, ranks
+// [fs, fs + S) with fs = (sequences with tokens) - K.  The pieces are coded
+// b * 4 + kPiece*: ranks below fs whole, then the two halves of each split
+// sequence, then the other ranks whole, then the empty sequences, then -1 for
+// the K - S slots left.  tail_info = {fs, S} tells the merge where the split
+// sequences' first halves sit in the order.
 constexpr int kOrderMaxSeqs = 4096;  // sequences held in shared memory (2 x 16 KiB)
 __global__ void __launch_bounds__(128) piece_order_kernel(const int32_t* __restrict__ context_lens, int num_seqs,
                                                           int partition_size, int num_partitions,
-                                                          int32_t* __restrict__ piece_order) {
+                                                          int32_t* __restrict__ piece_order, int tail_seqs,
+                                                          int32_t* __restrict__ tail_info) {
   __shared__ int32_t s_np[kOrderMaxSeqs];    // pieces with tokens
   __shared__ int32_t s_last[kOrderMaxSeqs];  // tokens of the last of them
+  __shared__ int32_t s_lmax;
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int PS = partition_size, NP = num_partitions;
+  if (threadIdx.x == 0) s_lmax = 0;
+  __syncthreads();
+  int lmax = 0;
   for (int i = threadIdx.x; i < num_seqs; i += blockDim.x) {
     const int L = max(context_lens[i], 0);
     const int n = min((L + PS - 1) / PS, NP);
     s_np[i] = n;
     s_last[i] = n > 0 ? L - (n - 1) * PS : 0;
+    lmax = max(lmax, L);
   }
+  if (tail_seqs > 0) atomicMax(&s_lmax, lmax);
   __syncthreads();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= num_seqs) return;
   const int n_b = s_np[b], last_b = s_last[b];
   int full = 0, full_before = 0, lasts = 0, last_rank = 0, empty_before = 0;
+  int half_long = 0;  // tail split: sequences with at least half the longest one's tokens
+  const int lhalf = (s_lmax + 1) / 2;
   for (int i = 0; i < num_seqs; ++i) {
     const int n = s_np[i];
     const int f = n > 0 ? n - 1 : 0;
     full += f;
     lasts += n > 0;
+    half_long += n > 0 && s_last[i] >= lhalf;
     if (i < b) {
       full_before += f;
       empty_before += NP - n;
@@ -269,6 +300,28 @@ __global__ void __launch_bounds__(128) piece_order_kernel(const int32_t* __restr
       const int li = s_last[i];
       last_rank += (li > last_b) | ((li == last_b) & (i < b));
     }
+  }
+  if (tail_seqs > 0) {  // NP = 1: full = 0, n_b is 0 or 1, last_rank the rank among sequences with tokens
+    // (with NP = 1 the last piece's tokens are the sequence's, so the half-long
+    // sequences are exactly ranks [0, half_long))
+    const int fs = lasts - min(tail_seqs, lasts);
+    const int S = max(0, min(half_long, lasts) - fs);
+    if (n_b == 0)
+      piece_order[lasts + S + empty_before] = b * 4 + kPieceWhole;
+    else if (last_rank < fs)
+      piece_order[last_rank] = b * 4 + kPieceWhole;
+    else if (last_rank < fs + S) {
+      const int at = fs + 2 * (last_rank - fs);
+      piece_order[at] = b * 4 + kPieceFirstHalf;
+      piece_order[at + 1] = b * 4 + kPieceSecondHalf;
+    } else
+      piece_order[last_rank + S] = b * 4 + kPieceWhole;
+    if (b < tail_seqs - S) piece_order[num_seqs + S + b] = -1;
+    if (b == 0) {
+      tail_info[0] = fs;
+      tail_info[1] = S;
+    }
+    return;
   }
   const int base = b * NP;
   for (int j = 0; j + 1 < n_b; ++j) piece_order[full_before + j] = base + j;

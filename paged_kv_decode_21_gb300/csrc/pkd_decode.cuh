@@ -72,7 +72,18 @@ struct DecodeParams {
   unsigned long long timeout_ns;
   const int32_t* piece_order;  // nullable: grid piece p -> b * NP + j (longest first); tensor-core path only
   int parts_per_cta;           // tcgen05 path: consecutive partitions per CTA (0 or 1: one; needs no piece order)
+  int tail_split;              // tcgen05 path with piece_order: pieces are b * 4 + a kPiece* code (a split tail)
 };
+
+// A grid walked longest first whose last round would be short splits its
+// shortest sequences in two (the tcgen05 path; piece_order_kernel chooses
+// them).  Piece codes, piece = b * 4 + code (-1: no piece):
+constexpr int kPieceWhole = 0;       // the whole sequence, written to out
+constexpr int kPieceFirstHalf = 1;   // tokens [0, tail_half_partition(L)), a partial
+constexpr int kPieceSecondHalf = 2;  // the rest, a partial
+// The partition of such a split sequence of L tokens: half of it, rounded up
+// to whole 64-token tiles (so a sequence of at most 64 tokens stays whole).
+__host__ __device__ __forceinline__ int tail_half_partition(int L) { return ((L + 1) / 2 + 63) / 64 * 64; }
 
 template <int D, int BS, int G, int VARIANT>
 struct DecodeTraits {

@@ -178,12 +178,20 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, K
   const int rest = blockIdx.x / P.q_chunks;
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   int j, b, g;
+  bool half = false;  // a half of a sequence the order split (its own partition size)
   if (P.piece_order) {
     g = rest % P.num_kv_heads;
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int piece = P.piece_order[rest / P.num_kv_heads];
-    b = piece / np_grid;
-    j = piece % np_grid;
+    if (P.tail_split) {
+      if (piece < 0) return;  // a slot past the batch's pieces
+      b = piece >> 2;
+      j = (piece & 3) == kPieceSecondHalf ? 1 : 0;
+      half = (piece & 3) != kPieceWhole;
+    } else {
+      b = piece / np_grid;
+      j = piece % np_grid;
+    }
   } else {
     const int nruns = (np_grid + R - 1) / R;
     j = (rest % nruns) * R;
@@ -196,7 +204,7 @@ __global__ void __launch_bounds__(TcTraits<BS, KVB, HD>::THREADS, TcTraits<BS, K
   const int jq0 = qc * (T::ROWS / G);         // first query token of this CTA
   const int nq = min(T::ROWS / G, QL - jq0);  // its query tokens (>= 1)
   const int rows = G * nq;                    // tile rows in use
-  const int PS = P.partition_size;
+  const int PS = half ? tail_half_partition(L) : P.partition_size;
   const int np_b = min((L + PS - 1) / PS, np_grid);
   const bool final_out = (P.mode == 0) && np_b <= 1;
   const int Hq = P.num_q_heads;

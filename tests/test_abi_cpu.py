@@ -243,6 +243,33 @@ def test_small_grid_split_fills_one_wave():
     assert ops.paged_decode_call_plan(1, 1, 32, 32, 128, 16, 2048, variant="tma_staged")[1] == 512
 
 
+def test_tcgen05_tail_split_plan():
+    # An unsplit, longest-first tcgen05 grid whose last round of resident CTAs (two per SM,
+    # 148 SMs without a GPU) is at most half full sizes its grid for splitting its K shortest
+    # sequences in two, K = ceil(CTAs of the last round / CTAs per sequence): grid (B + K) x kv
+    # heads x query chunks (the order kernel splits those of them at least half as long as the
+    # longest sequence; the other slots exit at once).
+    from paged_kv_decode_21_gb300 import ops
+    slots = 2 * 148
+    for B, Hq, Hkv, q_len, L in [(160, 28, 4, 8, 2048), (256, 28, 4, 8, 8192), (128, 32, 8, 8, 4096),
+                                 (300, 28, 4, 8, 2048), (76, 32, 8, 8, 2048)]:
+        for fp8 in (False, True):
+            n, part, ordered, var, grid, _ = ops.paged_decode_call_plan(B, q_len, Hq, Hkv, 128, 16, L, kv_fp8=fp8)
+            units = B * Hkv
+            last = units - (units - 1) // slots * slots
+            k = -(-last // Hkv) if units > slots and 2 * last <= slots else 0
+            assert var.startswith("tcgen05") and part == -1 and ordered, (B, L, var, part)
+            assert grid == (B + k) * Hkv and n == (3 if k else 2), (B, L, fp8, grid, k)
+            ws = ops.paged_decode_multi_workspace_size(B, q_len, Hq, Hkv, 128, 16, L, 0)
+            rows = B * q_len * Hq
+            if k:  # partials of two partitions per row, the order of B + K pieces and its tail record
+                assert ws >= rows * 2 * 128 * 4 + 2 * rows * 2 * 4 + (B + k) * 4 + 8
+    # an explicit partition, short contexts, or a path other than tcgen05: no tail split
+    assert ops.paged_decode_call_plan(256, 8, 28, 4, 128, 16, 8192, partition_size=-1)[4] == 1024
+    assert ops.paged_decode_call_plan(256, 8, 28, 4, 128, 16, 512)[4] == 1024
+    assert ops.paged_decode_call_plan(256, 1, 28, 4, 128, 16, 8192, variant="tma_mma")[4] == 1024 * 4
+
+
 def test_tcgen05_partition_runs_plan():
     # Explicit partitions of up to 1024 tokens on the tcgen05 path at head_dim 128: a CTA takes
     # a run of up to 4096 tokens of consecutive partitions while the grid keeps four waves of
@@ -397,9 +424,11 @@ def test_tcgen05_split_policy(L):
     # below six waves, into partitions of at most 2048 tokens
     from paged_kv_decode_21_gb300 import ops
     sms = 148  # no device here: the library's default SM count
-    # GQA 7:1, 256 x 8192 tokens, q_len 8: 1024 units, three waves and more
+    # GQA 7:1, 256 x 8192 tokens, q_len 8: 1024 units, three waves and more, unsplit and walked
+    # longest first; the last round of 296 slots holds 1024 - 3 * 296 = 136 CTAs, so the order
+    # splits the 34 shortest sequences in two (three launches: order, decode, merge)
     n, part, ordered, var, grid, _ = ops.paged_decode_call_plan(256, 8, 28, 4, 128, 16, 8192)
-    assert var.startswith("tcgen05") and part == -1 and grid == 1024
+    assert var.startswith("tcgen05") and part == -1 and ordered and n == 3 and grid == (256 + 34) * 4
     n, part, ordered, var, grid, _ = ops.paged_decode_call_plan(256, 8, 28, 4, 128, 16, 8192, variant="tma_mma")
     assert part == -1 and grid == 256 * 4 * 4  # four 16-row chunks: many waves, unsplit too
     n, part, ordered, var, grid, _ = ops.paged_decode_call_plan(256, 1, 28, 4, 128, 16, 8192)

@@ -121,3 +121,76 @@ def test_tcgen05_partition_runs(B, Hq, q_len, P, fp8):
         ref = oracle.attention_multi(q.cpu(), inp.k_cache.cpu(), inp.v_cache.cpu(), *host, inp.scale)
         assert_close(out, ref, "fp16 runs")
     assert ops.pkd_read_device_error(ew) == 0
+
+
+def tail_seqs(B, Hkv, q_chunks=1):
+    # sequences the longest-first order of a tcgen05 grid splits in two: the last round of
+    # resident CTAs (two per SM) at most half full
+    slots = slots_of(2)
+    units = B * Hkv * q_chunks
+    last = units - (units - 1) // slots * slots
+    return -(-last // (Hkv * q_chunks)) if units > slots and 2 * last <= slots else 0
+
+
+def slots_of(per_sm):
+    return torch.cuda.get_device_properties(0).multi_processor_count * per_sm
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("kind", ["uniform", "ragged", "tiny", "mostly_empty", "gqa4", "q_len4"])
+def test_tcgen05_tail_split(kind, fp8):
+    # An unsplit tcgen05 grid walked longest first whose last round is short: of the K shortest
+    # sequences the order kernel splits those at least half as long as the longest in two
+    # halves, each CTA of a half writes a partial, and the merge combines those sequences only.
+    # Ragged lengths put shorter sequences among the K (they stay whole); "tiny" contexts (the
+    # longest 130 tokens) split sequences of 65-130 tokens, whose second half can be one token,
+    # next to whole ones of 1-64 tokens, shorter than the query; a mostly empty batch has fewer
+    # sequences with tokens than K (the order pads with empty slots).
+    Hq, Hkv, q_len = (32, 8, 8) if kind == "gqa4" else (28, 4, 4 if kind == "q_len4" else 8)
+    B = -(-(slots_of(2) * 2 + 32) // Hkv)  # two full rounds and a short third one
+    L = 2048
+    if kind == "ragged":
+        rng = torch.Generator().manual_seed(41)
+        lens = torch.randint(1024, L + 1, (B,), generator=rng).tolist()
+        lens[:10] = [L, 0, 1, 5, 64, 65, 100, 129, 700, 0]
+    elif kind == "tiny":
+        rng = torch.Generator().manual_seed(42)
+        lens = torch.randint(65, 131, (B,), generator=rng).tolist()
+        lens[:10] = [130, 0, 1, 5, 64, 65, 66, 100, 127, 129]
+    elif kind == "mostly_empty":
+        lens = [0] * B
+        lens[3], lens[7], lens[20] = L, 1500, 90
+    else:
+        lens = [L] * B
+    K = tail_seqs(B, Hkv)
+    assert K > 0
+    n, part, ordered, var, grid, _ = ops.paged_decode_call_plan(B, q_len, Hq, Hkv, 128, 16, L, kv_fp8=fp8)
+    assert var.startswith("tcgen05") and part == -1 and ordered and grid == (B + K) * Hkv and n == 3
+    # table rows of L tokens: the call passes max_context_len = L whatever the lengths
+    inp = workloads.make_custom(B, Hq, Hkv, 128, 16, lens, seed=43, device="cuda", max_blocks_per_seq=L // 16)
+    g = torch.Generator(device="cuda").manual_seed(44)
+    q = workloads.randn_f16((B, q_len, Hq, 128), g, "cuda")
+    ew = torch.zeros(1, dtype=torch.int32, device="cuda")
+    host = (inp.block_tables.cpu(), inp.context_lens.cpu())
+    if fp8:
+        k8 = workloads.rand_e4m3(inp.k_cache.shape, g, "cuda")
+        v8 = workloads.rand_e4m3(inp.v_cache.shape, g, "cuda")
+        out = ops.paged_decode_attention_fp8(q, k8, v8, inp.block_tables, inp.context_lens, inp.scale, KS, VS,
+                                             max_context_len=L, error_word=ew)
+        ref = oracle.attention_fp8(q.cpu(), k8.cpu(), v8.cpu(), *host, inp.scale, KS, VS)
+        absref = oracle.attention_fp8(q.cpu(), k8.cpu(), e4m3_magnitudes(v8).cpu(), *host, inp.scale, KS, VS)
+        assert_close_weighted(out, ref, absref, 448.0 * VS, L, f"E4M3 tail split {kind}")
+    else:
+        out = ops.paged_decode_attention_multi(q, inp.k_cache, inp.v_cache, inp.block_tables, inp.context_lens,
+                                               inp.scale, max_context_len=L, error_word=ew)
+        ref = oracle.attention_multi(q.cpu(), inp.k_cache.cpu(), inp.v_cache.cpu(), *host, inp.scale)
+        assert_close(out, ref, f"fp16 tail split {kind}")
+    assert ops.pkd_read_device_error(ew) == 0
+    # the same call with a workspace too small for the tail split runs it unsplit, to the same result
+    if not fp8:
+        small = ops.alloc_workspace(ops.paged_decode_workspace_size(B, Hq, Hkv, 128, 16, L, -1, "tcgen05+longest_first"),
+                                    "cuda")
+        out2 = ops.paged_decode_attention_multi(q, inp.k_cache, inp.v_cache, inp.block_tables, inp.context_lens,
+                                                inp.scale, max_context_len=L, workspace=small, error_word=ew)
+        assert_close(out2, ref, f"fp16 tail split {kind}, small workspace")
+        assert ops.pkd_read_device_error(ew) == 0
