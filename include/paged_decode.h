@@ -202,7 +202,13 @@ pkd_status paged_decode_attention_host(const void* q, const void* k_cache, const
  *                   streams up to 4096 tokens of consecutive partitions of
  *                   its (sequence, kv head) and writes each one's partial,
  *                   while the grid keeps four waves of CTAs; the result is
- *                   the same.  The automatic choice splits only
+ *                   the same.  On the tcgen05 path an unsplit grid walked
+ *                   longest first whose last round of resident CTAs would
+ *                   be at most half full has that round's sequences, those
+ *                   at least half as long as the batch's longest, split in
+ *                   two halves merged like partitions (when the workspace
+ *                   has room: the *_workspace_size functions count it for
+ *                   partition_size 0).  The automatic choice splits only
  *                   grids of fewer than two waves of (sequence, kv head)
  *                   units (on the mma.sync path also contexts of 8192
  *                   tokens or more below six waves), into power-of-two
