@@ -20,7 +20,7 @@ from paged_kv_decode_21_gb300 import ops, workloads
 pytestmark = pytest.mark.gpu
 
 KS, VS = workloads.E4M3_SCALES["full"]
-N_CASES = 24
+N_CASES = 48
 
 
 @pytest.fixture(scope="module", autouse=True)
