@@ -9,7 +9,12 @@
 // head r % G) for up to kTcRows rows: every query head of the group and up to
 // kTcRows / G query tokens share one pass over the partition's K and V, so a
 // multi-token query (speculative verification) reads the cache once per
-// chunk of kTcRows / G tokens rather than once per 16 / G.
+// chunk of kTcRows / G tokens rather than once per 16 / G.  Two variations of
+// the split: the RUNS build takes R consecutive partitions of its (b, g) in
+// one stream of tiles and writes each one's partial (short partitions would
+// each pay the CTA's fill); and a grid walked longest first whose last round
+// would be short reads pieces coded whole sequence / first half / second half
+// (tail_split), a half being its own partition of tail_half_partition(L).
 //
 // Roles (five warps over fp16 caches, six over E4M3):
 //   fp16: warps 2    producers: 3-D tensor copies of the partition's K (warp 2)
