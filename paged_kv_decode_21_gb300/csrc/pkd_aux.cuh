@@ -263,16 +263,19 @@ __global__ void __launch_bounds__(128) piece_order_kernel(const int32_t* __restr
                                                           int partition_size, int num_partitions,
                                                           int32_t* __restrict__ piece_order, int tail_seqs,
                                                           int32_t* __restrict__ tail_info) {
-  __shared__ int32_t s_np[kOrderMaxSeqs];    // pieces with tokens
-  __shared__ int32_t s_last[kOrderMaxSeqs];  // tokens of the last of them
+  __shared__ __align__(16) int32_t s_np[kOrderMaxSeqs];    // pieces with tokens
+  __shared__ __align__(16) int32_t s_last[kOrderMaxSeqs];  // tokens of the last of them
   __shared__ int32_t s_lmax;
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int PS = partition_size, NP = num_partitions;
   if (threadIdx.x == 0) s_lmax = 0;
   __syncthreads();
+  // the sequences in quads (four per shared-memory read below); the padding
+  // has no piece and so counts for nothing
+  const int n4 = (num_seqs + 3) / 4;
   int lmax = 0;
-  for (int i = threadIdx.x; i < num_seqs; i += blockDim.x) {
-    const int L = max(context_lens[i], 0);
+  for (int i = threadIdx.x; i < 4 * n4; i += blockDim.x) {
+    const int L = i < num_seqs ? max(context_lens[i], 0) : 0;
     const int n = min((L + PS - 1) / PS, NP);
     s_np[i] = n;
     s_last[i] = n > 0 ? L - (n - 1) * PS : 0;
@@ -286,20 +289,24 @@ __global__ void __launch_bounds__(128) piece_order_kernel(const int32_t* __restr
   int full = 0, full_before = 0, lasts = 0, last_rank = 0, empty_before = 0;
   int half_long = 0;  // tail split: sequences with at least half the longest one's tokens
   const int lhalf = (s_lmax + 1) / 2;
-  for (int i = 0; i < num_seqs; ++i) {
-    const int n = s_np[i];
+  auto count = [&](int n, int li, int i) {
     const int f = n > 0 ? n - 1 : 0;
+    const bool before = i < b;
     full += f;
     lasts += n > 0;
-    half_long += n > 0 && s_last[i] >= lhalf;
-    if (i < b) {
-      full_before += f;
-      empty_before += NP - n;
-    }
-    if (n > 0) {
-      const int li = s_last[i];
-      last_rank += (li > last_b) | ((li == last_b) & (i < b));
-    }
+    half_long += n > 0 && li >= lhalf;
+    full_before += before ? f : 0;
+    empty_before += before ? NP - n : 0;
+    last_rank += (n > 0) & ((li > last_b) | ((li == last_b) & before));
+  };
+#pragma unroll 4
+  for (int q = 0; q < n4; ++q) {
+    const int4 nn = reinterpret_cast<const int4*>(s_np)[q];
+    const int4 ll = reinterpret_cast<const int4*>(s_last)[q];
+    count(nn.x, ll.x, 4 * q);
+    count(nn.y, ll.y, 4 * q + 1);
+    count(nn.z, ll.z, 4 * q + 2);
+    count(nn.w, ll.w, 4 * q + 3);
   }
   if (tail_seqs > 0) {  // NP = 1: full = 0, n_b is 0 or 1, last_rank the rank among sequences with tokens
     // (with NP = 1 the last piece's tokens are the sequence's, so the half-long
