@@ -383,9 +383,10 @@ pkd_status paged_decode_attention_multi_ex(const void* q, const void* k_cache, c
  * partition, or -1 when unsplit), *longest_first (1 when the batch is walked
  * longest first, given a workspace of the size the *_workspace_size
  * functions return), *variant_out (the data path with the PKD_FLAG_* bits
- * that apply), *grid_out (decode CTAs) and *prefetch_distance_out (the L2
- * prefetch distance the call runs with prefetch_distance 0; 0 = none); any
- * pointer may be NULL.
+ * that apply), *grid_out (decode CTAs; with the tcgen05 path's split of a
+ * short last round, room for its extra halves) and *prefetch_distance_out
+ * (the L2 prefetch distance the call runs with prefetch_distance 0; 0 =
+ * none); any pointer may be NULL.
  * Returns the kernel launches (decode grid, split-K merge, order kernel; 0
  * for an empty batch), or -2 for a shape, partition or variant the call
  * would refuse.
@@ -451,7 +452,8 @@ int paged_decode_prefetch_model(int num_seqs, int q_len, int num_q_heads, int nu
  * partition, or -1 when unsplit) and *longest_first (1 when the batch is
  * walked longest first, given a workspace of the size the *_workspace_size
  * functions return); either pointer may be NULL.  Returns the kernel launches
- * the call makes (the decode grid, plus the split-K merge, plus the order
+ * the call makes (the decode grid, plus the split-K merge when split or when
+ * the order splits a short last round on the tcgen05 path, plus the order
  * kernel; 0 for an empty batch), or -2 on an invalid shape.
  */
 int paged_decode_auto_plan(int num_seqs, int q_len, int num_q_heads, int num_kv_heads, int head_dim,
